@@ -1,0 +1,163 @@
+"""fp64 CPU oracle for scaled dot-product attention (test infrastructure).
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package. The CUDA library and its Python binding
+never import it, and it imports nothing from them.
+
+The arithmetic lives in ``attn_oracle.c`` (plain C, fp64, OpenMP over heads
+and rows). This module only compiles it (``build()``), loads it with ctypes
+and converts arrays: bf16 inputs are upcast to fp64 exactly, so the oracle
+sees the very bytes the GPU sees.
+
+Functions:
+  weights(q, k, causal, scale)             -> (S, P) of one head       (§3.2.1, Fig. 2)
+  fwd(q, k, v, causal, scale, rows=None)   -> (O, lse)                 (eq. (1))
+  bwd(q, k, v, dO, causal, scale)          -> (dQ, dK, dV, O, lse)     (derivative of eq. (1))
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+from typing import Optional, Sequence
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "attn_oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+CFLAGS = ["-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp", "-ffp-contract=off",
+          "-fno-fast-math"]
+
+
+def build(force: bool = False) -> str:
+    """Compile attn_oracle.c into liboracle.so next to it (gcc, no fast-math)."""
+    if not force and os.path.exists(_LIB) and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC):
+        return _LIB
+    tmp = _LIB + f".tmp{os.getpid()}"
+    cmd = ["gcc", *CFLAGS, "-o", tmp, _SRC, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            lib = ctypes.CDLL(_LIB)
+            dp = ctypes.POINTER(ctypes.c_double)
+            lp = ctypes.POINTER(ctypes.c_long)
+            L, I, D = ctypes.c_long, ctypes.c_int, ctypes.c_double
+            lib.oracle_attn_weights.argtypes = [dp, dp, L, L, L, I, D, dp, dp]
+            lib.oracle_attn_fwd.argtypes = [dp, dp, dp, dp, dp, L, L, L, L, L, L, I, D, lp, L]
+            lib.oracle_attn_bwd.argtypes = [dp, dp, dp, dp, dp, dp, dp, dp, dp,
+                                            L, L, L, L, L, L, I, D]
+            for f in (lib.oracle_attn_weights, lib.oracle_attn_fwd, lib.oracle_attn_bwd):
+                f.restype = ctypes.c_int
+            lib.oracle_num_threads.restype = ctypes.c_int
+            _lib = lib
+    return _lib
+
+
+def _f64(x) -> np.ndarray:
+    """Exact upcast to a C-contiguous float64 numpy array (bf16 -> fp64 is lossless)."""
+    try:
+        import torch
+        if isinstance(x, torch.Tensor):
+            return np.ascontiguousarray(x.detach().to("cpu", torch.float64).numpy())
+    except ImportError:  # pragma: no cover
+        pass
+    return np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+
+
+def _ptr(a: Optional[np.ndarray]):
+    if a is None:
+        return None
+    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_double))
+
+
+def _as4(a: np.ndarray) -> np.ndarray:
+    if a.ndim == 2:
+        return a[None, None]
+    if a.ndim == 3:
+        return a[None]
+    if a.ndim != 4:
+        raise ValueError("expected a [S,d], [h,S,d] or [B,h,S,d] array")
+    return a
+
+
+def _check(status: int, what: str):
+    if status != 0:
+        raise RuntimeError(f"oracle {what} failed with status {status}")
+
+
+def num_threads() -> int:
+    return int(_load().oracle_num_threads())
+
+
+def weights(q, k, causal: bool, scale: float):
+    """Scaled scores S (masked = -inf) and weights P of ONE head, each n x m."""
+    Q, K = _f64(q), _f64(k)
+    n, dk = Q.shape
+    m = K.shape[0]
+    S = np.empty((n, m))
+    P = np.empty((n, m))
+    _check(_load().oracle_attn_weights(_ptr(Q), _ptr(K), n, m, dk, int(causal), float(scale),
+                                       _ptr(S), _ptr(P)), "weights")
+    return S, P
+
+
+def fwd(q, k, v, causal: bool, scale: float, rows: Optional[Sequence[int]] = None):
+    """O (fp64, shape of q with d_v) and lse ([..., n]) by eq. (1).
+
+    With ``rows`` only those query rows are computed; the others are NaN.
+    """
+    Q, K, V = _as4(_f64(q)), _as4(_f64(k)), _as4(_f64(v))
+    B, h, n, dk = Q.shape
+    m, dv = K.shape[2], V.shape[3]
+    if K.shape != (B, h, m, dk) or V.shape != (B, h, m, dv):
+        raise ValueError("q/k/v shapes disagree")
+    O = np.full((B, h, n, dv), np.nan)
+    lse = np.full((B, h, n), np.nan)
+    r = None
+    nr = 0
+    if rows is not None:
+        r = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+        nr = int(r.size)
+    _check(_load().oracle_attn_fwd(
+        _ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(lse), B, h, n, m, dk, dv, int(causal),
+        float(scale), None if r is None else r.ctypes.data_as(ctypes.POINTER(ctypes.c_long)),
+        nr), "fwd")
+    shape_o = tuple(np.shape(q)[:-1]) + (dv,)
+    return O.reshape(shape_o), lse.reshape(shape_o[:-1])
+
+
+def bwd(q, k, v, dO, causal: bool, scale: float, need=("dq", "dk", "dv")):
+    """dQ, dK, dV of L = sum(dO * O) for O = Attention(q, k, v); also O and lse."""
+    Q, K, V, G = _as4(_f64(q)), _as4(_f64(k)), _as4(_f64(v)), _as4(_f64(dO))
+    B, h, n, dk = Q.shape
+    m, dv = K.shape[2], V.shape[3]
+    if K.shape != (B, h, m, dk) or V.shape != (B, h, m, dv) or G.shape != (B, h, n, dv):
+        raise ValueError("q/k/v/dO shapes disagree")
+    dQ = np.zeros((B, h, n, dk)) if "dq" in need else None
+    dK = np.zeros((B, h, m, dk)) if "dk" in need else None
+    dV = np.zeros((B, h, m, dv)) if "dv" in need else None
+    O = np.empty((B, h, n, dv))
+    lse = np.empty((B, h, n))
+    _check(_load().oracle_attn_bwd(_ptr(Q), _ptr(K), _ptr(V), _ptr(G), _ptr(dQ), _ptr(dK),
+                                   _ptr(dV), _ptr(O), _ptr(lse), B, h, n, m, dk, dv,
+                                   int(causal), float(scale)), "bwd")
+    lead_q = tuple(q.shape[:-2])
+    lead_k = tuple(k.shape[:-2])
+
+    def shp(a, lead, S, d):
+        return None if a is None else a.reshape(lead + (S, d))
+
+    return (shp(dQ, lead_q, n, dk), shp(dK, lead_k, m, dk), shp(dV, lead_k, m, dv),
+            O.reshape(lead_q + (n, dv)), lse.reshape(lead_q + (n,)))

@@ -1,0 +1,291 @@
+/*
+ * fp64 CPU oracle for multi-head scaled dot-product attention.
+ *
+ * TEST INFRASTRUCTURE. Only the tests, the smoke check and the CPU-baseline
+ * leg of the benchmark may build, load or call this file. The CUDA library
+ * never links it, and it includes nothing from the CUDA path.
+ *
+ * What it computes is the plain definition, with no tiling, no online
+ * softmax and no reordering beyond what the definition states:
+ *
+ *   "Attention Is All You Need", §3.2.1 eq. (1):
+ *       Attention(Q, K, V) = softmax(Q K^T / sqrt(d_k)) V
+ *   Figure 2 (left): MatMul -> Scale -> Mask (opt.) -> SoftMax -> MatMul.
+ *   §3.2.3: in decoder self-attention every illegal connection (key j after
+ *   query i) is set to -inf in the softmax input; position i itself stays
+ *   visible. Masked weights are therefore exactly zero.
+ *   §3.2.2: the h heads are independent problems run in parallel.
+ *
+ * The softmax subtracts the row maximum before exponentiating. That is a
+ * numerical device only (exp(s - M) / sum exp(s - M) equals
+ * exp(s) / sum exp(s) exactly in real arithmetic); the pages' numpy sketch of
+ * eq. (1) does the same.
+ *
+ * The backward pass is the analytic derivative of the above for an upstream
+ * gradient dO (the pages train the model, §5, but never write the derivative):
+ *   D_i   = sum_c dO_ic O_ic
+ *   dP_ij = sum_c dO_ic v_jc
+ *   dS_ij = P_ij (dP_ij - D_i)
+ *   dQ_i  = scale sum_j dS_ij k_j
+ *   dK_j  = scale sum_i dS_ij q_i
+ *   dV_j  = sum_i P_ij dO_i
+ *
+ * Readings where the pages are silent (each listed in the design notes):
+ *   - scale is an explicit argument; callers pass 1/sqrt(d_k) for eq. (1).
+ *   - causal masking is top-left aligned: key j is visible to query i iff
+ *     j <= i, for any n and m.
+ *   - lse_i = M_i + ln(l_i) = ln sum_j exp(s_ij), in natural-log units of the
+ *     scaled score.
+ *
+ * Layout: every tensor is a contiguous row-major [B, h, S, d] array of
+ * doubles (lse is [B, h, n]). Built with -O2 -ffp-contract=off and without
+ * -ffast-math so the C library's fp64 exp/log and IEEE rounding are used.
+ */
+#include <math.h>
+#include <stddef.h>
+#include <stdlib.h>
+#include <string.h>
+
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define ORACLE_OK 0
+#define ORACLE_ERR_ARG 1
+#define ORACLE_ERR_NOMEM 2
+
+/* Number of keys visible to query i: all m, or j <= i when causal (§3.2.3). */
+static long visible_keys(long i, long m, int causal) {
+    if (!causal) return m;
+    return (i + 1 < m) ? (i + 1) : m;
+}
+
+/* Step MatMul + Scale + Mask of Figure 2 for one query row:
+ * s_j = scale * sum_c q_c k_jc for visible j, and -inf for masked j. */
+static void score_row(const double *qi, const double *K, long m, long dk,
+                      double scale, long visible, double *s) {
+    for (long j = 0; j < m; ++j) {
+        if (j >= visible) {
+            s[j] = -INFINITY;
+            continue;
+        }
+        const double *kj = K + j * dk;
+        double dot = 0.0;
+        for (long c = 0; c < dk; ++c) dot += qi[c] * kj[c];
+        s[j] = scale * dot;
+    }
+}
+
+/* Step SoftMax of Figure 2, in place: s_j -> P_j = exp(s_j - M) / l with
+ * M = max_j s_j and l = sum_j exp(s_j - M). Returns lse = M + ln l.
+ * Masked entries hold -inf and come out as exactly 0. */
+static double softmax_row(double *s, long m) {
+    double M = -INFINITY;
+    for (long j = 0; j < m; ++j)
+        if (s[j] > M) M = s[j];
+    double l = 0.0;
+    for (long j = 0; j < m; ++j) {
+        s[j] = exp(s[j] - M);
+        l += s[j];
+    }
+    for (long j = 0; j < m; ++j) s[j] = s[j] / l;
+    return M + log(l);
+}
+
+/* Second MatMul of Figure 2: O_i = sum_j P_j v_j. */
+static void weighted_sum(const double *P, const double *V, long m, long dv,
+                         double *oi) {
+    for (long c = 0; c < dv; ++c) oi[c] = 0.0;
+    for (long j = 0; j < m; ++j) {
+        if (P[j] == 0.0) continue; /* masked or underflowed: contributes 0 */
+        const double *vj = V + j * dv;
+        for (long c = 0; c < dv; ++c) oi[c] += P[j] * vj[c];
+    }
+}
+
+static int check_dims(long B, long h, long n, long m, long dk, long dv) {
+    if (B < 0 || h < 0 || n < 0 || m < 1 || dk < 1 || dv < 1) return ORACLE_ERR_ARG;
+    return ORACLE_OK;
+}
+
+/*
+ * Scaled scores and attention weights of ONE head (Q: n x dk, K: m x dk).
+ * s_out and p_out are n x m (either may be NULL). Masked scores are -inf.
+ * Intended for small cases (inspection of the weight matrix, §3.2.1).
+ */
+int oracle_attn_weights(const double *Q, const double *K, long n, long m,
+                        long dk, int causal, double scale, double *s_out,
+                        double *p_out) {
+    if (check_dims(1, 1, n, m, dk, 1) != ORACLE_OK) return ORACLE_ERR_ARG;
+    double *row = (double *)malloc(sizeof(double) * (size_t)m);
+    if (!row) return ORACLE_ERR_NOMEM;
+    for (long i = 0; i < n; ++i) {
+        score_row(Q + i * dk, K, m, dk, scale, visible_keys(i, m, causal), row);
+        if (s_out) memcpy(s_out + i * m, row, sizeof(double) * (size_t)m);
+        softmax_row(row, m);
+        if (p_out) memcpy(p_out + i * m, row, sizeof(double) * (size_t)m);
+    }
+    free(row);
+    return ORACLE_OK;
+}
+
+/*
+ * Forward pass, eq. (1) per (b, h) head.
+ * q: [B,h,n,dk], k: [B,h,m,dk], v: [B,h,m,dv] -> o: [B,h,n,dv], lse: [B,h,n]
+ * (lse may be NULL). rows/nrows: optional list of query indices to compute
+ * (NULL = all n rows); rows not listed are left untouched in o and lse.
+ */
+int oracle_attn_fwd(const double *q, const double *k, const double *v,
+                    double *o, double *lse, long B, long h, long n, long m,
+                    long dk, long dv, int causal, double scale,
+                    const long *rows, long nrows) {
+    if (check_dims(B, h, n, m, dk, dv) != ORACLE_OK) return ORACLE_ERR_ARG;
+    const long heads = B * h;
+    const long R = rows ? nrows : n;
+    if (rows)
+        for (long r = 0; r < nrows; ++r)
+            if (rows[r] < 0 || rows[r] >= n) return ORACLE_ERR_ARG;
+    int status = ORACLE_OK;
+#pragma omp parallel
+    {
+        double *row = (double *)malloc(sizeof(double) * (size_t)m);
+        if (!row) {
+#pragma omp atomic write
+            status = ORACLE_ERR_NOMEM;
+        }
+#pragma omp for collapse(2) schedule(dynamic, 4)
+        for (long bh = 0; bh < heads; ++bh) {
+            for (long r = 0; r < R; ++r) {
+                if (!row) continue;
+                const long i = rows ? rows[r] : r;
+                const double *Q = q + bh * n * dk;
+                const double *K = k + bh * m * dk;
+                const double *V = v + bh * m * dv;
+                score_row(Q + i * dk, K, m, dk, scale, visible_keys(i, m, causal), row);
+                const double l = softmax_row(row, m);
+                weighted_sum(row, V, m, dv, o + (bh * n + i) * dv);
+                if (lse) lse[bh * n + i] = l;
+            }
+        }
+        free(row);
+    }
+    return status;
+}
+
+/*
+ * Backward pass: gradients of L = sum(dO * O) with respect to q, k and v,
+ * for O from oracle_attn_fwd on the same inputs.
+ * dq: [B,h,n,dk], dk_out: [B,h,m,dk], dv_out: [B,h,m,dv]; each may be NULL
+ * to skip it. o_out / lse_out (optional) receive the forward results the
+ * backward used.
+ *
+ * Pass 1 (per query row i): P_i., O_i, lse_i, D_i and dQ_i.
+ * Pass 2 (per key row j): dK_j and dV_j, with P_ij = exp(s_ij - lse_i)
+ * (the softmax of pass 1 written through its normaliser) and dS_ij as above.
+ */
+int oracle_attn_bwd(const double *q, const double *k, const double *v,
+                    const double *dO, double *dq, double *dk_out,
+                    double *dv_out, double *o_out, double *lse_out, long B,
+                    long h, long n, long m, long dk, long dv, int causal,
+                    double scale) {
+    if (check_dims(B, h, n, m, dk, dv) != ORACLE_OK) return ORACLE_ERR_ARG;
+    const long heads = B * h;
+    double *lse = (double *)malloc(sizeof(double) * (size_t)(heads * n + 1));
+    double *D = (double *)malloc(sizeof(double) * (size_t)(heads * n + 1));
+    if (!lse || !D) {
+        free(lse);
+        free(D);
+        return ORACLE_ERR_NOMEM;
+    }
+    int status = ORACLE_OK;
+#pragma omp parallel
+    {
+        double *row = (double *)malloc(sizeof(double) * (size_t)m);
+        double *oi = (double *)malloc(sizeof(double) * (size_t)dv);
+        if (!row || !oi) {
+#pragma omp atomic write
+            status = ORACLE_ERR_NOMEM;
+        }
+        /* pass 1: forward row, D_i and dQ_i */
+#pragma omp for collapse(2) schedule(dynamic, 4)
+        for (long bh = 0; bh < heads; ++bh) {
+            for (long i = 0; i < n; ++i) {
+                if (!row || !oi) continue;
+                const double *Q = q + bh * n * dk;
+                const double *K = k + bh * m * dk;
+                const double *V = v + bh * m * dv;
+                const double *dOi = dO + (bh * n + i) * dv;
+                score_row(Q + i * dk, K, m, dk, scale, visible_keys(i, m, causal), row);
+                const double l = softmax_row(row, m);
+                weighted_sum(row, V, m, dv, oi);
+                double Di = 0.0;
+                for (long c = 0; c < dv; ++c) Di += dOi[c] * oi[c];
+                lse[bh * n + i] = l;
+                D[bh * n + i] = Di;
+                if (o_out) memcpy(o_out + (bh * n + i) * dv, oi, sizeof(double) * (size_t)dv);
+                if (lse_out) lse_out[bh * n + i] = l;
+                if (dq) {
+                    double *dqi = dq + (bh * n + i) * dk;
+                    for (long c = 0; c < dk; ++c) dqi[c] = 0.0;
+                    for (long j = 0; j < m; ++j) {
+                        if (row[j] == 0.0) continue; /* P_ij = 0 => dS_ij = 0 */
+                        const double *vj = V + j * dv;
+                        double dP = 0.0;
+                        for (long c = 0; c < dv; ++c) dP += dOi[c] * vj[c];
+                        const double dS = row[j] * (dP - Di);
+                        const double *kj = K + j * dk;
+                        for (long c = 0; c < dk; ++c) dqi[c] += dS * kj[c];
+                    }
+                    for (long c = 0; c < dk; ++c) dqi[c] *= scale;
+                }
+            }
+        }
+        /* implicit barrier: lse and D are complete */
+        /* pass 2: dK_j and dV_j */
+        if (dk_out || dv_out) {
+#pragma omp for collapse(2) schedule(dynamic, 4)
+            for (long bh = 0; bh < heads; ++bh) {
+                for (long j = 0; j < m; ++j) {
+                    const double *Q = q + bh * n * dk;
+                    const double *kj = k + (bh * m + j) * dk;
+                    const double *vj = v + (bh * m + j) * dv;
+                    double *dkj = dk_out ? dk_out + (bh * m + j) * dk : NULL;
+                    double *dvj = dv_out ? dv_out + (bh * m + j) * dv : NULL;
+                    if (dkj) for (long c = 0; c < dk; ++c) dkj[c] = 0.0;
+                    if (dvj) for (long c = 0; c < dv; ++c) dvj[c] = 0.0;
+                    for (long i = 0; i < n; ++i) {
+                        if (j >= visible_keys(i, m, causal)) continue; /* masked: P_ij = 0 */
+                        const double *qi = Q + i * dk;
+                        const double *dOi = dO + (bh * n + i) * dv;
+                        double dot = 0.0;
+                        for (long c = 0; c < dk; ++c) dot += qi[c] * kj[c];
+                        const double P = exp(scale * dot - lse[bh * n + i]);
+                        if (dvj)
+                            for (long c = 0; c < dv; ++c) dvj[c] += P * dOi[c];
+                        if (dkj) {
+                            double dP = 0.0;
+                            for (long c = 0; c < dv; ++c) dP += dOi[c] * vj[c];
+                            const double dS = P * (dP - D[bh * n + i]);
+                            for (long c = 0; c < dk; ++c) dkj[c] += dS * qi[c];
+                        }
+                    }
+                    if (dkj) for (long c = 0; c < dk; ++c) dkj[c] *= scale;
+                }
+            }
+        }
+        free(row);
+        free(oi);
+    }
+    free(lse);
+    free(D);
+    return status;
+}
+
+/* Threads the oracle will use (OpenMP team size), for reporting. */
+int oracle_num_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}

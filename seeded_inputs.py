@@ -1,0 +1,135 @@
+"""Seeded synthetic inputs for scaled dot-product attention.
+
+This module only draws random numbers and names workload shapes. It holds none
+of the attention arithmetic, so both the CUDA path and the fp64 oracle can be
+fed from it without sharing any of the method.
+
+Input model: every tensor is i.i.d. N(0, 1), drawn in fp32 on the CPU from a
+``torch.Generator`` with a fixed seed and rounded to bf16 (round-to-nearest-even).
+That is the footnote-4 model of "Attention Is All You Need" §3.2.1 (query and
+key components independent with mean 0 and variance 1). The pages measure on
+WMT 2014 EN-DE / EN-FR batches (§5.1, roughly 25000 source + 25000 target
+tokens per batch); no dataset is used here, the shapes below stand in for them:
+base model h=8, d_k=d_v=64 (§3.2.2), big model h=16 with d_model=1024
+(Table 3 "big" row), and the Table 3 (A) head shapes (h, d_k) = (4, 128) and
+(16, 32). 96 sequences x 256 tokens ~ 24.6k tokens matches the batch size.
+"""
+from __future__ import annotations
+
+import dataclasses
+import math
+from typing import Dict, Iterator, List, Optional
+
+import torch
+
+__all__ = [
+    "Workload",
+    "WORKLOADS",
+    "normal_bf16",
+    "workload_inputs",
+    "ragged_workloads",
+]
+
+
+@dataclasses.dataclass(frozen=True)
+class Workload:
+    """One attention problem: B sequences x h heads, n queries, m keys."""
+
+    name: str
+    B: int
+    h: int
+    n: int
+    m: int
+    d_k: int
+    d_v: int
+    causal: bool
+    cfg: int  # seed family: Q=1000+cfg, K=2000+cfg, V=3000+cfg, dO=4000+cfg
+    q_mult: float = 1.0  # power-of-two multiplier applied before the bf16 cast
+
+    @property
+    def heads(self) -> int:
+        return self.B * self.h
+
+    @property
+    def default_scale(self) -> float:
+        # 1/sqrt(d_k): the scale named in §3.2.1 (uses d_k, not d_v)
+        return 1.0 / math.sqrt(self.d_k)
+
+    def fwd_flops(self) -> float:
+        """Algorithmic forward FLOPs: 4*B*h*n*m*d_k, halved when causal."""
+        f = 4.0 * self.B * self.h * self.n * self.m * self.d_k
+        return f / 2 if self.causal else f
+
+    def bwd_flops(self) -> float:
+        """Algorithmic backward FLOPs: 2.5x the forward count (five GEMMs)."""
+        return 2.5 * self.fwd_flops()
+
+
+def _wl(name, B, h, n, m, d, causal, cfg, q_mult=1.0) -> Workload:
+    return Workload(name, B, h, n, m, d, d, causal, cfg, q_mult)
+
+
+def _build_table() -> Dict[str, Workload]:
+    t: List[Workload] = [
+        _wl("tiny", 2, 2, 16, 16, 64, False, 1),
+        _wl("tiny_causal", 2, 2, 16, 16, 64, True, 1),
+        _wl("encoder", 96, 8, 256, 256, 64, False, 2),
+        _wl("encoder_sat", 96, 8, 256, 256, 64, False, 2, q_mult=4.0),
+        _wl("decoder", 96, 8, 256, 256, 64, True, 3),
+        _wl("cross", 48, 16, 256, 320, 64, False, 4),
+        _wl("cross_h4_d128", 48, 4, 256, 320, 128, False, 4),
+        _wl("cross_h16_d32", 48, 16, 256, 320, 32, False, 4),
+    ]
+    for n in (1024, 4096, 16384):
+        for d in (64, 128):
+            for causal in (False, True):
+                tag = "c" if causal else "nc"
+                t.append(_wl(f"long_n{n}_d{d}_{tag}", 4, 16, n, n, d, causal, 5))
+    return {w.name: w for w in t}
+
+
+WORKLOADS: Dict[str, Workload] = _build_table()
+
+
+def normal_bf16(shape, seed: int, mult: float = 1.0, device: str = "cpu") -> torch.Tensor:
+    """i.i.d. N(0,1) drawn in fp32 from ``seed``, times ``mult``, rounded to bf16."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(int(seed))
+    x = torch.randn(tuple(shape), generator=g, dtype=torch.float32)
+    if mult != 1.0:
+        x.mul_(mult)
+    x = x.to(torch.bfloat16)
+    return x if device == "cpu" else x.to(device)
+
+
+def workload_inputs(w: Workload, with_grad: bool = False, device: str = "cpu",
+                    heads: Optional[int] = None):
+    """Q, K, V (and dO) for workload ``w`` in the [B, h, S, d] layout, bf16.
+
+    ``heads`` (optional) truncates the batch to the first ``heads`` (b, h)
+    pairs of a [1, heads, S, d] view; the values are the same bytes as the
+    corresponding heads of the full tensors only when heads == B*h, so it is
+    meant for bounded CPU samples, not for parity against full runs.
+    """
+    B, h = (w.B, w.h) if heads is None else (1, heads)
+    q = normal_bf16((B, h, w.n, w.d_k), 1000 + w.cfg, w.q_mult, device)
+    k = normal_bf16((B, h, w.m, w.d_k), 2000 + w.cfg, 1.0, device)
+    v = normal_bf16((B, h, w.m, w.d_v), 3000 + w.cfg, 1.0, device)
+    if not with_grad:
+        return q, k, v
+    do = normal_bf16((B, h, w.n, w.d_v), 4000 + w.cfg, 1.0, device)
+    return q, k, v, do
+
+
+def ragged_workloads() -> Iterator[Workload]:
+    """Small shapes that are not tile multiples: ragged tails, n != m, m = 1."""
+    cases = [
+        (1, 1, 1, 1, 64, False), (1, 1, 1, 1, 64, True),
+        (1, 2, 17, 17, 64, True), (2, 1, 127, 129, 64, False),
+        (1, 3, 129, 127, 64, True), (1, 2, 320, 320, 64, True),
+        (2, 2, 200, 77, 32, False), (1, 2, 130, 300, 128, False),
+        (1, 1, 255, 257, 128, True), (1, 1, 64, 1, 32, False),
+        (3, 1, 300, 300, 32, True), (1, 1, 5, 400, 64, False),
+    ]
+    for i, (B, h, n, m, d, c) in enumerate(cases):
+        yield _wl(f"ragged{i}_B{B}h{h}n{n}m{m}d{d}{'c' if c else ''}", B, h, n, m, d, c, 50 + i)

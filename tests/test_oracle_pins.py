@@ -1,0 +1,284 @@
+"""Pins of the fp64 oracle to facts that do not come from the oracle itself.
+
+Each test ties the oracle to something the pages print, a closed form, an
+invariant of eq. (1), brute-force finite differences, or an independent
+library routine. A plausible slip in the oracle (a dropped scale, a wrong
+mask index, a transposed operand, a sign error in the backward) fails at
+least one of them.
+"""
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from seeded_inputs import normal_bf16
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _half_unit(printed: str) -> float:
+    """Half a unit in the last printed digit ("4.0" -> 0.05, "66" -> 0.5)."""
+    if "." in printed:
+        return 0.5 * 10.0 ** (-len(printed.split(".")[1]))
+    return 0.5
+
+
+def _read_rows(name):
+    with open(os.path.join(GOLDEN, name), encoding="utf-8") as f:
+        return [ln.split() for ln in f if ln.strip() and not ln.startswith("#")]
+
+
+# ---------------------------------------------------------------- printed values
+
+def test_worked_example_scores_and_weights():
+    """The 2-d example of the close-reading page (query "它" over seven keys).
+
+    Scores q.k/sqrt(2) and weights must match the printed values to the
+    printed precision.
+    """
+    rows = _read_rows("worked_example_2d.txt")
+    q = np.array([[float(rows[0][1]), float(rows[0][2])]])
+    assert rows[1][0] == "scale_denominator_sqrt"
+    scale = 1.0 / math.sqrt(float(rows[1][1]))
+    keys = rows[2:]
+    K = np.array([[float(r[1]), float(r[2])] for r in keys])
+    S, P = oracle.weights(q, K, causal=False, scale=scale)
+    for j, r in enumerate(keys):
+        assert abs(S[0, j] - float(r[3])) <= _half_unit(r[3]) + 1e-12, (r, S[0, j])
+        assert abs(100.0 * P[0, j] - float(r[4])) <= _half_unit(r[4]) + 1e-12, (r, P[0, j])
+    # the printed weights are those of one softmax row: they add up to 100 %
+    assert abs(P.sum() - 1.0) < 1e-15
+
+
+def test_saturation_example_weights_and_derivative():
+    """Scores 8 and 0 at d_k=64: weights ~0.9997, derivative ~0.0003; /8: 0.73/0.27, ~0.20.
+
+    The derivative p(1-p) of the softmax weight with respect to its own score
+    is read off the oracle's backward: with v_a = 1, v_b = 0 (d_v = 1) the
+    output is O = p_a, and with dO = 1 and k_b = 0 the query gradient is
+    dQ = scale * dS_a * k_a, where dS_a = dO/ds_a = p_a (1 - p_a).
+    """
+    for r in _read_rows("saturation.txt"):
+        dk, sa, sb, scale = int(r[0]), float(r[1]), float(r[2]), float(r[3])
+        wa, wb, dp, tol_w, tol_dp = map(float, r[4:9])
+        assert sb == 0.0
+        q = np.zeros((1, dk))
+        q[0, 0] = sa                      # q . k_a = sa with k_a = e_0
+        K = np.zeros((2, dk))
+        K[0, 0] = 1.0                     # k_b = 0 gives q . k_b = 0
+        S, P = oracle.weights(q, K, causal=False, scale=scale)
+        assert S[0, 0] == pytest.approx(sa * scale, abs=1e-15)
+        assert abs(P[0, 0] - wa) <= tol_w
+        assert abs(P[0, 1] - wb) <= tol_w
+        V = np.array([[1.0], [0.0]])
+        dO = np.ones((1, 1))
+        dQ, dK, dV, O, lse = oracle.bwd(q, K, V, dO, causal=False, scale=scale)
+        assert O[0, 0] == pytest.approx(P[0, 0], rel=1e-15)
+        deriv = dQ[0, 0] / scale          # = dS_a
+        assert abs(deriv - dp) <= tol_dp
+        assert deriv == pytest.approx(P[0, 0] * (1 - P[0, 0]), rel=1e-9)
+
+
+def test_footnote4_score_statistics():
+    """Footnote 4 of §3.2.1: for independent N(0,1) components q.k has mean 0, variance d_k.
+
+    Checked statistically on the oracle's unscaled scores (scale = 1), and the
+    variance returns to ~1 after the 1/sqrt(d_k) scale.
+    """
+    dk = 64
+    q = normal_bf16((256, dk), 7).double().numpy()
+    k = normal_bf16((256, dk), 8).double().numpy()
+    S1, _ = oracle.weights(q, k, causal=False, scale=1.0)
+    S8, _ = oracle.weights(q, k, causal=False, scale=1.0 / math.sqrt(dk))
+    assert abs(S1.mean()) < 0.25
+    assert S1.var() == pytest.approx(dk, rel=0.05)
+    assert S8.var() == pytest.approx(1.0, rel=0.05)
+
+
+# ---------------------------------------------------------------- invariants
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_rows_sum_to_one_and_masked_weights_are_zero(causal):
+    """Each softmax row sums to 100 %; illegal connections (j > i) weigh exactly 0 (§3.2.3)."""
+    n, m, dk = 37, 53, 16
+    q = normal_bf16((n, dk), 11).double().numpy() * 3
+    k = normal_bf16((m, dk), 12).double().numpy()
+    S, P = oracle.weights(q, k, causal=causal, scale=0.25)
+    assert np.all(np.abs(P.sum(axis=1) - 1.0) < 1e-14)
+    for i in range(n):
+        for j in range(m):
+            if causal and j > i:
+                assert P[i, j] == 0.0 and S[i, j] == -np.inf
+            else:
+                assert P[i, j] > 0.0 and np.isfinite(S[i, j])
+    # the diagonal is included: query i always sees key i ("including that position")
+    if causal:
+        assert all(P[i, i] > 0 for i in range(min(n, m)))
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_equal_scores_give_mean_of_values(causal):
+    """Q = 0 (or scale = 0) makes every visible score equal: O_i = mean of the visible v_j.
+
+    lse_i is then ln(number of visible keys): ln m, or ln(i+1) when causal.
+    """
+    B, h, n, m, d = 1, 2, 9, 7, 8
+    v = normal_bf16((B, h, m, d), 13).double().numpy()
+    k = normal_bf16((B, h, m, d), 14).double().numpy()
+    for q, scale in ((np.zeros((B, h, n, d)), 0.125),
+                     (normal_bf16((B, h, n, d), 15).double().numpy(), 0.0)):
+        O, lse = oracle.fwd(q, k, v, causal, scale)
+        for i in range(n):
+            vis = min(i + 1, m) if causal else m
+            np.testing.assert_allclose(O[:, :, i], v[:, :, :vis].mean(axis=2), rtol=0, atol=1e-14)
+            np.testing.assert_allclose(lse[:, :, i], math.log(vis), rtol=0, atol=1e-14)
+
+
+def test_permutation_equivariance():
+    """O is a weighted sum over key/value pairs: permuting them jointly changes nothing.
+
+    Permuting the queries permutes the output rows (non-causal).
+    """
+    B, h, n, m, d = 2, 2, 11, 13, 8
+    q = normal_bf16((B, h, n, d), 21).double().numpy()
+    k = normal_bf16((B, h, m, d), 22).double().numpy()
+    v = normal_bf16((B, h, m, d), 23).double().numpy()
+    O, lse = oracle.fwd(q, k, v, False, 0.3)
+    perm = np.random.default_rng(0).permutation(m)
+    O2, lse2 = oracle.fwd(q, k[:, :, perm], v[:, :, perm], False, 0.3)
+    np.testing.assert_allclose(O2, O, rtol=0, atol=1e-13)
+    np.testing.assert_allclose(lse2, lse, rtol=0, atol=1e-13)
+    qperm = np.random.default_rng(1).permutation(n)
+    O3, lse3 = oracle.fwd(q[:, :, qperm], k, v, False, 0.3)
+    assert np.array_equal(O3, O[:, :, qperm]) and np.array_equal(lse3, lse[:, :, qperm])
+
+
+def test_single_key_closed_form():
+    """m = 1: the only weight is 1, so O = v_0, lse = s_00, and every gradient of q and k is 0."""
+    B, h, n, d = 1, 3, 5, 16
+    q = normal_bf16((B, h, n, d), 31).double().numpy()
+    k = normal_bf16((B, h, 1, d), 32).double().numpy()
+    v = normal_bf16((B, h, 1, d), 33).double().numpy()
+    dO = normal_bf16((B, h, n, d), 34).double().numpy()
+    for causal in (False, True):
+        O, lse = oracle.fwd(q, k, v, causal, 0.25)
+        np.testing.assert_array_equal(O, np.broadcast_to(v, O.shape))
+        s00 = 0.25 * np.einsum("bhnd,bhd->bhn", q, k[:, :, 0])
+        np.testing.assert_allclose(lse, s00, rtol=1e-15, atol=1e-15)
+        dQ, dK, dV, _, _ = oracle.bwd(q, k, v, dO, causal, 0.25)
+        assert np.all(dQ == 0.0) and np.all(dK == 0.0)
+        np.testing.assert_allclose(dV[:, :, 0], dO.sum(axis=2), rtol=1e-14, atol=1e-14)
+
+
+def test_causal_prefix_invariance():
+    """Causal row i depends only on keys/values 0..i: changing later ones leaves it unchanged."""
+    B, h, n, d = 1, 2, 12, 8
+    q = normal_bf16((B, h, n, d), 41).double().numpy()
+    k = normal_bf16((B, h, n, d), 42).double().numpy()
+    v = normal_bf16((B, h, n, d), 43).double().numpy()
+    O, lse = oracle.fwd(q, k, v, True, 0.35)
+    for i in range(n):
+        k2, v2 = k.copy(), v.copy()
+        k2[:, :, i + 1:] = 1000.0
+        v2[:, :, i + 1:] = -1000.0
+        O2, lse2 = oracle.fwd(q, k2, v2, True, 0.35)
+        assert np.array_equal(O2[:, :, : i + 1], O[:, :, : i + 1])
+        assert np.array_equal(lse2[:, :, : i + 1], lse[:, :, : i + 1])
+    # row 0 sees only key 0: O_0 = v_0, lse_0 = s_00
+    np.testing.assert_array_equal(O[:, :, 0], v[:, :, 0])
+
+
+def test_row_subset_matches_full():
+    B, h, n, m, d = 2, 1, 20, 9, 4
+    q = normal_bf16((B, h, n, d), 51).double().numpy()
+    k = normal_bf16((B, h, m, d), 52).double().numpy()
+    v = normal_bf16((B, h, m, 6), 53).double().numpy()
+    O, lse = oracle.fwd(q, k, v, True, 0.5)
+    rows = [0, 3, 19]
+    Os, lses = oracle.fwd(q, k, v, True, 0.5, rows=rows)
+    np.testing.assert_array_equal(Os[:, :, rows], O[:, :, rows])
+    np.testing.assert_array_equal(lses[:, :, rows], lse[:, :, rows])
+    assert np.isnan(Os[:, :, 1]).all()
+
+
+# ---------------------------------------------------------------- backward
+
+def _loss(q, k, v, dO, causal, scale):
+    O, _ = oracle.fwd(q, k, v, causal, scale)
+    return float((dO * O).sum())
+
+
+@pytest.mark.parametrize("causal,n,m,dk,dv", [(False, 4, 6, 3, 2), (True, 6, 6, 4, 4),
+                                              (True, 5, 3, 2, 3), (False, 1, 5, 4, 1)])
+def test_backward_matches_central_differences(causal, n, m, dk, dv):
+    """dQ, dK, dV agree with fp64 central differences of L = sum(dO * O)."""
+    rng = np.random.default_rng(n * 100 + m)
+    q = rng.standard_normal((1, 1, n, dk))
+    k = rng.standard_normal((1, 1, m, dk))
+    v = rng.standard_normal((1, 1, m, dv))
+    dO = rng.standard_normal((1, 1, n, dv))
+    scale = 0.7
+    dQ, dK, dV, _, _ = oracle.bwd(q, k, v, dO, causal, scale)
+    eps = 1e-6
+    for name, x, g in (("q", q, dQ), ("k", k, dK), ("v", v, dV)):
+        num = np.zeros_like(x)
+        for idx in np.ndindex(x.shape):
+            xp, xm = x.copy(), x.copy()
+            xp[idx] += eps
+            xm[idx] -= eps
+            args_p = {"q": q, "k": k, "v": v}
+            args_m = {"q": q, "k": k, "v": v}
+            args_p[name], args_m[name] = xp, xm
+            num[idx] = (_loss(args_p["q"], args_p["k"], args_p["v"], dO, causal, scale)
+                        - _loss(args_m["q"], args_m["k"], args_m["v"], dO, causal, scale)) / (2 * eps)
+        err = np.abs(num - g).max()
+        assert err <= 1e-8 * max(1.0, np.abs(g).max()), (name, err)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_backward_sum_invariants(causal):
+    """sum_j dK_j = 0 (rows of dS sum to 0) and sum_j dV_j = sum_i dO_i (rows of P sum to 1)."""
+    B, h, n, m, d = 2, 2, 24, 24, 16
+    q = normal_bf16((B, h, n, d), 61).double().numpy()
+    k = normal_bf16((B, h, m, d), 62).double().numpy()
+    v = normal_bf16((B, h, m, d), 63).double().numpy()
+    dO = normal_bf16((B, h, n, d), 64).double().numpy()
+    dQ, dK, dV, _, _ = oracle.bwd(q, k, v, dO, causal, 0.25)
+    np.testing.assert_allclose(dK.sum(axis=2), 0.0, atol=1e-12)
+    np.testing.assert_allclose(dV.sum(axis=2), dO.sum(axis=2), atol=1e-12)
+
+
+# ---------------------------------------------------------------- library special case
+
+@pytest.mark.parametrize("causal,n,m,dk,dv", [(False, 7, 5, 8, 8), (True, 9, 9, 16, 16),
+                                              (True, 6, 10, 4, 4), (False, 3, 8, 4, 6)])
+def test_against_torch_cpu_fp64_library(causal, n, m, dk, dv):
+    """torch CPU fp64 scaled_dot_product_attention + autograd as an independent routine.
+
+    torch's is_causal mask is lower-triangular from the top-left corner, the
+    same reading of "illegal connections" used here.
+    """
+    F = torch.nn.functional
+    g = torch.Generator().manual_seed(n * 31 + m)
+    q = torch.randn(2, 2, n, dk, dtype=torch.float64, generator=g, requires_grad=True)
+    k = torch.randn(2, 2, m, dk, dtype=torch.float64, generator=g, requires_grad=True)
+    v = torch.randn(2, 2, m, dv, dtype=torch.float64, generator=g, requires_grad=True)
+    dO = torch.randn(2, 2, n, dv, dtype=torch.float64, generator=g)
+    scale = 1.0 / math.sqrt(dk)
+    O_t = F.scaled_dot_product_attention(q, k, v, is_causal=causal, scale=scale)
+    O_t.backward(dO)
+    with torch.no_grad():
+        sc = (q @ k.transpose(-1, -2)) * scale
+        if causal:
+            sc = sc.masked_fill(torch.ones(n, m, dtype=torch.bool).triu(1), float("-inf"))
+        lse_t = torch.logsumexp(sc, dim=-1)
+    O, lse = oracle.fwd(q.detach(), k.detach(), v.detach(), causal, scale)
+    dQ, dK, dV, _, _ = oracle.bwd(q.detach(), k.detach(), v.detach(), dO, causal, scale)
+    np.testing.assert_allclose(O, O_t.detach().numpy(), rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(lse, lse_t.numpy(), rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(dQ, q.grad.numpy(), rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(dK, k.grad.numpy(), rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(dV, v.grad.numpy(), rtol=1e-10, atol=1e-12)
