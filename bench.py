@@ -1,0 +1,503 @@
+#!/usr/bin/env python3
+"""Throughput of multi-head scaled dot-product attention, forward + backward, on GB300.
+
+One step = attn_fwd followed by attn_bwd (the whole path: O, lse, dQ, dK, dV)
+over one synthetic batch of the chosen workload, inputs resident in HBM.
+Default workload: encoder self-attention of the base model, B=96, h=8,
+n=m=256, d_k=d_v=64, non-causal (the paper's base model, §3.2.2).
+
+metric: attention TFLOPS (bf16, fwd and bwd) with the FLOP convention
+4*B*h*n*m*d_k for the forward (halved when causal) and 2.5x that for the
+backward (five GEMMs), i.e. 3.5 * 4*B*h*n*m*d_k per step.
+
+Multi-GPU (torchrun): every rank runs its own batch (the heads are
+independent problems, §3.2.2); no collective touches the data path.
+``--impl reference`` times the fp64 CPU oracle on a bounded sample instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from seeded_inputs import WORKLOADS, Workload  # noqa: E402
+
+METRIC = "attention TFLOPS (bf16, fwd and bwd) and % of GB300 dense BF16 tensor peak"
+UNIT = "TFLOP/s"
+PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+CSRC = os.path.join(ROOT, "transformer_scaled_dot_attn_gb300", "csrc")
+
+
+def step_flops(w: Workload) -> float:
+    return w.fwd_flops() + w.bwd_flops()
+
+
+def kernel_model(w: Workload):
+    """Algorithmic FLOPs and bytes per launch of the two tensor-core kernels.
+
+    fwd:      reads Q, K, V (bf16); writes O (bf16) and lse (fp32).
+    bwd_main: reads Q, dO, K, V (bf16) and the two fp32 row statistics;
+              writes dK, dV (bf16) and the fp32 dQ accumulator once.
+    """
+    H, n, m, d = w.heads, w.n, w.m, w.d_k
+    fwd_bytes = H * (2 * (2 * n * d + 2 * m * d) + 4 * n)
+    bwd_bytes = H * (2 * (2 * n * d + 2 * m * d) + 8 * n + 2 * (2 * m * d) + 4 * n * d)
+    return {
+        "fwd": {"flops": w.fwd_flops(), "bytes": fwd_bytes},
+        "bwd_main": {"flops": w.bwd_flops(), "bytes": bwd_bytes},
+    }
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(PEAKS_FALLBACK), "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in sorted(os.listdir(CSRC)):
+        if f.endswith((".cu", ".cuh")):
+            with open(os.path.join(CSRC, f), "rb") as fh:
+                h.update(f.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from a committed ncu capture, if it matches the current sources."""
+    if not os.path.exists(TRAFFIC_FILE):
+        return None
+    with open(TRAFFIC_FILE) as f:
+        d = json.load(f)
+    rec = d.get(workload, {}).get(kernel)
+    if not rec or rec.get("source_hash") != kernel_source_hash():
+        return None
+    return rec.get("bytes_per_launch")
+
+
+# ----------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi samples (every 20 ms) around the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.samples = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "20"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), line.strip()))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=5)
+
+    def summary(self, t0: float, t1: float, margin: float = 0.25):
+        rows = []
+        for ts, line in self.samples:
+            if t0 - margin <= ts <= t1 + margin:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        mx = [num(r[2]) for r in rows if num(r[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows),
+                "power_w_max": max((num(r[3]) or 0.0) for r in rows)}
+
+
+# ----------------------------------------------------------------- distributed
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+            dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        else:
+            dist.init_process_group("gloo")
+    return world, rank, local
+
+
+def _reduce(x: float, op_name: str) -> float:
+    import torch
+    import torch.distributed as dist
+    on_gpu = dist.get_backend() == "nccl"
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if on_gpu else "cpu")
+    dist.all_reduce(t, op=getattr(dist.ReduceOp, op_name))
+    return float(t.item())
+
+
+def reduce_max(x: float, world: int) -> float:
+    """Max over ranks (the slowest rank's time bounds the whole job)."""
+    return x if world == 1 else _reduce(x, "MAX")
+
+
+def reduce_sum(x: float, world: int) -> float:
+    """Sum over ranks (units of work processed by all ranks)."""
+    return x if world == 1 else _reduce(x, "SUM")
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ----------------------------------------------------------------- CPU oracle sample
+
+def oracle_sample(w: Workload, target_s: float):
+    """Time the fp64 oracle (forward + backward) on the first few heads of ``w``.
+
+    Heads are added until about ``target_s`` seconds of CPU work (at most all
+    of them). Returns (TFLOP/s in the step's FLOP convention, seconds, heads, threads).
+    """
+    import oracle
+    from seeded_inputs import workload_inputs
+    oracle.build()
+    per_head = step_flops(w) / w.heads
+
+    def run(heads):
+        q, k, v, do = workload_inputs(w, with_grad=True, heads=heads)
+        t0 = time.perf_counter()
+        oracle.bwd(q, k, v, do, w.causal, w.default_scale)
+        return time.perf_counter() - t0
+
+    probe = 1
+    t = run(probe)
+    while t < 0.5 and probe < w.heads:
+        probe = min(w.heads, probe * 4)
+        t = run(probe)
+    heads = max(1, min(w.heads, int(probe * target_s / max(t, 1e-9))))
+    if heads != probe:
+        t = run(heads)
+    return per_head * heads / t / 1e12, t, heads, oracle.num_threads()
+
+
+# ----------------------------------------------------------------- GPU arm
+
+def make_inputs(w: Workload, seed: int, device):
+    import torch
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    q = (torch.randn(w.B, w.h, w.n, w.d_k, device=device, generator=g) * w.q_mult).bfloat16()
+    k = torch.randn(w.B, w.h, w.m, w.d_k, device=device, generator=g).bfloat16()
+    v = torch.randn(w.B, w.h, w.m, w.d_v, device=device, generator=g).bfloat16()
+    do = torch.randn(w.B, w.h, w.n, w.d_v, device=device, generator=g).bfloat16()
+    return q, k, v, do
+
+
+def run_gpu(args, w: Workload, world, rank, local):
+    import torch
+    import transformer_scaled_dot_attn_gb300 as A
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    A.load_library()
+    scale = w.default_scale
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    set_bytes = 2 * (2 * w.heads * w.n * w.d_k + 2 * w.heads * w.m * w.d_k)
+    n_sets = max(1, min(8, math.ceil(2 * l2 / max(set_bytes, 1)) + 1))
+    sets = [make_inputs(w, 1000 * rank + 17 * s + w.cfg, dev) for s in range(n_sets)]
+    o = torch.empty(w.B, w.h, w.n, w.d_v, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(w.B, w.h, w.n, dtype=torch.float32, device=dev)
+    dq = torch.empty(w.B, w.h, w.n, w.d_k, dtype=torch.bfloat16, device=dev)
+    dk = torch.empty(w.B, w.h, w.m, w.d_k, dtype=torch.bfloat16, device=dev)
+    dv = torch.empty(w.B, w.h, w.m, w.d_v, dtype=torch.bfloat16, device=dev)
+    ws_bytes = A.attn_bwd_workspace_bytes(w.B, w.h, w.n, w.m, w.d_k, w.d_v, w.causal)
+    ws = torch.empty(max(ws_bytes, 16) // 4 + 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(i):
+        q, k, v, do = sets[i % n_sets]
+        A.attn_fwd(q, k, v, causal=w.causal, scale=scale, out=o, lse=lse)
+        A.attn_bwd(q, k, v, o, lse, do, causal=w.causal, scale=scale, dq=dq, dk=dk, dv=dv,
+                   workspace=ws)
+
+    # settle clocks, then the counted warm-up
+    t_soak = time.time()
+    i = 0
+    while time.time() - t_soak < args.soak_seconds:
+        step(i)
+        i += 1
+        if i % 64 == 0:
+            torch.cuda.synchronize()
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    if A.attn_get_device_status() != A.ATTN_OK:
+        raise RuntimeError("device watchdog fired during warm-up")
+
+    sampler = ClockSampler(local) if rank == 0 else None
+    if sampler:
+        sampler.start()
+        time.sleep(0.3)
+    A.attn_profile_enable(True)
+    for kind in A.KERNEL_KINDS:
+        A.attn_profile_read(kind)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    t0 = time.time()
+    start.record(stream)
+    for i in range(args.steps):
+        step(i)
+    end.record(stream)
+    torch.cuda.synchronize()
+    t1 = time.time()
+    barrier(world)
+    A.attn_profile_enable(False)
+    ms = start.elapsed_time(end)
+    prof = {kind: A.attn_profile_read(kind) for kind in A.KERNEL_KINDS}
+    if sampler:
+        time.sleep(0.3)
+        sampler.stop()
+    status = A.attn_get_device_status()
+    if status != A.ATTN_OK:
+        raise RuntimeError(f"device status {A.attn_status_string(status)} in the timed region")
+    launches = sum(n for n, _ in prof.values())
+
+    ms_max = reduce_max(ms, world)
+    total_flops = reduce_sum(step_flops(w) * args.steps, world)
+    value = total_flops / (ms_max / 1e3) / 1e12
+
+    # ---- end to end: pinned host inputs -> device -> fwd+bwd -> O, dQ, dK, dV back to host
+    hq, hk, hv, hdo = [t.cpu().pin_memory() for t in sets[0]]
+    d_in = [torch.empty_like(t) for t in sets[0]]
+    outs_h = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (o, dq, dk, dv)]
+    e2e_steps = max(1, min(args.steps, 20))
+
+    def e2e_step():
+        for dst, src in zip(d_in, (hq, hk, hv, hdo)):
+            dst.copy_(src, non_blocking=True)
+        A.attn_fwd(d_in[0], d_in[1], d_in[2], causal=w.causal, scale=scale, out=o, lse=lse)
+        A.attn_bwd(d_in[0], d_in[1], d_in[2], o, lse, d_in[3], causal=w.causal, scale=scale,
+                   dq=dq, dk=dk, dv=dv, workspace=ws)
+        for dst, src in zip(outs_h, (o, dq, dk, dv)):
+            dst.copy_(src, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    barrier(world)
+    s2, e2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s2.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e2.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = reduce_max(s2.elapsed_time(e2), world)
+    e2e_value = reduce_sum(step_flops(w) * e2e_steps, world) / (e2e_ms / 1e3) / 1e12
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hdo))
+    d2h = sum(t.numel() * t.element_size() for t in outs_h)
+
+    # ---- roofline of the dominant kernel
+    peaks, peak_src = load_peaks()
+    model = kernel_model(w)
+    kinds = {"fwd": prof["fwd"], "bwd_main": prof["bwd_main"]}
+    dom = max(kinds, key=lambda k: kinds[k][1])
+    n_launch, tot_ms = kinds[dom]
+    avg_s = tot_ms / max(n_launch, 1) / 1e3
+    ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
+    intensity = model[dom]["flops"] / model[dom]["bytes"]
+    if intensity < ridge:
+        achieved = model[dom]["bytes"] / avg_s / 1e9
+        peak = peaks["hbm_gbs"]
+        roof = {"bound": "hbm", "unit": "GB/s"}
+    else:
+        achieved = model[dom]["flops"] / avg_s / 1e12
+        peak = peaks["bf16_tflops"]
+        roof = {"bound": "tensor", "unit": "TFLOP/s"}
+    roof.update({"kernel": dom, "achieved": round(achieved, 2), "peak": peak,
+                 "peak_source": peak_src, "frac": round(achieved / peak, 4),
+                 "traffic": recorded_traffic(dom, w.name),
+                 "algorithmic_bytes": model[dom]["bytes"], "algorithmic_flops": model[dom]["flops"],
+                 "avg_launch_us": round(avg_s * 1e6, 2)})
+    per_kernel = {k: {"launches": n, "avg_us": round(t / max(n, 1) * 1e3, 2)} for k, (n, t) in prof.items()}
+    for k in ("fwd", "bwd_main"):
+        n_, t_ = prof[k]
+        a = t_ / max(n_, 1) / 1e3
+        per_kernel[k]["tflops"] = round(model[k]["flops"] / a / 1e12, 1) if n_ else None
+        per_kernel[k]["gbs"] = round(model[k]["bytes"] / a / 1e9, 1) if n_ else None
+    clocks = sampler.summary(t0, t1) if sampler else None
+    return {
+        "value": value, "ms_per_step": ms_max / args.steps, "launches": launches,
+        "e2e": {"value": round(e2e_value, 3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+        "roofline": roof, "kernels": per_kernel, "clocks": clocks, "n_sets": n_sets,
+        "l2_bytes": l2, "set_bytes": set_bytes, "peaks": peaks,
+    }
+
+
+def run_sweep(args, local):
+    """Quick per-configuration throughput of attn_fwd and attn_bwd (rank 0, N=1 only)."""
+    import torch
+    import transformer_scaled_dot_attn_gb300 as A
+    dev = torch.device("cuda", local)
+    peaks, _ = load_peaks()
+    out = {}
+    names = ["encoder", "encoder_sat", "decoder", "cross", "cross_h4_d128", "cross_h16_d32"]
+    names += [f"long_n{n}_d{d}_{c}" for n in (1024, 4096, 16384) for d in (64, 128) for c in ("nc", "c")]
+    for name in names:
+        w = WORKLOADS[name]
+        q, k, v, do = make_inputs(w, 99, dev)
+        o, lse = A.attn_fwd(q, k, v, causal=w.causal, scale=w.default_scale)
+        dq, dk, dv = A.attn_bwd(q, k, v, o, lse, do, causal=w.causal, scale=w.default_scale)
+        torch.cuda.synchronize()
+        iters = max(3, min(50, int(2e12 / max(step_flops(w), 1))))
+        A.attn_profile_enable(True)
+        for kind in A.KERNEL_KINDS:
+            A.attn_profile_read(kind)
+        for _ in range(iters):
+            A.attn_fwd(q, k, v, causal=w.causal, scale=w.default_scale, out=o, lse=lse)
+            A.attn_bwd(q, k, v, o, lse, do, causal=w.causal, scale=w.default_scale, dq=dq, dk=dk, dv=dv)
+        torch.cuda.synchronize()
+        A.attn_profile_enable(False)
+        prof = {kind: A.attn_profile_read(kind) for kind in A.KERNEL_KINDS}
+        f_ms = prof["fwd"][1] / max(prof["fwd"][0], 1)
+        b_ms = sum(prof[kd][1] for kd in ("bwd_pre", "bwd_main", "bwd_post")) / max(prof["bwd_main"][0], 1)
+        ftf = w.fwd_flops() / (f_ms / 1e3) / 1e12
+        btf = w.bwd_flops() / (b_ms / 1e3) / 1e12
+        out[name] = {"fwd_us": round(f_ms * 1e3, 1), "fwd_tflops": round(ftf, 1),
+                     "fwd_frac_peak": round(ftf / peaks["bf16_tflops"], 3),
+                     "bwd_us": round(b_ms * 1e3, 1), "bwd_tflops": round(btf, 1),
+                     "bwd_frac_peak": round(btf / peaks["bf16_tflops"], 3), "iters": iters}
+        del q, k, v, do, o, lse, dq, dk, dv
+        torch.cuda.empty_cache()
+    if A.attn_get_device_status() != A.ATTN_OK:
+        raise RuntimeError("device watchdog fired in the sweep")
+    return out
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", default="encoder", choices=sorted(WORKLOADS))
+    ap.add_argument("--no-sweep", action="store_true", help="skip the per-configuration sweep")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--soak-seconds", type=float, default=1.0,
+                    help="untimed steps before the warm-up so clocks settle (0 for profiler runs)")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    world, rank, local = dist_setup()
+    w = WORKLOADS[args.workload]
+    config = {"workload": f"{w.name}: B={w.B}, h={w.h}, n={w.n}, m={w.m}, d_k=d_v={w.d_k}, "
+                          f"causal={w.causal}" + (f", Q x {w.q_mult:g}" if w.q_mult != 1 else ""),
+              "global_batch": w.B * world, "seq_len": w.n, "kv_len": w.m, "heads": w.h,
+              "head_dim": w.d_k, "causal": w.causal, "parallelism": f"replicas x{world} (independent batches)",
+              "step": "attn_fwd + attn_bwd"}
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        per_step = []
+        heads = threads = 0
+        seconds = max(1.0, min(args.cpu_seconds, 60.0 / max(1, args.steps + args.warmup)))
+        for s in range(args.warmup + args.steps):
+            tf, t, heads, threads = oracle_sample(w, seconds)
+            if s >= args.warmup:
+                per_step.append((tf, t))
+        value = statistics.median(tf for tf, _ in per_step)
+        ms = statistics.median(t for _, t in per_step) * 1e3
+        sample = f"{heads} of {w.heads} heads of {w.name} per step (fwd+bwd, fp64 C oracle)"
+        line = {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": UNIT,
+                "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 2),
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                "data": "synthetic", "config": config,
+                "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": threads,
+                                 "kind": "oracle", "sample": sample},
+                "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}}
+        print(json.dumps(line), flush=True)
+        return
+
+    res = run_gpu(args, w, world, rank, local)
+    sweep = None
+    if world == 1 and not args.no_sweep:
+        sweep = run_sweep(args, local)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        tf, t, heads, threads = oracle_sample(w, args.cpu_seconds)
+        cpu = {"value": round(tf, 6), "unit": UNIT, "cores": threads, "kind": "oracle",
+               "sample": f"{heads} of {w.heads} heads of {w.name}, fwd+bwd, {t:.1f} s"}
+    if rank != 0:
+        return
+    config["l2"] = (f"rotating {res['n_sets']} input sets of {res['set_bytes'] / 1e6:.0f} MB "
+                    f"(> 2x the {res['l2_bytes'] / 1e6:.0f} MB L2)")
+    peak = res["peaks"]["bf16_tflops"]
+    line = {
+        "metric": METRIC, "value": round(res["value"], 3), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(res["ms_per_step"], 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (i.i.d. N(0,1) bf16, seeded)", "config": config,
+        "frac_of_bf16_peak": round(res["value"] / world / peak, 4),
+        "roofline": res["roofline"], "cpu_baseline": cpu, "e2e": res["e2e"],
+        "gpu_launches": res["launches"], "clocks": res["clocks"], "kernels": res["kernels"],
+    }
+    if sweep is not None:
+        line["sweep"] = sweep
+    print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,135 @@
+/*
+ * attn.h - C ABI of the GB300 (sm_103a) scaled dot-product attention library.
+ *
+ * The operation is eq. (1) of "Attention Is All You Need", §3.2.1:
+ *
+ *     Attention(Q, K, V) = softmax(Q K^T * scale) V,   scale = 1/sqrt(d_k) in the paper,
+ *
+ * computed independently for every (b, h) head (§3.2.2, "in parallel"), with
+ * the optional decoder mask of §3.2.3 / Figure 2 ("Mask (opt.)"): every
+ * illegal connection, key j after query i, is set to -inf before the softmax.
+ * Position i itself stays visible. The three uses named in §3.2.3 (encoder
+ * self-attention, masked decoder self-attention, encoder-decoder attention
+ * with n != m) are all this one call.
+ *
+ * Conventions shared by every entry point:
+ *   - Tensors are bf16, contiguous, laid out [B, h, S, d] with d fastest:
+ *     Q, O, dO, dQ are [B, h, n, d]; K, V, dK, dV are [B, h, m, d].
+ *     lse is fp32 [B, h, n].
+ *   - Every tensor pointer is a DEVICE pointer owned by the caller and must
+ *     be 16-byte aligned. The library keeps no reference after the call.
+ *   - Calls are asynchronous: work is enqueued on `stream` (a cudaStream_t;
+ *     NULL is the legacy default stream) and the call returns without
+ *     synchronising. Launch failures are reported as ATTN_ERR_CUDA. A device
+ *     watchdog turns a stalled pipeline into an error flag instead of a hang;
+ *     read it with attn_get_device_status().
+ *   - Supported head sizes: d_k == d_v in {32, 64, 128}. The paper's base and
+ *     big models use 64 (§3.2.2, Table 3), Table 3 (A) also lists 32 and 128.
+ *   - causal: key j is visible to query i iff j <= i (top-left aligned), for
+ *     any n and m. With m >= 1 no row is ever fully masked.
+ *   - scale: any finite value. 0 gives equal weights (the mean of the visible
+ *     values); 1 is the unscaled dot-product attention of §3.2.1.
+ *   - Empty batches (B*h*n == 0) are a no-op returning ATTN_OK.
+ *   - Thread safety: calls may be made concurrently from several host threads.
+ */
+#ifndef ATTN_GB300_H
+#define ATTN_GB300_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; declared here so the header needs no CUDA include. */
+typedef struct CUstream_st* attn_stream_t;
+
+typedef enum {
+  ATTN_OK = 0,
+  ATTN_ERR_INVALID_ARG = 1, /* null/misaligned pointer, negative size, m < 1, non-finite scale */
+  ATTN_ERR_UNSUPPORTED = 2, /* d_k != d_v, or d not in {32, 64, 128}, or sizes beyond int32 indexing */
+  ATTN_ERR_CUDA = 3,        /* a CUDA runtime/driver call or a kernel launch failed */
+  ATTN_ERR_TIMEOUT = 4      /* the device watchdog fired: a pipeline wait ran out of time */
+} attn_status_t;
+
+/*
+ * Forward pass, eq. (1), plus the per-row log-sum-exp.
+ *   q [B,h,n,d_k], k [B,h,m,d_k], v [B,h,m,d_v]      inputs (bf16, device)
+ *   o [B,h,n,d_v]                                     output (bf16, device)
+ *   lse [B,h,n]                                       output (fp32, device) or NULL
+ * lse_i = ln sum_j exp(scale * q_i . k_j) over the visible keys, in natural-log
+ * units of the scaled score (not on the pages; needed by attn_bwd).
+ * Accumulation is fp32; the weights P are rounded to bf16 before the P.V product.
+ */
+int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int h,
+             int n, int m, int d_k, int d_v, int causal, float scale, attn_stream_t stream);
+
+/*
+ * Bytes of device workspace attn_bwd needs for these sizes (fp32 dQ
+ * accumulator plus padded per-row statistics). 0 when B*h*n == 0.
+ */
+size_t attn_bwd_workspace_bytes(int B, int h, int n, int m, int d_k, int d_v, int causal);
+
+/*
+ * Backward pass: gradients of L = sum(dO * O) for O = attn_fwd(q, k, v), the
+ * analytic derivative of eq. (1) (the pages train the model, §5, but never
+ * write the derivative out):
+ *   D_i = sum_c dO_ic O_ic,  dS_ij = P_ij (dO_i . v_j - D_i),
+ *   dQ_i = scale sum_j dS_ij k_j,  dK_j = scale sum_i dS_ij q_i,  dV_j = sum_i P_ij dO_i.
+ *   q, k, v, o, lse   as produced/consumed by attn_fwd (lse is required)
+ *   dO [B,h,n,d_v]    upstream gradient (bf16, device)
+ *   dq, dk, dv        outputs (bf16, device), shaped like q, k, v
+ *   workspace         caller-owned device memory of at least
+ *                     attn_bwd_workspace_bytes(...) bytes, 16-byte aligned;
+ *                     its contents on entry do not matter (the call clears
+ *                     what it needs on `stream`). It must not be shared by
+ *                     calls that run concurrently.
+ */
+int attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+             const void* dO, void* dq, void* dk, void* dv, int B, int h, int n, int m, int d_k,
+             int d_v, int causal, float scale, void* workspace, size_t workspace_bytes,
+             attn_stream_t stream);
+
+/*
+ * Synchronises `stream`, then reports and clears the device-side error word of
+ * the current device: ATTN_OK, or ATTN_ERR_TIMEOUT if any kernel's watchdog
+ * fired since the last call. ATTN_ERR_CUDA if the synchronisation failed.
+ */
+int attn_get_device_status(attn_stream_t stream);
+
+/* Static, human-readable name of a status code. */
+const char* attn_status_string(int status);
+
+/*
+ * Watchdog budget in nanoseconds for every device-side pipeline wait
+ * (default 2e9 = 2 s). 0 restores the default. Returns ATTN_OK.
+ */
+int attn_set_watchdog_ns(unsigned long long budget_ns);
+
+/*
+ * Test hook for the failure path: mode 1 makes the NEXT attn_fwd launch skip
+ * one value-tile load, so a consumer wait runs out and the watchdog reports
+ * ATTN_ERR_TIMEOUT (no fault, no hang). mode 0 clears it. Returns ATTN_OK,
+ * or ATTN_ERR_INVALID_ARG for an unknown mode.
+ */
+int attn_debug_inject(int mode);
+
+/*
+ * Per-kernel device timing, for profiling. While enabled (on != 0), every
+ * kernel that attn_fwd / attn_bwd launches is bracketed by two CUDA events
+ * recorded on the caller's stream. attn_profile_read synchronises the
+ * recorded events, adds their elapsed times into per-kind totals, and returns
+ * and clears the totals of one kind:
+ *   kind 0 forward, 1 backward pre-pass (D, padded lse, dQ clear),
+ *   kind 2 backward main kernel, 3 backward dQ conversion.
+ * launches / total_ms may be NULL. Returns ATTN_OK, ATTN_ERR_INVALID_ARG for an
+ * unknown kind, or ATTN_ERR_CUDA. Enabling costs two event records per launch.
+ */
+int attn_profile_enable(int on);
+int attn_profile_read(int kind, int* launches, double* total_ms);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN_GB300_H */

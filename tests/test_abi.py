@@ -1,0 +1,114 @@
+"""The C-ABI library builds for sm_103a, loads, exports what include/attn.h declares,
+and rejects bad arguments on the host (no GPU needed: no call here reaches CUDA)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import transformer_scaled_dot_attn_gb300 as A
+from transformer_scaled_dot_attn_gb300 import native_build as B
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "attn.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    B.build()
+    return A.load_library()
+
+
+def _declared_functions():
+    text = open(HEADER, encoding="utf-8").read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w[\w\s\*]*?\b(attn_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_entry_points():
+    assert _declared_functions() == sorted(A.EXPORTED_SYMBOLS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _declared_functions():
+        assert hasattr(lib, name), name
+    # and the exported names really are C symbols (no C++ mangling)
+    out = os.popen(f"nm -D --defined-only {A.library_path()}").read()
+    for name in _declared_functions():
+        assert re.search(rf"\bT {name}$", out, flags=re.M), name
+
+
+def test_status_strings(lib):
+    assert A.attn_status_string(0) == "ATTN_OK"
+    assert A.attn_status_string(4) == "ATTN_ERR_TIMEOUT"
+    assert A.attn_status_string(99) == "ATTN_ERR_UNKNOWN"
+
+
+FAKE = 0x10000  # never dereferenced: every call below fails validation first
+
+
+def _fwd(lib, B_=1, h=1, n=8, m=8, dk=64, dv=64, causal=0, scale=0.125, ptrs=(FAKE,) * 4, lse=None):
+    vp = [ctypes.c_void_p(p) if p else None for p in ptrs]
+    return lib.attn_fwd(vp[0], vp[1], vp[2], vp[3], lse, B_, h, n, m, dk, dv, causal, scale, None)
+
+
+def test_fwd_argument_checks(lib):
+    assert _fwd(lib, B_=-1) == A.ATTN_ERR_INVALID_ARG
+    assert _fwd(lib, n=-1) == A.ATTN_ERR_INVALID_ARG
+    assert _fwd(lib, m=0) == A.ATTN_ERR_INVALID_ARG
+    assert _fwd(lib, scale=float("nan")) == A.ATTN_ERR_INVALID_ARG
+    assert _fwd(lib, scale=float("inf")) == A.ATTN_ERR_INVALID_ARG
+    assert _fwd(lib, dk=48, dv=48) == A.ATTN_ERR_UNSUPPORTED
+    assert _fwd(lib, dk=64, dv=32) == A.ATTN_ERR_UNSUPPORTED
+    assert _fwd(lib, dk=256, dv=256) == A.ATTN_ERR_UNSUPPORTED
+    assert _fwd(lib, n=256 * 65536) == A.ATTN_ERR_UNSUPPORTED
+    assert _fwd(lib, ptrs=(FAKE, 0, FAKE, FAKE)) == A.ATTN_ERR_INVALID_ARG
+    assert _fwd(lib, ptrs=(FAKE + 8, FAKE, FAKE, FAKE)) == A.ATTN_ERR_INVALID_ARG
+    bad_lse = ctypes.cast(ctypes.c_void_p(FAKE + 2), ctypes.POINTER(ctypes.c_float))
+    assert _fwd(lib, lse=bad_lse) == A.ATTN_ERR_INVALID_ARG
+    # empty batches are a no-op, even with null pointers
+    assert _fwd(lib, B_=0, ptrs=(0, 0, 0, 0)) == A.ATTN_OK
+    assert _fwd(lib, n=0, ptrs=(0, 0, 0, 0)) == A.ATTN_OK
+
+
+def test_bwd_argument_checks(lib):
+    vp = ctypes.c_void_p
+    f = ctypes.cast(vp(FAKE), ctypes.POINTER(ctypes.c_float))
+
+    def call(n=8, m=8, d=64, ws_bytes=1 << 30, ws=FAKE, dq=FAKE, lse=f, scale=0.125):
+        return lib.attn_bwd(vp(FAKE), vp(FAKE), vp(FAKE), vp(FAKE), lse, vp(FAKE), vp(dq) if dq else None,
+                            vp(FAKE), vp(FAKE), 1, 1, n, m, d, d, 0, scale, vp(ws) if ws else None,
+                            ws_bytes, None)
+
+    assert call(m=0) == A.ATTN_ERR_INVALID_ARG
+    assert call(d=96) == A.ATTN_ERR_UNSUPPORTED
+    assert call(ws=0) == A.ATTN_ERR_INVALID_ARG
+    assert call(dq=0) == A.ATTN_ERR_INVALID_ARG
+    assert call(lse=None) == A.ATTN_ERR_INVALID_ARG
+    assert call(ws_bytes=16) == A.ATTN_ERR_INVALID_ARG
+    assert call(scale=float("nan")) == A.ATTN_ERR_INVALID_ARG
+
+
+def test_workspace_size(lib):
+    # fp32 dQ accumulator + two fp32 per-row statistics, rows padded to 128
+    assert A.attn_bwd_workspace_bytes(2, 3, 200, 77, 64, 64) == 2 * 3 * 256 * (64 + 2) * 4
+    assert A.attn_bwd_workspace_bytes(1, 1, 128, 1, 32, 32, True) == 128 * 34 * 4
+    assert A.attn_bwd_workspace_bytes(0, 3, 200, 77, 64, 64) == 0
+    assert A.attn_bwd_workspace_bytes(1, 1, 0, 77, 64, 64) == 0
+
+
+def test_debug_hooks(lib):
+    assert A.attn_debug_inject(2) == A.ATTN_ERR_INVALID_ARG
+    assert A.attn_debug_inject(0) == A.ATTN_OK
+    assert A.attn_set_watchdog_ns(0) == A.ATTN_OK
+
+
+def test_built_for_sm103a():
+    """The build command targets sm_103a only (one -gencode, arch=compute_103a,code=sm_103a)."""
+    assert B.ARCH == ["-gencode", "arch=compute_103a,code=sm_103a"]
+
+
+def test_binding_refuses_cpu_tensors(lib):
+    import torch
+    q = torch.zeros(1, 1, 4, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="CUDA"):
+        A.attn_fwd(q, q, q)

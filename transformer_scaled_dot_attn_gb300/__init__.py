@@ -1,0 +1,221 @@
+"""GB300 (sm_103a) multi-head scaled dot-product attention.
+
+Python binding of the C ABI declared in ``include/attn.h``. It only checks and
+marshals arguments (torch tensors give device pointers and the current CUDA
+stream); every step of the computation runs in the library's CUDA kernels.
+There is no CPU fallback: if the library is not built, calls raise.
+
+    O = softmax(Q K^T * scale) V      ("Attention Is All You Need", §3.2.1 eq. (1))
+
+Tensors are bf16, contiguous, shaped [B, h, S, d] (d fastest); lse is fp32
+[B, h, n]. ``scale`` defaults to 1/sqrt(d_k). ``causal`` applies the decoder
+mask of §3.2.3 (key j visible to query i iff j <= i).
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+from typing import Optional, Tuple
+
+from .native_build import LIB_PATH, build  # noqa: F401  (re-exported for __graft_entry__)
+
+__all__ = [
+    "AttnError", "ATTN_OK", "ATTN_ERR_INVALID_ARG", "ATTN_ERR_UNSUPPORTED", "ATTN_ERR_CUDA",
+    "ATTN_ERR_TIMEOUT", "load_library", "library_path", "attn_fwd", "attn_bwd",
+    "attn_bwd_workspace_bytes", "attn_get_device_status", "attn_status_string",
+    "attn_set_watchdog_ns", "attn_debug_inject", "attn_profile_enable", "attn_profile_read",
+    "EXPORTED_SYMBOLS", "KERNEL_KINDS",
+]
+
+ATTN_OK = 0
+ATTN_ERR_INVALID_ARG = 1
+ATTN_ERR_UNSUPPORTED = 2
+ATTN_ERR_CUDA = 3
+ATTN_ERR_TIMEOUT = 4
+
+# Every entry point include/attn.h declares.
+EXPORTED_SYMBOLS = (
+    "attn_fwd", "attn_bwd", "attn_bwd_workspace_bytes", "attn_get_device_status",
+    "attn_status_string", "attn_set_watchdog_ns", "attn_debug_inject", "attn_profile_enable",
+    "attn_profile_read",
+)
+
+# Kernel kinds of attn_profile_read.
+KERNEL_KINDS = {"fwd": 0, "bwd_pre": 1, "bwd_main": 2, "bwd_post": 3}
+
+_lock = threading.Lock()
+_lib = None
+
+
+class AttnError(RuntimeError):
+    """A non-zero status returned by the library."""
+
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {attn_status_string(status)} ({status})")
+
+
+def library_path() -> str:
+    return LIB_PATH
+
+
+def load_library():
+    """Load ``libattn_gb300.so`` (ctypes) and declare every entry point's signature."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                f"{LIB_PATH} is missing: build the CUDA library first "
+                "(python -c 'import __graft_entry__ as g; g.build()')")
+        lib = ctypes.CDLL(LIB_PATH)
+        vp, I, F, SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+        fp = ctypes.POINTER(ctypes.c_float)
+        lib.attn_fwd.argtypes = [vp, vp, vp, vp, fp, I, I, I, I, I, I, I, F, vp]
+        lib.attn_fwd.restype = I
+        lib.attn_bwd.argtypes = [vp, vp, vp, vp, fp, vp, vp, vp, vp, I, I, I, I, I, I, I, F,
+                                 vp, SZ, vp]
+        lib.attn_bwd.restype = I
+        lib.attn_bwd_workspace_bytes.argtypes = [I, I, I, I, I, I, I]
+        lib.attn_bwd_workspace_bytes.restype = SZ
+        lib.attn_get_device_status.argtypes = [vp]
+        lib.attn_get_device_status.restype = I
+        lib.attn_status_string.argtypes = [I]
+        lib.attn_status_string.restype = ctypes.c_char_p
+        lib.attn_set_watchdog_ns.argtypes = [ctypes.c_ulonglong]
+        lib.attn_set_watchdog_ns.restype = I
+        lib.attn_debug_inject.argtypes = [I]
+        lib.attn_debug_inject.restype = I
+        lib.attn_profile_enable.argtypes = [I]
+        lib.attn_profile_enable.restype = I
+        lib.attn_profile_read.argtypes = [I, ctypes.POINTER(I), ctypes.POINTER(ctypes.c_double)]
+        lib.attn_profile_read.restype = I
+        _lib = lib
+        return lib
+
+
+def attn_status_string(status: int) -> str:
+    return load_library().attn_status_string(int(status)).decode()
+
+
+def _stream_handle(stream) -> Optional[int]:
+    import torch
+    s = torch.cuda.current_stream() if stream is None else stream
+    return s.cuda_stream
+
+
+def _check_tensor(name, t, shape=None, dtype=None):
+    import torch
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor (the library has no CPU path)")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+
+
+def _fptr(t):
+    return None if t is None else ctypes.cast(t.data_ptr(), ctypes.POINTER(ctypes.c_float))
+
+
+def _vptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def attn_fwd(q, k, v, causal: bool = False, scale: Optional[float] = None, out=None, lse=None,
+             need_lse: bool = True, stream=None) -> Tuple["torch.Tensor", Optional["torch.Tensor"]]:
+    """O, lse = attention(q, k, v) on the GPU. q [B,h,n,d], k/v [B,h,m,d], bf16."""
+    import torch
+    lib = load_library()
+    if q.dim() != 4 or k.dim() != 4 or v.dim() != 4:
+        raise ValueError("q, k, v must be [B, h, S, d]")
+    B, h, n, dk = q.shape
+    m, dv = k.shape[2], v.shape[3]
+    _check_tensor("q", q, dtype=torch.bfloat16)
+    _check_tensor("k", k, (B, h, m, dk), torch.bfloat16)
+    _check_tensor("v", v, (B, h, m, dv), torch.bfloat16)
+    if scale is None:
+        scale = 1.0 / math.sqrt(dk)
+    if out is None:
+        out = torch.empty((B, h, n, dv), dtype=torch.bfloat16, device=q.device)
+    _check_tensor("out", out, (B, h, n, dv), torch.bfloat16)
+    if need_lse and lse is None:
+        lse = torch.empty((B, h, n), dtype=torch.float32, device=q.device)
+    if lse is not None:
+        _check_tensor("lse", lse, (B, h, n), torch.float32)
+    st = lib.attn_fwd(_vptr(q), _vptr(k), _vptr(v), _vptr(out), _fptr(lse), B, h, n, m, dk, dv,
+                      int(bool(causal)), float(scale), _stream_handle(stream))
+    if st != ATTN_OK:
+        raise AttnError(st, "attn_fwd")
+    return out, lse
+
+
+def attn_bwd_workspace_bytes(B, h, n, m, d_k, d_v, causal=False) -> int:
+    return int(load_library().attn_bwd_workspace_bytes(B, h, n, m, d_k, d_v, int(bool(causal))))
+
+
+def attn_bwd(q, k, v, o, lse, dO, causal: bool = False, scale: Optional[float] = None,
+             dq=None, dk=None, dv=None, workspace=None, stream=None):
+    """dQ, dK, dV of sum(dO * O) for O = attention(q, k, v), from attn_fwd's O and lse."""
+    import torch
+    lib = load_library()
+    B, h, n, d_k = q.shape
+    m, d_v = k.shape[2], v.shape[3]
+    _check_tensor("q", q, dtype=torch.bfloat16)
+    _check_tensor("k", k, (B, h, m, d_k), torch.bfloat16)
+    _check_tensor("v", v, (B, h, m, d_v), torch.bfloat16)
+    _check_tensor("o", o, (B, h, n, d_v), torch.bfloat16)
+    _check_tensor("lse", lse, (B, h, n), torch.float32)
+    _check_tensor("dO", dO, (B, h, n, d_v), torch.bfloat16)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d_k)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    for name, t, ref in (("dq", dq, q), ("dk", dk, k), ("dv", dv, v)):
+        _check_tensor(name, t, tuple(ref.shape), torch.bfloat16)
+    need = attn_bwd_workspace_bytes(B, h, n, m, d_k, d_v, causal)
+    if workspace is None:
+        workspace = torch.empty((max(need, 16) + 15) // 16 * 4, dtype=torch.float32, device=q.device)
+    _check_tensor("workspace", workspace)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    st = lib.attn_bwd(_vptr(q), _vptr(k), _vptr(v), _vptr(o), _fptr(lse), _vptr(dO), _vptr(dq),
+                      _vptr(dk), _vptr(dv), B, h, n, m, d_k, d_v, int(bool(causal)), float(scale),
+                      _vptr(workspace), ws_bytes, _stream_handle(stream))
+    if st != ATTN_OK:
+        raise AttnError(st, "attn_bwd")
+    return dq, dk, dv
+
+
+def attn_get_device_status(stream=None) -> int:
+    return int(load_library().attn_get_device_status(_stream_handle(stream)))
+
+
+def attn_set_watchdog_ns(budget_ns: int) -> int:
+    return int(load_library().attn_set_watchdog_ns(int(budget_ns)))
+
+
+def attn_debug_inject(mode: int) -> int:
+    return int(load_library().attn_debug_inject(int(mode)))
+
+
+def attn_profile_enable(on: bool) -> int:
+    return int(load_library().attn_profile_enable(int(bool(on))))
+
+
+def attn_profile_read(kind) -> Tuple[int, float]:
+    """(launches, total device ms) of one kernel kind since the last read; clears them."""
+    k = KERNEL_KINDS[kind] if isinstance(kind, str) else int(kind)
+    n = ctypes.c_int(0)
+    ms = ctypes.c_double(0.0)
+    st = load_library().attn_profile_read(k, ctypes.byref(n), ctypes.byref(ms))
+    if st != ATTN_OK:
+        raise AttnError(st, "attn_profile_read")
+    return int(n.value), float(ms.value)

@@ -1,0 +1,349 @@
+// C ABI of the attention library: argument checks, TMA tensor-map encoding,
+// kernel launches and the device error word. The declarations, with the
+// meaning of every argument, are in include/attn.h.
+#include "attn.h"
+#include "attn_kernels.cuh"
+
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+#include <vector>
+
+namespace {
+
+using attn::BwdParams;
+using attn::BwdPostParams;
+using attn::BwdPreParams;
+using attn::FwdParams;
+
+constexpr unsigned long long kDefaultWatchdogNs = 2000000000ull;  // 2 s per wait
+constexpr int kMaxDevices = 64;
+
+std::atomic<unsigned long long> g_watchdog_ns{kDefaultWatchdogNs};
+std::atomic<int> g_inject{0};
+
+// One device error word per device, allocated on first use and kept until exit.
+std::mutex g_status_mu;
+uint32_t* g_status[kMaxDevices] = {nullptr};
+
+cudaError_t device_status_word(uint32_t** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_status_mu);
+  if (g_status[dev] == nullptr) {
+    uint32_t* p = nullptr;
+    e = cudaMalloc(&p, sizeof(uint32_t));
+    if (e != cudaSuccess) return e;
+    e = cudaMemset(p, 0, sizeof(uint32_t));
+    if (e != cudaSuccess) {
+      cudaFree(p);
+      return e;
+    }
+    g_status[dev] = p;
+  }
+  *out = g_status[dev];
+  return cudaSuccess;
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return static_cast<EncodeTiledFn>(nullptr);
+    return reinterpret_cast<EncodeTiledFn>(f);
+  }();
+  return fn;
+}
+
+// 3-D map over a [BH, S, d] bf16 tensor: box = (atom, 128 rows, 1 head).
+// Rows past S read as zero (out-of-bounds fill), so ragged tiles never touch
+// the next head.
+bool make_tile_map(CUtensorMap* map, const void* base, long long BH, long long S, int d) {
+  EncodeTiledFn enc = encode_fn();
+  if (enc == nullptr) return false;
+  const int atom = d >= 64 ? 64 : d;
+  const CUtensorMapSwizzle sw = d >= 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(S),
+                        static_cast<cuuint64_t>(BH)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(S) * d * 2};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(atom), 128u, 1u};
+  cuuint32_t estr[3] = {1u, 1u, 1u};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+constexpr double kLog2e = 1.4426950408889634074;
+
+// Shared checks of attn_fwd / attn_bwd. Returns ATTN_OK to proceed, or the
+// status to return; *empty is set when there is nothing to compute.
+int check_common(int B, int h, int n, int m, int d_k, int d_v, float scale, bool* empty) {
+  *empty = false;
+  if (B < 0 || h < 0 || n < 0 || m < 1 || d_k < 1 || d_v < 1) return ATTN_ERR_INVALID_ARG;
+  if (!std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
+  if (d_k != d_v) return ATTN_ERR_UNSUPPORTED;
+  if (d_k != 32 && d_k != 64 && d_k != 128) return ATTN_ERR_UNSUPPORTED;
+  const long long BH = static_cast<long long>(B) * h;
+  if (BH > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
+  if ((static_cast<long long>(n) + 255) / 256 > 65535) return ATTN_ERR_UNSUPPORTED;
+  if ((static_cast<long long>(m) + 127) / 128 > 65535) return ATTN_ERR_UNSUPPORTED;
+  if (BH == 0 || n == 0) *empty = true;
+  return ATTN_OK;
+}
+
+long long round_up(long long x, long long a) { return (x + a - 1) / a * a; }
+
+// ---------------------------------------------------------------- profiling
+
+struct EventPair {
+  cudaEvent_t begin = nullptr, end = nullptr;
+  int kind = 0;
+};
+
+std::atomic<int> g_prof_on{0};
+std::mutex g_prof_mu;
+std::vector<EventPair> g_prof_pending;  // recorded, not yet read
+std::vector<EventPair> g_prof_free;     // created, reusable
+EventPair g_prof_open[attn::kNumKinds];  // begun, waiting for prof_end
+double g_prof_ms[attn::kNumKinds] = {0, 0, 0, 0};
+int g_prof_count[attn::kNumKinds] = {0, 0, 0, 0};
+
+// Moves every pending pair's elapsed time into the per-kind totals.
+cudaError_t prof_drain_locked() {
+  for (EventPair& ep : g_prof_pending) {
+    cudaError_t e = cudaEventSynchronize(ep.end);
+    if (e != cudaSuccess) return e;
+    float ms = 0.f;
+    e = cudaEventElapsedTime(&ms, ep.begin, ep.end);
+    if (e != cudaSuccess) return e;
+    g_prof_ms[ep.kind] += ms;
+    g_prof_count[ep.kind] += 1;
+    g_prof_free.push_back(ep);
+  }
+  g_prof_pending.clear();
+  return cudaSuccess;
+}
+
+}  // namespace
+
+namespace attn {
+
+void prof_begin(int kind, cudaStream_t stream) {
+  if (!g_prof_on.load(std::memory_order_relaxed)) return;
+  std::lock_guard<std::mutex> lock(g_prof_mu);
+  EventPair ep;
+  if (!g_prof_free.empty()) {
+    ep = g_prof_free.back();
+    g_prof_free.pop_back();
+  } else if (cudaEventCreate(&ep.begin) != cudaSuccess || cudaEventCreate(&ep.end) != cudaSuccess) {
+    return;
+  }
+  ep.kind = kind;
+  cudaEventRecord(ep.begin, stream);
+  g_prof_open[kind] = ep;
+}
+
+void prof_end(int kind, cudaStream_t stream) {
+  if (!g_prof_on.load(std::memory_order_relaxed)) return;
+  std::lock_guard<std::mutex> lock(g_prof_mu);
+  EventPair ep = g_prof_open[kind];
+  if (ep.begin == nullptr) return;
+  g_prof_open[kind] = EventPair{};
+  cudaEventRecord(ep.end, stream);
+  g_prof_pending.push_back(ep);
+}
+
+}  // namespace attn
+
+extern "C" {
+
+int attn_profile_enable(int on) {
+  g_prof_on.store(on ? 1 : 0);
+  return ATTN_OK;
+}
+
+int attn_profile_read(int kind, int* launches, double* total_ms) {
+  if (kind < 0 || kind >= attn::kNumKinds) return ATTN_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lock(g_prof_mu);
+  if (prof_drain_locked() != cudaSuccess) return ATTN_ERR_CUDA;
+  if (launches) *launches = g_prof_count[kind];
+  if (total_ms) *total_ms = g_prof_ms[kind];
+  g_prof_count[kind] = 0;
+  g_prof_ms[kind] = 0.0;
+  return ATTN_OK;
+}
+
+const char* attn_status_string(int status) {
+  switch (status) {
+    case ATTN_OK: return "ATTN_OK";
+    case ATTN_ERR_INVALID_ARG: return "ATTN_ERR_INVALID_ARG";
+    case ATTN_ERR_UNSUPPORTED: return "ATTN_ERR_UNSUPPORTED";
+    case ATTN_ERR_CUDA: return "ATTN_ERR_CUDA";
+    case ATTN_ERR_TIMEOUT: return "ATTN_ERR_TIMEOUT";
+    default: return "ATTN_ERR_UNKNOWN";
+  }
+}
+
+int attn_set_watchdog_ns(unsigned long long budget_ns) {
+  g_watchdog_ns.store(budget_ns == 0 ? kDefaultWatchdogNs : budget_ns);
+  return ATTN_OK;
+}
+
+int attn_debug_inject(int mode) {
+  if (mode != 0 && mode != 1) return ATTN_ERR_INVALID_ARG;
+  g_inject.store(mode);
+  return ATTN_OK;
+}
+
+int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int h, int n,
+             int m, int d_k, int d_v, int causal, float scale, attn_stream_t stream) {
+  bool empty = false;
+  int st = check_common(B, h, n, m, d_k, d_v, scale, &empty);
+  if (st != ATTN_OK) return st;
+  if (empty) return ATTN_OK;
+  if (!q || !k || !v || !o) return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return ATTN_ERR_INVALID_ARG;
+  if (lse != nullptr && (reinterpret_cast<uintptr_t>(lse) & 3u) != 0) return ATTN_ERR_INVALID_ARG;
+  const long long BH = static_cast<long long>(B) * h;
+  CUtensorMap tq, tk, tv;
+  if (!make_tile_map(&tq, q, BH, n, d_k) || !make_tile_map(&tk, k, BH, m, d_k) ||
+      !make_tile_map(&tv, v, BH, m, d_v))
+    return ATTN_ERR_CUDA;
+  uint32_t* status = nullptr;
+  if (device_status_word(&status) != cudaSuccess) return ATTN_ERR_CUDA;
+  FwdParams p{};
+  p.o = static_cast<__nv_bfloat16*>(o);
+  p.lse = lse;
+  p.n = n;
+  p.m = m;
+  p.causal = causal ? 1 : 0;
+  p.neg = scale < 0.f ? 1 : 0;
+  p.c = static_cast<float>(std::fabs(static_cast<double>(scale)) * kLog2e);
+  p.num_qblocks = static_cast<int>((n + 255) / 256);
+  p.inject = g_inject.exchange(0);
+  p.wd.status = status;
+  p.wd.budget_ns = g_watchdog_ns.load();
+  cudaError_t e = attn::launch_fwd(d_k, tq, tk, tv, p, static_cast<int>(BH),
+                                   reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+size_t attn_bwd_workspace_bytes(int B, int h, int n, int m, int d_k, int d_v, int causal) {
+  (void)m;
+  (void)d_v;
+  (void)causal;
+  if (B <= 0 || h <= 0 || n <= 0 || d_k <= 0) return 0;
+  const long long BH = static_cast<long long>(B) * h;
+  const long long n_pad = round_up(n, 128);
+  // dQ accumulator [BH, n_pad, d] + lse*log2(e) [BH, n_pad] + D [BH, n_pad], fp32
+  return static_cast<size_t>(BH * n_pad * (static_cast<long long>(d_k) + 2) * 4);
+}
+
+int attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+             const void* dO, void* dq, void* dk, void* dv, int B, int h, int n, int m, int d_k,
+             int d_v, int causal, float scale, void* workspace, size_t workspace_bytes,
+             attn_stream_t stream) {
+  bool empty = false;
+  int st = check_common(B, h, n, m, d_k, d_v, scale, &empty);
+  if (st != ATTN_OK) return st;
+  if (!k || !v || !dk || !dv) return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(k) || !aligned16(v) || !aligned16(dk) || !aligned16(dv)) return ATTN_ERR_INVALID_ARG;
+  const long long BH = static_cast<long long>(B) * h;
+  if (empty) {
+    // No query rows: every gradient is zero. dK and dV still have BH*m rows.
+    if (BH == 0) return ATTN_OK;
+    const size_t bytes = static_cast<size_t>(BH) * m * d_k * 2;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (cudaMemsetAsync(dk, 0, bytes, s) != cudaSuccess) return ATTN_ERR_CUDA;
+    if (cudaMemsetAsync(dv, 0, bytes, s) != cudaSuccess) return ATTN_ERR_CUDA;
+    return ATTN_OK;
+  }
+  if (!q || !o || !lse || !dO || !dq || !workspace) return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(o) || !aligned16(dO) || !aligned16(dq) || !aligned16(workspace))
+    return ATTN_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(lse) & 3u) != 0) return ATTN_ERR_INVALID_ARG;
+  if (workspace_bytes < attn_bwd_workspace_bytes(B, h, n, m, d_k, d_v, causal))
+    return ATTN_ERR_INVALID_ARG;
+
+  const long long n_pad = round_up(n, 128);
+  float* ws = static_cast<float*>(workspace);
+  float* dq_acc = ws;
+  float* lse2 = dq_acc + BH * n_pad * d_k;
+  float* Dsum = lse2 + BH * n_pad;
+
+  CUtensorMap tq, tk, tv, tdo;
+  if (!make_tile_map(&tq, q, BH, n, d_k) || !make_tile_map(&tk, k, BH, m, d_k) ||
+      !make_tile_map(&tv, v, BH, m, d_v) || !make_tile_map(&tdo, dO, BH, n, d_v))
+    return ATTN_ERR_CUDA;
+  uint32_t* status = nullptr;
+  if (device_status_word(&status) != cudaSuccess) return ATTN_ERR_CUDA;
+
+  BwdPreParams pre{};
+  pre.o = static_cast<const __nv_bfloat16*>(o);
+  pre.dO = static_cast<const __nv_bfloat16*>(dO);
+  pre.lse = lse;
+  pre.lse2 = lse2;
+  pre.Dsum = Dsum;
+  pre.dq_acc = dq_acc;
+  pre.n = n;
+  pre.n_pad = static_cast<int>(n_pad);
+  pre.d = d_k;
+  pre.BH = static_cast<int>(BH);
+
+  BwdParams p{};
+  p.dk = static_cast<__nv_bfloat16*>(dk);
+  p.dv = static_cast<__nv_bfloat16*>(dv);
+  p.lse2 = lse2;
+  p.Dsum = Dsum;
+  p.dq_acc = dq_acc;
+  p.n = n;
+  p.m = m;
+  p.n_pad = static_cast<int>(n_pad);
+  p.causal = causal ? 1 : 0;
+  p.neg = scale < 0.f ? 1 : 0;
+  p.c = static_cast<float>(std::fabs(static_cast<double>(scale)) * kLog2e);
+  p.scale = scale;
+  p.num_kblocks = static_cast<int>((m + 127) / 128);
+  p.wd.status = status;
+  p.wd.budget_ns = g_watchdog_ns.load();
+
+  BwdPostParams post{};
+  post.dq_acc = dq_acc;
+  post.dq = static_cast<__nv_bfloat16*>(dq);
+  post.scale = scale;
+  post.n = n;
+  post.n_pad = static_cast<int>(n_pad);
+  post.d = d_k;
+  post.BH = static_cast<int>(BH);
+
+  cudaError_t e = attn::launch_bwd(d_k, tq, tk, tv, tdo, pre, p, post, static_cast<int>(BH),
+                                   reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+int attn_get_device_status(attn_stream_t stream) {
+  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return ATTN_ERR_CUDA;
+  uint32_t* status = nullptr;
+  if (device_status_word(&status) != cudaSuccess) return ATTN_ERR_CUDA;
+  uint32_t v = 0;
+  if (cudaMemcpy(&v, status, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return ATTN_ERR_CUDA;
+  if (v == 0) return ATTN_OK;
+  if (cudaMemset(status, 0, sizeof(uint32_t)) != cudaSuccess) return ATTN_ERR_CUDA;
+  return ATTN_ERR_TIMEOUT;
+}
+
+}  // extern "C"

@@ -1,0 +1,561 @@
+// Backward kernels: dQ, dK, dV of L = sum(dO * O) for O = softmax(Q K^T * scale) V.
+//
+// The pages train the model (§5 of "Attention Is All You Need") but never
+// write the derivative of eq. (1) out; it is the analytic one:
+//   P_ij = exp(scale q_i.k_j - lse_i)         (recomputed, never stored)
+//   D_i  = sum_c dO_ic O_ic
+//   dS_ij = P_ij (dO_i . v_j - D_i)
+//   dV_j = sum_i P_ij dO_i,  dK_j = scale sum_i dS_ij q_i,  dQ_i = scale sum_j dS_ij k_j
+// Masked pairs (key j after query i, §3.2.3) have P_ij = 0 and drop out.
+//
+// Three launches on the caller's stream:
+//   pre   D_i, lse_i * log2(e) into padded rows of the workspace; zero the fp32
+//         dQ accumulator. Bandwidth bound.
+//   main  one CTA per (head, 128-key tile j). K_j and V_j stay in shared
+//         memory; 128-query tiles i stream through a two-stage TMA ring.
+//         Five tcgen05 products per tile, all with 128 TMEM lanes:
+//           S^T  = K_j Q_i^T        (lanes: keys)            -> TMEM
+//           dP^T = V_j dO_i^T                                 -> TMEM
+//           dV_j += P^T dO_i        (P^T bf16 in TMEM, aliasing S^T)
+//           dK_j += dS^T Q_i        (dS^T bf16 in shared memory, K-major view)
+//           dQ_i  = dS K_j          (same buffer read as an MN-major operand)
+//         warps 0-3  one thread per key row: P, dS, and the dK/dV epilogue.
+//         warps 4-7  one thread per query row: add dQ_i into the fp32
+//                    accumulator with vector atomics.
+//         warp 8     TMA producer, warp 9 MMA issuer.
+//   post  dQ = bf16(scale * accumulator).
+//
+// TMEM columns: S^T [0,128), dP^T [128,256), dV [256,256+D), dK [256+D,256+2D),
+// dQ [256+2D,256+3D) for D <= 64; for D = 128 dQ reuses the dP^T columns.
+#include "attn_kernels.cuh"
+
+#include <mutex>
+
+namespace attn {
+namespace {
+
+using namespace sm103;
+
+constexpr float kLog2e = 1.4426950408889634074f;
+
+// ---------------------------------------------------------------- pre
+
+// One group of D/8 lanes per row: each lane reads 8 bf16 of O and dO.
+template <int D>
+__global__ void __launch_bounds__(256) attn_bwd_pre_kernel(const BwdPreParams p) {
+  constexpr int LPR = D / 8;           // lanes per row
+  constexpr int RPB = 256 / LPR;       // rows per block
+  const long long row = static_cast<long long>(blockIdx.x) * RPB + threadIdx.x / LPR;
+  const int sub = threadIdx.x % LPR;
+  const long long total = static_cast<long long>(p.BH) * p.n_pad;
+  float dot = 0.f;
+  bool valid = false;
+  long long bh = 0, i = 0;
+  if (row < total) {
+    bh = row / p.n_pad;
+    i = row - bh * p.n_pad;
+    valid = i < p.n;
+    if (valid) {
+      const size_t off = (static_cast<size_t>(bh) * p.n + i) * D + sub * 8;
+      const uint4 a = *reinterpret_cast<const uint4*>(p.o + off);
+      const uint4 b = *reinterpret_cast<const uint4*>(p.dO + off);
+      const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
+      const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&b);
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        const float2 x = __bfloat1622float2(a2[t]);
+        const float2 y = __bfloat1622float2(b2[t]);
+        dot = fmaf(x.x, y.x, dot);
+        dot = fmaf(x.y, y.y, dot);
+      }
+    }
+    // zero this row's slice of the dQ accumulator (D floats = D/4 float4, 2 per lane)
+    float4* acc = reinterpret_cast<float4*>(p.dq_acc + static_cast<size_t>(row) * D) + sub * 2;
+    acc[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+    acc[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+#pragma unroll
+  for (int off = LPR / 2; off > 0; off >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off, LPR);
+  if (row < total && sub == 0) {
+    p.Dsum[row] = valid ? dot : 0.f;
+    p.lse2[row] = valid ? p.lse[static_cast<size_t>(bh) * p.n + i] * kLog2e : INFINITY;
+  }
+}
+
+// ---------------------------------------------------------------- post
+
+template <int D>
+__global__ void __launch_bounds__(256) attn_bwd_post_kernel(const BwdPostParams p) {
+  constexpr int CPR = D / 8;  // 8-element chunks per row
+  const long long idx = static_cast<long long>(blockIdx.x) * 256 + threadIdx.x;
+  const long long total = static_cast<long long>(p.BH) * p.n * CPR;
+  if (idx >= total) return;
+  const long long row = idx / CPR;
+  const int ch = static_cast<int>(idx - row * CPR);
+  const long long bh = row / p.n;
+  const long long i = row - bh * p.n;
+  const float4* src = reinterpret_cast<const float4*>(p.dq_acc + (static_cast<size_t>(bh) * p.n_pad + i) * D) + ch * 2;
+  const float4 a = src[0], b = src[1];
+  uint4 out;
+  out.x = pack_bf16x2(a.x * p.scale, a.y * p.scale);
+  out.y = pack_bf16x2(a.z * p.scale, a.w * p.scale);
+  out.z = pack_bf16x2(b.x * p.scale, b.y * p.scale);
+  out.w = pack_bf16x2(b.z * p.scale, b.w * p.scale);
+  reinterpret_cast<uint4*>(p.dq + static_cast<size_t>(row) * D)[ch] = out;
+}
+
+// ---------------------------------------------------------------- main
+
+template <int D>
+struct Bwd {
+  static constexpr int ATOM = (D >= 64) ? 64 : D;
+  static constexpr int NATOM = D / ATOM;
+  static constexpr uint32_t SWZ = (D >= 64) ? 2u : 4u;
+  static constexpr uint32_t SBO = 8u * ATOM * 2u;
+  static constexpr uint32_t TILE = 128u * D * 2u;
+  static constexpr uint32_t BOX = 128u * ATOM * 2u;
+  static constexpr uint32_t OFF_K = 0;
+  static constexpr uint32_t OFF_V = TILE;
+  static constexpr uint32_t OFF_Q = 2 * TILE;          // 2 stages
+  static constexpr uint32_t OFF_DO = 4 * TILE;         // 2 stages
+  static constexpr uint32_t OFF_DS = 6 * TILE;         // dS^T: 2 regions [128 keys][64 queries], 128B swizzle
+  static constexpr uint32_t DS_REGION = 128u * 64u * 2u;
+  static constexpr uint32_t SMEM = OFF_DS + 2 * DS_REGION + 1024;
+  static constexpr int THREADS = 320;
+  static constexpr bool ALIAS_DQ = (D > 64);
+  static constexpr uint32_t TM_S = 0, TM_DP = 128, TM_DV = 256, TM_DK = 256 + D;
+  static constexpr uint32_t TM_DQ = ALIAS_DQ ? 128u : (256u + 2u * D);
+};
+
+struct BwdShared {
+  uint64_t kv_full;
+  uint64_t qdo_full[2], qdo_empty[2];
+  uint64_t s_full, dp_full, p_full, ds_full, ds_empty, dq_full, dq_empty, dkv_full, drain;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+__device__ __forceinline__ float ex2f(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ void drain_wait_b(uint64_t* bar, uint32_t parity, const Watchdog& wd) {
+  if (mbar_try_wait(bar, parity)) return;
+  const uint64_t t0 = global_timer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (global_timer_ns() - t0 > wd.budget_ns) {
+      atomicCAS(wd.status, 0u, kDevTimeout | kSiteDrain);
+      return;
+    }
+  }
+}
+
+template <int D>
+__global__ void __launch_bounds__(320, 1)
+attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                const BwdParams p) {
+  using C = Bwd<D>;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) BwdShared sh;
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int bh = blockIdx.x;
+  const int kb = blockIdx.y;
+  const int k0 = kb * 128;
+  volatile int* abort_flag = &sh.abort_flag;
+  const Watchdog wd = p.wd;
+  const int n_qt = (p.n + 127) / 128;
+  // Causal: query tiles wholly above this key tile see none of its keys.
+  const int i_start = p.causal ? min(k0 / 128, n_qt) : 0;
+  const int T = n_qt - i_start;
+
+  if (tid == 0) {
+    mbar_init(&sh.kv_full, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&sh.qdo_full[s], 1);
+      mbar_init(&sh.qdo_empty[s], 1);
+    }
+    mbar_init(&sh.s_full, 1);
+    mbar_init(&sh.dp_full, 1);
+    mbar_init(&sh.p_full, 128);
+    mbar_init(&sh.ds_full, 128);
+    mbar_init(&sh.ds_empty, 1);
+    mbar_init(&sh.dq_full, 1);
+    mbar_init(&sh.dq_empty, 128);
+    mbar_init(&sh.dkv_full, 1);
+    mbar_init(&sh.drain, 1);
+    sh.abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 9) {
+    tmem_alloc<512>(&sh.tmem_base);
+    tmem_relinquish();
+  }
+  if (warp == 8 && lane == 0) {
+    prefetch_tensormap(&tm_q);
+    prefetch_tensormap(&tm_k);
+    prefetch_tensormap(&tm_v);
+    prefetch_tensormap(&tm_do);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sh.tmem_base;
+
+  if (warp == 8) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0 && T > 0) {
+      int last[2] = {-1, -1};
+      mbar_arrive_expect_tx(&sh.kv_full, 2 * C::TILE);
+      for (int a = 0; a < C::NATOM; ++a) {
+        tma_load_3d(smem + C::OFF_K + a * C::BOX, &tm_k, &sh.kv_full, a * C::ATOM, k0, bh);
+        tma_load_3d(smem + C::OFF_V + a * C::BOX, &tm_v, &sh.kv_full, a * C::ATOM, k0, bh);
+      }
+      for (int t = 0; t < T; ++t) {
+        const int st = t & 1;
+        const uint32_t ph = (t >> 1) & 1;
+        if (t >= 2 && !guarded_wait(&sh.qdo_empty[st], ph ^ 1, abort_flag, wd, kSiteBwdFree)) break;
+        const int q_row = (i_start + t) * 128;
+        mbar_arrive_expect_tx(&sh.qdo_full[st], 2 * C::TILE);
+        for (int a = 0; a < C::NATOM; ++a) {
+          tma_load_3d(smem + C::OFF_Q + st * C::TILE + a * C::BOX, &tm_q, &sh.qdo_full[st], a * C::ATOM, q_row, bh);
+          tma_load_3d(smem + C::OFF_DO + st * C::TILE + a * C::BOX, &tm_do, &sh.qdo_full[st], a * C::ATOM, q_row, bh);
+        }
+        last[st] = static_cast<int>(ph);
+      }
+      drain_wait_b(&sh.kv_full, 0, wd);
+      for (int s = 0; s < 2; ++s)
+        if (last[s] >= 0) drain_wait_b(&sh.qdo_full[s], static_cast<uint32_t>(last[s]), wd);
+    }
+  } else if (warp == 9) {
+    // ------------------------------------------------------------ MMA issuer
+    const uint32_t sK = smem_u32(smem + C::OFF_K), sV = smem_u32(smem + C::OFF_V);
+    const uint32_t sQ = smem_u32(smem + C::OFF_Q), sDO = smem_u32(smem + C::OFF_DO);
+    const uint32_t sDS = smem_u32(smem + C::OFF_DS);
+    const uint32_t id_s = idesc_bf16_f32(128, 128, false, false) | (p.neg ? (1u << 13) : 0u);
+    const uint32_t id_dp = idesc_bf16_f32(128, 128, false, false);
+    const uint32_t id_kv = idesc_bf16_f32(128, D, false, true);   // dV, dK: B = dO / Q, MN-major
+    const uint32_t id_dq = idesc_bf16_f32(128, D, true, true);    // dQ: A = dS (MN-major), B = K (MN-major)
+    // X = A_tile (rows in TMEM lanes) times B_tile^T, both K-major over d.
+    auto issue_kmajor = [&](uint32_t d_tmem, uint32_t a_base, uint32_t b_base, uint32_t idesc) {
+#pragma unroll
+      for (int k = 0; k < D / 16; ++k) {
+        const int a = k / (C::ATOM / 16), w = k % (C::ATOM / 16);
+        const uint64_t da = smem_desc(a_base + a * C::BOX + w * 32, 16, C::SBO, C::SWZ);
+        const uint64_t db = smem_desc(b_base + a * C::BOX + w * 32, 16, C::SBO, C::SWZ);
+        mma_ss(d_tmem, da, db, idesc, k > 0 ? 1u : 0u);
+      }
+    };
+    // B operand: a [128 rows][D] tile read MN-major, K = 16 rows per step.
+    auto b_mn = [&](uint32_t base, int k) {
+      return smem_desc(base + k * 16 * C::ATOM * 2, C::BOX, C::SBO, C::SWZ);
+    };
+    auto wait_all = [&](uint64_t* bar, uint32_t parity, uint32_t site) {
+      return __all_sync(0xffffffffu, guarded_wait(bar, parity, abort_flag, wd, site));
+    };
+    bool ok = true;
+    if (T > 0) {
+      ok = wait_all(&sh.kv_full, 0, kSiteBwdLoad) && wait_all(&sh.qdo_full[0], 0, kSiteBwdLoad);
+      if (ok && lane == 0) {
+        tc_fence_after();
+        issue_kmajor(tmem + C::TM_S, sK, sQ, id_s);
+        mma_commit(&sh.s_full);
+        issue_kmajor(tmem + C::TM_DP, sV, sDO, id_dp);
+        mma_commit(&sh.dp_full);
+      }
+      __syncwarp();
+    }
+    for (int t = 0; ok && t < T; ++t) {
+      const int st = t & 1;
+      const uint32_t q_off = st * C::TILE;
+      // dV += P^T dO
+      if (!(ok = wait_all(&sh.p_full, t & 1, kSiteBwdS))) break;
+      if (lane == 0) {
+        tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          mma_ts(tmem + C::TM_DV, tmem + C::TM_S + k * 8, b_mn(sDO + q_off, k), id_kv, (t > 0 || k > 0) ? 1u : 0u);
+      }
+      __syncwarp();
+      // next S^T while the compute warps form dS
+      if (t + 1 < T) {
+        if (!(ok = wait_all(&sh.qdo_full[st ^ 1], ((t + 1) >> 1) & 1, kSiteBwdLoad))) break;
+        if (lane == 0) {
+          issue_kmajor(tmem + C::TM_S, sK, sQ + (st ^ 1) * C::TILE, id_s);
+          mma_commit(&sh.s_full);
+        }
+        __syncwarp();
+      }
+      if (!(ok = wait_all(&sh.ds_full, t & 1, kSiteBwdDS))) break;
+      if (!C::ALIAS_DQ && t >= 1) {
+        if (!(ok = wait_all(&sh.dq_empty, (t - 1) & 1, kSiteBwdDQ))) break;
+      }
+      if (lane == 0) {
+        tc_fence_after();
+        // dK += dS^T Q : A = dS^T (K-major over queries), B = Q (MN-major)
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const uint64_t da = smem_desc(sDS + (k >> 2) * C::DS_REGION + (k & 3) * 32, 16, 1024, 2);
+          mma_ss(tmem + C::TM_DK, da, b_mn(sQ + q_off, k), id_kv, (t > 0 || k > 0) ? 1u : 0u);
+        }
+        // dQ = dS K : A = dS (MN-major: queries contiguous), B = K (MN-major)
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const uint64_t da = smem_desc(sDS + k * 16 * 128, C::DS_REGION, 1024, 2);
+          mma_ss(tmem + C::TM_DQ, da, b_mn(sK, k), id_dq, k > 0 ? 1u : 0u);
+        }
+        mma_commit(&sh.dq_full);
+        mma_commit(&sh.ds_empty);
+        mma_commit(&sh.qdo_empty[st]);
+      }
+      __syncwarp();
+      if (t + 1 < T) {
+        if (C::ALIAS_DQ) {
+          if (!(ok = wait_all(&sh.dq_empty, t & 1, kSiteBwdDQ))) break;
+        }
+        if (lane == 0) {
+          tc_fence_after();
+          issue_kmajor(tmem + C::TM_DP, sV, sDO + (st ^ 1) * C::TILE, id_dp);
+          mma_commit(&sh.dp_full);
+        }
+        __syncwarp();
+      }
+    }
+    if (lane == 0 && T > 0) mma_commit(&sh.dkv_full);
+    if (lane == 0) mma_commit(&sh.drain);
+    __syncwarp();
+    drain_wait_b(&sh.drain, 0, wd);
+  } else if (warp < 4) {
+    // ------------------------------------------------------------ P, dS, dK/dV epilogue
+    const int r = tid;                                 // key row within the tile = TMEM lane
+    const int key = k0 + r;
+    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    const uint32_t t_s = tmem + lane_base + C::TM_S;
+    const uint32_t t_dp = tmem + lane_base + C::TM_DP;
+    const float c = p.c;
+    const float* lse2_h = p.lse2 + static_cast<size_t>(bh) * p.n_pad;
+    const float* D_h = p.Dsum + static_cast<size_t>(bh) * p.n_pad;
+    uint8_t* ds_row0 = smem + C::OFF_DS + r * 128;     // region 0, row r
+    const int sw = r & 7;
+    bool ok = true;
+    for (int t = 0; t < T; ++t) {
+      const int q_row0 = (i_start + t) * 128;
+      // queries [lo, hi) of this tile may attend to this key
+      const int lo = p.causal ? max(0, key - q_row0) : 0;
+      const int hi = (key < p.m) ? min(128, p.n - q_row0) : 0;
+      const bool masked = __any_sync(0xffffffffu, lo > 0 || hi < 128);
+      ok = __all_sync(0xffffffffu, guarded_wait(&sh.s_full, t & 1, abort_flag, wd, kSiteBwdS));
+      if (!ok) break;
+      tc_fence_after();
+      // P^T, kept as packed bf16 pairs: the same values feed the dV product
+      // (from TMEM) and dS below.
+      uint32_t Pk[64];
+      {
+        uint32_t s[4][32];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) tmem_ld32(t_s + q * 32, s[q]);
+        tmem_ld_wait();
+        const float4* l4 = reinterpret_cast<const float4*>(lse2_h + q_row0);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+#pragma unroll
+          for (int i4 = 0; i4 < 8; ++i4) {
+            const float4 L = __ldg(l4 + q * 8 + i4);
+            const float Lv[4] = {L.x, L.y, L.z, L.w};
+            float pv[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const int col = q * 32 + i4 * 4 + u;
+              float x = fmaf(__uint_as_float(s[q][i4 * 4 + u]), c, -Lv[u]);
+              if (masked && (col < lo || col >= hi)) x = -INFINITY;
+              pv[u] = ex2f(x);
+            }
+            Pk[q * 16 + i4 * 2 + 0] = pack_bf16x2(pv[0], pv[1]);
+            Pk[q * 16 + i4 * 2 + 1] = pack_bf16x2(pv[2], pv[3]);
+          }
+        }
+      }
+      // P^T (bf16) into the S^T columns for the dV product
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) pk[i] = Pk[q * 16 + i];
+        tmem_st16(t_s + q * 16, pk);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(&sh.p_full);
+      // dS = P (dP - D)
+      ok = __all_sync(0xffffffffu, guarded_wait(&sh.dp_full, t & 1, abort_flag, wd, kSiteBwdDP));
+      if (!ok) break;
+      tc_fence_after();
+      if (t >= 1) {
+        ok = __all_sync(0xffffffffu, guarded_wait(&sh.ds_empty, (t - 1) & 1, abort_flag, wd, kSiteBwdDS));
+        if (!ok) break;
+      }
+      const float4* d4 = reinterpret_cast<const float4*>(D_h + q_row0);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        uint32_t dp[32];
+        tmem_ld32(t_dp + q * 32, dp);
+        tmem_ld_wait();
+        uint32_t pk[16];
+#pragma unroll
+        for (int i4 = 0; i4 < 8; ++i4) {
+          const float4 Dv = __ldg(d4 + q * 8 + i4);
+          const float2 p01 = unpack_bf16x2(Pk[q * 16 + i4 * 2 + 0]);
+          const float2 p23 = unpack_bf16x2(Pk[q * 16 + i4 * 2 + 1]);
+          const float ds0 = p01.x * (__uint_as_float(dp[i4 * 4 + 0]) - Dv.x);
+          const float ds1 = p01.y * (__uint_as_float(dp[i4 * 4 + 1]) - Dv.y);
+          const float ds2 = p23.x * (__uint_as_float(dp[i4 * 4 + 2]) - Dv.z);
+          const float ds3 = p23.y * (__uint_as_float(dp[i4 * 4 + 3]) - Dv.w);
+          pk[i4 * 2 + 0] = pack_bf16x2(ds0, ds1);
+          pk[i4 * 2 + 1] = pack_bf16x2(ds2, ds3);
+        }
+        // 32 queries = 4 chunks of 16 bytes; queries q*32.. land in region q/2, chunks (q&1)*4..+3
+        uint8_t* reg = ds_row0 + (q >> 1) * C::DS_REGION;
+#pragma unroll
+        for (int ch = 0; ch < 4; ++ch) {
+          const int chunk = (q & 1) * 4 + ch;
+          *reinterpret_cast<uint4*>(reg + ((chunk ^ sw) << 4)) =
+              make_uint4(pk[ch * 4], pk[ch * 4 + 1], pk[ch * 4 + 2], pk[ch * 4 + 3]);
+        }
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(&sh.ds_full);
+    }
+    // epilogue: dV and scale * dK rows of this key tile
+    if (ok) {
+      if (T > 0) {
+        ok = __all_sync(0xffffffffu, guarded_wait(&sh.dkv_full, 0, abort_flag, wd, kSiteBwdFinal));
+        tc_fence_after();
+      }
+      if (ok) {
+        const bool store = key < p.m;
+        const size_t off = (static_cast<size_t>(bh) * p.m + (store ? key : 0)) * D;
+        uint4* dv_row = reinterpret_cast<uint4*>(p.dv + off);
+        uint4* dk_row = reinterpret_cast<uint4*>(p.dk + off);
+#pragma unroll
+        for (int which = 0; which < 2; ++which) {
+          const float mul = which ? p.scale : 1.f;
+          uint4* dst = which ? dk_row : dv_row;
+#pragma unroll
+          for (int q = 0; q < D / 32; ++q) {
+            uint32_t v[32];
+            if (T > 0) {
+              tmem_ld32(tmem + lane_base + (which ? C::TM_DK : C::TM_DV) + q * 32, v);
+              tmem_ld_wait();
+            } else {
+#pragma unroll
+              for (int i = 0; i < 32; ++i) v[i] = 0u;
+            }
+            uint32_t pk[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              pk[i] = pack_bf16x2(__uint_as_float(v[2 * i]) * mul, __uint_as_float(v[2 * i + 1]) * mul);
+            if (store) {
+#pragma unroll
+              for (int u = 0; u < 4; ++u)
+                dst[q * 4 + u] = make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+            }
+          }
+        }
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ dQ accumulation (warps 4-7)
+    const int r = tid - 128;                           // query row within the tile = TMEM lane
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t t_dq = tmem + lane_base + C::TM_DQ;
+    for (int t = 0; t < T; ++t) {
+      const int qrow = (i_start + t) * 128 + r;
+      if (!__all_sync(0xffffffffu, guarded_wait(&sh.dq_full, t & 1, abort_flag, wd, kSiteBwdDQ))) break;
+      tc_fence_after();
+      float4* acc = reinterpret_cast<float4*>(p.dq_acc + (static_cast<size_t>(bh) * p.n_pad + qrow) * D);
+#pragma unroll
+      for (int q = 0; q < D / 32; ++q) {
+        uint32_t v[32];
+        tmem_ld32(t_dq + q * 32, v);
+        tmem_ld_wait();
+        if (qrow < p.n) {
+#pragma unroll
+          for (int u = 0; u < 8; ++u)
+            atomicAdd(acc + q * 8 + u, make_float4(__uint_as_float(v[4 * u]), __uint_as_float(v[4 * u + 1]),
+                                                   __uint_as_float(v[4 * u + 2]), __uint_as_float(v[4 * u + 3])));
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&sh.dq_empty);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    tc_fence_after();
+    tmem_dealloc<512>(tmem);
+  }
+}
+
+template <int D>
+cudaError_t launch_bwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                         const CUtensorMap& tdo, const BwdPreParams& pre, const BwdParams& p,
+                         const BwdPostParams& post, int BH, cudaStream_t stream) {
+  using C = Bwd<D>;
+  static std::once_flag once[64];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  cudaError_t attr = cudaSuccess;
+  std::call_once(once[dev & 63], [&] {
+    attr = cudaFuncSetAttribute(attn_bwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                static_cast<int>(C::SMEM));
+  });
+  if (attr != cudaSuccess) return attr;
+  {
+    constexpr int RPB = 256 / (D / 8);
+    const long long rows = static_cast<long long>(pre.BH) * pre.n_pad;
+    const unsigned blocks = static_cast<unsigned>((rows + RPB - 1) / RPB);
+    prof_begin(kKindBwdPre, stream);
+    attn_bwd_pre_kernel<D><<<blocks, 256, 0, stream>>>(pre);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    prof_end(kKindBwdPre, stream);
+  }
+  {
+    dim3 grid(static_cast<unsigned>(BH), static_cast<unsigned>(p.num_kblocks));
+    prof_begin(kKindBwdMain, stream);
+    attn_bwd_kernel<D><<<grid, C::THREADS, C::SMEM, stream>>>(tq, tk, tv, tdo, p);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    prof_end(kKindBwdMain, stream);
+  }
+  {
+    const long long chunks = static_cast<long long>(post.BH) * post.n * (D / 8);
+    const unsigned blocks = static_cast<unsigned>((chunks + 255) / 256);
+    prof_begin(kKindBwdPost, stream);
+    attn_bwd_post_kernel<D><<<blocks, 256, 0, stream>>>(post);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    prof_end(kKindBwdPost, stream);
+  }
+  return cudaSuccess;
+}
+
+}  // namespace
+
+cudaError_t launch_bwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                       const CUtensorMap& tdo, const BwdPreParams& pre, const BwdParams& p,
+                       const BwdPostParams& post, int BH, cudaStream_t stream) {
+  switch (d) {
+    case 32: return launch_bwd_d<32>(tq, tk, tv, tdo, pre, p, post, BH, stream);
+    case 64: return launch_bwd_d<64>(tq, tk, tv, tdo, pre, p, post, BH, stream);
+    case 128: return launch_bwd_d<128>(tq, tk, tv, tdo, pre, p, post, BH, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace attn

@@ -1,0 +1,106 @@
+// Internal declarations shared by the attention kernels and the C-ABI host code.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <cstdint>
+
+#include "sm103_ptx.cuh"
+
+namespace attn {
+
+// Device error word values (0 = no error). The low byte names the wait site.
+constexpr uint32_t kDevTimeout = 0x100u;
+
+// Sites, for diagnosis of a watchdog report.
+enum WaitSite : uint32_t {
+  kSiteQFull = 1, kSiteKFull, kSiteVFull, kSiteKEmpty, kSiteVEmpty, kSiteSFull,
+  kSitePFull, kSiteOFull, kSiteDrain, kSiteBwdLoad, kSiteBwdS, kSiteBwdDP, kSiteBwdDS,
+  kSiteBwdDQ, kSiteBwdFree, kSiteBwdFinal
+};
+
+struct Watchdog {
+  uint32_t* status;      // device error word (global)
+  uint64_t budget_ns;    // per-wait limit
+};
+
+// Bounded mbarrier wait. Returns false when the CTA is aborting or this wait
+// ran out of time (in which case it raises the CTA abort flag and records the
+// site in the device error word). Never traps, never spins forever.
+__device__ __forceinline__ bool guarded_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                             const Watchdog& wd, uint32_t site) {
+  if (sm103::mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = sm103::global_timer_ns();
+  while (true) {
+    if (sm103::mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (sm103::global_timer_ns() - t0 > wd.budget_ns) {
+      *abort_flag = 1;
+      atomicCAS(wd.status, 0u, kDevTimeout | site);
+      return false;
+    }
+  }
+}
+
+// Profiling hooks (implemented with the C ABI): bracket one kernel launch
+// with CUDA events on `stream` when profiling is enabled; no-ops otherwise.
+enum KernelKind : int { kKindFwd = 0, kKindBwdPre = 1, kKindBwdMain = 2, kKindBwdPost = 3, kNumKinds = 4 };
+void prof_begin(int kind, cudaStream_t stream);
+void prof_end(int kind, cudaStream_t stream);
+
+// ---------------------------------------------------------------- forward
+
+struct FwdParams {
+  __nv_bfloat16* o;   // [BH, n, d]
+  float* lse;         // [BH, n] or nullptr
+  int n, m;           // queries, keys per head
+  int causal;
+  int neg;            // scale < 0: the score MMA negates Q K^T so that c >= 0
+  float c;            // |scale| * log2(e)
+  int num_qblocks;    // ceil(n / 256)
+  int inject;         // test hook: 1 = skip the first value-tile load
+  Watchdog wd;
+};
+
+cudaError_t launch_fwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                       const FwdParams& p, int BH, cudaStream_t stream);
+
+// ---------------------------------------------------------------- backward
+
+struct BwdPreParams {
+  const __nv_bfloat16* o;   // [BH, n, d]
+  const __nv_bfloat16* dO;  // [BH, n, d]
+  const float* lse;         // [BH, n]
+  float* lse2;              // [BH, n_pad]  lse * log2(e)  (padding rows: +inf)
+  float* Dsum;              // [BH, n_pad]  D_i = sum_c dO_ic O_ic (padding rows: 0)
+  float* dq_acc;            // [BH, n_pad, d] zeroed here
+  int n, n_pad, d, BH;
+};
+
+struct BwdParams {
+  __nv_bfloat16* dk;        // [BH, m, d]
+  __nv_bfloat16* dv;        // [BH, m, d]
+  const float* lse2;        // [BH, n_pad]
+  const float* Dsum;        // [BH, n_pad]
+  float* dq_acc;            // [BH, n_pad, d]
+  int n, m, n_pad;
+  int causal, neg;
+  float c;                  // |scale| * log2(e)
+  float scale;              // signed scale, applied to dK
+  int num_kblocks;          // ceil(m / 128)
+  Watchdog wd;
+};
+
+struct BwdPostParams {
+  const float* dq_acc;      // [BH, n_pad, d]
+  __nv_bfloat16* dq;        // [BH, n, d]
+  float scale;
+  int n, n_pad, d, BH;
+};
+
+cudaError_t launch_bwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                       const CUtensorMap& tdo, const BwdPreParams& pre, const BwdParams& p,
+                       const BwdPostParams& post, int BH, cudaStream_t stream);
+
+}  // namespace attn
