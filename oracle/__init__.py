@@ -13,6 +13,7 @@ Functions:
   weights(q, k, causal, scale)             -> (S, P) of one head       (§3.2.1, Fig. 2)
   fwd(q, k, v, causal, scale, rows=None)   -> (O, lse)                 (eq. (1))
   bwd(q, k, v, dO, causal, scale)          -> (dQ, dK, dV, O, lse)     (derivative of eq. (1))
+  bwd_rows(q, k, v, dO, causal, scale, qrows, krows) -> sampled rows of one head
 """
 from __future__ import annotations
 
@@ -58,6 +59,9 @@ def _load():
             lib.oracle_attn_fwd.argtypes = [dp, dp, dp, dp, dp, L, L, L, L, L, L, I, D, lp, L]
             lib.oracle_attn_bwd.argtypes = [dp, dp, dp, dp, dp, dp, dp, dp, dp,
                                             L, L, L, L, L, L, I, D]
+            lib.oracle_attn_bwd_rows.argtypes = [dp, dp, dp, dp, L, L, L, L, I, D, lp, L, dp,
+                                                 lp, L, dp, dp]
+            lib.oracle_attn_bwd_rows.restype = ctypes.c_int
             for f in (lib.oracle_attn_weights, lib.oracle_attn_fwd, lib.oracle_attn_bwd):
                 f.restype = ctypes.c_int
             lib.oracle_num_threads.restype = ctypes.c_int
@@ -161,3 +165,24 @@ def bwd(q, k, v, dO, causal: bool, scale: float, need=("dq", "dk", "dv")):
 
     return (shp(dQ, lead_q, n, dk), shp(dK, lead_k, m, dk), shp(dV, lead_k, m, dv),
             O.reshape(lead_q + (n, dv)), lse.reshape(lead_q + (n,)))
+
+
+def bwd_rows(q, k, v, dO, causal: bool, scale: float, qrows=(), krows=()):
+    """Sampled backward of ONE head: (dQ[qrows], dK[krows], dV[krows]), fp64.
+
+    q, dO: [n, d]; k, v: [m, d]. Key rows cost a full forward of the head.
+    """
+    Q, K, V, G = _f64(q), _f64(k), _f64(v), _f64(dO)
+    n, dk = Q.shape
+    m, dv = K.shape[0], V.shape[1]
+    qr = np.ascontiguousarray(np.asarray(qrows, dtype=np.int64).reshape(-1))
+    kr = np.ascontiguousarray(np.asarray(krows, dtype=np.int64).reshape(-1))
+    dQ = np.empty((max(qr.size, 1), dk))
+    dK = np.empty((max(kr.size, 1), dk))
+    dV = np.empty((max(kr.size, 1), dv))
+    lp = ctypes.POINTER(ctypes.c_long)
+    _check(_load().oracle_attn_bwd_rows(
+        _ptr(Q), _ptr(K), _ptr(V), _ptr(G), n, m, dk, dv, int(causal), float(scale),
+        qr.ctypes.data_as(lp), qr.size, _ptr(dQ), kr.ctypes.data_as(lp), kr.size, _ptr(dK),
+        _ptr(dV)), "bwd_rows")
+    return dQ[: qr.size], dK[: kr.size], dV[: kr.size]

@@ -173,6 +173,69 @@ int oracle_attn_fwd(const double *q, const double *k, const double *v,
 }
 
 /*
+ * Backward, one query row i of one head: the forward row (P_i., O_i,
+ * lse_i), D_i = dO_i . O_i and, if dqi != NULL,
+ * dQ_i = scale sum_j P_ij (dO_i . v_j - D_i) k_j.
+ * row (m doubles) and oi (dv doubles) are scratch.
+ */
+static void bwd_query_row(const double *Q, const double *K, const double *V,
+                          const double *dOi, long i, long m, long dk, long dv,
+                          int causal, double scale, double *row, double *oi,
+                          double *lse_i, double *D_i, double *dqi) {
+    score_row(Q + i * dk, K, m, dk, scale, visible_keys(i, m, causal), row);
+    const double l = softmax_row(row, m);
+    weighted_sum(row, V, m, dv, oi);
+    double Di = 0.0;
+    for (long c = 0; c < dv; ++c) Di += dOi[c] * oi[c];
+    *lse_i = l;
+    *D_i = Di;
+    if (dqi) {
+        for (long c = 0; c < dk; ++c) dqi[c] = 0.0;
+        for (long j = 0; j < m; ++j) {
+            if (row[j] == 0.0) continue; /* P_ij = 0 => dS_ij = 0 */
+            const double *vj = V + j * dv;
+            double dP = 0.0;
+            for (long c = 0; c < dv; ++c) dP += dOi[c] * vj[c];
+            const double dS = row[j] * (dP - Di);
+            const double *kj = K + j * dk;
+            for (long c = 0; c < dk; ++c) dqi[c] += dS * kj[c];
+        }
+        for (long c = 0; c < dk; ++c) dqi[c] *= scale;
+    }
+}
+
+/*
+ * Backward, one key row j of one head, given lse_i and D_i of every query:
+ * dK_j = scale sum_i dS_ij q_i and dV_j = sum_i P_ij dO_i with
+ * P_ij = exp(s_ij - lse_i) (the softmax written through its normaliser).
+ * Either output may be NULL.
+ */
+static void bwd_key_row(const double *Q, const double *kj, const double *vj,
+                        const double *dO, const double *lse, const double *D,
+                        long j, long n, long m, long dk, long dv, int causal,
+                        double scale, double *dkj, double *dvj) {
+    if (dkj) for (long c = 0; c < dk; ++c) dkj[c] = 0.0;
+    if (dvj) for (long c = 0; c < dv; ++c) dvj[c] = 0.0;
+    for (long i = 0; i < n; ++i) {
+        if (j >= visible_keys(i, m, causal)) continue; /* masked: P_ij = 0 */
+        const double *qi = Q + i * dk;
+        const double *dOi = dO + i * dv;
+        double dot = 0.0;
+        for (long c = 0; c < dk; ++c) dot += qi[c] * kj[c];
+        const double P = exp(scale * dot - lse[i]);
+        if (dvj)
+            for (long c = 0; c < dv; ++c) dvj[c] += P * dOi[c];
+        if (dkj) {
+            double dP = 0.0;
+            for (long c = 0; c < dv; ++c) dP += dOi[c] * vj[c];
+            const double dS = P * (dP - D[i]);
+            for (long c = 0; c < dk; ++c) dkj[c] += dS * qi[c];
+        }
+    }
+    if (dkj) for (long c = 0; c < dk; ++c) dkj[c] *= scale;
+}
+
+/*
  * Backward pass: gradients of L = sum(dO * O) with respect to q, k and v,
  * for O from oracle_attn_fwd on the same inputs.
  * dq: [B,h,n,dk], dk_out: [B,h,m,dk], dv_out: [B,h,m,dv]; each may be NULL
@@ -180,8 +243,7 @@ int oracle_attn_fwd(const double *q, const double *k, const double *v,
  * backward used.
  *
  * Pass 1 (per query row i): P_i., O_i, lse_i, D_i and dQ_i.
- * Pass 2 (per key row j): dK_j and dV_j, with P_ij = exp(s_ij - lse_i)
- * (the softmax of pass 1 written through its normaliser) and dS_ij as above.
+ * Pass 2 (per key row j): dK_j and dV_j.
  */
 int oracle_attn_bwd(const double *q, const double *k, const double *v,
                     const double *dO, double *dq, double *dk_out,
@@ -206,72 +268,91 @@ int oracle_attn_bwd(const double *q, const double *k, const double *v,
 #pragma omp atomic write
             status = ORACLE_ERR_NOMEM;
         }
-        /* pass 1: forward row, D_i and dQ_i */
 #pragma omp for collapse(2) schedule(dynamic, 4)
         for (long bh = 0; bh < heads; ++bh) {
             for (long i = 0; i < n; ++i) {
                 if (!row || !oi) continue;
-                const double *Q = q + bh * n * dk;
-                const double *K = k + bh * m * dk;
-                const double *V = v + bh * m * dv;
-                const double *dOi = dO + (bh * n + i) * dv;
-                score_row(Q + i * dk, K, m, dk, scale, visible_keys(i, m, causal), row);
-                const double l = softmax_row(row, m);
-                weighted_sum(row, V, m, dv, oi);
-                double Di = 0.0;
-                for (long c = 0; c < dv; ++c) Di += dOi[c] * oi[c];
-                lse[bh * n + i] = l;
-                D[bh * n + i] = Di;
+                bwd_query_row(q + bh * n * dk, k + bh * m * dk, v + bh * m * dv,
+                              dO + (bh * n + i) * dv, i, m, dk, dv, causal, scale,
+                              row, oi, &lse[bh * n + i], &D[bh * n + i],
+                              dq ? dq + (bh * n + i) * dk : NULL);
                 if (o_out) memcpy(o_out + (bh * n + i) * dv, oi, sizeof(double) * (size_t)dv);
-                if (lse_out) lse_out[bh * n + i] = l;
-                if (dq) {
-                    double *dqi = dq + (bh * n + i) * dk;
-                    for (long c = 0; c < dk; ++c) dqi[c] = 0.0;
-                    for (long j = 0; j < m; ++j) {
-                        if (row[j] == 0.0) continue; /* P_ij = 0 => dS_ij = 0 */
-                        const double *vj = V + j * dv;
-                        double dP = 0.0;
-                        for (long c = 0; c < dv; ++c) dP += dOi[c] * vj[c];
-                        const double dS = row[j] * (dP - Di);
-                        const double *kj = K + j * dk;
-                        for (long c = 0; c < dk; ++c) dqi[c] += dS * kj[c];
-                    }
-                    for (long c = 0; c < dk; ++c) dqi[c] *= scale;
-                }
+                if (lse_out) lse_out[bh * n + i] = lse[bh * n + i];
             }
         }
         /* implicit barrier: lse and D are complete */
-        /* pass 2: dK_j and dV_j */
         if (dk_out || dv_out) {
 #pragma omp for collapse(2) schedule(dynamic, 4)
             for (long bh = 0; bh < heads; ++bh) {
                 for (long j = 0; j < m; ++j) {
-                    const double *Q = q + bh * n * dk;
-                    const double *kj = k + (bh * m + j) * dk;
-                    const double *vj = v + (bh * m + j) * dv;
-                    double *dkj = dk_out ? dk_out + (bh * m + j) * dk : NULL;
-                    double *dvj = dv_out ? dv_out + (bh * m + j) * dv : NULL;
-                    if (dkj) for (long c = 0; c < dk; ++c) dkj[c] = 0.0;
-                    if (dvj) for (long c = 0; c < dv; ++c) dvj[c] = 0.0;
-                    for (long i = 0; i < n; ++i) {
-                        if (j >= visible_keys(i, m, causal)) continue; /* masked: P_ij = 0 */
-                        const double *qi = Q + i * dk;
-                        const double *dOi = dO + (bh * n + i) * dv;
-                        double dot = 0.0;
-                        for (long c = 0; c < dk; ++c) dot += qi[c] * kj[c];
-                        const double P = exp(scale * dot - lse[bh * n + i]);
-                        if (dvj)
-                            for (long c = 0; c < dv; ++c) dvj[c] += P * dOi[c];
-                        if (dkj) {
-                            double dP = 0.0;
-                            for (long c = 0; c < dv; ++c) dP += dOi[c] * vj[c];
-                            const double dS = P * (dP - D[bh * n + i]);
-                            for (long c = 0; c < dk; ++c) dkj[c] += dS * qi[c];
-                        }
-                    }
-                    if (dkj) for (long c = 0; c < dk; ++c) dkj[c] *= scale;
+                    bwd_key_row(q + bh * n * dk, k + (bh * m + j) * dk, v + (bh * m + j) * dv,
+                                dO + bh * n * dv, lse + bh * n, D + bh * n, j, n, m, dk, dv,
+                                causal, scale, dk_out ? dk_out + (bh * m + j) * dk : NULL,
+                                dv_out ? dv_out + (bh * m + j) * dv : NULL);
                 }
             }
+        }
+        free(row);
+        free(oi);
+    }
+    free(lse);
+    free(D);
+    return status;
+}
+
+/*
+ * Sampled backward of ONE head (q: n x dk, k: m x dk, v: m x dv, dO: n x dv):
+ * dQ for the listed query rows (dq_out: nq x dk) and dK, dV for the listed
+ * key rows (dk_out: nk x dk, dv_out: nk x dv). Same arithmetic as
+ * oracle_attn_bwd row by row; key rows need lse and D of all n queries, so
+ * they cost a full forward of the head.
+ */
+int oracle_attn_bwd_rows(const double *q, const double *k, const double *v,
+                         const double *dO, long n, long m, long dk, long dv,
+                         int causal, double scale, const long *qrows, long nq,
+                         double *dq_out, const long *krows, long nk,
+                         double *dk_out, double *dv_out) {
+    if (check_dims(1, 1, n, m, dk, dv) != ORACLE_OK || nq < 0 || nk < 0) return ORACLE_ERR_ARG;
+    for (long r = 0; r < nq; ++r)
+        if (qrows[r] < 0 || qrows[r] >= n) return ORACLE_ERR_ARG;
+    for (long r = 0; r < nk; ++r)
+        if (krows[r] < 0 || krows[r] >= m) return ORACLE_ERR_ARG;
+    const long nall = nk > 0 ? n : 0;
+    double *lse = (double *)malloc(sizeof(double) * (size_t)(nall + 1));
+    double *D = (double *)malloc(sizeof(double) * (size_t)(nall + 1));
+    if (!lse || !D) {
+        free(lse);
+        free(D);
+        return ORACLE_ERR_NOMEM;
+    }
+    int status = ORACLE_OK;
+#pragma omp parallel
+    {
+        double *row = (double *)malloc(sizeof(double) * (size_t)m);
+        double *oi = (double *)malloc(sizeof(double) * (size_t)dv);
+        if (!row || !oi) {
+#pragma omp atomic write
+            status = ORACLE_ERR_NOMEM;
+        }
+#pragma omp for schedule(dynamic, 4)
+        for (long r = 0; r < nq; ++r) {
+            if (!row || !oi) continue;
+            double l, Di;
+            const long i = qrows[r];
+            bwd_query_row(q, k, v, dO + i * dv, i, m, dk, dv, causal, scale, row, oi, &l, &Di,
+                          dq_out + r * dk);
+        }
+#pragma omp for schedule(dynamic, 16)
+        for (long i = 0; i < nall; ++i) {
+            if (!row || !oi) continue;
+            bwd_query_row(q, k, v, dO + i * dv, i, m, dk, dv, causal, scale, row, oi, &lse[i],
+                          &D[i], NULL);
+        }
+#pragma omp for schedule(dynamic, 1)
+        for (long r = 0; r < nk; ++r) {
+            const long j = krows[r];
+            bwd_key_row(q, k + j * dk, v + j * dv, dO, lse, D, j, n, m, dk, dv, causal, scale,
+                        dk_out + r * dk, dv_out + r * dv);
         }
         free(row);
         free(oi);

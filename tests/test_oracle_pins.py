@@ -282,3 +282,19 @@ def test_against_torch_cpu_fp64_library(causal, n, m, dk, dv):
     np.testing.assert_allclose(dQ, q.grad.numpy(), rtol=1e-10, atol=1e-12)
     np.testing.assert_allclose(dK, k.grad.numpy(), rtol=1e-10, atol=1e-12)
     np.testing.assert_allclose(dV, v.grad.numpy(), rtol=1e-10, atol=1e-12)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_sampled_backward_rows_equal_full_backward(causal):
+    """The sampled entry point (used at full sizes) returns the same rows as the full backward."""
+    n, m, d = 40, 33, 8
+    q = normal_bf16((n, d), 71).double().numpy()
+    k = normal_bf16((m, d), 72).double().numpy()
+    v = normal_bf16((m, d), 73).double().numpy()
+    dO = normal_bf16((n, d), 74).double().numpy()
+    dQ, dK, dV, _, _ = oracle.bwd(q, k, v, dO, causal, 0.3)
+    qr, kr = [0, 7, 39], [0, 5, 32]
+    sq, sk, sv = oracle.bwd_rows(q, k, v, dO, causal, 0.3, qr, kr)
+    np.testing.assert_array_equal(sq, dQ[qr])
+    np.testing.assert_array_equal(sk, dK[kr])
+    np.testing.assert_array_equal(sv, dV[kr])

@@ -121,7 +121,9 @@ struct Bwd {
   static constexpr uint32_t OFF_DS = 6 * TILE;         // dS^T: 2 regions [128 keys][64 queries], 128B swizzle
   static constexpr uint32_t DS_REGION = 128u * 64u * 2u;
   static constexpr uint32_t SMEM = OFF_DS + 2 * DS_REGION + 1024;
-  static constexpr int THREADS = 320;
+  static constexpr int THREADS = 384;   // 3 warpgroups; warps 10-11 only balance the register split
+  // setmaxnreg split (registers per thread): compute, dQ, producer/MMA warpgroups.
+  static constexpr int REG_COMPUTE = 240, REG_DQ = 96, REG_OTHER = 88;
   static constexpr bool ALIAS_DQ = (D > 64);
   static constexpr uint32_t TM_S = 0, TM_DP = 128, TM_DV = 256, TM_DK = 256 + D;
   static constexpr uint32_t TM_DQ = ALIAS_DQ ? 128u : (256u + 2u * D);
@@ -153,7 +155,7 @@ __device__ __forceinline__ void drain_wait_b(uint64_t* bar, uint32_t parity, con
 }
 
 template <int D>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(384, 1)
 attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                 const BwdParams p) {
@@ -206,6 +208,9 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   tc_fence_after();
   const uint32_t tmem = sh.tmem_base;
 
+  if (warp >= 8) {
+    reg_dealloc<C::REG_OTHER>();
+  }
   if (warp == 8) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0 && T > 0) {
@@ -329,8 +334,11 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     if (lane == 0) mma_commit(&sh.drain);
     __syncwarp();
     drain_wait_b(&sh.drain, 0, wd);
+  } else if (warp >= 10) {
+    // idle warps: they only complete the third warpgroup for the register split
   } else if (warp < 4) {
     // ------------------------------------------------------------ P, dS, dK/dV epilogue
+    reg_alloc<C::REG_COMPUTE>();
     const int r = tid;                                 // key row within the tile = TMEM lane
     const int key = k0 + r;
     const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
@@ -351,9 +359,9 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       ok = __all_sync(0xffffffffu, guarded_wait(&sh.s_full, t & 1, abort_flag, wd, kSiteBwdS));
       if (!ok) break;
       tc_fence_after();
-      // P^T, kept as packed bf16 pairs: the same values feed the dV product
-      // (from TMEM) and dS below.
-      uint32_t Pk[64];
+      // P^T in fp32: dS below uses the unrounded weights; the dV product
+      // takes them rounded to bf16 (written into the S^T columns of TMEM).
+      float P[128];
       {
         uint32_t s[4][32];
 #pragma unroll
@@ -366,25 +374,21 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           for (int i4 = 0; i4 < 8; ++i4) {
             const float4 L = __ldg(l4 + q * 8 + i4);
             const float Lv[4] = {L.x, L.y, L.z, L.w};
-            float pv[4];
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
               const int col = q * 32 + i4 * 4 + u;
               float x = fmaf(__uint_as_float(s[q][i4 * 4 + u]), c, -Lv[u]);
               if (masked && (col < lo || col >= hi)) x = -INFINITY;
-              pv[u] = ex2f(x);
+              P[col] = ex2f(x);
             }
-            Pk[q * 16 + i4 * 2 + 0] = pack_bf16x2(pv[0], pv[1]);
-            Pk[q * 16 + i4 * 2 + 1] = pack_bf16x2(pv[2], pv[3]);
           }
         }
       }
-      // P^T (bf16) into the S^T columns for the dV product
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         uint32_t pk[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) pk[i] = Pk[q * 16 + i];
+        for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(P[q * 32 + 2 * i], P[q * 32 + 2 * i + 1]);
         tmem_st16(t_s + q * 16, pk);
       }
       tmem_st_wait();
@@ -408,12 +412,10 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 #pragma unroll
         for (int i4 = 0; i4 < 8; ++i4) {
           const float4 Dv = __ldg(d4 + q * 8 + i4);
-          const float2 p01 = unpack_bf16x2(Pk[q * 16 + i4 * 2 + 0]);
-          const float2 p23 = unpack_bf16x2(Pk[q * 16 + i4 * 2 + 1]);
-          const float ds0 = p01.x * (__uint_as_float(dp[i4 * 4 + 0]) - Dv.x);
-          const float ds1 = p01.y * (__uint_as_float(dp[i4 * 4 + 1]) - Dv.y);
-          const float ds2 = p23.x * (__uint_as_float(dp[i4 * 4 + 2]) - Dv.z);
-          const float ds3 = p23.y * (__uint_as_float(dp[i4 * 4 + 3]) - Dv.w);
+          const float ds0 = P[q * 32 + i4 * 4 + 0] * (__uint_as_float(dp[i4 * 4 + 0]) - Dv.x);
+          const float ds1 = P[q * 32 + i4 * 4 + 1] * (__uint_as_float(dp[i4 * 4 + 1]) - Dv.y);
+          const float ds2 = P[q * 32 + i4 * 4 + 2] * (__uint_as_float(dp[i4 * 4 + 2]) - Dv.z);
+          const float ds3 = P[q * 32 + i4 * 4 + 3] * (__uint_as_float(dp[i4 * 4 + 3]) - Dv.w);
           pk[i4 * 2 + 0] = pack_bf16x2(ds0, ds1);
           pk[i4 * 2 + 1] = pack_bf16x2(ds2, ds3);
         }
@@ -470,6 +472,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     }
   } else {
     // ------------------------------------------------------------ dQ accumulation (warps 4-7)
+    reg_dealloc<C::REG_DQ>();
     const int r = tid - 128;                           // query row within the tile = TMEM lane
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t t_dq = tmem + lane_base + C::TM_DQ;
@@ -518,6 +521,18 @@ cudaError_t launch_bwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
                                 static_cast<int>(C::SMEM));
   });
   if (attr != cudaSuccess) return attr;
+  {
+    // setmaxnreg.inc waits until registers are free: the split must fit in the
+    // registers the CTA is launched with, or the kernel would never proceed.
+    static int regs_per_thread[64] = {0};
+    if (regs_per_thread[dev & 63] == 0) {
+      cudaFuncAttributes fa;
+      if ((e = cudaFuncGetAttributes(&fa, attn_bwd_kernel<D>)) != cudaSuccess) return e;
+      regs_per_thread[dev & 63] = fa.numRegs;
+    }
+    const int need = 128 * (C::REG_COMPUTE + C::REG_DQ + C::REG_OTHER);
+    if (regs_per_thread[dev & 63] * C::THREADS < need) return cudaErrorInvalidConfiguration;
+  }
   {
     constexpr int RPB = 256 / (D / 8);
     const long long rows = static_cast<long long>(pre.BH) * pre.n_pad;
