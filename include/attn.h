@@ -115,6 +115,14 @@ int attn_set_watchdog_ns(unsigned long long budget_ns);
 int attn_debug_inject(int mode);
 
 /*
+ * Test hook: y_poly[i] = 2^x[i] computed by the forward kernel's FMA-pipe
+ * polynomial, y_mufu[i] = 2^x[i] by the hardware approximation (ex2.approx),
+ * for n device floats (either output may be NULL). Enqueued on `stream`.
+ * Returns ATTN_OK, ATTN_ERR_INVALID_ARG (null x, n < 0) or ATTN_ERR_CUDA.
+ */
+int attn_debug_exp2(const float* x, float* y_poly, float* y_mufu, int n, attn_stream_t stream);
+
+/*
  * Per-kernel device timing, for profiling. While enabled (on != 0), every
  * kernel that attn_fwd / attn_bwd launches is bracketed by two CUDA events
  * recorded on the caller's stream. attn_profile_read synchronises the

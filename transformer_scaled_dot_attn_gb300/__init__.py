@@ -26,7 +26,7 @@ __all__ = [
     "ATTN_ERR_TIMEOUT", "load_library", "library_path", "attn_fwd", "attn_bwd",
     "attn_bwd_workspace_bytes", "attn_get_device_status", "attn_status_string",
     "attn_set_watchdog_ns", "attn_debug_inject", "attn_profile_enable", "attn_profile_read",
-    "EXPORTED_SYMBOLS", "KERNEL_KINDS",
+    "attn_debug_exp2", "EXPORTED_SYMBOLS", "KERNEL_KINDS",
 ]
 
 ATTN_OK = 0
@@ -39,7 +39,7 @@ ATTN_ERR_TIMEOUT = 4
 EXPORTED_SYMBOLS = (
     "attn_fwd", "attn_bwd", "attn_bwd_workspace_bytes", "attn_get_device_status",
     "attn_status_string", "attn_set_watchdog_ns", "attn_debug_inject", "attn_profile_enable",
-    "attn_profile_read",
+    "attn_profile_read", "attn_debug_exp2",
 )
 
 # Kernel kinds of attn_profile_read.
@@ -89,6 +89,8 @@ def load_library():
         lib.attn_set_watchdog_ns.restype = I
         lib.attn_debug_inject.argtypes = [I]
         lib.attn_debug_inject.restype = I
+        lib.attn_debug_exp2.argtypes = [vp, vp, vp, I, vp]
+        lib.attn_debug_exp2.restype = I
         lib.attn_profile_enable.argtypes = [I]
         lib.attn_profile_enable.restype = I
         lib.attn_profile_read.argtypes = [I, ctypes.POINTER(I), ctypes.POINTER(ctypes.c_double)]
@@ -219,3 +221,15 @@ def attn_profile_read(kind) -> Tuple[int, float]:
     if st != ATTN_OK:
         raise AttnError(st, "attn_profile_read")
     return int(n.value), float(ms.value)
+
+
+def attn_debug_exp2(x, stream=None):
+    """(2^x by the forward's FMA-pipe polynomial, 2^x by ex2.approx) for a CUDA fp32 tensor."""
+    import torch
+    _check_tensor("x", x, dtype=torch.float32)
+    yp = torch.empty_like(x)
+    ym = torch.empty_like(x)
+    st = load_library().attn_debug_exp2(_vptr(x), _vptr(yp), _vptr(ym), x.numel(), _stream_handle(stream))
+    if st != ATTN_OK:
+        raise AttnError(st, "attn_debug_exp2")
+    return yp, ym

@@ -66,10 +66,11 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// 3-D map over a [BH, S, d] bf16 tensor: box = (atom, 128 rows, 1 head).
+// 3-D map over a [BH, S, d] bf16 tensor: box = (atom, box_rows, 1 head).
 // Rows past S read as zero (out-of-bounds fill), so ragged tiles never touch
 // the next head.
-bool make_tile_map(CUtensorMap* map, const void* base, long long BH, long long S, int d) {
+bool make_tile_map(CUtensorMap* map, const void* base, long long BH, long long S, int d,
+                   int box_rows = 128) {
   EncodeTiledFn enc = encode_fn();
   if (enc == nullptr) return false;
   const int atom = d >= 64 ? 64 : d;
@@ -77,7 +78,7 @@ bool make_tile_map(CUtensorMap* map, const void* base, long long BH, long long S
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(S),
                         static_cast<cuuint64_t>(BH)};
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(S) * d * 2};
-  cuuint32_t box[3] = {static_cast<cuuint32_t>(atom), 128u, 1u};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(atom), static_cast<cuuint32_t>(box_rows), 1u};
   cuuint32_t estr[3] = {1u, 1u, 1u};
   CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -171,6 +172,14 @@ void prof_end(int kind, cudaStream_t stream) {
 
 extern "C" {
 
+int attn_debug_exp2(const float* x, float* y_poly, float* y_mufu, int n, attn_stream_t stream) {
+  if (x == nullptr || n < 0) return ATTN_ERR_INVALID_ARG;
+  return attn::launch_exp2_probe(x, y_poly, y_mufu, n, reinterpret_cast<cudaStream_t>(stream)) ==
+                 cudaSuccess
+             ? ATTN_OK
+             : ATTN_ERR_CUDA;
+}
+
 int attn_profile_enable(int on) {
   g_prof_on.store(on ? 1 : 0);
   return ATTN_OK;
@@ -220,8 +229,9 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
   if (lse != nullptr && (reinterpret_cast<uintptr_t>(lse) & 3u) != 0) return ATTN_ERR_INVALID_ARG;
   const long long BH = static_cast<long long>(B) * h;
   CUtensorMap tq, tk, tv;
-  if (!make_tile_map(&tq, q, BH, n, d_k) || !make_tile_map(&tk, k, BH, m, d_k) ||
-      !make_tile_map(&tv, v, BH, m, d_v))
+  const int bn = attn::fwd_key_tile(d_k, n);
+  if (!make_tile_map(&tq, q, BH, n, d_k) || !make_tile_map(&tk, k, BH, m, d_k, bn) ||
+      !make_tile_map(&tv, v, BH, m, d_v, bn))
     return ATTN_ERR_CUDA;
   uint32_t* status = nullptr;
   if (device_status_word(&status) != cudaSuccess) return ATTN_ERR_CUDA;
@@ -233,7 +243,7 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
   p.causal = causal ? 1 : 0;
   p.neg = scale < 0.f ? 1 : 0;
   p.c = static_cast<float>(std::fabs(static_cast<double>(scale)) * kLog2e);
-  p.num_qblocks = static_cast<int>((n + 255) / 256);
+  p.num_qblocks = 0;  // set by the launcher for its query-tile configuration
   p.inject = g_inject.exchange(0);
   p.wd.status = status;
   p.wd.budget_ns = g_watchdog_ns.load();

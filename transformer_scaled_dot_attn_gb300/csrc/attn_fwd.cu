@@ -6,24 +6,23 @@
 // the tcgen05 tensor cores and the softmax is streamed over key tiles with a
 // running maximum, so the n x m weight matrix never leaves the SM.
 //
-// One CTA owns 256 query rows of one head as two 128-row tiles Q0, Q1 and
-// streams 128-key tiles K_j, V_j through a TMA/mbarrier ring:
-//   warp 8      TMA producer: Q0, Q1 once, then K_j and V_j per stage.
-//   warp 9      MMA issuer (one lane): S_g = Q_g K_j^T into TMEM, then
-//               O_g += P_g V_j with P_g read from TMEM (aliasing S_g).
-//   warps 0-3   softmax for Q0, warps 4-7 for Q1: one thread per row. Each
-//               loads its S row from TMEM, takes the row max, computes
-//               p = 2^(s*c - m) with c = scale*log2(e), accumulates the row
-//               sum, writes bf16 P back into TMEM, rescales its O row when the
-//               running max grew by more than 2^8, and finally writes O / l
-//               and lse.
-// The issue order S0(j+1) after PV0(j) lets each softmax group work on tile
-// j+1 while the tensor cores run the other group's products; a commit that
-// signals S_g(j) also proves PV_g(j-1) finished, so the O rescale needs no
-// extra wait. With the causal mask only the key tiles at or below the
-// diagonal are loaded and multiplied.
+// One CTA owns NQ query tiles of 128 rows of one head and streams BN-key
+// tiles K_j, V_j through a TMA/mbarrier ring:
+//   warp 4*NQ      TMA producer: the Q tiles once, then K_j and V_j per stage.
+//   warp 4*NQ + 1  MMA issuer (one lane): S_g = Q_g K_j^T into TMEM, then
+//                  O_g += P_g V_j with P_g read from TMEM (aliasing S_g).
+//   warps 4g..4g+3 softmax of query tile g, one thread per row: load the S
+//                  row from TMEM, row max, p = 2^(s*c - m) with
+//                  c = scale*log2(e), row sum, bf16 P back into TMEM, rescale
+//                  of the O row when the running max grew by more than 2^8,
+//                  and finally O / l and lse.
+// Issue order per key tile j: PV_0(j), S_0(j+1), PV_1(j), S_1(j+1), ...; each
+// softmax group works on tile j+1 while the tensor cores run the other
+// groups' products, and the commit that signals S_g(j+1) also proves that
+// PV_g(j) finished, so the O rescale needs no further wait. With the causal
+// mask only the key tiles at or below the diagonal are loaded and multiplied.
 //
-// TMEM columns: S0 [0,128), S1 [128,256), O0 [256,256+D), O1 [256+D,256+2D).
+// TMEM columns: S_g at [g*BN, (g+1)*BN), O_g at [NQ*BN + g*D, NQ*BN + (g+1)*D).
 #include "attn_kernels.cuh"
 
 #include <mutex>
@@ -39,27 +38,43 @@ constexpr float kLn2 = 0.69314718055994530942f;
 // final division by the row sum.
 constexpr float kRescaleThreshold = 8.0f;
 
-template <int D>
+constexpr uint32_t tmem_cols_for(uint32_t c) {
+  return c <= 32 ? 32 : c <= 64 ? 64 : c <= 128 ? 128 : c <= 256 ? 256 : 512;
+}
+
+template <int D, int NQ, int BN>
 struct Fwd {
-  static constexpr int STAGES = (D >= 128) ? 2 : 3;
-  static constexpr int ATOM = (D >= 64) ? 64 : D;       // bf16 elements per swizzle row
-  static constexpr int NATOM = D / ATOM;                 // TMA boxes per 128-row tile
-  static constexpr uint32_t SWZ = (D >= 64) ? 2u : 4u;   // descriptor code: 128B / 64B swizzle
-  static constexpr uint32_t SBO = 8u * ATOM * 2u;        // bytes between 8-row groups
-  static constexpr uint32_t TILE = 128u * D * 2u;        // one 128-row bf16 tile
-  static constexpr uint32_t BOX = 128u * ATOM * 2u;      // one TMA box
+  static_assert(NQ * (BN + D) <= 512, "TMEM holds at most 512 fp32 columns");
+  static constexpr int ATOM = (D >= 64) ? 64 : D;        // bf16 elements per swizzle row
+  static constexpr int NATOM = D / ATOM;                  // TMA boxes per tile
+  static constexpr uint32_t SWZ = (D >= 64) ? 2u : 4u;    // descriptor code: 128B / 64B swizzle
+  static constexpr uint32_t SBO = 8u * ATOM * 2u;         // bytes between 8-row groups
+  static constexpr uint32_t QTILE = 128u * D * 2u;        // one 128-row query tile
+  static constexpr uint32_t QBOX = 128u * ATOM * 2u;
+  static constexpr uint32_t KTILE = BN * D * 2u;          // one key (or value) tile
+  static constexpr uint32_t KBOX = BN * ATOM * 2u;
+  static constexpr int STAGES = (NQ * QTILE + 4 * 2 * KTILE <= 200u * 1024u) ? 4
+                                : (NQ * QTILE + 3 * 2 * KTILE <= 200u * 1024u) ? 3 : 2;
   static constexpr uint32_t OFF_Q = 0;
-  static constexpr uint32_t OFF_K = 2 * TILE;
-  static constexpr uint32_t OFF_V = OFF_K + STAGES * TILE;
-  static constexpr uint32_t SMEM = OFF_V + STAGES * TILE + 1024;  // + alignment slack
-  static constexpr int THREADS = 320;
-  static constexpr uint32_t TM_S0 = 0, TM_S1 = 128, TM_O0 = 256, TM_O1 = 256 + D;
+  static constexpr uint32_t OFF_K = NQ * QTILE;
+  static constexpr uint32_t OFF_V = OFF_K + STAGES * KTILE;
+  static constexpr uint32_t SMEM = OFF_V + STAGES * KTILE + 1024;  // + alignment slack
+  static constexpr int THREADS = NQ * 128 + 64;
+  static constexpr uint32_t TMEM_COLS = tmem_cols_for(NQ * (BN + D));
+  static constexpr int MIN_BLOCKS = (TMEM_COLS <= 256 && SMEM <= 110u * 1024u) ? 2 : 1;
+  static constexpr int PRODUCER = 4 * NQ, ISSUER = 4 * NQ + 1;
+  static constexpr int CHUNKS = BN / 32;                  // 32-column TMEM loads per row
+  __host__ __device__ static constexpr uint32_t tm_s(int g) { return g * BN; }
+  __host__ __device__ static constexpr uint32_t tm_o(int g) { return NQ * BN + g * D; }
 };
+
+constexpr int kMaxNQ = 4;
+constexpr int kMaxStages = 4;
 
 struct FwdShared {
   uint64_t q_full;
-  uint64_t k_full[4], k_empty[4], v_full[4], v_empty[4];
-  uint64_t s_full[2], p_full[2], o_full[2];
+  uint64_t k_full[kMaxStages], k_empty[kMaxStages], v_full[kMaxStages], v_empty[kMaxStages];
+  uint64_t s_full[kMaxNQ], p_full[kMaxNQ], o_full[kMaxNQ];
   uint64_t drain;
   uint32_t tmem_base;
   int abort_flag;
@@ -71,10 +86,11 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
-// Key tiles needed by query rows [r_lo, r_hi] (r_hi clipped to n-1 by the caller).
+// Key tiles of BN needed by query rows up to r_hi (already clipped to n-1).
+template <int BN>
 __device__ __forceinline__ int key_tiles(int r_hi, int m, int causal) {
   const int kv_hi = causal ? min(r_hi, m - 1) : (m - 1);
-  return kv_hi / 128 + 1;
+  return kv_hi / BN + 1;
 }
 
 // Waits without looking at the abort flag: used to let copies and MMAs that
@@ -90,11 +106,32 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, const
   }
 }
 
-template <int D>
-__global__ void __launch_bounds__(320, 1)
+// p = 2^(s*c - m) for one 32-column chunk of a row held in registers; packs
+// the bf16 weights and adds the fp32 weights into lsum2. MASKED: columns at
+// or past `rem` (keys this row may not see) get weight exactly 0.
+template <bool MASKED>
+__device__ __forceinline__ void exp_chunk(const uint32_t (&s)[32], int col0, int rem, uint64_t c2,
+                                          uint64_t nm2, uint64_t (&lsum2)[2], uint32_t (&pk)[16]) {
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const uint64_t x2 = fma2(f2_pack(__uint_as_float(s[2 * i]), __uint_as_float(s[2 * i + 1])), c2, nm2);
+    float x0, x1;
+    f2_unpack(x2, x0, x1);
+    if (MASKED) {
+      if (col0 + 2 * i >= rem) x0 = -INFINITY;
+      if (col0 + 2 * i + 1 >= rem) x1 = -INFINITY;
+    }
+    const uint64_t p2 = f2_pack(ex2(x0), ex2(x1));
+    lsum2[i & 1] = add2(lsum2[i & 1], p2);
+    pk[i] = pack_bf16x2_pair(p2);
+  }
+}
+
+template <int D, int NQ, int BN>
+__global__ void __launch_bounds__(Fwd<D, NQ, BN>::THREADS, Fwd<D, NQ, BN>::MIN_BLOCKS)
 attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
-  using C = Fwd<D>;
+  using C = Fwd<D, NQ, BN>;
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) FwdShared sh;
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -102,13 +139,20 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int bh = blockIdx.x;
   const int qb = p.causal ? (p.num_qblocks - 1 - static_cast<int>(blockIdx.y)) : blockIdx.y;
-  const int q0 = qb * 256;
+  const int q0 = qb * (NQ * 128);
   volatile int* abort_flag = &sh.abort_flag;
   const Watchdog wd = p.wd;
 
-  const int n0 = key_tiles(min(q0 + 127, p.n - 1), p.m, p.causal);
-  const int n1 = (q0 + 128 < p.n) ? key_tiles(min(q0 + 255, p.n - 1), p.m, p.causal) : 0;
-  const int nt = max(n0, n1);
+  // key tiles per query tile (0 for tiles past n); nondecreasing in g
+  int ntile[NQ];
+  int nt = 0, nq_valid = 0;
+#pragma unroll
+  for (int g = 0; g < NQ; ++g) {
+    const int r0 = q0 + g * 128;
+    ntile[g] = (r0 < p.n) ? key_tiles<BN>(min(r0 + 127, p.n - 1), p.m, p.causal) : 0;
+    nt = max(nt, ntile[g]);
+    nq_valid += (r0 < p.n) ? 1 : 0;
+  }
 
   if (tid == 0) {
     mbar_init(&sh.q_full, 1);
@@ -118,7 +162,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       mbar_init(&sh.v_full[s], 1);
       mbar_init(&sh.v_empty[s], 1);
     }
-    for (int g = 0; g < 2; ++g) {
+    for (int g = 0; g < NQ; ++g) {
       mbar_init(&sh.s_full[g], 1);
       mbar_init(&sh.p_full[g], 128);
       mbar_init(&sh.o_full[g], 1);
@@ -127,11 +171,11 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     sh.abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 9) {
-    tmem_alloc<512>(&sh.tmem_base);
+  if (warp == C::ISSUER) {
+    tmem_alloc<C::TMEM_COLS>(&sh.tmem_base);
     tmem_relinquish();
   }
-  if (warp == 8 && lane == 0) {
+  if (warp == C::PRODUCER && lane == 0) {
     prefetch_tensormap(&tm_q);
     prefetch_tensormap(&tm_k);
     prefetch_tensormap(&tm_v);
@@ -141,31 +185,30 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   tc_fence_after();
   const uint32_t tmem = sh.tmem_base;
 
-  if (warp == 8) {
+  if (warp == C::PRODUCER) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
-      int k_last[4] = {-1, -1, -1, -1}, v_last[4] = {-1, -1, -1, -1};
-      const int nq = (n1 > 0) ? 2 : 1;
-      mbar_arrive_expect_tx(&sh.q_full, nq * C::TILE);
-      for (int t = 0; t < nq; ++t)
+      int k_last[kMaxStages] = {-1, -1, -1, -1}, v_last[kMaxStages] = {-1, -1, -1, -1};
+      mbar_arrive_expect_tx(&sh.q_full, nq_valid * C::QTILE);
+      for (int t = 0; t < nq_valid; ++t)
         for (int a = 0; a < C::NATOM; ++a)
-          tma_load_3d(smem + C::OFF_Q + t * C::TILE + a * C::BOX, &tm_q, &sh.q_full, a * C::ATOM,
+          tma_load_3d(smem + C::OFF_Q + t * C::QTILE + a * C::QBOX, &tm_q, &sh.q_full, a * C::ATOM,
                       q0 + t * 128, bh);
       for (int j = 0; j < nt; ++j) {
         const int st = j % C::STAGES;
         const uint32_t ph = (j / C::STAGES) & 1;
         if (j >= C::STAGES && !guarded_wait(&sh.k_empty[st], ph ^ 1, abort_flag, wd, kSiteKEmpty)) break;
-        mbar_arrive_expect_tx(&sh.k_full[st], C::TILE);
+        mbar_arrive_expect_tx(&sh.k_full[st], C::KTILE);
         for (int a = 0; a < C::NATOM; ++a)
-          tma_load_3d(smem + C::OFF_K + st * C::TILE + a * C::BOX, &tm_k, &sh.k_full[st],
-                      a * C::ATOM, j * 128, bh);
+          tma_load_3d(smem + C::OFF_K + st * C::KTILE + a * C::KBOX, &tm_k, &sh.k_full[st],
+                      a * C::ATOM, j * BN, bh);
         k_last[st] = static_cast<int>(ph);
         if (j >= C::STAGES && !guarded_wait(&sh.v_empty[st], ph ^ 1, abort_flag, wd, kSiteVEmpty)) break;
         if (p.inject == 1 && j == 0) continue;  // test hook: this value tile never arrives
-        mbar_arrive_expect_tx(&sh.v_full[st], C::TILE);
+        mbar_arrive_expect_tx(&sh.v_full[st], C::KTILE);
         for (int a = 0; a < C::NATOM; ++a)
-          tma_load_3d(smem + C::OFF_V + st * C::TILE + a * C::BOX, &tm_v, &sh.v_full[st],
-                      a * C::ATOM, j * 128, bh);
+          tma_load_3d(smem + C::OFF_V + st * C::KTILE + a * C::KBOX, &tm_v, &sh.v_full[st],
+                      a * C::ATOM, j * BN, bh);
         v_last[st] = static_cast<int>(ph);
       }
       // Let every copy this thread started land before shared memory is released.
@@ -175,30 +218,27 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         if (v_last[s] >= 0) drain_wait(&sh.v_full[s], static_cast<uint32_t>(v_last[s]), wd);
       }
     }
-  } else if (warp == 9) {
+  } else if (warp == C::ISSUER) {
     // ------------------------------------------------------------ MMA issuer
-    const uint32_t idesc_s = idesc_bf16_f32(128, 128, false, false) | (p.neg ? (1u << 13) : 0u);
+    const uint32_t idesc_s = idesc_bf16_f32(128, BN, false, false) | (p.neg ? (1u << 13) : 0u);
     const uint32_t idesc_o = idesc_bf16_f32(128, D, false, true);
     const uint32_t sQ = smem_u32(smem + C::OFF_Q);
     const uint32_t sK = smem_u32(smem + C::OFF_K);
     const uint32_t sV = smem_u32(smem + C::OFF_V);
     auto issue_s = [&](int g, int st) {
-      const uint32_t d_tmem = tmem + (g ? C::TM_S1 : C::TM_S0);
 #pragma unroll
       for (int k = 0; k < D / 16; ++k) {
         const int a = k / (C::ATOM / 16), w = k % (C::ATOM / 16);
-        const uint64_t da = smem_desc(sQ + g * C::TILE + a * C::BOX + w * 32, 16, C::SBO, C::SWZ);
-        const uint64_t db = smem_desc(sK + st * C::TILE + a * C::BOX + w * 32, 16, C::SBO, C::SWZ);
-        mma_ss(d_tmem, da, db, idesc_s, k > 0 ? 1u : 0u);
+        const uint64_t da = smem_desc(sQ + g * C::QTILE + a * C::QBOX + w * 32, 16, C::SBO, C::SWZ);
+        const uint64_t db = smem_desc(sK + st * C::KTILE + a * C::KBOX + w * 32, 16, C::SBO, C::SWZ);
+        mma_ss(tmem + C::tm_s(g), da, db, idesc_s, k > 0 ? 1u : 0u);
       }
     };
     auto issue_pv = [&](int g, int st, bool acc) {
-      const uint32_t d_tmem = tmem + (g ? C::TM_O1 : C::TM_O0);
-      const uint32_t a_tmem = tmem + (g ? C::TM_S1 : C::TM_S0);
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const uint64_t db = smem_desc(sV + st * C::TILE + k * 16 * C::ATOM * 2, C::BOX, C::SBO, C::SWZ);
-        mma_ts(d_tmem, a_tmem + k * 8, db, idesc_o, (acc || k > 0) ? 1u : 0u);
+      for (int k = 0; k < BN / 16; ++k) {
+        const uint64_t db = smem_desc(sV + st * C::KTILE + k * 16 * C::ATOM * 2, C::KBOX, C::SBO, C::SWZ);
+        mma_ts(tmem + C::tm_o(g), tmem + C::tm_s(g) + k * 8, db, idesc_o, (acc || k > 0) ? 1u : 0u);
       }
     };
     auto wait_all = [&](uint64_t* bar, uint32_t parity, uint32_t site) {
@@ -209,52 +249,48 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       ok = wait_all(&sh.k_full[0], 0, kSiteKFull);
       if (ok && lane == 0) {
         tc_fence_after();
-        if (n0 > 0) { issue_s(0, 0); mma_commit(&sh.s_full[0]); }
-        if (n1 > 0) { issue_s(1, 0); mma_commit(&sh.s_full[1]); }
+#pragma unroll
+        for (int g = 0; g < NQ; ++g)
+          if (ntile[g] > 0) {
+            issue_s(g, 0);
+            mma_commit(&sh.s_full[g]);
+          }
         mma_commit(&sh.k_empty[0]);
       }
       __syncwarp();
     }
     for (int j = 0; ok && j < nt; ++j) {
       const int st = j % C::STAGES;
-      const uint32_t ph = (j / C::STAGES) & 1;
       const int jn = j + 1, stn = jn % C::STAGES;
-      if (!(ok = wait_all(&sh.v_full[st], ph, kSiteVFull))) break;
-      if (j < n0) {
-        if (!(ok = wait_all(&sh.p_full[0], j & 1, kSitePFull))) break;
-        if (lane == 0) {
-          tc_fence_after();
-          issue_pv(0, st, j > 0);
-          if (j == n0 - 1) mma_commit(&sh.o_full[0]);
+      if (!(ok = wait_all(&sh.v_full[st], (j / C::STAGES) & 1, kSiteVFull))) break;
+      bool k_next = false;
+#pragma unroll
+      for (int g = 0; g < NQ; ++g) {
+        if (j < ntile[g]) {
+          if (!(ok = wait_all(&sh.p_full[g], j & 1, kSitePFull))) break;
+          if (lane == 0) {
+            tc_fence_after();
+            issue_pv(g, st, j > 0);
+            if (j == ntile[g] - 1) mma_commit(&sh.o_full[g]);
+          }
+          __syncwarp();
         }
-        __syncwarp();
-      }
-      if (jn < nt) {
-        if (!(ok = wait_all(&sh.k_full[stn], (jn / C::STAGES) & 1, kSiteKFull))) break;
-        if (jn < n0 && lane == 0) {
-          issue_s(0, stn);
-          mma_commit(&sh.s_full[0]);
+        if (jn < ntile[g]) {
+          if (!k_next) {
+            if (!(ok = wait_all(&sh.k_full[stn], (jn / C::STAGES) & 1, kSiteKFull))) break;
+            k_next = true;
+          }
+          if (lane == 0) {
+            issue_s(g, stn);
+            mma_commit(&sh.s_full[g]);
+          }
+          __syncwarp();
         }
-        __syncwarp();
       }
-      if (j < n1) {
-        if (!(ok = wait_all(&sh.p_full[1], j & 1, kSitePFull))) break;
-        if (lane == 0) {
-          tc_fence_after();
-          issue_pv(1, st, j > 0);
-          if (j == n1 - 1) mma_commit(&sh.o_full[1]);
-        }
-        __syncwarp();
-      }
+      if (!ok) break;
       if (lane == 0) {
         mma_commit(&sh.v_empty[st]);
-        if (jn < nt) {
-          if (jn < n1) {
-            issue_s(1, stn);
-            mma_commit(&sh.s_full[1]);
-          }
-          mma_commit(&sh.k_empty[stn]);
-        }
+        if (k_next) mma_commit(&sh.k_empty[stn]);
       }
       __syncwarp();
     }
@@ -262,46 +298,54 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     if (lane == 0) mma_commit(&sh.drain);
     __syncwarp();
     drain_wait(&sh.drain, 0, wd);
-  } else {
+  } else if (warp < 4 * NQ) {
     // ------------------------------------------------------------ softmax groups
     const int g = warp >> 2;
     const int r = tid & 127;
     const int row = q0 + g * 128 + r;
-    const int ntile = g ? n1 : n0;
+    int my_tiles = 0;
+#pragma unroll
+    for (int gg = 0; gg < NQ; ++gg)
+      if (gg == g) my_tiles = ntile[gg];
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    const uint32_t t_s = tmem + lane_base + (g ? C::TM_S1 : C::TM_S0);
-    const uint32_t t_o = tmem + lane_base + (g ? C::TM_O1 : C::TM_O0);
+    const uint32_t t_s = tmem + lane_base + g * BN;
+    const uint32_t t_o = tmem + lane_base + NQ * BN + g * D;
     const int lim = p.causal ? min(row + 1, p.m) : p.m;  // keys [0, lim) are visible
     const float c = p.c;
+    const uint64_t c2 = f2_pack(c, c);
     float m_used = 0.f, l = 0.f;
     bool ok = true;
-    for (int j = 0; j < ntile; ++j) {
+    for (int j = 0; j < my_tiles; ++j) {
       ok = __all_sync(0xffffffffu, guarded_wait(&sh.s_full[g], j & 1, abort_flag, wd, kSiteSFull));
       if (!ok) break;
       tc_fence_after();
-      uint32_t s[4][32];
+      uint32_t s[C::CHUNKS][32];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) tmem_ld32(t_s + q * 32, s[q]);
+      for (int q = 0; q < C::CHUNKS; ++q) tmem_ld32(t_s + q * 32, s[q]);
       tmem_ld_wait();
-      const int rem = lim - j * 128;  // visible keys of this row inside the tile
-      const bool masked = __any_sync(0xffffffffu, rem < 128);
+      const int rem = lim - j * BN;  // visible keys of this row inside the tile
+      const bool masked = __any_sync(0xffffffffu, rem < BN);
       if (masked) {
 #pragma unroll
-        for (int q = 0; q < 4; ++q)
+        for (int q = 0; q < C::CHUNKS; ++q)
 #pragma unroll
           for (int i = 0; i < 32; ++i)
             if (q * 32 + i >= rem) s[q][i] = __float_as_uint(-INFINITY);
       }
-      float mx8[8];
+      // row max: four chains of 3-input max, seeded with columns 0..7; every
+      // later step covers 8 columns, ending exactly at BN
+      float mx4[4];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) mx8[i] = __uint_as_float(s[0][i]);
+      for (int u = 0; u < 4; ++u)
+        mx4[u] = fmaxf(__uint_as_float(s[0][2 * u]), __uint_as_float(s[0][2 * u + 1]));
 #pragma unroll
-      for (int q = 0; q < 4; ++q)
+      for (int e = 8; e < BN; e += 8) {
 #pragma unroll
-        for (int i = 0; i < 32; ++i)
-          if (q > 0 || i >= 8) mx8[i & 7] = fmaxf(mx8[i & 7], __uint_as_float(s[q][i]));
-      const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+        for (int u = 0; u < 4; ++u)
+          mx4[u] = max3(mx4[u], __uint_as_float(s[(e + 2 * u) >> 5][(e + 2 * u) & 31]),
+                        __uint_as_float(s[(e + 2 * u + 1) >> 5][(e + 2 * u + 1) & 31]));
+      }
+      const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
       const float m_new = mx * c;
       float alpha = 1.f;
       bool rescale = false;
@@ -312,26 +356,23 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         m_used = m_new;
         rescale = true;
       }
-      const float neg_m = -m_used;
-      float ls[4] = {0.f, 0.f, 0.f, 0.f};
+      const uint64_t nm2 = f2_pack(-m_used, -m_used);
+      uint64_t lsum2[2] = {0ull, 0ull};
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
+      for (int q = 0; q < C::CHUNKS; ++q) {
         uint32_t pk[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          float x0 = fmaf(__uint_as_float(s[q][2 * i]), c, neg_m);
-          float x1 = fmaf(__uint_as_float(s[q][2 * i + 1]), c, neg_m);
-          if (masked) {
-            if (q * 32 + 2 * i >= rem) x0 = -INFINITY;
-            if (q * 32 + 2 * i + 1 >= rem) x1 = -INFINITY;
-          }
-          const float p0 = ex2(x0), p1 = ex2(x1);
-          ls[i & 3] += p0 + p1;
-          pk[i] = pack_bf16x2(p0, p1);
-        }
+        if (masked)
+          exp_chunk<true>(s[q], q * 32, rem, c2, nm2, lsum2, pk);
+        else
+          exp_chunk<false>(s[q], q * 32, rem, c2, nm2, lsum2, pk);
         tmem_st16(t_s + q * 16, pk);
       }
-      l = l * alpha + ((ls[0] + ls[1]) + (ls[2] + ls[3]));
+      {
+        float a0, a1, b0, b1;
+        f2_unpack(lsum2[0], a0, a1);
+        f2_unpack(lsum2[1], b0, b1);
+        l = l * alpha + ((a0 + a1) + (b0 + b1));
+      }
       tmem_st_wait();
       if (j > 0 && __any_sync(0xffffffffu, rescale)) {
 #pragma unroll
@@ -348,7 +389,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       tc_fence_before();
       mbar_arrive(&sh.p_full[g]);
     }
-    if (ok && ntile > 0) {
+    if (ok && my_tiles > 0) {
       ok = __all_sync(0xffffffffu, guarded_wait(&sh.o_full[g], 0, abort_flag, wd, kSiteOFull));
       if (ok) {
         tc_fence_after();
@@ -378,42 +419,79 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 9) {
+  if (warp == C::ISSUER) {
     tc_fence_after();
-    tmem_dealloc<512>(tmem);
+    tmem_dealloc<C::TMEM_COLS>(tmem);
   }
 }
 
-template <int D>
-cudaError_t launch_fwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                         const FwdParams& p, int BH, cudaStream_t stream) {
-  using C = Fwd<D>;
+template <int D, int NQ, int BN>
+cudaError_t launch_fwd_cfg(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                           FwdParams p, int BH, cudaStream_t stream) {
+  using C = Fwd<D, NQ, BN>;
   static std::once_flag once[64];
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   cudaError_t attr = cudaSuccess;
   std::call_once(once[dev & 63], [&] {
-    attr = cudaFuncSetAttribute(attn_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    attr = cudaFuncSetAttribute(attn_fwd_kernel<D, NQ, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 static_cast<int>(C::SMEM));
   });
   if (attr != cudaSuccess) return attr;
+  p.num_qblocks = (p.n + NQ * 128 - 1) / (NQ * 128);
   dim3 grid(static_cast<unsigned>(BH), static_cast<unsigned>(p.num_qblocks));
   prof_begin(kKindFwd, stream);
-  attn_fwd_kernel<D><<<grid, C::THREADS, C::SMEM, stream>>>(tq, tk, tv, p);
+  attn_fwd_kernel<D, NQ, BN><<<grid, C::THREADS, C::SMEM, stream>>>(tq, tk, tv, p);
   e = cudaGetLastError();
   prof_end(kKindFwd, stream);
   return e;
 }
 
+__global__ void exp2_probe_kernel(const float* x, float* y_poly, float* y_mufu, int n) {
+  const int i = 2 * (blockIdx.x * blockDim.x + threadIdx.x);
+  if (i >= n) return;
+  const float x0 = x[i];
+  const float x1 = (i + 1 < n) ? x[i + 1] : 0.f;
+  float p0, p1;
+  f2_unpack(exp2_poly2(f2_pack(x0, x1)), p0, p1);
+  if (y_poly) {
+    y_poly[i] = p0;
+    if (i + 1 < n) y_poly[i + 1] = p1;
+  }
+  if (y_mufu) {
+    y_mufu[i] = ex2(x0);
+    if (i + 1 < n) y_mufu[i + 1] = ex2(x1);
+  }
+}
+
 }  // namespace
 
+int fwd_key_tile(int d, int n) { return (d >= 128 || n > 256) ? 128 : 64; }
+
+cudaError_t launch_exp2_probe(const float* x, float* y_poly, float* y_mufu, int n,
+                              cudaStream_t stream) {
+  if (n == 0) return cudaSuccess;
+  const int pairs = (n + 1) / 2;
+  exp2_probe_kernel<<<(pairs + 255) / 256, 256, 0, stream>>>(x, y_poly, y_mufu, n);
+  return cudaGetLastError();
+}
+
+// Configuration: two 128-row query tiles per CTA. Key tiles of 128 (TMEM
+// 2 x (128 + D) columns, one CTA per SM) except for d <= 64 with n <= 256,
+// where 64-key tiles halve TMEM to 256 columns so two CTAs share an SM and
+// hide each other's prologue and epilogue latency (fwd_key_tile).
 cudaError_t launch_fwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const FwdParams& p, int BH, cudaStream_t stream) {
+  const bool small_tiles = fwd_key_tile(d, p.n) == 64;
   switch (d) {
-    case 32: return launch_fwd_d<32>(tq, tk, tv, p, BH, stream);
-    case 64: return launch_fwd_d<64>(tq, tk, tv, p, BH, stream);
-    case 128: return launch_fwd_d<128>(tq, tk, tv, p, BH, stream);
+    case 32:
+      return small_tiles ? launch_fwd_cfg<32, 2, 64>(tq, tk, tv, p, BH, stream)
+                         : launch_fwd_cfg<32, 2, 128>(tq, tk, tv, p, BH, stream);
+    case 64:
+      return small_tiles ? launch_fwd_cfg<64, 2, 64>(tq, tk, tv, p, BH, stream)
+                         : launch_fwd_cfg<64, 2, 128>(tq, tk, tv, p, BH, stream);
+    case 128: return launch_fwd_cfg<128, 2, 128>(tq, tk, tv, p, BH, stream);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -58,10 +58,17 @@ struct FwdParams {
   int causal;
   int neg;            // scale < 0: the score MMA negates Q K^T so that c >= 0
   float c;            // |scale| * log2(e)
-  int num_qblocks;    // ceil(n / 256)
+  int num_qblocks;    // query blocks (set by the launcher)
   int inject;         // test hook: 1 = skip the first value-tile load
   Watchdog wd;
 };
+
+cudaError_t launch_exp2_probe(const float* x, float* y_poly, float* y_mufu, int n,
+                              cudaStream_t stream);
+
+// Keys per tile the forward kernel streams for head size d and n queries
+// (the K/V TMA box height).
+int fwd_key_tile(int d, int n);
 
 cudaError_t launch_fwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const FwdParams& p, int BH, cudaStream_t stream);

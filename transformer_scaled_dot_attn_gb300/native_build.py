@@ -18,7 +18,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB_NAME = "libattn_gb300.so"
-LIB_PATH = os.path.join(PKG, LIB_NAME)
+# ATTN_GB300_LIBRARY may point the binding at another build of the same library.
+LIB_PATH = os.environ.get("ATTN_GB300_LIBRARY") or os.path.join(PKG, LIB_NAME)
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2",
