@@ -91,6 +91,34 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const f
              attn_stream_t stream);
 
 /*
+ * attn_bwd without a workspace argument, for callers that cannot allocate
+ * device memory at the call site: a process whose device memory is held by a
+ * pooling allocator that a stray cudaMalloc would bypass or exhaust, a
+ * latency-bound loop that cannot afford cudaMalloc's implicit device
+ * synchronisation, or code running inside another library's callback where
+ * allocation is off limits. This is an addition of this library; the paper
+ * has no counterpart.
+ *
+ * Same arguments and results as attn_bwd, minus workspace/workspace_bytes.
+ * The scratch (fp32 dQ accumulator and two padded per-row statistics, as
+ * sized by attn_bwd_workspace_bytes) lives in one fixed 32 MiB device array
+ * inside the library: every GPU that loads the library holds it until the
+ * process exits. Sizes whose scratch exceeds 32 MiB are refused with
+ * ATTN_ERR_UNSUPPORTED before anything is launched. The call makes no
+ * cudaMalloc/cudaFree and no other allocation. Its first call on a device
+ * looks up the array's device address (cudaGetSymbolAddress) with that
+ * device current; make that first call before any stream capture. Every
+ * call shares the one array and clears on its stream what must start at
+ * zero, so calls that can overlap on the GPU (different streams, no
+ * ordering between them) race and must not be issued. Watchdog reports go to
+ * the word attn_get_device_status reads once any other call of this library
+ * has created it on the device.
+ */
+int attn_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                     const void* dO, void* dq, void* dk, void* dv, int B, int h, int n, int m,
+                     int d_k, int d_v, int causal, float scale, attn_stream_t stream);
+
+/*
  * Synchronises `stream`, then reports and clears the device-side error word of
  * the current device: ATTN_OK, or ATTN_ERR_TIMEOUT if any kernel's watchdog
  * fired since the last call. ATTN_ERR_CUDA if the synchronisation failed.

@@ -26,7 +26,7 @@ __all__ = [
     "ATTN_ERR_TIMEOUT", "load_library", "library_path", "attn_fwd", "attn_bwd",
     "attn_bwd_workspace_bytes", "attn_get_device_status", "attn_status_string",
     "attn_set_watchdog_ns", "attn_debug_inject", "attn_profile_enable", "attn_profile_read",
-    "attn_debug_exp2", "EXPORTED_SYMBOLS", "KERNEL_KINDS",
+    "attn_debug_exp2", "attn_bwd_noalloc", "EXPORTED_SYMBOLS", "KERNEL_KINDS",
 ]
 
 ATTN_OK = 0
@@ -39,7 +39,7 @@ ATTN_ERR_TIMEOUT = 4
 EXPORTED_SYMBOLS = (
     "attn_fwd", "attn_bwd", "attn_bwd_workspace_bytes", "attn_get_device_status",
     "attn_status_string", "attn_set_watchdog_ns", "attn_debug_inject", "attn_profile_enable",
-    "attn_profile_read", "attn_debug_exp2",
+    "attn_profile_read", "attn_debug_exp2", "attn_bwd_noalloc",
 )
 
 # Kernel kinds of attn_profile_read.
@@ -89,6 +89,9 @@ def load_library():
         lib.attn_set_watchdog_ns.restype = I
         lib.attn_debug_inject.argtypes = [I]
         lib.attn_debug_inject.restype = I
+        lib.attn_bwd_noalloc.argtypes = [vp, vp, vp, vp, fp, vp, vp, vp, vp, I, I, I, I, I, I, I, F,
+                                         vp]
+        lib.attn_bwd_noalloc.restype = I
         lib.attn_debug_exp2.argtypes = [vp, vp, vp, I, vp]
         lib.attn_debug_exp2.restype = I
         lib.attn_profile_enable.argtypes = [I]
@@ -233,3 +236,35 @@ def attn_debug_exp2(x, stream=None):
     if st != ATTN_OK:
         raise AttnError(st, "attn_debug_exp2")
     return yp, ym
+
+
+def attn_bwd_noalloc(q, k, v, o, lse, dO, causal: bool = False, scale: Optional[float] = None,
+                     dq=None, dk=None, dv=None, stream=None):
+    """attn_bwd whose scratch lives in the library's fixed device array (no workspace).
+
+    For callers that cannot allocate device memory at the call site; see
+    include/attn.h for the size limit and the one-call-at-a-time rule.
+    """
+    import torch
+    lib = load_library()
+    B, h, n, d_k = q.shape
+    m, d_v = k.shape[2], v.shape[3]
+    _check_tensor("q", q, dtype=torch.bfloat16)
+    _check_tensor("k", k, (B, h, m, d_k), torch.bfloat16)
+    _check_tensor("v", v, (B, h, m, d_v), torch.bfloat16)
+    _check_tensor("o", o, (B, h, n, d_v), torch.bfloat16)
+    _check_tensor("lse", lse, (B, h, n), torch.float32)
+    _check_tensor("dO", dO, (B, h, n, d_v), torch.bfloat16)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d_k)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    for name, t, ref in (("dq", dq, q), ("dk", dk, k), ("dv", dv, v)):
+        _check_tensor(name, t, tuple(ref.shape), torch.bfloat16)
+    st = lib.attn_bwd_noalloc(_vptr(q), _vptr(k), _vptr(v), _vptr(o), _fptr(lse), _vptr(dO),
+                              _vptr(dq), _vptr(dk), _vptr(dv), B, h, n, m, d_k, d_v,
+                              int(bool(causal)), float(scale), _stream_handle(stream))
+    if st != ATTN_OK:
+        raise AttnError(st, "attn_bwd_noalloc")
+    return dq, dk, dv

@@ -357,3 +357,126 @@ int attn_get_device_status(attn_stream_t stream) {
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------- allocation-free backward
+//
+// Scratch of attn_bwd_noalloc: the fp32 dQ accumulator and the two padded
+// per-row statistics live in this fixed device array instead of a
+// caller-provided workspace. It exists once per device that loads the
+// library and stays until the process exits.
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = size_t(32) << 20;  // 32 MiB
+
+__device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+// Watchdog word for devices on which no attn_fwd/attn_bwd call has created
+// the per-device error word yet (that word needs an allocation).
+__device__ uint32_t g_noalloc_status;
+
+std::once_flag g_noalloc_once[kMaxDevices];
+void* g_noalloc_scratch_ptr[kMaxDevices] = {nullptr};
+uint32_t* g_noalloc_status_ptr[kMaxDevices] = {nullptr};
+cudaError_t g_noalloc_setup_err[kMaxDevices] = {cudaSuccess};
+
+}  // namespace
+
+extern "C" int attn_bwd_noalloc(const void* q, const void* k, const void* v, const void* o,
+                                const float* lse, const void* dO, void* dq, void* dk, void* dv,
+                                int B, int h, int n, int m, int d_k, int d_v, int causal,
+                                float scale, attn_stream_t stream) {
+  bool empty = false;
+  int st = check_common(B, h, n, m, d_k, d_v, scale, &empty);
+  if (st != ATTN_OK) return st;
+  if (!k || !v || !dk || !dv) return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(k) || !aligned16(v) || !aligned16(dk) || !aligned16(dv)) return ATTN_ERR_INVALID_ARG;
+  const long long BH = static_cast<long long>(B) * h;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (empty) {
+    if (BH == 0) return ATTN_OK;
+    const size_t bytes = static_cast<size_t>(BH) * m * d_k * 2;
+    if (cudaMemsetAsync(dk, 0, bytes, s) != cudaSuccess) return ATTN_ERR_CUDA;
+    if (cudaMemsetAsync(dv, 0, bytes, s) != cudaSuccess) return ATTN_ERR_CUDA;
+    return ATTN_OK;
+  }
+  if (!q || !o || !lse || !dO || !dq) return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(o) || !aligned16(dO) || !aligned16(dq)) return ATTN_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(lse) & 3u) != 0) return ATTN_ERR_INVALID_ARG;
+  // Sizes whose scratch does not fit the fixed array are refused up front.
+  if (attn_bwd_workspace_bytes(B, h, n, m, d_k, d_v, causal) > kNoAllocScratchBytes)
+    return ATTN_ERR_UNSUPPORTED;
+
+  // Set-up, once per device, with that device current: the device address of
+  // the scratch array (and of the fallback watchdog word).
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return ATTN_ERR_CUDA;
+  std::call_once(g_noalloc_once[dev], [dev] {
+    void* ptr = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+    if (e == cudaSuccess) {
+      g_noalloc_scratch_ptr[dev] = ptr;
+      void* sp = nullptr;
+      e = cudaGetSymbolAddress(&sp, g_noalloc_status);
+      if (e == cudaSuccess) g_noalloc_status_ptr[dev] = static_cast<uint32_t*>(sp);
+    }
+    g_noalloc_setup_err[dev] = e;
+  });
+  if (g_noalloc_setup_err[dev] != cudaSuccess || g_noalloc_scratch_ptr[dev] == nullptr)
+    return ATTN_ERR_CUDA;
+  uint32_t* status = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_status_mu);
+    status = g_status[dev];  // read only: never allocated here
+  }
+  if (status == nullptr) status = g_noalloc_status_ptr[dev];
+
+  const long long n_pad = round_up(n, 128);
+  float* dq_acc = static_cast<float*>(g_noalloc_scratch_ptr[dev]);
+  float* lse2 = dq_acc + BH * n_pad * d_k;
+  float* Dsum = lse2 + BH * n_pad;
+
+  CUtensorMap tq, tk, tv, tdo;
+  if (!make_tile_map(&tq, q, BH, n, d_k) || !make_tile_map(&tk, k, BH, m, d_k) ||
+      !make_tile_map(&tv, v, BH, m, d_v) || !make_tile_map(&tdo, dO, BH, n, d_v))
+    return ATTN_ERR_CUDA;
+
+  BwdPreParams pre{};
+  pre.o = static_cast<const __nv_bfloat16*>(o);
+  pre.dO = static_cast<const __nv_bfloat16*>(dO);
+  pre.lse = lse;
+  pre.lse2 = lse2;
+  pre.Dsum = Dsum;
+  pre.dq_acc = dq_acc;
+  pre.n = n;
+  pre.n_pad = static_cast<int>(n_pad);
+  pre.d = d_k;
+  pre.BH = static_cast<int>(BH);
+
+  BwdParams p{};
+  p.dk = static_cast<__nv_bfloat16*>(dk);
+  p.dv = static_cast<__nv_bfloat16*>(dv);
+  p.lse2 = lse2;
+  p.Dsum = Dsum;
+  p.dq_acc = dq_acc;
+  p.n = n;
+  p.m = m;
+  p.n_pad = static_cast<int>(n_pad);
+  p.causal = causal ? 1 : 0;
+  p.neg = scale < 0.f ? 1 : 0;
+  p.c = static_cast<float>(std::fabs(static_cast<double>(scale)) * kLog2e);
+  p.scale = scale;
+  p.num_kblocks = static_cast<int>((m + 127) / 128);
+  p.wd.status = status;
+  p.wd.budget_ns = g_watchdog_ns.load();
+
+  BwdPostParams post{};
+  post.dq_acc = dq_acc;
+  post.dq = static_cast<__nv_bfloat16*>(dq);
+  post.scale = scale;
+  post.n = n;
+  post.n_pad = static_cast<int>(n_pad);
+  post.d = d_k;
+  post.BH = static_cast<int>(BH);
+
+  cudaError_t e = attn::launch_bwd(d_k, tq, tk, tv, tdo, pre, p, post, static_cast<int>(BH), s);
+  return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
