@@ -86,6 +86,21 @@ bool make_tile_map(CUtensorMap* map, const void* base, long long BH, long long S
   return r == CUDA_SUCCESS;
 }
 
+// 2-D map over the fp32 dQ accumulator [rows, d]: box = (32 columns, 128 rows),
+// 128-byte swizzle (the layout the backward kernel stages its dQ tile in).
+bool make_dq_map(CUtensorMap* map, const float* base, long long rows, int d) {
+  EncodeTiledFn enc = encode_fn();
+  if (enc == nullptr) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(d) * 4};
+  cuuint32_t box[2] = {32u, 128u};
+  cuuint32_t estr[2] = {1u, 1u};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(base), dims, strides, box,
+                   estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 constexpr double kLog2e = 1.4426950408889634074;
@@ -295,9 +310,10 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const f
   float* lse2 = dq_acc + BH * n_pad * d_k;
   float* Dsum = lse2 + BH * n_pad;
 
-  CUtensorMap tq, tk, tv, tdo;
+  CUtensorMap tq, tk, tv, tdo, tdq;
   if (!make_tile_map(&tq, q, BH, n, d_k) || !make_tile_map(&tk, k, BH, m, d_k) ||
-      !make_tile_map(&tv, v, BH, m, d_v) || !make_tile_map(&tdo, dO, BH, n, d_v))
+      !make_tile_map(&tv, v, BH, m, d_v) || !make_tile_map(&tdo, dO, BH, n, d_v) ||
+      !make_dq_map(&tdq, dq_acc, BH * n_pad, d_k))
     return ATTN_ERR_CUDA;
   uint32_t* status = nullptr;
   if (device_status_word(&status) != cudaSuccess) return ATTN_ERR_CUDA;
@@ -340,7 +356,7 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const f
   post.d = d_k;
   post.BH = static_cast<int>(BH);
 
-  cudaError_t e = attn::launch_bwd(d_k, tq, tk, tv, tdo, pre, p, post, static_cast<int>(BH),
+  cudaError_t e = attn::launch_bwd(d_k, tq, tk, tv, tdo, tdq, pre, p, post, static_cast<int>(BH),
                                    reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
@@ -434,9 +450,10 @@ extern "C" int attn_bwd_noalloc(const void* q, const void* k, const void* v, con
   float* lse2 = dq_acc + BH * n_pad * d_k;
   float* Dsum = lse2 + BH * n_pad;
 
-  CUtensorMap tq, tk, tv, tdo;
+  CUtensorMap tq, tk, tv, tdo, tdq;
   if (!make_tile_map(&tq, q, BH, n, d_k) || !make_tile_map(&tk, k, BH, m, d_k) ||
-      !make_tile_map(&tv, v, BH, m, d_v) || !make_tile_map(&tdo, dO, BH, n, d_v))
+      !make_tile_map(&tv, v, BH, m, d_v) || !make_tile_map(&tdo, dO, BH, n, d_v) ||
+      !make_dq_map(&tdq, dq_acc, BH * n_pad, d_k))
     return ATTN_ERR_CUDA;
 
   BwdPreParams pre{};
@@ -477,6 +494,6 @@ extern "C" int attn_bwd_noalloc(const void* q, const void* k, const void* v, con
   post.d = d_k;
   post.BH = static_cast<int>(BH);
 
-  cudaError_t e = attn::launch_bwd(d_k, tq, tk, tv, tdo, pre, p, post, static_cast<int>(BH), s);
+  cudaError_t e = attn::launch_bwd(d_k, tq, tk, tv, tdo, tdq, pre, p, post, static_cast<int>(BH), s);
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }

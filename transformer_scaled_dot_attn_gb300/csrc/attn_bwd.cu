@@ -19,14 +19,21 @@
 //           dV_j += P^T dO_i        (P^T bf16 in TMEM, aliasing S^T)
 //           dK_j += dS^T Q_i        (dS^T bf16 in shared memory, K-major view)
 //           dQ_i  = dS K_j          (same buffer read as an MN-major operand)
-//         warps 0-3  one thread per key row: P, dS, and the dK/dV epilogue.
-//         warps 4-7  one thread per query row: add dQ_i into the fp32
-//                    accumulator with vector atomics.
-//         warp 8     TMA producer, warp 9 MMA issuer.
+//         warps 0-7  two warpgroups, one thread per key row each, on
+//                    disjoint query columns: P, dS, and the dK/dV epilogue.
+//         warps 8-11 one thread per query row: add dQ_i into the fp32
+//                    accumulator (TMA reduce-add, or vector atomics for d = 128).
+//         warp 12    TMA producer (tiles, and the per-row statistics by
+//                    bulk copy), warp 13 MMA issuer.
 //   post  dQ = bf16(scale * accumulator).
 //
 // TMEM columns: S^T [0,128), dP^T [128,256), dV [256,256+D), dK [256+D,256+2D),
 // dQ [256+2D,256+3D) for D <= 64; for D = 128 dQ reuses the dP^T columns.
+// dQ leaves the SM by a TMA reduce-add of a staged fp32 tile (d <= 64) or by
+// vector atomics (d = 128, no shared memory left for staging).
+// Warps (512 threads): 0-3 and 4-7 the two compute warpgroups (query columns
+// 0..63 / 64..127 of every tile), 8-11 dQ accumulation, 12 TMA producer,
+// 13 MMA issuer; registers split 160 / 160 / 72 / 56 with setmaxnreg.
 #include "attn_kernels.cuh"
 
 #include <mutex>
@@ -114,16 +121,29 @@ struct Bwd {
   static constexpr uint32_t SBO = 8u * ATOM * 2u;
   static constexpr uint32_t TILE = 128u * D * 2u;
   static constexpr uint32_t BOX = 128u * ATOM * 2u;
+  static constexpr uint32_t DS_REGION = 128u * 64u * 2u;
   static constexpr uint32_t OFF_K = 0;
   static constexpr uint32_t OFF_V = TILE;
-  static constexpr uint32_t OFF_Q = 2 * TILE;          // 2 stages
-  static constexpr uint32_t OFF_DO = 4 * TILE;         // 2 stages
-  static constexpr uint32_t OFF_DS = 6 * TILE;         // dS^T: 2 regions [128 keys][64 queries], 128B swizzle
-  static constexpr uint32_t DS_REGION = 128u * 64u * 2u;
-  static constexpr uint32_t SMEM = OFF_DS + 2 * DS_REGION + 1024;
-  static constexpr int THREADS = 384;   // 3 warpgroups; warps 10-11 only balance the register split
+  static constexpr uint32_t OFF_Q = 2 * TILE;                    // 2 stages
+  static constexpr uint32_t OFF_DO = 4 * TILE;                   // 2 stages
+  static constexpr uint32_t OFF_DS = 6 * TILE;                   // dS^T: 2 regions [128 keys][64 queries]
+  static constexpr uint32_t OFF_STAT = OFF_DS + 2 * DS_REGION;   // per stage: lse*log2(e)[128], D[128]
+  static constexpr uint32_t STAT_BYTES = 2u * 128u * 4u;
+  // d <= 64: the fp32 dQ tile is staged in shared memory (128-byte swizzled
+  // boxes of 32 columns) and added into the accumulator by one TMA reduce;
+  // d = 128 has no room left and adds with vector atomics instead.
+  static constexpr bool DQ_TMA = (D <= 64);
+  static constexpr uint32_t DQ_BOX = 128u * 32u * 4u;
+  static constexpr uint32_t OFF_DQS = OFF_STAT + 2 * STAT_BYTES;
+  static constexpr uint32_t DQS_BYTES = DQ_TMA ? (D / 32) * DQ_BOX : 0u;
+  static constexpr uint32_t OFF_BAR = OFF_DQS + DQS_BYTES;
+  static constexpr uint32_t PAYLOAD = OFF_BAR + 256;
+  static constexpr uint32_t SMEM_LIMIT = 232448;                 // opt-in maximum per block
+  // + up to 1 KB to align the tiles; for D = 128 only what fits under the limit
+  static constexpr uint32_t SMEM = (PAYLOAD + 1024 <= SMEM_LIMIT) ? PAYLOAD + 1024 : SMEM_LIMIT;
+  static constexpr int THREADS = 512;
   // setmaxnreg split (registers per thread): compute, dQ, producer/MMA warpgroups.
-  static constexpr int REG_COMPUTE = 240, REG_DQ = 96, REG_OTHER = 88;
+  static constexpr int REG_COMPUTE = 152, REG_DQ = 96, REG_OTHER = 80;
   static constexpr bool ALIAS_DQ = (D > 64);
   static constexpr uint32_t TM_S = 0, TM_DP = 128, TM_DV = 256, TM_DK = 256 + D;
   static constexpr uint32_t TM_DQ = ALIAS_DQ ? 128u : (256u + 2u * D);
@@ -136,6 +156,7 @@ struct BwdShared {
   uint32_t tmem_base;
   int abort_flag;
 };
+static_assert(sizeof(BwdShared) <= 256, "barrier block must fit its slot");
 
 __device__ __forceinline__ float ex2f(float x) {
   float y;
@@ -155,25 +176,35 @@ __device__ __forceinline__ void drain_wait_b(uint64_t* bar, uint32_t parity, con
 }
 
 template <int D>
-__global__ void __launch_bounds__(384, 1)
+__global__ void __launch_bounds__(512, 1)
 attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-                const BwdParams p) {
+                const __grid_constant__ CUtensorMap tm_dq, const BwdParams p) {
   using C = Bwd<D>;
   extern __shared__ uint8_t smem_raw[];
-  __shared__ __align__(8) BwdShared sh;
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~static_cast<uintptr_t>(1023));
+  const Watchdog wd = p.wd;
+  // The tiles need 1024-byte alignment (128-byte swizzle atoms). The kernel
+  // declares no static shared memory, so the dynamic window starts aligned in
+  // practice; if it ever did not leave room, report it and do nothing.
+  const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
+  if (pad + C::PAYLOAD > C::SMEM) {
+    if (threadIdx.x == 0) atomicCAS(wd.status, 0u, kDevLayout);
+    return;
+  }
+  uint8_t* smem = smem_raw + pad;
+  BwdShared& sh = *reinterpret_cast<BwdShared*>(smem + C::OFF_BAR);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int bh = blockIdx.x;
   const int kb = blockIdx.y;
   const int k0 = kb * 128;
   volatile int* abort_flag = &sh.abort_flag;
-  const Watchdog wd = p.wd;
   const int n_qt = (p.n + 127) / 128;
   // Causal: query tiles wholly above this key tile see none of its keys.
   const int i_start = p.causal ? min(k0 / 128, n_qt) : 0;
   const int T = n_qt - i_start;
+  // Every key-tile CTA of a head walks the query tiles in the same order, so
+  // the Q and dO tiles it streams are read from DRAM once and then from L2.
+  auto qtile_row = [&](int t) { return (i_start + t) * 128; };
 
   if (tid == 0) {
     mbar_init(&sh.kv_full, 1);
@@ -183,8 +214,8 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     }
     mbar_init(&sh.s_full, 1);
     mbar_init(&sh.dp_full, 1);
-    mbar_init(&sh.p_full, 128);
-    mbar_init(&sh.ds_full, 128);
+    mbar_init(&sh.p_full, 256);
+    mbar_init(&sh.ds_full, 256);
     mbar_init(&sh.ds_empty, 1);
     mbar_init(&sh.dq_full, 1);
     mbar_init(&sh.dq_empty, 128);
@@ -193,25 +224,27 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     sh.abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 9) {
+  if (warp == 13) {
     tmem_alloc<512>(&sh.tmem_base);
     tmem_relinquish();
   }
-  if (warp == 8 && lane == 0) {
+  if (warp == 12 && lane == 0) {
     prefetch_tensormap(&tm_q);
     prefetch_tensormap(&tm_k);
     prefetch_tensormap(&tm_v);
     prefetch_tensormap(&tm_do);
+    if (C::DQ_TMA) prefetch_tensormap(&tm_dq);
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = sh.tmem_base;
+  float* stat = reinterpret_cast<float*>(smem + C::OFF_STAT);  // [stage][lse2 | D][128]
 
-  if (warp >= 8) {
+  if (warp >= 12) {
     reg_dealloc<C::REG_OTHER>();
   }
-  if (warp == 8) {
+  if (warp == 12) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0 && T > 0) {
       int last[2] = {-1, -1};
@@ -220,23 +253,27 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         tma_load_3d(smem + C::OFF_K + a * C::BOX, &tm_k, &sh.kv_full, a * C::ATOM, k0, bh);
         tma_load_3d(smem + C::OFF_V + a * C::BOX, &tm_v, &sh.kv_full, a * C::ATOM, k0, bh);
       }
+      const float* lse2_h = p.lse2 + static_cast<size_t>(bh) * p.n_pad;
+      const float* D_h = p.Dsum + static_cast<size_t>(bh) * p.n_pad;
       for (int t = 0; t < T; ++t) {
         const int st = t & 1;
         const uint32_t ph = (t >> 1) & 1;
         if (t >= 2 && !guarded_wait(&sh.qdo_empty[st], ph ^ 1, abort_flag, wd, kSiteBwdFree)) break;
-        const int q_row = (i_start + t) * 128;
-        mbar_arrive_expect_tx(&sh.qdo_full[st], 2 * C::TILE);
+        const int q_row = qtile_row(t);
+        mbar_arrive_expect_tx(&sh.qdo_full[st], 2 * C::TILE + C::STAT_BYTES);
         for (int a = 0; a < C::NATOM; ++a) {
           tma_load_3d(smem + C::OFF_Q + st * C::TILE + a * C::BOX, &tm_q, &sh.qdo_full[st], a * C::ATOM, q_row, bh);
           tma_load_3d(smem + C::OFF_DO + st * C::TILE + a * C::BOX, &tm_do, &sh.qdo_full[st], a * C::ATOM, q_row, bh);
         }
+        bulk_load(stat + st * 256, lse2_h + q_row, 512, &sh.qdo_full[st]);
+        bulk_load(stat + st * 256 + 128, D_h + q_row, 512, &sh.qdo_full[st]);
         last[st] = static_cast<int>(ph);
       }
       drain_wait_b(&sh.kv_full, 0, wd);
       for (int s = 0; s < 2; ++s)
         if (last[s] >= 0) drain_wait_b(&sh.qdo_full[s], static_cast<uint32_t>(last[s]), wd);
     }
-  } else if (warp == 9) {
+  } else if (warp == 13) {
     // ------------------------------------------------------------ MMA issuer
     const uint32_t sK = smem_u32(smem + C::OFF_K), sV = smem_u32(smem + C::OFF_V);
     const uint32_t sQ = smem_u32(smem + C::OFF_Q), sDO = smem_u32(smem + C::OFF_DO);
@@ -277,13 +314,15 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     for (int t = 0; ok && t < T; ++t) {
       const int st = t & 1;
       const uint32_t q_off = st * C::TILE;
-      // dV += P^T dO
+      // dV += P^T dO; P^T (bf16) sits in TMEM columns [0,32) and [64,96) of S^T,
+      // one block per compute warpgroup (queries 0..63 and 64..127)
       if (!(ok = wait_all(&sh.p_full, t & 1, kSiteBwdS))) break;
       if (lane == 0) {
         tc_fence_after();
 #pragma unroll
         for (int k = 0; k < 8; ++k)
-          mma_ts(tmem + C::TM_DV, tmem + C::TM_S + k * 8, b_mn(sDO + q_off, k), id_kv, (t > 0 || k > 0) ? 1u : 0u);
+          mma_ts(tmem + C::TM_DV, tmem + C::TM_S + (k >> 2) * 64 + (k & 3) * 8, b_mn(sDO + q_off, k), id_kv,
+                 (t > 0 || k > 0) ? 1u : 0u);
       }
       __syncwarp();
       // next S^T while the compute warps form dS
@@ -334,58 +373,62 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     if (lane == 0) mma_commit(&sh.drain);
     __syncwarp();
     drain_wait_b(&sh.drain, 0, wd);
-  } else if (warp >= 10) {
-    // idle warps: they only complete the third warpgroup for the register split
-  } else if (warp < 4) {
+  } else if (warp >= 14) {
+    // idle warps: they only complete the fourth warpgroup for the register split
+  } else if (warp < 8) {
     // ------------------------------------------------------------ P, dS, dK/dV epilogue
+    // Two warpgroups on the same key rows (TMEM lanes): group h owns query
+    // columns [64h, 64h+64) of every tile.
     reg_alloc<C::REG_COMPUTE>();
-    const int r = tid;                                 // key row within the tile = TMEM lane
+    const int h = warp >> 2;
+    const int col0 = 64 * h;
+    const int r = tid & 127;                            // key row within the tile = TMEM lane
     const int key = k0 + r;
-    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
-    const uint32_t t_s = tmem + lane_base + C::TM_S;
-    const uint32_t t_dp = tmem + lane_base + C::TM_DP;
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t t_s = tmem + lane_base + C::TM_S + col0;
+    const uint32_t t_dp = tmem + lane_base + C::TM_DP + col0;
     const float c = p.c;
-    const float* lse2_h = p.lse2 + static_cast<size_t>(bh) * p.n_pad;
-    const float* D_h = p.Dsum + static_cast<size_t>(bh) * p.n_pad;
-    uint8_t* ds_row0 = smem + C::OFF_DS + r * 128;     // region 0, row r
+    uint8_t* ds_row = smem + C::OFF_DS + h * C::DS_REGION + r * 128;
     const int sw = r & 7;
     bool ok = true;
     for (int t = 0; t < T; ++t) {
-      const int q_row0 = (i_start + t) * 128;
+      const int st = t & 1;
+      const int q_row0 = qtile_row(t);
       // queries [lo, hi) of this tile may attend to this key
       const int lo = p.causal ? max(0, key - q_row0) : 0;
       const int hi = (key < p.m) ? min(128, p.n - q_row0) : 0;
-      const bool masked = __any_sync(0xffffffffu, lo > 0 || hi < 128);
-      ok = __all_sync(0xffffffffu, guarded_wait(&sh.s_full, t & 1, abort_flag, wd, kSiteBwdS));
+      const bool masked = __any_sync(0xffffffffu, lo > col0 || hi < col0 + 64);
+      ok = __all_sync(0xffffffffu, guarded_wait(&sh.s_full, t & 1, abort_flag, wd, kSiteBwdS) &&
+                                       guarded_wait(&sh.qdo_full[st], (t >> 1) & 1, abort_flag, wd, kSiteBwdLoad));
       if (!ok) break;
       tc_fence_after();
-      // P^T in fp32: dS below uses the unrounded weights; the dV product
-      // takes them rounded to bf16 (written into the S^T columns of TMEM).
-      float P[128];
+      const float* lse2_s = stat + st * 256 + col0;
+      const float* D_s = stat + st * 256 + 128 + col0;
+      // P^T in fp32 for dS below; rounded to bf16 for the dV product
+      float P[64];
       {
-        uint32_t s[4][32];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) tmem_ld32(t_s + q * 32, s[q]);
+        uint32_t s[2][32];
+        tmem_ld32(t_s, s[0]);
+        tmem_ld32(t_s + 32, s[1]);
         tmem_ld_wait();
-        const float4* l4 = reinterpret_cast<const float4*>(lse2_h + q_row0);
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
+        for (int q = 0; q < 2; ++q) {
 #pragma unroll
           for (int i4 = 0; i4 < 8; ++i4) {
-            const float4 L = __ldg(l4 + q * 8 + i4);
+            const float4 L = *reinterpret_cast<const float4*>(lse2_s + q * 32 + i4 * 4);
             const float Lv[4] = {L.x, L.y, L.z, L.w};
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
-              const int col = q * 32 + i4 * 4 + u;
+              const int col = col0 + q * 32 + i4 * 4 + u;
               float x = fmaf(__uint_as_float(s[q][i4 * 4 + u]), c, -Lv[u]);
               if (masked && (col < lo || col >= hi)) x = -INFINITY;
-              P[col] = ex2f(x);
+              P[q * 32 + i4 * 4 + u] = ex2f(x);
             }
           }
         }
       }
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
+      for (int q = 0; q < 2; ++q) {
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(P[q * 32 + 2 * i], P[q * 32 + 2 * i + 1]);
@@ -402,16 +445,15 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         ok = __all_sync(0xffffffffu, guarded_wait(&sh.ds_empty, (t - 1) & 1, abort_flag, wd, kSiteBwdDS));
         if (!ok) break;
       }
-      const float4* d4 = reinterpret_cast<const float4*>(D_h + q_row0);
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
+      for (int q = 0; q < 2; ++q) {
         uint32_t dp[32];
         tmem_ld32(t_dp + q * 32, dp);
         tmem_ld_wait();
         uint32_t pk[16];
 #pragma unroll
         for (int i4 = 0; i4 < 8; ++i4) {
-          const float4 Dv = __ldg(d4 + q * 8 + i4);
+          const float4 Dv = *reinterpret_cast<const float4*>(D_s + q * 32 + i4 * 4);
           const float ds0 = P[q * 32 + i4 * 4 + 0] * (__uint_as_float(dp[i4 * 4 + 0]) - Dv.x);
           const float ds1 = P[q * 32 + i4 * 4 + 1] * (__uint_as_float(dp[i4 * 4 + 1]) - Dv.y);
           const float ds2 = P[q * 32 + i4 * 4 + 2] * (__uint_as_float(dp[i4 * 4 + 2]) - Dv.z);
@@ -419,12 +461,11 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           pk[i4 * 2 + 0] = pack_bf16x2(ds0, ds1);
           pk[i4 * 2 + 1] = pack_bf16x2(ds2, ds3);
         }
-        // 32 queries = 4 chunks of 16 bytes; queries q*32.. land in region q/2, chunks (q&1)*4..+3
-        uint8_t* reg = ds_row0 + (q >> 1) * C::DS_REGION;
+        // these 32 queries are 16-byte chunks 4q..4q+3 of this row of region h
 #pragma unroll
         for (int ch = 0; ch < 4; ++ch) {
-          const int chunk = (q & 1) * 4 + ch;
-          *reinterpret_cast<uint4*>(reg + ((chunk ^ sw) << 4)) =
+          const int chunk = q * 4 + ch;
+          *reinterpret_cast<uint4*>(ds_row + ((chunk ^ sw) << 4)) =
               make_uint4(pk[ch * 4], pk[ch * 4 + 1], pk[ch * 4 + 2], pk[ch * 4 + 3]);
         }
       }
@@ -432,7 +473,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       tc_fence_before();
       mbar_arrive(&sh.ds_full);
     }
-    // epilogue: dV and scale * dK rows of this key tile
+    // epilogue: group 0 writes dV, group 1 writes scale * dK, rows of this key tile
     if (ok) {
       if (T > 0) {
         ok = __all_sync(0xffffffffu, guarded_wait(&sh.dkv_full, 0, abort_flag, wd, kSiteBwdFinal));
@@ -441,66 +482,97 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       if (ok) {
         const bool store = key < p.m;
         const size_t off = (static_cast<size_t>(bh) * p.m + (store ? key : 0)) * D;
-        uint4* dv_row = reinterpret_cast<uint4*>(p.dv + off);
-        uint4* dk_row = reinterpret_cast<uint4*>(p.dk + off);
+        uint4* dst = reinterpret_cast<uint4*>((h ? p.dk : p.dv) + off);
+        const float mul = h ? p.scale : 1.f;
 #pragma unroll
-        for (int which = 0; which < 2; ++which) {
-          const float mul = which ? p.scale : 1.f;
-          uint4* dst = which ? dk_row : dv_row;
+        for (int q = 0; q < D / 32; ++q) {
+          uint32_t v[32];
+          if (T > 0) {
+            tmem_ld32(tmem + lane_base + (h ? C::TM_DK : C::TM_DV) + q * 32, v);
+            tmem_ld_wait();
+          } else {
 #pragma unroll
-          for (int q = 0; q < D / 32; ++q) {
-            uint32_t v[32];
-            if (T > 0) {
-              tmem_ld32(tmem + lane_base + (which ? C::TM_DK : C::TM_DV) + q * 32, v);
-              tmem_ld_wait();
-            } else {
+            for (int i = 0; i < 32; ++i) v[i] = 0u;
+          }
+          uint32_t pk[16];
 #pragma unroll
-              for (int i = 0; i < 32; ++i) v[i] = 0u;
-            }
-            uint32_t pk[16];
+          for (int i = 0; i < 16; ++i)
+            pk[i] = pack_bf16x2(__uint_as_float(v[2 * i]) * mul, __uint_as_float(v[2 * i + 1]) * mul);
+          if (store) {
 #pragma unroll
-            for (int i = 0; i < 16; ++i)
-              pk[i] = pack_bf16x2(__uint_as_float(v[2 * i]) * mul, __uint_as_float(v[2 * i + 1]) * mul);
-            if (store) {
-#pragma unroll
-              for (int u = 0; u < 4; ++u)
-                dst[q * 4 + u] = make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
-            }
+            for (int u = 0; u < 4; ++u)
+              dst[q * 4 + u] = make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
           }
         }
       }
     }
   } else {
-    // ------------------------------------------------------------ dQ accumulation (warps 4-7)
+    // ------------------------------------------------------------ dQ accumulation (warps 8-11)
     reg_dealloc<C::REG_DQ>();
-    const int r = tid - 128;                           // query row within the tile = TMEM lane
+    const int r = tid - 256;                           // query row within the tile = TMEM lane
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t t_dq = tmem + lane_base + C::TM_DQ;
+    uint8_t* stage_row = smem + C::OFF_DQS + r * 128;
+    const int sw = r & 7;
     for (int t = 0; t < T; ++t) {
-      const int qrow = (i_start + t) * 128 + r;
-      if (!__all_sync(0xffffffffu, guarded_wait(&sh.dq_full, t & 1, abort_flag, wd, kSiteBwdDQ))) break;
-      tc_fence_after();
-      float4* acc = reinterpret_cast<float4*>(p.dq_acc + (static_cast<size_t>(bh) * p.n_pad + qrow) * D);
+      const int qrow0 = qtile_row(t);
+      const bool ok = __all_sync(0xffffffffu, guarded_wait(&sh.dq_full, t & 1, abort_flag, wd, kSiteBwdDQ));
+      if (C::DQ_TMA) {
+        // the previous tile's reduce must have read the staging tile
+        if (ok && r == 0) bulk_wait_read_all();
+        // every warp of the group reaches the barrier; a failed wait has set the
+        // CTA abort flag, so all four warps then leave together
+        named_bar_sync(1, 128);
+        if (*abort_flag) break;
+        tc_fence_after();
 #pragma unroll
-      for (int q = 0; q < D / 32; ++q) {
-        uint32_t v[32];
-        tmem_ld32(t_dq + q * 32, v);
-        tmem_ld_wait();
-        if (qrow < p.n) {
+        for (int q = 0; q < D / 32; ++q) {
+          uint32_t v[32];
+          tmem_ld32(t_dq + q * 32, v);
+          tmem_ld_wait();
 #pragma unroll
-          for (int u = 0; u < 8; ++u)
-            atomicAdd(acc + q * 8 + u, make_float4(__uint_as_float(v[4 * u]), __uint_as_float(v[4 * u + 1]),
-                                                   __uint_as_float(v[4 * u + 2]), __uint_as_float(v[4 * u + 3])));
+          for (int ch = 0; ch < 8; ++ch)
+            *reinterpret_cast<uint4*>(stage_row + q * C::DQ_BOX + ((ch ^ sw) << 4)) =
+                make_uint4(v[4 * ch], v[4 * ch + 1], v[4 * ch + 2], v[4 * ch + 3]);
         }
+        tc_fence_before();
+        mbar_arrive(&sh.dq_empty);
+        fence_proxy_async_smem();
+        named_bar_sync(1, 128);
+        if (r == 0) {
+#pragma unroll
+          for (int q = 0; q < D / 32; ++q)
+            tma_reduce_add_2d(&tm_dq, smem + C::OFF_DQS + q * C::DQ_BOX, q * 32, bh * p.n_pad + qrow0);
+          tma_store_commit();
+        }
+      } else {
+        if (!ok) break;
+        tc_fence_after();
+        const int qrow = qrow0 + r;
+        float4* acc = reinterpret_cast<float4*>(p.dq_acc + (static_cast<size_t>(bh) * p.n_pad + qrow) * D);
+#pragma unroll
+        for (int q = 0; q < D / 32; ++q) {
+          uint32_t v[32];
+          tmem_ld32(t_dq + q * 32, v);
+          tmem_ld_wait();
+          if (qrow < p.n) {
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+              atomicAdd(acc + q * 8 + u, make_float4(__uint_as_float(v[4 * u]), __uint_as_float(v[4 * u + 1]),
+                                                     __uint_as_float(v[4 * u + 2]), __uint_as_float(v[4 * u + 3])));
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(&sh.dq_empty);
       }
-      tc_fence_before();
-      mbar_arrive(&sh.dq_empty);
     }
+    // the reduces read shared memory until they complete
+    if (C::DQ_TMA && r == 0) tma_store_wait_all();
   }
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 9) {
+  if (warp == 13) {
     tc_fence_after();
     tmem_dealloc<512>(tmem);
   }
@@ -508,8 +580,8 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 
 template <int D>
 cudaError_t launch_bwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                         const CUtensorMap& tdo, const BwdPreParams& pre, const BwdParams& p,
-                         const BwdPostParams& post, int BH, cudaStream_t stream) {
+                         const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdPreParams& pre,
+                         const BwdParams& p, const BwdPostParams& post, int BH, cudaStream_t stream) {
   using C = Bwd<D>;
   static std::once_flag once[64];
   int dev = 0;
@@ -545,7 +617,7 @@ cudaError_t launch_bwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
   {
     dim3 grid(static_cast<unsigned>(BH), static_cast<unsigned>(p.num_kblocks));
     prof_begin(kKindBwdMain, stream);
-    attn_bwd_kernel<D><<<grid, C::THREADS, C::SMEM, stream>>>(tq, tk, tv, tdo, p);
+    attn_bwd_kernel<D><<<grid, C::THREADS, C::SMEM, stream>>>(tq, tk, tv, tdo, tdq, p);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     prof_end(kKindBwdMain, stream);
   }
@@ -563,12 +635,12 @@ cudaError_t launch_bwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
 }  // namespace
 
 cudaError_t launch_bwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                       const CUtensorMap& tdo, const BwdPreParams& pre, const BwdParams& p,
-                       const BwdPostParams& post, int BH, cudaStream_t stream) {
+                       const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdPreParams& pre,
+                       const BwdParams& p, const BwdPostParams& post, int BH, cudaStream_t stream) {
   switch (d) {
-    case 32: return launch_bwd_d<32>(tq, tk, tv, tdo, pre, p, post, BH, stream);
-    case 64: return launch_bwd_d<64>(tq, tk, tv, tdo, pre, p, post, BH, stream);
-    case 128: return launch_bwd_d<128>(tq, tk, tv, tdo, pre, p, post, BH, stream);
+    case 32: return launch_bwd_d<32>(tq, tk, tv, tdo, tdq, pre, p, post, BH, stream);
+    case 64: return launch_bwd_d<64>(tq, tk, tv, tdo, tdq, pre, p, post, BH, stream);
+    case 128: return launch_bwd_d<128>(tq, tk, tv, tdo, tdq, pre, p, post, BH, stream);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -12,6 +12,8 @@ namespace attn {
 
 // Device error word values (0 = no error). The low byte names the wait site.
 constexpr uint32_t kDevTimeout = 0x100u;
+// A kernel could not place its shared-memory tiles (alignment); it did no work.
+constexpr uint32_t kDevLayout = 0x200u;
 
 // Sites, for diagnosis of a watchdog report.
 enum WaitSite : uint32_t {
@@ -106,8 +108,9 @@ struct BwdPostParams {
   int n, n_pad, d, BH;
 };
 
+// tdq: 2-D fp32 map over the dQ accumulator [BH*n_pad, d], box 32 x 128, 128-byte swizzle.
 cudaError_t launch_bwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                       const CUtensorMap& tdo, const BwdPreParams& pre, const BwdParams& p,
-                       const BwdPostParams& post, int BH, cudaStream_t stream);
+                       const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdPreParams& pre,
+                       const BwdParams& p, const BwdPostParams& post, int BH, cudaStream_t stream);
 
 }  // namespace attn
