@@ -22,15 +22,15 @@
 //         warps 0-7  two warpgroups, one thread per key row each, on
 //                    disjoint query columns: P, dS, and the dK/dV epilogue.
 //         warps 8-11 one thread per query row: add dQ_i into the fp32
-//                    accumulator (TMA reduce-add, or vector atomics for d = 128).
+//                    accumulator with TMA reduce-adds.
 //         warp 12    TMA producer (tiles, and the per-row statistics by
 //                    bulk copy), warp 13 MMA issuer.
 //   post  dQ = bf16(scale * accumulator).
 //
 // TMEM columns: S^T [0,128), dP^T [128,256), dV [256,256+D), dK [256+D,256+2D),
 // dQ [256+2D,256+3D) for D <= 64; for D = 128 dQ reuses the dP^T columns.
-// dQ leaves the SM by a TMA reduce-add of a staged fp32 tile (d <= 64) or by
-// vector atomics (d = 128, no shared memory left for staging).
+// dQ leaves the SM by TMA reduce-adds of a staged fp32 tile (d = 128 stages
+// it through the dS buffer, two rounds of 64 columns).
 // Warps (512 threads): 0-3 and 4-7 the two compute warpgroups (query columns
 // 0..63 / 64..127 of every tile), 8-11 dQ accumulation, 12 TMA producer,
 // 13 MMA issuer; registers split 160 / 160 / 72 / 56 with setmaxnreg.
@@ -129,13 +129,17 @@ struct Bwd {
   static constexpr uint32_t OFF_DS = 6 * TILE;                   // dS^T: 2 regions [128 keys][64 queries]
   static constexpr uint32_t OFF_STAT = OFF_DS + 2 * DS_REGION;   // per stage: lse*log2(e)[128], D[128]
   static constexpr uint32_t STAT_BYTES = 2u * 128u * 4u;
-  // d <= 64: the fp32 dQ tile is staged in shared memory (128-byte swizzled
-  // boxes of 32 columns) and added into the accumulator by one TMA reduce;
-  // d = 128 has no room left and adds with vector atomics instead.
-  static constexpr bool DQ_TMA = (D <= 64);
+  // The fp32 dQ tile is staged in shared memory (128-byte swizzled boxes of
+  // 32 columns) and added into the accumulator by TMA reduces. d <= 64 has a
+  // staging area of its own; d = 128 has no room left and stages through the
+  // dS buffer (free once dK and dQ have read it) in two rounds of 64 columns,
+  // releasing the buffer to the next tile's dS when the reduces have read it.
   static constexpr uint32_t DQ_BOX = 128u * 32u * 4u;
+  static constexpr bool DQ_IN_DS = (D > 64);
+  static constexpr int DQ_ROUNDS = DQ_IN_DS ? 2 : 1;
+  static constexpr int DQ_BOXES_PER_ROUND = (D / 32) / DQ_ROUNDS;
   static constexpr uint32_t OFF_DQS = OFF_STAT + 2 * STAT_BYTES;
-  static constexpr uint32_t DQS_BYTES = DQ_TMA ? (D / 32) * DQ_BOX : 0u;
+  static constexpr uint32_t DQS_BYTES = DQ_IN_DS ? 0u : (D / 32) * DQ_BOX;
   static constexpr uint32_t OFF_BAR = OFF_DQS + DQS_BYTES;
   static constexpr uint32_t PAYLOAD = OFF_BAR + 256;
   static constexpr uint32_t SMEM_LIMIT = 232448;                 // opt-in maximum per block
@@ -233,7 +237,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     prefetch_tensormap(&tm_k);
     prefetch_tensormap(&tm_v);
     prefetch_tensormap(&tm_do);
-    if (C::DQ_TMA) prefetch_tensormap(&tm_dq);
+    prefetch_tensormap(&tm_dq);
   }
   tc_fence_before();
   __syncthreads();
@@ -353,7 +357,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           mma_ss(tmem + C::TM_DQ, da, b_mn(sK, k), id_dq, k > 0 ? 1u : 0u);
         }
         mma_commit(&sh.dq_full);
-        mma_commit(&sh.ds_empty);
+        if (!C::DQ_IN_DS) mma_commit(&sh.ds_empty);  // else the dQ warpgroup releases it
         mma_commit(&sh.qdo_empty[st]);
       }
       __syncwarp();
@@ -512,62 +516,55 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     const int r = tid - 256;                           // query row within the tile = TMEM lane
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t t_dq = tmem + lane_base + C::TM_DQ;
-    uint8_t* stage_row = smem + C::OFF_DQS + r * 128;
+    uint8_t* stage = smem + (C::DQ_IN_DS ? C::OFF_DS : C::OFF_DQS);
+    uint8_t* stage_row = stage + r * 128;
     const int sw = r & 7;
     for (int t = 0; t < T; ++t) {
       const int qrow0 = qtile_row(t);
       const bool ok = __all_sync(0xffffffffu, guarded_wait(&sh.dq_full, t & 1, abort_flag, wd, kSiteBwdDQ));
-      if (C::DQ_TMA) {
-        // the previous tile's reduce must have read the staging tile
+      // every warp of the group reaches the barriers; a failed wait has set the
+      // CTA abort flag, so all four warps then leave together
+#pragma unroll
+      for (int round = 0; round < C::DQ_ROUNDS; ++round) {
+        // the previous reduce must have read the staging tile
         if (ok && r == 0) bulk_wait_read_all();
-        // every warp of the group reaches the barrier; a failed wait has set the
-        // CTA abort flag, so all four warps then leave together
         named_bar_sync(1, 128);
         if (*abort_flag) break;
         tc_fence_after();
 #pragma unroll
-        for (int q = 0; q < D / 32; ++q) {
+        for (int b = 0; b < C::DQ_BOXES_PER_ROUND; ++b) {
+          const int q = round * C::DQ_BOXES_PER_ROUND + b;  // 32-column box of dQ
           uint32_t v[32];
           tmem_ld32(t_dq + q * 32, v);
           tmem_ld_wait();
 #pragma unroll
           for (int ch = 0; ch < 8; ++ch)
-            *reinterpret_cast<uint4*>(stage_row + q * C::DQ_BOX + ((ch ^ sw) << 4)) =
+            *reinterpret_cast<uint4*>(stage_row + b * C::DQ_BOX + ((ch ^ sw) << 4)) =
                 make_uint4(v[4 * ch], v[4 * ch + 1], v[4 * ch + 2], v[4 * ch + 3]);
         }
-        tc_fence_before();
-        mbar_arrive(&sh.dq_empty);
+        if (round == C::DQ_ROUNDS - 1) {
+          tc_fence_before();
+          mbar_arrive(&sh.dq_empty);
+        }
         fence_proxy_async_smem();
         named_bar_sync(1, 128);
         if (r == 0) {
 #pragma unroll
-          for (int q = 0; q < D / 32; ++q)
-            tma_reduce_add_2d(&tm_dq, smem + C::OFF_DQS + q * C::DQ_BOX, q * 32, bh * p.n_pad + qrow0);
+          for (int b = 0; b < C::DQ_BOXES_PER_ROUND; ++b)
+            tma_reduce_add_2d(&tm_dq, stage + b * C::DQ_BOX, (round * C::DQ_BOXES_PER_ROUND + b) * 32,
+                              bh * p.n_pad + qrow0);
           tma_store_commit();
         }
-      } else {
-        if (!ok) break;
-        tc_fence_after();
-        const int qrow = qrow0 + r;
-        float4* acc = reinterpret_cast<float4*>(p.dq_acc + (static_cast<size_t>(bh) * p.n_pad + qrow) * D);
-#pragma unroll
-        for (int q = 0; q < D / 32; ++q) {
-          uint32_t v[32];
-          tmem_ld32(t_dq + q * 32, v);
-          tmem_ld_wait();
-          if (qrow < p.n) {
-#pragma unroll
-            for (int u = 0; u < 8; ++u)
-              atomicAdd(acc + q * 8 + u, make_float4(__uint_as_float(v[4 * u]), __uint_as_float(v[4 * u + 1]),
-                                                     __uint_as_float(v[4 * u + 2]), __uint_as_float(v[4 * u + 3])));
-          }
-        }
-        tc_fence_before();
-        mbar_arrive(&sh.dq_empty);
+      }
+      if (*abort_flag) break;
+      if (C::DQ_IN_DS && r == 0) {
+        // the dS buffer is free for the next tile once these reduces have read it
+        bulk_wait_read_all();
+        mbar_arrive(&sh.ds_empty);
       }
     }
     // the reduces read shared memory until they complete
-    if (C::DQ_TMA && r == 0) tma_store_wait_all();
+    if (r == 0) tma_store_wait_all();
   }
 
   tc_fence_before();
