@@ -122,11 +122,14 @@ struct Bwd {
   static constexpr uint32_t TILE = 128u * D * 2u;
   static constexpr uint32_t BOX = 128u * ATOM * 2u;
   static constexpr uint32_t DS_REGION = 128u * 64u * 2u;
+  // K/V tiles: two sets for d <= 64 so the next work item's keys load while
+  // the current one finishes; one set for d = 128 (shared memory is full).
+  static constexpr int KV_SETS = (D <= 64) ? 2 : 1;
   static constexpr uint32_t OFF_K = 0;
-  static constexpr uint32_t OFF_V = TILE;
-  static constexpr uint32_t OFF_Q = 2 * TILE;                    // 2 stages
-  static constexpr uint32_t OFF_DO = 4 * TILE;                   // 2 stages
-  static constexpr uint32_t OFF_DS = 6 * TILE;                   // dS^T: 2 regions [128 keys][64 queries]
+  static constexpr uint32_t OFF_V = KV_SETS * TILE;
+  static constexpr uint32_t OFF_Q = 2 * KV_SETS * TILE;          // 2 stages
+  static constexpr uint32_t OFF_DO = OFF_Q + 2 * TILE;           // 2 stages
+  static constexpr uint32_t OFF_DS = OFF_DO + 2 * TILE;          // dS^T: 2 regions [128 keys][64 queries]
   static constexpr uint32_t OFF_STAT = OFF_DS + 2 * DS_REGION;   // per stage: lse*log2(e)[128], D[128]
   static constexpr uint32_t STAT_BYTES = 2u * 128u * 4u;
   // The fp32 dQ tile is staged in shared memory (128-byte swizzled boxes of
@@ -147,16 +150,16 @@ struct Bwd {
   static constexpr uint32_t SMEM = (PAYLOAD + 1024 <= SMEM_LIMIT) ? PAYLOAD + 1024 : SMEM_LIMIT;
   static constexpr int THREADS = 512;
   // setmaxnreg split (registers per thread): compute, dQ, producer/MMA warpgroups.
-  static constexpr int REG_COMPUTE = 152, REG_DQ = 96, REG_OTHER = 80;
+  static constexpr int REG_COMPUTE = 152, REG_DQ = 96, REG_OTHER = 88;
   static constexpr bool ALIAS_DQ = (D > 64);
   static constexpr uint32_t TM_S = 0, TM_DP = 128, TM_DV = 256, TM_DK = 256 + D;
   static constexpr uint32_t TM_DQ = ALIAS_DQ ? 128u : (256u + 2u * D);
 };
 
 struct BwdShared {
-  uint64_t kv_full;
+  uint64_t kv_full[2], kv_empty[2];
   uint64_t qdo_full[2], qdo_empty[2];
-  uint64_t s_full, dp_full, p_full, ds_full, ds_empty, dq_full, dq_empty, dkv_full, drain;
+  uint64_t s_full, dp_full, p_full, ds_full, ds_empty, dq_full, dq_empty, dkv_full, acc_free, drain;
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -198,20 +201,26 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   uint8_t* smem = smem_raw + pad;
   BwdShared& sh = *reinterpret_cast<BwdShared*>(smem + C::OFF_BAR);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int bh = blockIdx.x;
-  const int kb = blockIdx.y;
-  const int k0 = kb * 128;
   volatile int* abort_flag = &sh.abort_flag;
   const int n_qt = (p.n + 127) / 128;
-  // Causal: query tiles wholly above this key tile see none of its keys.
-  const int i_start = p.causal ? min(k0 / 128, n_qt) : 0;
-  const int T = n_qt - i_start;
-  // Every key-tile CTA of a head walks the query tiles in the same order, so
-  // the Q and dO tiles it streams are read from DRAM once and then from L2.
-  auto qtile_row = [&](int t) { return (i_start + t) * 128; };
+  // Work item it = (key tile kb, head bh), key-tile major, so that under the
+  // causal mask the items with the most query tiles come first. Every CTA
+  // takes items it = blockIdx.x, blockIdx.x + gridDim.x, ...; the query tiles
+  // of an item: [i_start, n_qt) (causal: tiles wholly above the key tile see
+  // none of its keys). All CTAs of a head walk the query tiles in the same
+  // order, so the streamed Q and dO tiles come from DRAM once, then from L2.
+  auto item_of = [&](int it, int& bh, int& kb, int& i_start, int& T) {
+    kb = it / p.BH;
+    bh = it - kb * p.BH;
+    i_start = p.causal ? min(kb, n_qt) : 0;
+    T = n_qt - i_start;
+  };
 
   if (tid == 0) {
-    mbar_init(&sh.kv_full, 1);
+    for (int s = 0; s < C::KV_SETS; ++s) {
+      mbar_init(&sh.kv_full[s], 1);
+      mbar_init(&sh.kv_empty[s], 1);
+    }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&sh.qdo_full[s], 1);
       mbar_init(&sh.qdo_empty[s], 1);
@@ -224,6 +233,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     mbar_init(&sh.dq_full, 1);
     mbar_init(&sh.dq_empty, 128);
     mbar_init(&sh.dkv_full, 1);
+    mbar_init(&sh.acc_free, 256);
     mbar_init(&sh.drain, 1);
     sh.abort_flag = 0;
     fence_mbar_init();
@@ -250,36 +260,53 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   }
   if (warp == 12) {
     // ------------------------------------------------------------ TMA producer
-    if (lane == 0 && T > 0) {
-      int last[2] = {-1, -1};
-      mbar_arrive_expect_tx(&sh.kv_full, 2 * C::TILE);
-      for (int a = 0; a < C::NATOM; ++a) {
-        tma_load_3d(smem + C::OFF_K + a * C::BOX, &tm_k, &sh.kv_full, a * C::ATOM, k0, bh);
-        tma_load_3d(smem + C::OFF_V + a * C::BOX, &tm_v, &sh.kv_full, a * C::ATOM, k0, bh);
-      }
-      const float* lse2_h = p.lse2 + static_cast<size_t>(bh) * p.n_pad;
-      const float* D_h = p.Dsum + static_cast<size_t>(bh) * p.n_pad;
-      for (int t = 0; t < T; ++t) {
-        const int st = t & 1;
-        const uint32_t ph = (t >> 1) & 1;
-        if (t >= 2 && !guarded_wait(&sh.qdo_empty[st], ph ^ 1, abort_flag, wd, kSiteBwdFree)) break;
-        const int q_row = qtile_row(t);
-        mbar_arrive_expect_tx(&sh.qdo_full[st], 2 * C::TILE + C::STAT_BYTES);
+    if (lane == 0) {
+      // parity of the last fill of each K/V set and each Q/dO stage (-1: never filled);
+      // scalars rather than arrays so that they stay in registers
+      int kv_last0 = -1, kv_last1 = -1, q_last0 = -1, q_last1 = -1;
+      int g = 0, li = 0;
+      bool ok = true;
+      for (int it = blockIdx.x; ok && it < p.num_items; it += gridDim.x, ++li) {
+        int bh, kb, i_start, T;
+        item_of(it, bh, kb, i_start, T);
+        const int set = li % C::KV_SETS, use = li / C::KV_SETS;
+        if (li >= C::KV_SETS && !guarded_wait(&sh.kv_empty[set], (use - 1) & 1, abort_flag, wd, kSiteBwdFree)) break;
+        mbar_arrive_expect_tx(&sh.kv_full[set], 2 * C::TILE);
         for (int a = 0; a < C::NATOM; ++a) {
-          tma_load_3d(smem + C::OFF_Q + st * C::TILE + a * C::BOX, &tm_q, &sh.qdo_full[st], a * C::ATOM, q_row, bh);
-          tma_load_3d(smem + C::OFF_DO + st * C::TILE + a * C::BOX, &tm_do, &sh.qdo_full[st], a * C::ATOM, q_row, bh);
+          tma_load_3d(smem + C::OFF_K + set * C::TILE + a * C::BOX, &tm_k, &sh.kv_full[set], a * C::ATOM,
+                      kb * 128, bh);
+          tma_load_3d(smem + C::OFF_V + set * C::TILE + a * C::BOX, &tm_v, &sh.kv_full[set], a * C::ATOM,
+                      kb * 128, bh);
         }
-        bulk_load(stat + st * 256, lse2_h + q_row, 512, &sh.qdo_full[st]);
-        bulk_load(stat + st * 256 + 128, D_h + q_row, 512, &sh.qdo_full[st]);
-        last[st] = static_cast<int>(ph);
+        if (set == 0) kv_last0 = use & 1; else kv_last1 = use & 1;
+        const float* lse2_h = p.lse2 + static_cast<size_t>(bh) * p.n_pad;
+        const float* D_h = p.Dsum + static_cast<size_t>(bh) * p.n_pad;
+        for (int t = 0; t < T; ++t, ++g) {
+          const int st = g & 1;
+          const uint32_t ph = (g >> 1) & 1;
+          if (g >= 2 && !guarded_wait(&sh.qdo_empty[st], ph ^ 1, abort_flag, wd, kSiteBwdFree)) {
+            ok = false;
+            break;
+          }
+          const int q_row = (i_start + t) * 128;
+          mbar_arrive_expect_tx(&sh.qdo_full[st], 2 * C::TILE + C::STAT_BYTES);
+          for (int a = 0; a < C::NATOM; ++a) {
+            tma_load_3d(smem + C::OFF_Q + st * C::TILE + a * C::BOX, &tm_q, &sh.qdo_full[st], a * C::ATOM, q_row, bh);
+            tma_load_3d(smem + C::OFF_DO + st * C::TILE + a * C::BOX, &tm_do, &sh.qdo_full[st], a * C::ATOM, q_row, bh);
+          }
+          bulk_load(stat + st * 256, lse2_h + q_row, 512, &sh.qdo_full[st]);
+          bulk_load(stat + st * 256 + 128, D_h + q_row, 512, &sh.qdo_full[st]);
+          if (st == 0) q_last0 = static_cast<int>(ph); else q_last1 = static_cast<int>(ph);
+        }
       }
-      drain_wait_b(&sh.kv_full, 0, wd);
-      for (int s = 0; s < 2; ++s)
-        if (last[s] >= 0) drain_wait_b(&sh.qdo_full[s], static_cast<uint32_t>(last[s]), wd);
+      // Let every copy this thread started land before shared memory is released.
+      if (kv_last0 >= 0) drain_wait_b(&sh.kv_full[0], static_cast<uint32_t>(kv_last0), wd);
+      if (kv_last1 >= 0) drain_wait_b(&sh.kv_full[1], static_cast<uint32_t>(kv_last1), wd);
+      if (q_last0 >= 0) drain_wait_b(&sh.qdo_full[0], static_cast<uint32_t>(q_last0), wd);
+      if (q_last1 >= 0) drain_wait_b(&sh.qdo_full[1], static_cast<uint32_t>(q_last1), wd);
     }
   } else if (warp == 13) {
     // ------------------------------------------------------------ MMA issuer
-    const uint32_t sK = smem_u32(smem + C::OFF_K), sV = smem_u32(smem + C::OFF_V);
     const uint32_t sQ = smem_u32(smem + C::OFF_Q), sDO = smem_u32(smem + C::OFF_DO);
     const uint32_t sDS = smem_u32(smem + C::OFF_DS);
     const uint32_t id_s = idesc_bf16_f32(128, 128, false, false) | (p.neg ? (1u << 13) : 0u);
@@ -304,76 +331,101 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       return __all_sync(0xffffffffu, guarded_wait(bar, parity, abort_flag, wd, site));
     };
     bool ok = true;
-    if (T > 0) {
-      ok = wait_all(&sh.kv_full, 0, kSiteBwdLoad) && wait_all(&sh.qdo_full[0], 0, kSiteBwdLoad);
-      if (ok && lane == 0) {
-        tc_fence_after();
-        issue_kmajor(tmem + C::TM_S, sK, sQ, id_s);
-        mma_commit(&sh.s_full);
-        issue_kmajor(tmem + C::TM_DP, sV, sDO, id_dp);
-        mma_commit(&sh.dp_full);
-      }
-      __syncwarp();
-    }
-    for (int t = 0; ok && t < T; ++t) {
-      const int st = t & 1;
-      const uint32_t q_off = st * C::TILE;
-      // dV += P^T dO; P^T (bf16) sits in TMEM columns [0,32) and [64,96) of S^T,
-      // one block per compute warpgroup (queries 0..63 and 64..127)
-      if (!(ok = wait_all(&sh.p_full, t & 1, kSiteBwdS))) break;
-      if (lane == 0) {
-        tc_fence_after();
-#pragma unroll
-        for (int k = 0; k < 8; ++k)
-          mma_ts(tmem + C::TM_DV, tmem + C::TM_S + (k >> 2) * 64 + (k & 3) * 8, b_mn(sDO + q_off, k), id_kv,
-                 (t > 0 || k > 0) ? 1u : 0u);
-      }
-      __syncwarp();
-      // next S^T while the compute warps form dS
-      if (t + 1 < T) {
-        if (!(ok = wait_all(&sh.qdo_full[st ^ 1], ((t + 1) >> 1) & 1, kSiteBwdLoad))) break;
+    int g = 0, li = 0;
+    for (int it = blockIdx.x; ok && it < p.num_items; it += gridDim.x, ++li) {
+      int bh, kb, i_start, T;
+      item_of(it, bh, kb, i_start, T);
+      const int set = li % C::KV_SETS, use = li / C::KV_SETS;
+      const uint32_t sK = smem_u32(smem + C::OFF_K + set * C::TILE);
+      const uint32_t sV = smem_u32(smem + C::OFF_V + set * C::TILE);
+      // The previous item's epilogue must have read dK, dV out of TMEM (this
+      // also keeps the issuer at most one item ahead of the compute warps).
+      if (li >= 1 && !(ok = wait_all(&sh.acc_free, (li - 1) & 1, kSiteBwdFinal))) break;
+      if (!(ok = wait_all(&sh.kv_full[set], use & 1, kSiteBwdLoad))) break;
+      if (T > 0) {
+        if (!(ok = wait_all(&sh.qdo_full[g & 1], (g >> 1) & 1, kSiteBwdLoad))) break;
         if (lane == 0) {
-          issue_kmajor(tmem + C::TM_S, sK, sQ + (st ^ 1) * C::TILE, id_s);
+          tc_fence_after();
+          issue_kmajor(tmem + C::TM_S, sK, sQ + (g & 1) * C::TILE, id_s);
           mma_commit(&sh.s_full);
         }
         __syncwarp();
-      }
-      if (!(ok = wait_all(&sh.ds_full, t & 1, kSiteBwdDS))) break;
-      if (!C::ALIAS_DQ && t >= 1) {
-        if (!(ok = wait_all(&sh.dq_empty, (t - 1) & 1, kSiteBwdDQ))) break;
-      }
-      if (lane == 0) {
-        tc_fence_after();
-        // dK += dS^T Q : A = dS^T (K-major over queries), B = Q (MN-major)
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const uint64_t da = smem_desc(sDS + (k >> 2) * C::DS_REGION + (k & 3) * 32, 16, 1024, 2);
-          mma_ss(tmem + C::TM_DK, da, b_mn(sQ + q_off, k), id_kv, (t > 0 || k > 0) ? 1u : 0u);
-        }
-        // dQ = dS K : A = dS (MN-major: queries contiguous), B = K (MN-major)
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const uint64_t da = smem_desc(sDS + k * 16 * 128, C::DS_REGION, 1024, 2);
-          mma_ss(tmem + C::TM_DQ, da, b_mn(sK, k), id_dq, k > 0 ? 1u : 0u);
-        }
-        mma_commit(&sh.dq_full);
-        if (!C::DQ_IN_DS) mma_commit(&sh.ds_empty);  // else the dQ warpgroup releases it
-        mma_commit(&sh.qdo_empty[st]);
-      }
-      __syncwarp();
-      if (t + 1 < T) {
-        if (C::ALIAS_DQ) {
-          if (!(ok = wait_all(&sh.dq_empty, t & 1, kSiteBwdDQ))) break;
-        }
+        // for d = 128 dP shares its TMEM columns with the previous tile's dQ
+        if (C::ALIAS_DQ && g >= 1 && !(ok = wait_all(&sh.dq_empty, (g - 1) & 1, kSiteBwdDQ))) break;
         if (lane == 0) {
           tc_fence_after();
-          issue_kmajor(tmem + C::TM_DP, sV, sDO + (st ^ 1) * C::TILE, id_dp);
+          issue_kmajor(tmem + C::TM_DP, sV, sDO + (g & 1) * C::TILE, id_dp);
           mma_commit(&sh.dp_full);
         }
         __syncwarp();
       }
+      for (int t = 0; ok && t < T; ++t) {
+        const int gt = g + t;
+        const int st = gt & 1;
+        const uint32_t q_off = st * C::TILE;
+        // dV += P^T dO; P^T (bf16) sits in TMEM columns [0,32) and [64,96) of S^T,
+        // one block per compute warpgroup (queries 0..63 and 64..127)
+        if (!(ok = wait_all(&sh.p_full, gt & 1, kSiteBwdS))) break;
+        if (lane == 0) {
+          tc_fence_after();
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            mma_ts(tmem + C::TM_DV, tmem + C::TM_S + (k >> 2) * 64 + (k & 3) * 8, b_mn(sDO + q_off, k), id_kv,
+                   (t > 0 || k > 0) ? 1u : 0u);
+        }
+        __syncwarp();
+        // next S^T while the compute warps form dS
+        if (t + 1 < T) {
+          if (!(ok = wait_all(&sh.qdo_full[st ^ 1], ((gt + 1) >> 1) & 1, kSiteBwdLoad))) break;
+          if (lane == 0) {
+            issue_kmajor(tmem + C::TM_S, sK, sQ + (st ^ 1) * C::TILE, id_s);
+            mma_commit(&sh.s_full);
+          }
+          __syncwarp();
+        }
+        if (!(ok = wait_all(&sh.ds_full, gt & 1, kSiteBwdDS))) break;
+        if (!C::ALIAS_DQ && gt >= 1) {
+          if (!(ok = wait_all(&sh.dq_empty, (gt - 1) & 1, kSiteBwdDQ))) break;
+        }
+        if (lane == 0) {
+          tc_fence_after();
+          // dK += dS^T Q : A = dS^T (K-major over queries), B = Q (MN-major)
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const uint64_t da = smem_desc(sDS + (k >> 2) * C::DS_REGION + (k & 3) * 32, 16, 1024, 2);
+            mma_ss(tmem + C::TM_DK, da, b_mn(sQ + q_off, k), id_kv, (t > 0 || k > 0) ? 1u : 0u);
+          }
+          // dQ = dS K : A = dS (MN-major: queries contiguous), B = K (MN-major)
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const uint64_t da = smem_desc(sDS + k * 16 * 128, C::DS_REGION, 1024, 2);
+            mma_ss(tmem + C::TM_DQ, da, b_mn(sK, k), id_dq, k > 0 ? 1u : 0u);
+          }
+          mma_commit(&sh.dq_full);
+          if (!C::DQ_IN_DS) mma_commit(&sh.ds_empty);  // else the dQ warpgroup releases it
+          mma_commit(&sh.qdo_empty[st]);
+        }
+        __syncwarp();
+        if (t + 1 < T) {
+          if (C::ALIAS_DQ) {
+            if (!(ok = wait_all(&sh.dq_empty, gt & 1, kSiteBwdDQ))) break;
+          }
+          if (lane == 0) {
+            tc_fence_after();
+            issue_kmajor(tmem + C::TM_DP, sV, sDO + (st ^ 1) * C::TILE, id_dp);
+            mma_commit(&sh.dp_full);
+          }
+          __syncwarp();
+        }
+      }
+      if (!ok) break;
+      if (lane == 0) {
+        mma_commit(&sh.dkv_full);
+        mma_commit(&sh.kv_empty[set]);
+      }
+      __syncwarp();
+      g += T;
     }
-    if (lane == 0 && T > 0) mma_commit(&sh.dkv_full);
     if (lane == 0) mma_commit(&sh.drain);
     __syncwarp();
     drain_wait_b(&sh.drain, 0, wd);
@@ -387,7 +439,6 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     const int h = warp >> 2;
     const int col0 = 64 * h;
     const int r = tid & 127;                            // key row within the tile = TMEM lane
-    const int key = k0 + r;
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t t_s = tmem + lane_base + C::TM_S + col0;
     const uint32_t t_dp = tmem + lane_base + C::TM_DP + col0;
@@ -395,120 +446,129 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     uint8_t* ds_row = smem + C::OFF_DS + h * C::DS_REGION + r * 128;
     const int sw = r & 7;
     bool ok = true;
-    for (int t = 0; t < T; ++t) {
-      const int st = t & 1;
-      const int q_row0 = qtile_row(t);
-      // queries [lo, hi) of this tile may attend to this key
-      const int lo = p.causal ? max(0, key - q_row0) : 0;
-      const int hi = (key < p.m) ? min(128, p.n - q_row0) : 0;
-      const bool masked = __any_sync(0xffffffffu, lo > col0 || hi < col0 + 64);
-      ok = __all_sync(0xffffffffu, guarded_wait(&sh.s_full, t & 1, abort_flag, wd, kSiteBwdS) &&
-                                       guarded_wait(&sh.qdo_full[st], (t >> 1) & 1, abort_flag, wd, kSiteBwdLoad));
-      if (!ok) break;
-      tc_fence_after();
-      const float* lse2_s = stat + st * 256 + col0;
-      const float* D_s = stat + st * 256 + 128 + col0;
-      // P^T in fp32 for dS below; rounded to bf16 for the dV product
-      float P[64];
-      {
-        uint32_t s[2][32];
-        tmem_ld32(t_s, s[0]);
-        tmem_ld32(t_s + 32, s[1]);
-        tmem_ld_wait();
+    int g = 0, li = 0;
+    for (int it = blockIdx.x; ok && it < p.num_items; it += gridDim.x, ++li) {
+      int bh, kb, i_start, T;
+      item_of(it, bh, kb, i_start, T);
+      const int key = kb * 128 + r;
+      for (int t = 0; t < T; ++t) {
+        const int gt = g + t;
+        const int st = gt & 1;
+        const int q_row0 = (i_start + t) * 128;
+        // queries [lo, hi) of this tile may attend to this key
+        const int lo = p.causal ? max(0, key - q_row0) : 0;
+        const int hi = (key < p.m) ? min(128, p.n - q_row0) : 0;
+        const bool masked = __any_sync(0xffffffffu, lo > col0 || hi < col0 + 64);
+        ok = __all_sync(0xffffffffu, guarded_wait(&sh.s_full, gt & 1, abort_flag, wd, kSiteBwdS) &&
+                                         guarded_wait(&sh.qdo_full[st], (gt >> 1) & 1, abort_flag, wd, kSiteBwdLoad));
+        if (!ok) break;
+        tc_fence_after();
+        const float* lse2_s = stat + st * 256 + col0;
+        const float* D_s = stat + st * 256 + 128 + col0;
+        // P^T in fp32 for dS below; rounded to bf16 for the dV product
+        float P[64];
+        {
+          uint32_t s[2][32];
+          tmem_ld32(t_s, s[0]);
+          tmem_ld32(t_s + 32, s[1]);
+          tmem_ld_wait();
 #pragma unroll
-        for (int q = 0; q < 2; ++q) {
+          for (int q = 0; q < 2; ++q) {
 #pragma unroll
-          for (int i4 = 0; i4 < 8; ++i4) {
-            const float4 L = *reinterpret_cast<const float4*>(lse2_s + q * 32 + i4 * 4);
-            const float Lv[4] = {L.x, L.y, L.z, L.w};
+            for (int i4 = 0; i4 < 8; ++i4) {
+              const float4 L = *reinterpret_cast<const float4*>(lse2_s + q * 32 + i4 * 4);
+              const float Lv[4] = {L.x, L.y, L.z, L.w};
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              const int col = col0 + q * 32 + i4 * 4 + u;
-              float x = fmaf(__uint_as_float(s[q][i4 * 4 + u]), c, -Lv[u]);
-              if (masked && (col < lo || col >= hi)) x = -INFINITY;
-              P[q * 32 + i4 * 4 + u] = ex2f(x);
+              for (int u = 0; u < 4; ++u) {
+                const int col = col0 + q * 32 + i4 * 4 + u;
+                float x = fmaf(__uint_as_float(s[q][i4 * 4 + u]), c, -Lv[u]);
+                if (masked && (col < lo || col >= hi)) x = -INFINITY;
+                P[q * 32 + i4 * 4 + u] = ex2f(x);
+              }
             }
           }
         }
-      }
 #pragma unroll
-      for (int q = 0; q < 2; ++q) {
-        uint32_t pk[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(P[q * 32 + 2 * i], P[q * 32 + 2 * i + 1]);
-        tmem_st16(t_s + q * 16, pk);
-      }
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(&sh.p_full);
-      // dS = P (dP - D)
-      ok = __all_sync(0xffffffffu, guarded_wait(&sh.dp_full, t & 1, abort_flag, wd, kSiteBwdDP));
-      if (!ok) break;
-      tc_fence_after();
-      if (t >= 1) {
-        ok = __all_sync(0xffffffffu, guarded_wait(&sh.ds_empty, (t - 1) & 1, abort_flag, wd, kSiteBwdDS));
-        if (!ok) break;
-      }
-#pragma unroll
-      for (int q = 0; q < 2; ++q) {
-        uint32_t dp[32];
-        tmem_ld32(t_dp + q * 32, dp);
-        tmem_ld_wait();
-        uint32_t pk[16];
-#pragma unroll
-        for (int i4 = 0; i4 < 8; ++i4) {
-          const float4 Dv = *reinterpret_cast<const float4*>(D_s + q * 32 + i4 * 4);
-          const float ds0 = P[q * 32 + i4 * 4 + 0] * (__uint_as_float(dp[i4 * 4 + 0]) - Dv.x);
-          const float ds1 = P[q * 32 + i4 * 4 + 1] * (__uint_as_float(dp[i4 * 4 + 1]) - Dv.y);
-          const float ds2 = P[q * 32 + i4 * 4 + 2] * (__uint_as_float(dp[i4 * 4 + 2]) - Dv.z);
-          const float ds3 = P[q * 32 + i4 * 4 + 3] * (__uint_as_float(dp[i4 * 4 + 3]) - Dv.w);
-          pk[i4 * 2 + 0] = pack_bf16x2(ds0, ds1);
-          pk[i4 * 2 + 1] = pack_bf16x2(ds2, ds3);
-        }
-        // these 32 queries are 16-byte chunks 4q..4q+3 of this row of region h
-#pragma unroll
-        for (int ch = 0; ch < 4; ++ch) {
-          const int chunk = q * 4 + ch;
-          *reinterpret_cast<uint4*>(ds_row + ((chunk ^ sw) << 4)) =
-              make_uint4(pk[ch * 4], pk[ch * 4 + 1], pk[ch * 4 + 2], pk[ch * 4 + 3]);
-        }
-      }
-      fence_proxy_async_smem();
-      tc_fence_before();
-      mbar_arrive(&sh.ds_full);
-    }
-    // epilogue: group 0 writes dV, group 1 writes scale * dK, rows of this key tile
-    if (ok) {
-      if (T > 0) {
-        ok = __all_sync(0xffffffffu, guarded_wait(&sh.dkv_full, 0, abort_flag, wd, kSiteBwdFinal));
-        tc_fence_after();
-      }
-      if (ok) {
-        const bool store = key < p.m;
-        const size_t off = (static_cast<size_t>(bh) * p.m + (store ? key : 0)) * D;
-        uint4* dst = reinterpret_cast<uint4*>((h ? p.dk : p.dv) + off);
-        const float mul = h ? p.scale : 1.f;
-#pragma unroll
-        for (int q = 0; q < D / 32; ++q) {
-          uint32_t v[32];
-          if (T > 0) {
-            tmem_ld32(tmem + lane_base + (h ? C::TM_DK : C::TM_DV) + q * 32, v);
-            tmem_ld_wait();
-          } else {
-#pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] = 0u;
-          }
+        for (int q = 0; q < 2; ++q) {
           uint32_t pk[16];
 #pragma unroll
-          for (int i = 0; i < 16; ++i)
-            pk[i] = pack_bf16x2(__uint_as_float(v[2 * i]) * mul, __uint_as_float(v[2 * i + 1]) * mul);
-          if (store) {
+          for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(P[q * 32 + 2 * i], P[q * 32 + 2 * i + 1]);
+          tmem_st16(t_s + q * 16, pk);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(&sh.p_full);
+        // dS = P (dP - D)
+        ok = __all_sync(0xffffffffu, guarded_wait(&sh.dp_full, gt & 1, abort_flag, wd, kSiteBwdDP));
+        if (!ok) break;
+        tc_fence_after();
+        if (gt >= 1) {
+          ok = __all_sync(0xffffffffu, guarded_wait(&sh.ds_empty, (gt - 1) & 1, abort_flag, wd, kSiteBwdDS));
+          if (!ok) break;
+        }
 #pragma unroll
-            for (int u = 0; u < 4; ++u)
-              dst[q * 4 + u] = make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+        for (int q = 0; q < 2; ++q) {
+          uint32_t dp[32];
+          tmem_ld32(t_dp + q * 32, dp);
+          tmem_ld_wait();
+          uint32_t pk[16];
+#pragma unroll
+          for (int i4 = 0; i4 < 8; ++i4) {
+            const float4 Dv = *reinterpret_cast<const float4*>(D_s + q * 32 + i4 * 4);
+            const float ds0 = P[q * 32 + i4 * 4 + 0] * (__uint_as_float(dp[i4 * 4 + 0]) - Dv.x);
+            const float ds1 = P[q * 32 + i4 * 4 + 1] * (__uint_as_float(dp[i4 * 4 + 1]) - Dv.y);
+            const float ds2 = P[q * 32 + i4 * 4 + 2] * (__uint_as_float(dp[i4 * 4 + 2]) - Dv.z);
+            const float ds3 = P[q * 32 + i4 * 4 + 3] * (__uint_as_float(dp[i4 * 4 + 3]) - Dv.w);
+            pk[i4 * 2 + 0] = pack_bf16x2(ds0, ds1);
+            pk[i4 * 2 + 1] = pack_bf16x2(ds2, ds3);
+          }
+          // these 32 queries are 16-byte chunks 4q..4q+3 of this row of region h
+#pragma unroll
+          for (int ch = 0; ch < 4; ++ch) {
+            const int chunk = q * 4 + ch;
+            *reinterpret_cast<uint4*>(ds_row + ((chunk ^ sw) << 4)) =
+                make_uint4(pk[ch * 4], pk[ch * 4 + 1], pk[ch * 4 + 2], pk[ch * 4 + 3]);
           }
         }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive(&sh.ds_full);
       }
+      if (!ok) break;
+      // epilogue: group 0 writes dV, group 1 writes scale * dK, rows of this key tile.
+      // The wait is taken for items without query tiles too: it keeps these warps
+      // from running more than one item ahead of the MMA warp, so that no
+      // barrier is waited on two phases ahead.
+      ok = __all_sync(0xffffffffu, guarded_wait(&sh.dkv_full, li & 1, abort_flag, wd, kSiteBwdFinal));
+      if (!ok) break;
+      tc_fence_after();
+      const bool store = key < p.m;
+      const size_t off = (static_cast<size_t>(bh) * p.m + (store ? key : 0)) * D;
+      uint4* dst = reinterpret_cast<uint4*>((h ? p.dk : p.dv) + off);
+      const float mul = h ? p.scale : 1.f;
+#pragma unroll
+      for (int q = 0; q < D / 32; ++q) {
+        uint32_t v[32];
+        if (T > 0) {
+          tmem_ld32(tmem + lane_base + (h ? C::TM_DK : C::TM_DV) + q * 32, v);
+          tmem_ld_wait();
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] = 0u;
+        }
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          pk[i] = pack_bf16x2(__uint_as_float(v[2 * i]) * mul, __uint_as_float(v[2 * i + 1]) * mul);
+        if (store) {
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+            dst[q * 4 + u] = make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&sh.acc_free);
+      g += T;
     }
   } else {
     // ------------------------------------------------------------ dQ accumulation (warps 8-11)
@@ -519,49 +579,60 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     uint8_t* stage = smem + (C::DQ_IN_DS ? C::OFF_DS : C::OFF_DQS);
     uint8_t* stage_row = stage + r * 128;
     const int sw = r & 7;
-    for (int t = 0; t < T; ++t) {
-      const int qrow0 = qtile_row(t);
-      const bool ok = __all_sync(0xffffffffu, guarded_wait(&sh.dq_full, t & 1, abort_flag, wd, kSiteBwdDQ));
-      // every warp of the group reaches the barriers; a failed wait has set the
-      // CTA abort flag, so all four warps then leave together
+    int g = 0;
+    bool stop = false;
+    for (int it = blockIdx.x; !stop && it < p.num_items; it += gridDim.x) {
+      int bh, kb, i_start, T;
+      item_of(it, bh, kb, i_start, T);
+      for (int t = 0; t < T; ++t) {
+        const int gt = g + t;
+        const int qrow0 = (i_start + t) * 128;
+        const bool ok = __all_sync(0xffffffffu, guarded_wait(&sh.dq_full, gt & 1, abort_flag, wd, kSiteBwdDQ));
+        // Every warp of the group reaches the barriers. The decision to leave is
+        // ORed over the group at a barrier, so all four warps leave together
+        // even when another role raises the abort flag meanwhile.
 #pragma unroll
-      for (int round = 0; round < C::DQ_ROUNDS; ++round) {
-        // the previous reduce must have read the staging tile
-        if (ok && r == 0) bulk_wait_read_all();
-        named_bar_sync(1, 128);
-        if (*abort_flag) break;
-        tc_fence_after();
+        for (int round = 0; round < C::DQ_ROUNDS; ++round) {
+          // the previous reduce must have read the staging tile
+          if (ok && r == 0) bulk_wait_read_all();
+          if (named_bar_or(1, 128, !ok || *abort_flag != 0)) {
+            stop = true;
+            break;
+          }
+          tc_fence_after();
 #pragma unroll
-        for (int b = 0; b < C::DQ_BOXES_PER_ROUND; ++b) {
-          const int q = round * C::DQ_BOXES_PER_ROUND + b;  // 32-column box of dQ
-          uint32_t v[32];
-          tmem_ld32(t_dq + q * 32, v);
-          tmem_ld_wait();
+          for (int b = 0; b < C::DQ_BOXES_PER_ROUND; ++b) {
+            const int q = round * C::DQ_BOXES_PER_ROUND + b;  // 32-column box of dQ
+            uint32_t v[32];
+            tmem_ld32(t_dq + q * 32, v);
+            tmem_ld_wait();
 #pragma unroll
-          for (int ch = 0; ch < 8; ++ch)
-            *reinterpret_cast<uint4*>(stage_row + b * C::DQ_BOX + ((ch ^ sw) << 4)) =
-                make_uint4(v[4 * ch], v[4 * ch + 1], v[4 * ch + 2], v[4 * ch + 3]);
+            for (int ch = 0; ch < 8; ++ch)
+              *reinterpret_cast<uint4*>(stage_row + b * C::DQ_BOX + ((ch ^ sw) << 4)) =
+                  make_uint4(v[4 * ch], v[4 * ch + 1], v[4 * ch + 2], v[4 * ch + 3]);
+          }
+          if (round == C::DQ_ROUNDS - 1) {
+            tc_fence_before();
+            mbar_arrive(&sh.dq_empty);
+          }
+          fence_proxy_async_smem();
+          named_bar_sync(1, 128);
+          if (r == 0) {
+#pragma unroll
+            for (int b = 0; b < C::DQ_BOXES_PER_ROUND; ++b)
+              tma_reduce_add_2d(&tm_dq, stage + b * C::DQ_BOX, (round * C::DQ_BOXES_PER_ROUND + b) * 32,
+                                bh * p.n_pad + qrow0);
+            tma_store_commit();
+          }
         }
-        if (round == C::DQ_ROUNDS - 1) {
-          tc_fence_before();
-          mbar_arrive(&sh.dq_empty);
-        }
-        fence_proxy_async_smem();
-        named_bar_sync(1, 128);
-        if (r == 0) {
-#pragma unroll
-          for (int b = 0; b < C::DQ_BOXES_PER_ROUND; ++b)
-            tma_reduce_add_2d(&tm_dq, stage + b * C::DQ_BOX, (round * C::DQ_BOXES_PER_ROUND + b) * 32,
-                              bh * p.n_pad + qrow0);
-          tma_store_commit();
+        if (stop) break;
+        if (C::DQ_IN_DS && r == 0) {
+          // the dS buffer is free for the next tile once these reduces have read it
+          bulk_wait_read_all();
+          mbar_arrive(&sh.ds_empty);
         }
       }
-      if (*abort_flag) break;
-      if (C::DQ_IN_DS && r == 0) {
-        // the dS buffer is free for the next tile once these reduces have read it
-        bulk_wait_read_all();
-        mbar_arrive(&sh.ds_empty);
-      }
+      g += T;
     }
     // the reduces read shared memory until they complete
     if (r == 0) tma_store_wait_all();
@@ -599,7 +670,7 @@ cudaError_t launch_bwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
       if ((e = cudaFuncGetAttributes(&fa, attn_bwd_kernel<D>)) != cudaSuccess) return e;
       regs_per_thread[dev & 63] = fa.numRegs;
     }
-    const int need = 128 * (C::REG_COMPUTE + C::REG_DQ + C::REG_OTHER);
+    const int need = 128 * (2 * C::REG_COMPUTE + C::REG_DQ + C::REG_OTHER);  // four warpgroups
     if (regs_per_thread[dev & 63] * C::THREADS < need) return cudaErrorInvalidConfiguration;
   }
   {
@@ -612,9 +683,19 @@ cudaError_t launch_bwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
     prof_end(kKindBwdPre, stream);
   }
   {
-    dim3 grid(static_cast<unsigned>(BH), static_cast<unsigned>(p.num_kblocks));
+    // persistent: one CTA per SM (at most one per work item) loops over items
+    static int sm_count[64] = {0};
+    if (sm_count[dev & 63] == 0) {
+      int c = 0;
+      if ((e = cudaDeviceGetAttribute(&c, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+      sm_count[dev & 63] = c > 0 ? c : 1;
+    }
+    BwdParams pp = p;
+    pp.BH = BH;
+    pp.num_items = BH * p.num_kblocks;
+    const int grid = pp.num_items < sm_count[dev & 63] ? pp.num_items : sm_count[dev & 63];
     prof_begin(kKindBwdMain, stream);
-    attn_bwd_kernel<D><<<grid, C::THREADS, C::SMEM, stream>>>(tq, tk, tv, tdo, tdq, p);
+    attn_bwd_kernel<D><<<grid, C::THREADS, C::SMEM, stream>>>(tq, tk, tv, tdo, tdq, pp);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     prof_end(kKindBwdMain, stream);
   }

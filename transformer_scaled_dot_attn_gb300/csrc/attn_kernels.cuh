@@ -98,6 +98,8 @@ struct BwdParams {
   float c;                  // |scale| * log2(e)
   float scale;              // signed scale, applied to dK
   int num_kblocks;          // ceil(m / 128)
+  int BH;                   // heads (set by the launcher)
+  int num_items;            // BH * num_kblocks work items (set by the launcher)
   Watchdog wd;
 };
 
