@@ -8,21 +8,31 @@
 //
 // One CTA owns NQ query tiles of 128 rows of one head and streams BN-key
 // tiles K_j, V_j through a TMA/mbarrier ring:
-//   warp 4*NQ      TMA producer: the Q tiles once, then K_j and V_j per stage.
-//   warp 4*NQ + 1  MMA issuer (one lane): S_g = Q_g K_j^T into TMEM, then
-//                  O_g += P_g V_j with P_g read from TMEM (aliasing S_g).
-//   warps 4g..4g+3 softmax of query tile g, one thread per row: load the S
-//                  row from TMEM, row max, p = 2^(s*c - m) with
-//                  c = scale*log2(e), row sum, bf16 P back into TMEM, rescale
-//                  of the O row when the running max grew by more than 2^8,
-//                  and finally O / l and lse.
-// Issue order per key tile j: PV_0(j), S_0(j+1), PV_1(j), S_1(j+1), ...; each
-// softmax group works on tile j+1 while the tensor cores run the other
-// groups' products, and the commit that signals S_g(j+1) also proves that
-// PV_g(j) finished, so the O rescale needs no further wait. With the causal
+//   warp 4*NQ          TMA producer: the Q tiles once, then K_j and V_j per stage.
+//   warp 4*NQ + 1 + g  MMA issuer of query tile g (one lane): S_g = Q_g K_j^T
+//                      into TMEM, then O_g += P_g V_j with P_g read from TMEM.
+//   warps 4g..4g+3     softmax of query tile g, one thread per row: load the S
+//                      row from TMEM, row max, p = 2^(s*c - m) with
+//                      c = scale*log2(e), row sum, bf16 P back into TMEM,
+//                      rescale of the O row when the running max grew by more
+//                      than 2^8, and finally O / l and lse.
+// Each query tile has its own issuing thread. A thread that waits on an
+// mbarrier stops feeding the tensor pipe, whose queue holds only a few MMAs;
+// with one issuer per tile the other tiles' products fill those gaps, and the
+// tiles run out of step, so one softmax group works while the tensor cores
+// run the other group's products.
+//
+// Where TMEM has room (d <= 64 with 128-key tiles) P_g gets columns of its
+// own: the softmax releases S_g as soon as the row is in registers, and
+// S_g(j+1) is computed while the softmax of tile j still runs; the softmax
+// waits for PV_g(j-1) only before it overwrites P_g. Otherwise P_g aliases
+// S_g and the issue order per tile is PV_g(j), S_g(j+1); the commit that
+// signals S_g(j+1) then also proves that PV_g(j) finished. Either way the O
+// rescale of tile j runs after PV_g(j-1) and before PV_g(j). With the causal
 // mask only the key tiles at or below the diagonal are loaded and multiplied.
 //
-// TMEM columns: S_g at [g*BN, (g+1)*BN), O_g at [NQ*BN + g*D, NQ*BN + (g+1)*D).
+// TMEM columns: S_g at [g*BN, (g+1)*BN); with separate P, P_g (bf16 pairs) at
+// NQ*BN + g*BN/2; O_g after them, D columns each.
 #include "attn_kernels.cuh"
 
 #include <mutex>
@@ -42,9 +52,20 @@ constexpr uint32_t tmem_cols_for(uint32_t c) {
   return c <= 32 ? 32 : c <= 64 ? 64 : c <= 128 ? 128 : c <= 256 ? 256 : 512;
 }
 
+// Build option: 2 gives each query row two softmax threads (half of the key
+// columns each) in the one-CTA-per-SM configurations. On GB300 it measured
+// slower than one thread per row (the exchange of row maxima costs more than
+// the shorter rows save), so the default is 1.
+#ifndef ATTN_FWD_SPLIT
+#define ATTN_FWD_SPLIT 1
+#endif
+
 template <int D, int NQ, int BN>
 struct Fwd {
-  static_assert(NQ * (BN + D) <= 512, "TMEM holds at most 512 fp32 columns");
+  // P in TMEM columns of its own (see above)
+  static constexpr bool SEP_P = (D <= 64 && BN == 128 && NQ * (BN + BN / 2 + D) <= 512);
+  static constexpr uint32_t P_COLS = SEP_P ? BN / 2 : 0;
+  static_assert(NQ * (BN + P_COLS + D) <= 512, "TMEM holds at most 512 fp32 columns");
   static constexpr int ATOM = (D >= 64) ? 64 : D;        // bf16 elements per swizzle row
   static constexpr int NATOM = D / ATOM;                  // TMA boxes per tile
   static constexpr uint32_t SWZ = (D >= 64) ? 2u : 4u;    // descriptor code: 128B / 64B swizzle
@@ -58,14 +79,37 @@ struct Fwd {
   static constexpr uint32_t OFF_Q = 0;
   static constexpr uint32_t OFF_K = NQ * QTILE;
   static constexpr uint32_t OFF_V = OFF_K + STAGES * KTILE;
-  static constexpr uint32_t SMEM = OFF_V + STAGES * KTILE + 1024;  // + alignment slack
-  static constexpr int THREADS = NQ * 128 + 64;
-  static constexpr uint32_t TMEM_COLS = tmem_cols_for(NQ * (BN + D));
-  static constexpr int MIN_BLOCKS = (TMEM_COLS <= 256 && SMEM <= 110u * 1024u) ? 2 : 1;
-  static constexpr int PRODUCER = 4 * NQ, ISSUER = 4 * NQ + 1;
-  static constexpr int CHUNKS = BN / 32;                  // 32-column TMEM loads per row
+  static constexpr uint32_t TMEM_COLS = tmem_cols_for(NQ * (BN + P_COLS + D));
+  static constexpr int MIN_BLOCKS = (TMEM_COLS <= 256 && OFF_V + STAGES * KTILE + 1024 <= 110u * 1024u) ? 2 : 1;
+  // Threads per query row (see ATTN_FWD_SPLIT): with SPLIT = 2 two
+  // warpgroups share each query tile, one thread per row and half of the key
+  // columns each. Only with one CTA per SM, for the registers.
+  static constexpr int SPLIT = (ATTN_FWD_SPLIT == 2 && MIN_BLOCKS == 1) ? 2 : 1;
+  static constexpr int COLS = BN / SPLIT;                 // key columns per softmax thread
+  static constexpr int OCOLS = D / SPLIT;                 // O columns per softmax thread
+  // two threads per row: partial row maxima [key tile parity][query tile][half][row]
+  // and partial row sums [query tile][half][row], in fp32
+  static constexpr uint32_t OFF_MAX = OFF_V + STAGES * KTILE;
+  static constexpr uint32_t OFF_SUM = OFF_MAX + (SPLIT == 2 ? 2u * NQ * 2u * 128u * 4u : 0u);
+  static constexpr uint32_t SMEM = OFF_SUM + (SPLIT == 2 ? NQ * 2u * 128u * 4u : 0u) + 1024;  // + alignment slack
+  static constexpr int SOFT_WARPS = 4 * NQ * SPLIT;
+  // Softmax warpgroups, then one warpgroup with the producer, the NQ issuer
+  // warps and idle padding, so that setmaxnreg can move registers from it to
+  // the softmax warpgroups.
+  static_assert(NQ + 1 <= 4, "producer and issuers share one warpgroup");
+  static constexpr int THREADS = SOFT_WARPS * 32 + 128;
+  static constexpr int REG_LAUNCH = (65536 / (THREADS * MIN_BLOCKS)) / 8 * 8;
+  static constexpr int REG_OTHER = (MIN_BLOCKS == 2) ? 48 : 96;
+  static constexpr int REG_SOFTMAX = ((THREADS * REG_LAUNCH - 128 * REG_OTHER) / (SOFT_WARPS * 32)) / 8 * 8;
+  static_assert(REG_SOFTMAX * SOFT_WARPS * 32 + REG_OTHER * 128 <= THREADS * REG_LAUNCH,
+                "register split exceeds the launch allocation");
+  // a single CTA per SM with one thread per row has registers enough without a split
+  static constexpr bool REG_SPLIT = (MIN_BLOCKS == 2 || SPLIT == 2);
+  static constexpr int PRODUCER = SOFT_WARPS, ISSUER = SOFT_WARPS + 1;  // issuers: ISSUER .. ISSUER + NQ - 1
+  static constexpr int CHUNKS = COLS / 32;                // 32-column TMEM loads per row
   __host__ __device__ static constexpr uint32_t tm_s(int g) { return g * BN; }
-  __host__ __device__ static constexpr uint32_t tm_o(int g) { return NQ * BN + g * D; }
+  __host__ __device__ static constexpr uint32_t tm_p(int g) { return SEP_P ? NQ * BN + g * P_COLS : g * BN; }
+  __host__ __device__ static constexpr uint32_t tm_o(int g) { return NQ * (BN + P_COLS) + g * D; }
 };
 
 constexpr int kMaxNQ = 4;
@@ -73,9 +117,12 @@ constexpr int kMaxStages = 4;
 
 struct FwdShared {
   uint64_t q_full;
-  uint64_t k_full[kMaxStages], k_empty[kMaxStages], v_full[kMaxStages], v_empty[kMaxStages];
+  uint64_t kv_full[kMaxStages];
+  uint64_t kv_empty[kMaxNQ][kMaxStages];  // released by each query tile's issuer
   uint64_t s_full[kMaxNQ], p_full[kMaxNQ], o_full[kMaxNQ];
-  uint64_t drain;
+  uint64_t s_free[kMaxNQ], pv_done[kMaxNQ];  // separate P only
+  uint64_t exp_turn[2];  // two query tiles: their exponential phases alternate
+  uint64_t drain[kMaxNQ];
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -157,17 +204,19 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   if (tid == 0) {
     mbar_init(&sh.q_full, 1);
     for (int s = 0; s < C::STAGES; ++s) {
-      mbar_init(&sh.k_full[s], 1);
-      mbar_init(&sh.k_empty[s], 1);
-      mbar_init(&sh.v_full[s], 1);
-      mbar_init(&sh.v_empty[s], 1);
+      mbar_init(&sh.kv_full[s], 1);
+      for (int g = 0; g < NQ; ++g) mbar_init(&sh.kv_empty[g][s], 1);
     }
     for (int g = 0; g < NQ; ++g) {
       mbar_init(&sh.s_full[g], 1);
-      mbar_init(&sh.p_full[g], 128);
+      mbar_init(&sh.p_full[g], 128 * C::SPLIT);
       mbar_init(&sh.o_full[g], 1);
+      mbar_init(&sh.drain[g], 1);
+      mbar_init(&sh.s_free[g], 128 * C::SPLIT);
+      mbar_init(&sh.pv_done[g], 1);
     }
-    mbar_init(&sh.drain, 1);
+    mbar_init(&sh.exp_turn[0], 128 * C::SPLIT);
+    mbar_init(&sh.exp_turn[1], 128 * C::SPLIT);
     sh.abort_flag = 0;
     fence_mbar_init();
   }
@@ -187,144 +236,165 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 
   if (warp == C::PRODUCER) {
     // ------------------------------------------------------------ TMA producer
+    if (C::REG_SPLIT) reg_dealloc<C::REG_OTHER>();
     if (lane == 0) {
-      int k_last[kMaxStages] = {-1, -1, -1, -1}, v_last[kMaxStages] = {-1, -1, -1, -1};
+      // bit s of `filled`: stage s was loaded; bit s of `last_ph`: parity of its last fill
+      uint32_t filled = 0, last_ph = 0;
       mbar_arrive_expect_tx(&sh.q_full, nq_valid * C::QTILE);
       for (int t = 0; t < nq_valid; ++t)
         for (int a = 0; a < C::NATOM; ++a)
           tma_load_3d(smem + C::OFF_Q + t * C::QTILE + a * C::QBOX, &tm_q, &sh.q_full, a * C::ATOM,
                       q0 + t * 128, bh);
-      for (int j = 0; j < nt; ++j) {
+      bool ok = true;
+      for (int j = 0; ok && j < nt; ++j) {
         const int st = j % C::STAGES;
         const uint32_t ph = (j / C::STAGES) & 1;
-        if (j >= C::STAGES && !guarded_wait(&sh.k_empty[st], ph ^ 1, abort_flag, wd, kSiteKEmpty)) break;
-        mbar_arrive_expect_tx(&sh.k_full[st], C::KTILE);
+        // the stage's previous tile (j - STAGES) must be released by every
+        // query tile that used it
+        if (j >= C::STAGES) {
+#pragma unroll
+          for (int g = 0; g < NQ; ++g)
+            if (ok && ntile[g] > j - C::STAGES)
+              ok = guarded_wait(&sh.kv_empty[g][st], ph ^ 1, abort_flag, wd, kSiteKEmpty);
+          if (!ok) break;
+        }
+        mbar_arrive_expect_tx(&sh.kv_full[st], 2 * C::KTILE);
+        filled |= 1u << st;
+        last_ph = (last_ph & ~(1u << st)) | (ph << st);
         for (int a = 0; a < C::NATOM; ++a)
-          tma_load_3d(smem + C::OFF_K + st * C::KTILE + a * C::KBOX, &tm_k, &sh.k_full[st],
+          tma_load_3d(smem + C::OFF_K + st * C::KTILE + a * C::KBOX, &tm_k, &sh.kv_full[st],
                       a * C::ATOM, j * BN, bh);
-        k_last[st] = static_cast<int>(ph);
-        if (j >= C::STAGES && !guarded_wait(&sh.v_empty[st], ph ^ 1, abort_flag, wd, kSiteVEmpty)) break;
         if (p.inject == 1 && j == 0) continue;  // test hook: this value tile never arrives
-        mbar_arrive_expect_tx(&sh.v_full[st], C::KTILE);
         for (int a = 0; a < C::NATOM; ++a)
-          tma_load_3d(smem + C::OFF_V + st * C::KTILE + a * C::KBOX, &tm_v, &sh.v_full[st],
+          tma_load_3d(smem + C::OFF_V + st * C::KTILE + a * C::KBOX, &tm_v, &sh.kv_full[st],
                       a * C::ATOM, j * BN, bh);
-        v_last[st] = static_cast<int>(ph);
       }
       // Let every copy this thread started land before shared memory is released.
       drain_wait(&sh.q_full, 0, wd);
-      for (int s = 0; s < C::STAGES; ++s) {
-        if (k_last[s] >= 0) drain_wait(&sh.k_full[s], static_cast<uint32_t>(k_last[s]), wd);
-        if (v_last[s] >= 0) drain_wait(&sh.v_full[s], static_cast<uint32_t>(v_last[s]), wd);
-      }
+      for (int s = 0; s < C::STAGES; ++s)
+        if ((filled >> s) & 1u) drain_wait(&sh.kv_full[s], (last_ph >> s) & 1u, wd);
     }
-  } else if (warp == C::ISSUER) {
-    // ------------------------------------------------------------ MMA issuer
-    const uint32_t idesc_s = idesc_bf16_f32(128, BN, false, false) | (p.neg ? (1u << 13) : 0u);
-    const uint32_t idesc_o = idesc_bf16_f32(128, D, false, true);
-    const uint32_t sQ = smem_u32(smem + C::OFF_Q);
-    const uint32_t sK = smem_u32(smem + C::OFF_K);
-    const uint32_t sV = smem_u32(smem + C::OFF_V);
-    auto issue_s = [&](int g, int st) {
+  } else if (warp >= C::ISSUER) {
+    // ------------------------------------------------------------ MMA issuer of query tile g
+    if (C::REG_SPLIT) reg_dealloc<C::REG_OTHER>();
+    const int g = warp - C::ISSUER;
+    int T = 0;
 #pragma unroll
-      for (int k = 0; k < D / 16; ++k) {
-        const int a = k / (C::ATOM / 16), w = k % (C::ATOM / 16);
-        const uint64_t da = smem_desc(sQ + g * C::QTILE + a * C::QBOX + w * 32, 16, C::SBO, C::SWZ);
-        const uint64_t db = smem_desc(sK + st * C::KTILE + a * C::KBOX + w * 32, 16, C::SBO, C::SWZ);
-        mma_ss(tmem + C::tm_s(g), da, db, idesc_s, k > 0 ? 1u : 0u);
-      }
-    };
-    auto issue_pv = [&](int g, int st, bool acc) {
+    for (int gg = 0; gg < NQ; ++gg)
+      if (gg == g) T = ntile[gg];
+    if (lane == 0 && T > 0) {
+      const uint32_t idesc_s = idesc_bf16_f32(128, BN, false, false) | (p.neg ? (1u << 13) : 0u);
+      const uint32_t idesc_o = idesc_bf16_f32(128, D, false, true);
+      const uint32_t sQ = smem_u32(smem + C::OFF_Q) + g * C::QTILE;
+      const uint32_t sK = smem_u32(smem + C::OFF_K);
+      const uint32_t sV = smem_u32(smem + C::OFF_V);
+      const uint32_t t_s = tmem + C::tm_s(g), t_p = tmem + C::tm_p(g), t_o = tmem + C::tm_o(g);
+      auto issue_s = [&](int st) {
 #pragma unroll
-      for (int k = 0; k < BN / 16; ++k) {
-        const uint64_t db = smem_desc(sV + st * C::KTILE + k * 16 * C::ATOM * 2, C::KBOX, C::SBO, C::SWZ);
-        mma_ts(tmem + C::tm_o(g), tmem + C::tm_s(g) + k * 8, db, idesc_o, (acc || k > 0) ? 1u : 0u);
+        for (int k = 0; k < D / 16; ++k) {
+          const int a = k / (C::ATOM / 16), w = k % (C::ATOM / 16);
+          const uint64_t da = smem_desc(sQ + a * C::QBOX + w * 32, 16, C::SBO, C::SWZ);
+          const uint64_t db = smem_desc(sK + st * C::KTILE + a * C::KBOX + w * 32, 16, C::SBO, C::SWZ);
+          mma_ss(t_s, da, db, idesc_s, k > 0 ? 1u : 0u);
+        }
+      };
+      auto issue_pv = [&](int st, bool acc) {
+#pragma unroll
+        for (int k = 0; k < BN / 16; ++k) {
+          const uint64_t db = smem_desc(sV + st * C::KTILE + k * 16 * C::ATOM * 2, C::KBOX, C::SBO, C::SWZ);
+          mma_ts(t_o, t_p + k * 8, db, idesc_o, (acc || k > 0) ? 1u : 0u);
+        }
+      };
+      bool ok = guarded_wait(&sh.q_full, 0, abort_flag, wd, kSiteQFull) &&
+                guarded_wait(&sh.kv_full[0], 0, abort_flag, wd, kSiteKFull);
+      if (ok) {
+        issue_s(0);
+        mma_commit(&sh.s_full[g]);
       }
-    };
-    auto wait_all = [&](uint64_t* bar, uint32_t parity, uint32_t site) {
-      return __all_sync(0xffffffffu, guarded_wait(bar, parity, abort_flag, wd, site));
-    };
-    bool ok = wait_all(&sh.q_full, 0, kSiteQFull);
-    if (ok && nt > 0) {
-      ok = wait_all(&sh.k_full[0], 0, kSiteKFull);
-      if (ok && lane == 0) {
+      for (int j = 0; ok && j < T; ++j) {
+        const int st = j % C::STAGES;
+        if (C::SEP_P && j + 1 < T) {
+          // S_g(j+1) as soon as the softmax holds S_g(j) in registers
+          const int jn = j + 1, stn = jn % C::STAGES;
+          if (!(ok = guarded_wait(&sh.s_free[g], j & 1, abort_flag, wd, kSiteSFull))) break;
+          if (!(ok = guarded_wait(&sh.kv_full[stn], (jn / C::STAGES) & 1, abort_flag, wd, kSiteKFull))) break;
+          tc_fence_after();
+          issue_s(stn);
+          mma_commit(&sh.s_full[g]);
+        }
+        if (!(ok = guarded_wait(&sh.p_full[g], j & 1, abort_flag, wd, kSitePFull))) break;
         tc_fence_after();
-#pragma unroll
-        for (int g = 0; g < NQ; ++g)
-          if (ntile[g] > 0) {
-            issue_s(g, 0);
-            mma_commit(&sh.s_full[g]);
-          }
-        mma_commit(&sh.k_empty[0]);
-      }
-      __syncwarp();
-    }
-    for (int j = 0; ok && j < nt; ++j) {
-      const int st = j % C::STAGES;
-      const int jn = j + 1, stn = jn % C::STAGES;
-      if (!(ok = wait_all(&sh.v_full[st], (j / C::STAGES) & 1, kSiteVFull))) break;
-      bool k_next = false;
-#pragma unroll
-      for (int g = 0; g < NQ; ++g) {
-        if (j < ntile[g]) {
-          if (!(ok = wait_all(&sh.p_full[g], j & 1, kSitePFull))) break;
-          if (lane == 0) {
-            tc_fence_after();
-            issue_pv(g, st, j > 0);
-            if (j == ntile[g] - 1) mma_commit(&sh.o_full[g]);
-          }
-          __syncwarp();
-        }
-        if (jn < ntile[g]) {
-          if (!k_next) {
-            if (!(ok = wait_all(&sh.k_full[stn], (jn / C::STAGES) & 1, kSiteKFull))) break;
-            k_next = true;
-          }
-          if (lane == 0) {
-            issue_s(g, stn);
-            mma_commit(&sh.s_full[g]);
-          }
-          __syncwarp();
+        issue_pv(st, j > 0);
+        if (C::SEP_P) mma_commit(&sh.pv_done[g]);
+        if (j == T - 1) mma_commit(&sh.o_full[g]);
+        mma_commit(&sh.kv_empty[g][st]);  // K_j and V_j are no longer read by this tile
+        if (!C::SEP_P && j + 1 < T) {
+          const int jn = j + 1, stn = jn % C::STAGES;
+          if (!(ok = guarded_wait(&sh.kv_full[stn], (jn / C::STAGES) & 1, abort_flag, wd, kSiteKFull))) break;
+          issue_s(stn);
+          mma_commit(&sh.s_full[g]);
         }
       }
-      if (!ok) break;
-      if (lane == 0) {
-        mma_commit(&sh.v_empty[st]);
-        if (k_next) mma_commit(&sh.k_empty[stn]);
-      }
-      __syncwarp();
+      // Every MMA this thread issued must finish before TMEM is released.
+      mma_commit(&sh.drain[g]);
+      drain_wait(&sh.drain[g], 0, wd);
     }
-    // Every MMA this warp issued must finish before TMEM is released.
-    if (lane == 0) mma_commit(&sh.drain);
     __syncwarp();
-    drain_wait(&sh.drain, 0, wd);
-  } else if (warp < 4 * NQ) {
+  } else {
     // ------------------------------------------------------------ softmax groups
-    const int g = warp >> 2;
-    const int r = tid & 127;
+    // Query tile g, column half h: the thread owns row r of the tile (TMEM
+    // lane r) and key columns [h*COLS, (h+1)*COLS) of every key tile. The two
+    // halves of a row combine their row maxima and row sums through shared
+    // memory and a named barrier of the two warps that share those lanes.
+    if (C::REG_SPLIT) reg_alloc<C::REG_SOFTMAX>();
+    const int g = warp / (4 * C::SPLIT);
+    const int h = (warp >> 2) % C::SPLIT;
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;
     const int row = q0 + g * 128 + r;
+    const uint32_t pair_bar = 1 + g * 4 + quarter;      // named barrier of the two halves
+    float* part_max = reinterpret_cast<float*>(smem + C::OFF_MAX);
+    float* part_sum = reinterpret_cast<float*>(smem + C::OFF_SUM);
     int my_tiles = 0;
 #pragma unroll
     for (int gg = 0; gg < NQ; ++gg)
       if (gg == g) my_tiles = ntile[gg];
-    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    const uint32_t t_s = tmem + lane_base + g * BN;
-    const uint32_t t_o = tmem + lane_base + NQ * BN + g * D;
-    const int lim = p.causal ? min(row + 1, p.m) : p.m;  // keys [0, lim) are visible
+    const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
+    const uint32_t t_s = tmem + lane_base + C::tm_s(g) + h * C::COLS;
+    const uint32_t t_p = tmem + lane_base + C::tm_p(g) + h * (C::COLS / 2);
+    const uint32_t t_o = tmem + lane_base + C::tm_o(g) + h * C::OCOLS;
+    const int lim = (p.causal ? min(row + 1, p.m) : p.m) - h * C::COLS;  // visible keys, from column h*COLS
     const float c = p.c;
     const uint64_t c2 = f2_pack(c, c);
     float m_used = 0.f, l = 0.f;
+    // Failures are not acted on at once where the two halves must meet at a
+    // named barrier: they are voted on at the next one, so both leave together.
     bool ok = true;
+    // With two query tiles and P aliasing S, the exponentials of tile 0 and
+    // tile 1 take turns (0, 1, 0, 1, ... per key tile), so that one group's
+    // exponentials overlap the other group's MMAs instead of both groups
+    // computing at once and then both waiting for the tensor cores. Group 0
+    // waits for group 1's previous turn, group 1 for group 0's turn on the
+    // same key tile, each only while the other group still has that tile.
+    constexpr bool TURNS = (NQ == 2) && !C::SEP_P;
+    int other_tiles = 0;
+#pragma unroll
+    for (int gg = 0; gg < NQ; ++gg)
+      if (TURNS && gg == (g ^ 1)) other_tiles = ntile[gg];
+    if (TURNS && g == 1) mbar_arrive(&sh.exp_turn[0]);  // group 0 goes first
     for (int j = 0; j < my_tiles; ++j) {
-      ok = __all_sync(0xffffffffu, guarded_wait(&sh.s_full[g], j & 1, abort_flag, wd, kSiteSFull));
-      if (!ok) break;
+      ok = __all_sync(0xffffffffu, guarded_wait(&sh.s_full[g], j & 1, abort_flag, wd, kSiteSFull)) && ok;
       tc_fence_after();
       uint32_t s[C::CHUNKS][32];
 #pragma unroll
       for (int q = 0; q < C::CHUNKS; ++q) tmem_ld32(t_s + q * 32, s[q]);
       tmem_ld_wait();
-      const int rem = lim - j * BN;  // visible keys of this row inside the tile
-      const bool masked = __any_sync(0xffffffffu, rem < BN);
+      if (C::SEP_P) {
+        tc_fence_before();
+        mbar_arrive(&sh.s_free[g]);  // S_g may be overwritten by S_g(j+1)
+      }
+      const int rem = lim - j * BN;  // visible keys of this row among this thread's columns
+      const bool masked = __any_sync(0xffffffffu, rem < C::COLS);
       if (masked) {
 #pragma unroll
         for (int q = 0; q < C::CHUNKS; ++q)
@@ -333,19 +403,26 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             if (q * 32 + i >= rem) s[q][i] = __float_as_uint(-INFINITY);
       }
       // row max: four chains of 3-input max, seeded with columns 0..7; every
-      // later step covers 8 columns, ending exactly at BN
+      // later step covers 8 columns, ending exactly at COLS
       float mx4[4];
 #pragma unroll
       for (int u = 0; u < 4; ++u)
         mx4[u] = fmaxf(__uint_as_float(s[0][2 * u]), __uint_as_float(s[0][2 * u + 1]));
 #pragma unroll
-      for (int e = 8; e < BN; e += 8) {
+      for (int e = 8; e < C::COLS; e += 8) {
 #pragma unroll
         for (int u = 0; u < 4; ++u)
           mx4[u] = max3(mx4[u], __uint_as_float(s[(e + 2 * u) >> 5][(e + 2 * u) & 31]),
                         __uint_as_float(s[(e + 2 * u + 1) >> 5][(e + 2 * u + 1) & 31]));
       }
-      const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+      float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+      if (C::SPLIT == 2) {
+        part_max[(((j & 1) * NQ + g) * 2 + h) * 128 + r] = mx;
+        if (named_bar_or(pair_bar, 64, !ok || *abort_flag != 0)) break;
+        mx = fmaxf(mx, part_max[(((j & 1) * NQ + g) * 2 + (h ^ 1)) * 128 + r]);
+      } else if (!ok) {
+        break;
+      }
       const float m_new = mx * c;
       float alpha = 1.f;
       bool rescale = false;
@@ -357,6 +434,13 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         rescale = true;
       }
       const uint64_t nm2 = f2_pack(-m_used, -m_used);
+      if (TURNS && (g == 0 ? (j == 0 || j - 1 < other_tiles) : j < other_tiles))
+        ok = __all_sync(0xffffffffu, guarded_wait(&sh.exp_turn[g], j & 1, abort_flag, wd, kSiteExpTurn)) && ok;
+      if (C::SEP_P && j > 0) {
+        // PV_g(j-1) still reads P_g until it completes
+        ok = __all_sync(0xffffffffu, guarded_wait(&sh.pv_done[g], (j - 1) & 1, abort_flag, wd, kSitePFull)) && ok;
+        tc_fence_after();
+      }
       uint64_t lsum2[2] = {0ull, 0ull};
 #pragma unroll
       for (int q = 0; q < C::CHUNKS; ++q) {
@@ -365,8 +449,9 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           exp_chunk<true>(s[q], q * 32, rem, c2, nm2, lsum2, pk);
         else
           exp_chunk<false>(s[q], q * 32, rem, c2, nm2, lsum2, pk);
-        tmem_st16(t_s + q * 16, pk);
+        tmem_st16(t_p + q * 16, pk);
       }
+      if (TURNS) mbar_arrive(&sh.exp_turn[g ^ 1]);  // the other group's turn
       {
         float a0, a1, b0, b1;
         f2_unpack(lsum2[0], a0, a1);
@@ -376,42 +461,50 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       tmem_st_wait();
       if (j > 0 && __any_sync(0xffffffffu, rescale)) {
 #pragma unroll
-        for (int q = 0; q < D / 32; ++q) {
-          uint32_t o[32];
-          tmem_ld32(t_o + q * 32, o);
+        for (int q = 0; q < C::OCOLS / 16; ++q) {
+          uint32_t o[16];
+          tmem_ld16(t_o + q * 16, o);
           tmem_ld_wait();
 #pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-          tmem_st32(t_o + q * 32, o);
+          for (int i = 0; i < 16; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+          tmem_st16(t_o + q * 16, o);
         }
         tmem_st_wait();
       }
       tc_fence_before();
       mbar_arrive(&sh.p_full[g]);
+      if (C::SPLIT == 1 && !ok) break;
     }
-    if (ok && my_tiles > 0) {
-      ok = __all_sync(0xffffffffu, guarded_wait(&sh.o_full[g], 0, abort_flag, wd, kSiteOFull));
+    if (my_tiles > 0) {
+      ok = __all_sync(0xffffffffu, guarded_wait(&sh.o_full[g], 0, abort_flag, wd, kSiteOFull)) && ok;
+      if (C::SPLIT == 2) {
+        // a loop left early on a vote leaves both halves here together
+        part_sum[(g * 2 + h) * 128 + r] = l;
+        const bool failed = named_bar_or(pair_bar, 64, !ok || *abort_flag != 0);
+        l += part_sum[(g * 2 + (h ^ 1)) * 128 + r];
+        ok = !failed;
+      }
       if (ok) {
         tc_fence_after();
         const float inv_l = 1.f / l;
         const bool store = row < p.n;
-        uint4* orow = reinterpret_cast<uint4*>(p.o + (static_cast<size_t>(bh) * p.n + (store ? row : 0)) * D);
+        uint4* orow = reinterpret_cast<uint4*>(p.o + (static_cast<size_t>(bh) * p.n + (store ? row : 0)) * D +
+                                               h * C::OCOLS);
 #pragma unroll
-        for (int q = 0; q < D / 32; ++q) {
-          uint32_t o[32];
-          tmem_ld32(t_o + q * 32, o);
+        for (int q = 0; q < C::OCOLS / 16; ++q) {
+          uint32_t o[16];
+          tmem_ld16(t_o + q * 16, o);
           tmem_ld_wait();
-          uint32_t pk[16];
+          uint32_t pk[8];
 #pragma unroll
-          for (int i = 0; i < 16; ++i)
+          for (int i = 0; i < 8; ++i)
             pk[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
           if (store) {
-#pragma unroll
-            for (int v = 0; v < 4; ++v)
-              orow[q * 4 + v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+            orow[q * 2] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            orow[q * 2 + 1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
           }
         }
-        if (store && p.lse != nullptr)
+        if (store && h == 0 && p.lse != nullptr)
           p.lse[static_cast<size_t>(bh) * p.n + row] = (m_used + log2f(l)) * kLn2;
       }
     }
@@ -439,6 +532,18 @@ cudaError_t launch_fwd_cfg(const CUtensorMap& tq, const CUtensorMap& tk, const C
                                 static_cast<int>(C::SMEM));
   });
   if (attr != cudaSuccess) return attr;
+  if (C::REG_SPLIT) {
+    // setmaxnreg.inc waits until registers are free: the split must fit in the
+    // registers the CTA is launched with, or the kernel would never proceed.
+    static int regs_per_thread[64] = {0};
+    if (regs_per_thread[dev & 63] == 0) {
+      cudaFuncAttributes fa;
+      if ((e = cudaFuncGetAttributes(&fa, attn_fwd_kernel<D, NQ, BN>)) != cudaSuccess) return e;
+      regs_per_thread[dev & 63] = fa.numRegs;
+    }
+    if (regs_per_thread[dev & 63] * C::THREADS < C::SOFT_WARPS * 32 * C::REG_SOFTMAX + 128 * C::REG_OTHER)
+      return cudaErrorInvalidConfiguration;
+  }
   p.num_qblocks = (p.n + NQ * 128 - 1) / (NQ * 128);
   dim3 grid(static_cast<unsigned>(BH), static_cast<unsigned>(p.num_qblocks));
   prof_begin(kKindFwd, stream);

@@ -19,7 +19,7 @@ constexpr uint32_t kDevLayout = 0x200u;
 enum WaitSite : uint32_t {
   kSiteQFull = 1, kSiteKFull, kSiteVFull, kSiteKEmpty, kSiteVEmpty, kSiteSFull,
   kSitePFull, kSiteOFull, kSiteDrain, kSiteBwdLoad, kSiteBwdS, kSiteBwdDP, kSiteBwdDS,
-  kSiteBwdDQ, kSiteBwdFree, kSiteBwdFinal
+  kSiteBwdDQ, kSiteBwdFree, kSiteBwdFinal, kSiteExpTurn
 };
 
 struct Watchdog {
