@@ -44,16 +44,27 @@ def step_flops(w: Workload) -> float:
     return w.fwd_flops() + w.bwd_flops()
 
 
+def whole_head_backward(w: Workload) -> bool:
+    """True where the library runs the single-launch whole-head backward (it needs no workspace)."""
+    import transformer_scaled_dot_attn_gb300 as A
+    return A.attn_bwd_workspace_bytes(w.B, w.h, w.n, w.m, w.d_k, w.d_v, w.causal) == 0
+
+
 def kernel_model(w: Workload):
     """Algorithmic FLOPs and bytes per launch of the two tensor-core kernels.
 
     fwd:      reads Q, K, V (bf16); writes O (bf16) and lse (fp32).
-    bwd_main: reads Q, dO, K, V (bf16) and the two fp32 row statistics;
-              writes dK, dV (bf16) and the fp32 dQ accumulator once.
+    bwd_main: general path: reads Q, dO, K, V (bf16) and the two fp32 row
+              statistics; writes dK, dV (bf16) and the fp32 dQ accumulator once.
+              Whole-head path (n <= 256, d <= 64): reads Q, dO, O, K, V (bf16)
+              and lse (fp32); writes dQ, dK, dV (bf16).
     """
     H, n, m, d = w.heads, w.n, w.m, w.d_k
     fwd_bytes = H * (2 * (2 * n * d + 2 * m * d) + 4 * n)
-    bwd_bytes = H * (2 * (2 * n * d + 2 * m * d) + 8 * n + 2 * (2 * m * d) + 4 * n * d)
+    if whole_head_backward(w):
+        bwd_bytes = H * (2 * (3 * n * d + 2 * m * d) + 4 * n + 2 * (n * d + 2 * m * d))
+    else:
+        bwd_bytes = H * (2 * (2 * n * d + 2 * m * d) + 8 * n + 2 * (2 * m * d) + 4 * n * d)
     return {
         "fwd": {"flops": w.fwd_flops(), "bytes": fwd_bytes},
         "bwd_main": {"flops": w.bwd_flops(), "bytes": bwd_bytes},
@@ -368,7 +379,8 @@ def run_gpu(args, w: Workload, world, rank, local):
                  "traffic": recorded_traffic(dom, w.name),
                  "algorithmic_bytes": model[dom]["bytes"], "algorithmic_flops": model[dom]["flops"],
                  "avg_launch_us": round(avg_s * 1e6, 2)})
-    per_kernel = {k: {"launches": n, "avg_us": round(t / max(n, 1) * 1e3, 2)} for k, (n, t) in prof.items()}
+    per_kernel = {k: {"launches": n, "avg_us": round(t / max(n, 1) * 1e3, 2)} for k, (n, t) in prof.items()
+                  if n > 0}
     for k in ("fwd", "bwd_main"):
         n_, t_ = prof[k]
         a = t_ / max(n_, 1) / 1e3

@@ -66,7 +66,9 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
 
 /*
  * Bytes of device workspace attn_bwd needs for these sizes (fp32 dQ
- * accumulator plus padded per-row statistics). 0 when B*h*n == 0.
+ * accumulator plus padded per-row statistics). 0 when B*h*n == 0, and 0 when
+ * n <= 256 and d_k = d_v <= 64: those sizes run a single kernel that keeps
+ * each head's dQ on chip and needs no scratch.
  */
 size_t attn_bwd_workspace_bytes(int B, int h, int n, int m, int d_k, int d_v, int causal);
 
@@ -83,7 +85,8 @@ size_t attn_bwd_workspace_bytes(int B, int h, int n, int m, int d_k, int d_v, in
  *                     attn_bwd_workspace_bytes(...) bytes, 16-byte aligned;
  *                     its contents on entry do not matter (the call clears
  *                     what it needs on `stream`). It must not be shared by
- *                     calls that run concurrently.
+ *                     calls that run concurrently. May be NULL (with
+ *                     workspace_bytes 0) when that size is 0.
  */
 int attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
              const void* dO, void* dq, void* dk, void* dv, int B, int h, int n, int m, int d_k,
@@ -100,8 +103,9 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const f
  * has no counterpart.
  *
  * Same arguments and results as attn_bwd, minus workspace/workspace_bytes.
- * The scratch (fp32 dQ accumulator and two padded per-row statistics, as
- * sized by attn_bwd_workspace_bytes) lives in one fixed 32 MiB device array
+ * Sizes for which attn_bwd_workspace_bytes is 0 use no scratch at all.
+ * Otherwise the scratch (fp32 dQ accumulator and two padded per-row
+ * statistics, as sized by attn_bwd_workspace_bytes) lives in one fixed 32 MiB device array
  * inside the library: every GPU that loads the library holds it until the
  * process exits. Sizes whose scratch exceeds 32 MiB are refused with
  * ATTN_ERR_UNSUPPORTED before anything is launched. The call makes no

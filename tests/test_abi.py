@@ -74,7 +74,8 @@ def test_bwd_argument_checks(lib):
     vp = ctypes.c_void_p
     f = ctypes.cast(vp(FAKE), ctypes.POINTER(ctypes.c_float))
 
-    def call(n=8, m=8, d=64, ws_bytes=1 << 30, ws=FAKE, dq=FAKE, lse=f, scale=0.125):
+    # n = 300: the general path, which needs a workspace (n <= 256 with d <= 64 needs none)
+    def call(n=300, m=8, d=64, ws_bytes=1 << 30, ws=FAKE, dq=FAKE, lse=f, scale=0.125):
         return lib.attn_bwd(vp(FAKE), vp(FAKE), vp(FAKE), vp(FAKE), lse, vp(FAKE), vp(dq) if dq else None,
                             vp(FAKE), vp(FAKE), 1, 1, n, m, d, d, 0, scale, vp(ws) if ws else None,
                             ws_bytes, None)
@@ -89,9 +90,13 @@ def test_bwd_argument_checks(lib):
 
 
 def test_workspace_size(lib):
-    # fp32 dQ accumulator + two fp32 per-row statistics, rows padded to 128
-    assert A.attn_bwd_workspace_bytes(2, 3, 200, 77, 64, 64) == 2 * 3 * 256 * (64 + 2) * 4
-    assert A.attn_bwd_workspace_bytes(1, 1, 128, 1, 32, 32, True) == 128 * 34 * 4
+    # general path: fp32 dQ accumulator + two fp32 per-row statistics, rows padded to 128
+    assert A.attn_bwd_workspace_bytes(2, 3, 300, 77, 64, 64) == 2 * 3 * 384 * (64 + 2) * 4
+    assert A.attn_bwd_workspace_bytes(2, 3, 200, 77, 128, 128) == 2 * 3 * 256 * (128 + 2) * 4
+    assert A.attn_bwd_workspace_bytes(1, 1, 257, 1, 32, 32, True) == 384 * 34 * 4
+    # whole-head kernel (n <= 256, d <= 64): no workspace at all
+    assert A.attn_bwd_workspace_bytes(2, 3, 200, 77, 64, 64) == 0
+    assert A.attn_bwd_workspace_bytes(1, 1, 256, 1, 32, 32, True) == 0
     assert A.attn_bwd_workspace_bytes(0, 3, 200, 77, 64, 64) == 0
     assert A.attn_bwd_workspace_bytes(1, 1, 0, 77, 64, 64) == 0
 

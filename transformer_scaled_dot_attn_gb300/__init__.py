@@ -187,13 +187,15 @@ def attn_bwd(q, k, v, o, lse, dO, causal: bool = False, scale: Optional[float] =
     for name, t, ref in (("dq", dq, q), ("dk", dk, k), ("dv", dv, v)):
         _check_tensor(name, t, tuple(ref.shape), torch.bfloat16)
     need = attn_bwd_workspace_bytes(B, h, n, m, d_k, d_v, causal)
-    if workspace is None:
-        workspace = torch.empty((max(need, 16) + 15) // 16 * 4, dtype=torch.float32, device=q.device)
-    _check_tensor("workspace", workspace)
-    ws_bytes = workspace.numel() * workspace.element_size()
+    if workspace is None and need > 0:
+        workspace = torch.empty((need + 15) // 16 * 4, dtype=torch.float32, device=q.device)
+    if workspace is not None:
+        _check_tensor("workspace", workspace)
+    ws_ptr = _vptr(workspace) if workspace is not None else None
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     st = lib.attn_bwd(_vptr(q), _vptr(k), _vptr(v), _vptr(o), _fptr(lse), _vptr(dO), _vptr(dq),
                       _vptr(dk), _vptr(dv), B, h, n, m, d_k, d_v, int(bool(causal)), float(scale),
-                      _vptr(workspace), ws_bytes, _stream_handle(stream))
+                      ws_ptr, ws_bytes, _stream_handle(stream))
     if st != ATTN_OK:
         raise AttnError(st, "attn_bwd")
     return dq, dk, dv

@@ -12,6 +12,7 @@
 
 namespace {
 
+using attn::BwdHeadParams;
 using attn::BwdParams;
 using attn::BwdPostParams;
 using attn::BwdPreParams;
@@ -269,13 +270,43 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
 
 size_t attn_bwd_workspace_bytes(int B, int h, int n, int m, int d_k, int d_v, int causal) {
   (void)m;
-  (void)d_v;
   (void)causal;
   if (B <= 0 || h <= 0 || n <= 0 || d_k <= 0) return 0;
+  if (d_k == d_v && attn::bwd_head_supported(n, d_k)) return 0;  // whole-head kernel: no scratch
   const long long BH = static_cast<long long>(B) * h;
   const long long n_pad = round_up(n, 128);
   // dQ accumulator [BH, n_pad, d] + lse*log2(e) [BH, n_pad] + D [BH, n_pad], fp32
   return static_cast<size_t>(BH * n_pad * (static_cast<long long>(d_k) + 2) * 4);
+}
+
+// Short query sequences: the whole-head kernel (no scratch, one launch).
+static int bwd_head_path(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                         const void* dO, void* dq, void* dk, void* dv, long long BH, int n, int m,
+                         int d, int causal, float scale, uint32_t* status, cudaStream_t stream) {
+  CUtensorMap tq, tk, tv, tdo, tdq, tdk, tdv;
+  if (!make_tile_map(&tq, q, BH, n, d) || !make_tile_map(&tk, k, BH, m, d) ||
+      !make_tile_map(&tv, v, BH, m, d) || !make_tile_map(&tdo, dO, BH, n, d) ||
+      !make_tile_map(&tdq, dq, BH, n, d) || !make_tile_map(&tdk, dk, BH, m, d) ||
+      !make_tile_map(&tdv, dv, BH, m, d))
+    return ATTN_ERR_CUDA;
+  BwdHeadParams p{};
+  p.o = static_cast<const __nv_bfloat16*>(o);
+  p.dO = static_cast<const __nv_bfloat16*>(dO);
+  p.lse = lse;
+  p.dq = static_cast<__nv_bfloat16*>(dq);
+  p.dk = static_cast<__nv_bfloat16*>(dk);
+  p.dv = static_cast<__nv_bfloat16*>(dv);
+  p.BH = static_cast<int>(BH);
+  p.n = n;
+  p.m = m;
+  p.causal = causal ? 1 : 0;
+  p.neg = scale < 0.f ? 1 : 0;
+  p.c = static_cast<float>(std::fabs(static_cast<double>(scale)) * kLog2e);
+  p.scale = scale;
+  p.wd.status = status;
+  p.wd.budget_ns = g_watchdog_ns.load();
+  const cudaError_t e = attn::launch_bwd_head(d, tq, tk, tv, tdo, tdq, tdk, tdv, p, stream);
+  return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
 int attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
@@ -297,12 +328,17 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const f
     if (cudaMemsetAsync(dv, 0, bytes, s) != cudaSuccess) return ATTN_ERR_CUDA;
     return ATTN_OK;
   }
-  if (!q || !o || !lse || !dO || !dq || !workspace) return ATTN_ERR_INVALID_ARG;
-  if (!aligned16(q) || !aligned16(o) || !aligned16(dO) || !aligned16(dq) || !aligned16(workspace))
-    return ATTN_ERR_INVALID_ARG;
+  if (!q || !o || !lse || !dO || !dq) return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(o) || !aligned16(dO) || !aligned16(dq)) return ATTN_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(lse) & 3u) != 0) return ATTN_ERR_INVALID_ARG;
-  if (workspace_bytes < attn_bwd_workspace_bytes(B, h, n, m, d_k, d_v, causal))
-    return ATTN_ERR_INVALID_ARG;
+  const size_t ws_need = attn_bwd_workspace_bytes(B, h, n, m, d_k, d_v, causal);
+  if (ws_need == 0) {
+    uint32_t* status = nullptr;
+    if (device_status_word(&status) != cudaSuccess) return ATTN_ERR_CUDA;
+    return bwd_head_path(q, k, v, o, lse, dO, dq, dk, dv, BH, n, m, d_k, causal, scale, status,
+                         reinterpret_cast<cudaStream_t>(stream));
+  }
+  if (!workspace || !aligned16(workspace) || workspace_bytes < ws_need) return ATTN_ERR_INVALID_ARG;
 
   const long long n_pad = round_up(n, 128);
   float* ws = static_cast<float*>(workspace);
@@ -444,6 +480,8 @@ extern "C" int attn_bwd_noalloc(const void* q, const void* k, const void* v, con
     status = g_status[dev];  // read only: never allocated here
   }
   if (status == nullptr) status = g_noalloc_status_ptr[dev];
+  if (attn_bwd_workspace_bytes(B, h, n, m, d_k, d_v, causal) == 0)  // needs no scratch at all
+    return bwd_head_path(q, k, v, o, lse, dO, dq, dk, dv, BH, n, m, d_k, causal, scale, status, s);
 
   const long long n_pad = round_up(n, 128);
   float* dq_acc = static_cast<float*>(g_noalloc_scratch_ptr[dev]);

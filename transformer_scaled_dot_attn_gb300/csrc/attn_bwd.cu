@@ -338,10 +338,10 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       const int set = li % C::KV_SETS, use = li / C::KV_SETS;
       const uint32_t sK = smem_u32(smem + C::OFF_K + set * C::TILE);
       const uint32_t sV = smem_u32(smem + C::OFF_V + set * C::TILE);
-      // The previous item's epilogue must have read dK, dV out of TMEM (this
-      // also keeps the issuer at most one item ahead of the compute warps).
-      if (li >= 1 && !(ok = wait_all(&sh.acc_free, (li - 1) & 1, kSiteBwdFinal))) break;
       if (!(ok = wait_all(&sh.kv_full[set], use & 1, kSiteBwdLoad))) break;
+      // acc_free is waited once per item, in order: below before the first dV
+      // product, or here for an item without query tiles
+      if (T == 0 && li >= 1 && !(ok = wait_all(&sh.acc_free, (li - 1) & 1, kSiteBwdFinal))) break;
       if (T > 0) {
         if (!(ok = wait_all(&sh.qdo_full[g & 1], (g >> 1) & 1, kSiteBwdLoad))) break;
         if (lane == 0) {
@@ -366,6 +366,10 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         // dV += P^T dO; P^T (bf16) sits in TMEM columns [0,32) and [64,96) of S^T,
         // one block per compute warpgroup (queries 0..63 and 64..127)
         if (!(ok = wait_all(&sh.p_full, gt & 1, kSiteBwdS))) break;
+        // The item's first dV product overwrites the accumulators: the previous
+        // item's epilogue must have read dK and dV out of TMEM. (Waiting here,
+        // not at the item's start, lets this item's S^T and dP^T overlap it.)
+        if (t == 0 && li >= 1 && !(ok = wait_all(&sh.acc_free, (li - 1) & 1, kSiteBwdFinal))) break;
         if (lane == 0) {
           tc_fence_after();
 #pragma unroll

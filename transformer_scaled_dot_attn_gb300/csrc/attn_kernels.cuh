@@ -27,6 +27,8 @@ struct Watchdog {
   uint64_t budget_ns;    // per-wait limit
 };
 
+constexpr uint32_t kWaitSleepNs = 20000;  // longest suspension per try in guarded_wait
+
 // Bounded mbarrier wait. Returns false when the CTA is aborting or this wait
 // ran out of time (in which case it raises the CTA abort flag and records the
 // site in the device error word). Never traps, never spins forever.
@@ -35,7 +37,9 @@ __device__ __forceinline__ bool guarded_wait(uint64_t* bar, uint32_t parity, vol
   if (sm103::mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = sm103::global_timer_ns();
   while (true) {
-    if (sm103::mbar_try_wait(bar, parity)) return true;
+    // sleep in the barrier (woken by the phase completing) rather than spin:
+    // spinning warps take issue slots from the warps that do the work
+    if (sm103::mbar_try_wait_sleep(bar, parity, kWaitSleepNs)) return true;
     if (*abort_flag) return false;
     if (sm103::global_timer_ns() - t0 > wd.budget_ns) {
       *abort_flag = 1;
@@ -109,6 +113,26 @@ struct BwdPostParams {
   float scale;
   int n, n_pad, d, BH;
 };
+
+// Whole-head backward (n <= 256, d <= 64): one launch, no workspace.
+struct BwdHeadParams {
+  const __nv_bfloat16* o;   // [BH, n, d]
+  const __nv_bfloat16* dO;  // [BH, n, d]
+  const float* lse;         // [BH, n], natural log
+  __nv_bfloat16* dq;        // [BH, n, d]
+  __nv_bfloat16* dk;        // [BH, m, d]
+  __nv_bfloat16* dv;        // [BH, m, d]
+  int BH, n, m;
+  int causal, neg;
+  float c;                  // |scale| * log2(e)
+  float scale;              // signed scale, applied to dQ and dK
+  Watchdog wd;
+};
+bool bwd_head_supported(int n, int d);
+// tdq, tdk, tdv: maps over the bf16 outputs, the same shape of map as the inputs'.
+cudaError_t launch_bwd_head(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                            const CUtensorMap& tdo, const CUtensorMap& tdq, const CUtensorMap& tdk,
+                            const CUtensorMap& tdv, const BwdHeadParams& p, cudaStream_t stream);
 
 // tdq: 2-D fp32 map over the dQ accumulator [BH*n_pad, d], box 32 x 128, 128-byte swizzle.
 cudaError_t launch_bwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
