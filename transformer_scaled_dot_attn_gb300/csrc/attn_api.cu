@@ -244,10 +244,10 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return ATTN_ERR_INVALID_ARG;
   if (lse != nullptr && (reinterpret_cast<uintptr_t>(lse) & 3u) != 0) return ATTN_ERR_INVALID_ARG;
   const long long BH = static_cast<long long>(B) * h;
-  CUtensorMap tq, tk, tv;
+  CUtensorMap tq, tk, tv, to;
   const int bn = attn::fwd_key_tile(d_k, n);
   if (!make_tile_map(&tq, q, BH, n, d_k) || !make_tile_map(&tk, k, BH, m, d_k, bn) ||
-      !make_tile_map(&tv, v, BH, m, d_v, bn))
+      !make_tile_map(&tv, v, BH, m, d_v, bn) || !make_tile_map(&to, o, BH, n, d_v))
     return ATTN_ERR_CUDA;
   uint32_t* status = nullptr;
   if (device_status_word(&status) != cudaSuccess) return ATTN_ERR_CUDA;
@@ -263,7 +263,7 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
   p.inject = g_inject.exchange(0);
   p.wd.status = status;
   p.wd.budget_ns = g_watchdog_ns.load();
-  cudaError_t e = attn::launch_fwd(d_k, tq, tk, tv, p, static_cast<int>(BH),
+  cudaError_t e = attn::launch_fwd(d_k, tq, tk, tv, to, p, static_cast<int>(BH),
                                    reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }

@@ -122,6 +122,7 @@ struct FwdShared {
   uint64_t s_full[kMaxNQ], p_full[kMaxNQ], o_full[kMaxNQ];
   uint64_t s_free[kMaxNQ], pv_done[kMaxNQ];  // separate P only
   uint64_t exp_turn[2];  // two query tiles: their exponential phases alternate
+  uint64_t o_staged[kMaxNQ];
   uint64_t drain[kMaxNQ];
   uint32_t tmem_base;
   int abort_flag;
@@ -177,7 +178,8 @@ __device__ __forceinline__ void exp_chunk(const uint32_t (&s)[32], int col0, int
 template <int D, int NQ, int BN>
 __global__ void __launch_bounds__(Fwd<D, NQ, BN>::THREADS, Fwd<D, NQ, BN>::MIN_BLOCKS)
 attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
+                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                const FwdParams p) {
   using C = Fwd<D, NQ, BN>;
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) FwdShared sh;
@@ -215,6 +217,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       mbar_init(&sh.s_free[g], 128 * C::SPLIT);
       mbar_init(&sh.pv_done[g], 1);
     }
+    for (int g = 0; g < NQ; ++g) mbar_init(&sh.o_staged[g], 128 * C::SPLIT);
     mbar_init(&sh.exp_turn[0], 128 * C::SPLIT);
     mbar_init(&sh.exp_turn[1], 128 * C::SPLIT);
     sh.abort_flag = 0;
@@ -228,6 +231,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     prefetch_tensormap(&tm_q);
     prefetch_tensormap(&tm_k);
     prefetch_tensormap(&tm_v);
+    prefetch_tensormap(&tm_o);
   }
   tc_fence_before();
   __syncthreads();
@@ -487,9 +491,10 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       if (ok) {
         tc_fence_after();
         const float inv_l = 1.f / l;
-        const bool store = row < p.n;
-        uint4* orow = reinterpret_cast<uint4*>(p.o + (static_cast<size_t>(bh) * p.n + (store ? row : 0)) * D +
-                                               h * C::OCOLS);
+        // O leaves through the shared-memory tile of Q_g (no MMA reads it any
+        // more once o_full completed), written in the TMA map's swizzled layout
+        // and stored by one thread; rows past n are clipped by the map.
+        uint8_t* qtile = smem + C::OFF_Q + g * C::QTILE;
 #pragma unroll
         for (int q = 0; q < C::OCOLS / 16; ++q) {
           uint32_t o[16];
@@ -499,12 +504,27 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 #pragma unroll
           for (int i = 0; i < 8; ++i)
             pk[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
-          if (store) {
-            orow[q * 2] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-            orow[q * 2 + 1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const int c = (h * C::OCOLS + q * 16) / 8 + u;  // 16-byte chunk of the row
+            constexpr int CPA = C::ATOM / 8;                 // chunks per swizzle atom row
+            const int a = c / CPA, ca = c % CPA;
+            const int pc = (C::ATOM == 64) ? (ca ^ (r & 7)) : (ca ^ ((r >> 1) & 3));
+            *reinterpret_cast<uint4*>(qtile + a * C::QBOX + r * (C::ATOM * 2) + (pc << 4)) =
+                make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
           }
         }
-        if (store && h == 0 && p.lse != nullptr)
+        fence_proxy_async_smem();
+        mbar_arrive(&sh.o_staged[g]);
+        if (h == 0 && r == 0) {
+          if (guarded_wait(&sh.o_staged[g], 0, abort_flag, wd, kSiteOFull)) {
+            for (int a = 0; a < C::NATOM; ++a)
+              tma_store_3d(&tm_o, qtile + a * C::QBOX, a * C::ATOM, q0 + g * 128, bh);
+            tma_store_commit();
+            tma_store_wait_all();  // before the CTA (and its shared memory) goes away
+          }
+        }
+        if (row < p.n && h == 0 && p.lse != nullptr)
           p.lse[static_cast<size_t>(bh) * p.n + row] = (m_used + log2f(l)) * kLn2;
       }
     }
@@ -520,7 +540,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 
 template <int D, int NQ, int BN>
 cudaError_t launch_fwd_cfg(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                           FwdParams p, int BH, cudaStream_t stream) {
+                           const CUtensorMap& to, FwdParams p, int BH, cudaStream_t stream) {
   using C = Fwd<D, NQ, BN>;
   static std::once_flag once[64];
   int dev = 0;
@@ -547,7 +567,7 @@ cudaError_t launch_fwd_cfg(const CUtensorMap& tq, const CUtensorMap& tk, const C
   p.num_qblocks = (p.n + NQ * 128 - 1) / (NQ * 128);
   dim3 grid(static_cast<unsigned>(BH), static_cast<unsigned>(p.num_qblocks));
   prof_begin(kKindFwd, stream);
-  attn_fwd_kernel<D, NQ, BN><<<grid, C::THREADS, C::SMEM, stream>>>(tq, tk, tv, p);
+  attn_fwd_kernel<D, NQ, BN><<<grid, C::THREADS, C::SMEM, stream>>>(tq, tk, tv, to, p);
   e = cudaGetLastError();
   prof_end(kKindFwd, stream);
   return e;
@@ -587,16 +607,16 @@ cudaError_t launch_exp2_probe(const float* x, float* y_poly, float* y_mufu, int 
 // where 64-key tiles halve TMEM to 256 columns so two CTAs share an SM and
 // hide each other's prologue and epilogue latency (fwd_key_tile).
 cudaError_t launch_fwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                       const FwdParams& p, int BH, cudaStream_t stream) {
+                       const CUtensorMap& to, const FwdParams& p, int BH, cudaStream_t stream) {
   const bool small_tiles = fwd_key_tile(d, p.n) == 64;
   switch (d) {
     case 32:
-      return small_tiles ? launch_fwd_cfg<32, 2, 64>(tq, tk, tv, p, BH, stream)
-                         : launch_fwd_cfg<32, 2, 128>(tq, tk, tv, p, BH, stream);
+      return small_tiles ? launch_fwd_cfg<32, 2, 64>(tq, tk, tv, to, p, BH, stream)
+                         : launch_fwd_cfg<32, 2, 128>(tq, tk, tv, to, p, BH, stream);
     case 64:
-      return small_tiles ? launch_fwd_cfg<64, 2, 64>(tq, tk, tv, p, BH, stream)
-                         : launch_fwd_cfg<64, 2, 128>(tq, tk, tv, p, BH, stream);
-    case 128: return launch_fwd_cfg<128, 2, 128>(tq, tk, tv, p, BH, stream);
+      return small_tiles ? launch_fwd_cfg<64, 2, 64>(tq, tk, tv, to, p, BH, stream)
+                         : launch_fwd_cfg<64, 2, 128>(tq, tk, tv, to, p, BH, stream);
+    case 128: return launch_fwd_cfg<128, 2, 128>(tq, tk, tv, to, p, BH, stream);
     default: return cudaErrorInvalidValue;
   }
 }

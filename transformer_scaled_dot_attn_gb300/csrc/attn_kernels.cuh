@@ -77,6 +77,7 @@ cudaError_t launch_exp2_probe(const float* x, float* y_poly, float* y_mufu, int 
 int fwd_key_tile(int d, int n);
 
 cudaError_t launch_fwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                       const CUtensorMap& to,
                        const FwdParams& p, int BH, cudaStream_t stream);
 
 // ---------------------------------------------------------------- backward
