@@ -346,10 +346,11 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const f
   float* lse2 = dq_acc + BH * n_pad * d_k;
   float* Dsum = lse2 + BH * n_pad;
 
-  CUtensorMap tq, tk, tv, tdo, tdq;
+  CUtensorMap tq, tk, tv, tdo, tdq, tdk, tdv;
   if (!make_tile_map(&tq, q, BH, n, d_k) || !make_tile_map(&tk, k, BH, m, d_k) ||
       !make_tile_map(&tv, v, BH, m, d_v) || !make_tile_map(&tdo, dO, BH, n, d_v) ||
-      !make_dq_map(&tdq, dq_acc, BH * n_pad, d_k))
+      !make_dq_map(&tdq, dq_acc, BH * n_pad, d_k) || !make_tile_map(&tdk, dk, BH, m, d_k) ||
+      !make_tile_map(&tdv, dv, BH, m, d_v))
     return ATTN_ERR_CUDA;
   uint32_t* status = nullptr;
   if (device_status_word(&status) != cudaSuccess) return ATTN_ERR_CUDA;
@@ -392,7 +393,7 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const f
   post.d = d_k;
   post.BH = static_cast<int>(BH);
 
-  cudaError_t e = attn::launch_bwd(d_k, tq, tk, tv, tdo, tdq, pre, p, post, static_cast<int>(BH),
+  cudaError_t e = attn::launch_bwd(d_k, tq, tk, tv, tdk, tdv, tdo, tdq, pre, p, post, static_cast<int>(BH),
                                    reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
@@ -488,10 +489,11 @@ extern "C" int attn_bwd_noalloc(const void* q, const void* k, const void* v, con
   float* lse2 = dq_acc + BH * n_pad * d_k;
   float* Dsum = lse2 + BH * n_pad;
 
-  CUtensorMap tq, tk, tv, tdo, tdq;
+  CUtensorMap tq, tk, tv, tdo, tdq, tdk, tdv;
   if (!make_tile_map(&tq, q, BH, n, d_k) || !make_tile_map(&tk, k, BH, m, d_k) ||
       !make_tile_map(&tv, v, BH, m, d_v) || !make_tile_map(&tdo, dO, BH, n, d_v) ||
-      !make_dq_map(&tdq, dq_acc, BH * n_pad, d_k))
+      !make_dq_map(&tdq, dq_acc, BH * n_pad, d_k) || !make_tile_map(&tdk, dk, BH, m, d_k) ||
+      !make_tile_map(&tdv, dv, BH, m, d_v))
     return ATTN_ERR_CUDA;
 
   BwdPreParams pre{};
@@ -532,6 +534,6 @@ extern "C" int attn_bwd_noalloc(const void* q, const void* k, const void* v, con
   post.d = d_k;
   post.BH = static_cast<int>(BH);
 
-  cudaError_t e = attn::launch_bwd(d_k, tq, tk, tv, tdo, tdq, pre, p, post, static_cast<int>(BH), s);
+  cudaError_t e = attn::launch_bwd(d_k, tq, tk, tv, tdk, tdv, tdo, tdq, pre, p, post, static_cast<int>(BH), s);
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }

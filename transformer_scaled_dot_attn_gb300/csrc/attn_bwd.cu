@@ -149,6 +149,9 @@ struct Bwd {
   // + up to 1 KB to align the tiles; for D = 128 only what fits under the limit
   static constexpr uint32_t SMEM = (PAYLOAD + 1024 <= SMEM_LIMIT) ? PAYLOAD + 1024 : SMEM_LIMIT;
   static constexpr int THREADS = 512;
+  // d <= 64: the dV / dK tile (128 rows) fits a dS region and leaves by TMA store
+  static constexpr bool STAGE_OUT = (D <= 64);
+  static_assert(OFF_DS % 1024 == 0, "swizzled TMA tiles need 1024-byte alignment");
   // setmaxnreg split (registers per thread): compute, dQ, producer/MMA warpgroups.
   static constexpr int REG_COMPUTE = 152, REG_DQ = 96, REG_OTHER = 88;
   static constexpr bool ALIAS_DQ = (D > 64);
@@ -160,6 +163,7 @@ struct BwdShared {
   uint64_t kv_full[2], kv_empty[2];
   uint64_t qdo_full[2], qdo_empty[2];
   uint64_t s_full, dp_full, p_full, ds_full, ds_empty, dq_full, dq_empty, dkv_full, acc_free, drain;
+  uint64_t out_staged[2], out_free[2];  // d <= 64: dV / dK leave through dS region 0 / 1
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -186,7 +190,8 @@ template <int D>
 __global__ void __launch_bounds__(512, 1)
 attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-                const __grid_constant__ CUtensorMap tm_dq, const BwdParams p) {
+                const __grid_constant__ CUtensorMap tm_dq, const __grid_constant__ CUtensorMap tm_dk,
+                const __grid_constant__ CUtensorMap tm_dv, const BwdParams p) {
   using C = Bwd<D>;
   extern __shared__ uint8_t smem_raw[];
   const Watchdog wd = p.wd;
@@ -235,6 +240,10 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     mbar_init(&sh.dkv_full, 1);
     mbar_init(&sh.acc_free, 256);
     mbar_init(&sh.drain, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&sh.out_staged[i], 128);
+      mbar_init(&sh.out_free[i], 1);
+    }
     sh.abort_flag = 0;
     fence_mbar_init();
   }
@@ -248,6 +257,8 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     prefetch_tensormap(&tm_v);
     prefetch_tensormap(&tm_do);
     prefetch_tensormap(&tm_dq);
+    prefetch_tensormap(&tm_dk);
+    prefetch_tensormap(&tm_dv);
   }
   tc_fence_before();
   __syncthreads();
@@ -455,6 +466,12 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       int bh, kb, i_start, T;
       item_of(it, bh, kb, i_start, T);
       const int key = kb * 128 + r;
+      // region h carried the previous item's dV / dK out: its TMA store must
+      // have read it before dS (or this item's output) overwrites it
+      if (C::STAGE_OUT && li >= 1) {
+        ok = __all_sync(0xffffffffu, guarded_wait(&sh.out_free[h], (li - 1) & 1, abort_flag, wd, kSiteBwdFinal));
+        if (!ok) break;
+      }
       for (int t = 0; t < T; ++t) {
         const int gt = g + t;
         const int st = gt & 1;
@@ -550,6 +567,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       const size_t off = (static_cast<size_t>(bh) * p.m + (store ? key : 0)) * D;
       uint4* dst = reinterpret_cast<uint4*>((h ? p.dk : p.dv) + off);
       const float mul = h ? p.scale : 1.f;
+      uint8_t* region = smem + C::OFF_DS + h * C::DS_REGION;
 #pragma unroll
       for (int q = 0; q < D / 32; ++q) {
         uint32_t v[32];
@@ -564,7 +582,17 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 #pragma unroll
         for (int i = 0; i < 16; ++i)
           pk[i] = pack_bf16x2(__uint_as_float(v[2 * i]) * mul, __uint_as_float(v[2 * i + 1]) * mul);
-        if (store) {
+        if (C::STAGE_OUT) {
+          // row r of the tile in the map's swizzled layout: 128-byte rows with
+          // the 128-byte swizzle (d = 64), 64-byte rows with the 64-byte one (d = 32)
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int c = q * 4 + u;
+            const int pc = (D == 64) ? (c ^ (r & 7)) : (c ^ ((r >> 1) & 3));
+            *reinterpret_cast<uint4*>(region + r * (D * 2) + (pc << 4)) =
+                make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+          }
+        } else if (store) {
 #pragma unroll
           for (int u = 0; u < 4; ++u)
             dst[q * 4 + u] = make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
@@ -572,6 +600,19 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       }
       tc_fence_before();
       mbar_arrive(&sh.acc_free);
+      if (C::STAGE_OUT) {
+        // one thread stores the tile; rows past m are clipped by the map
+        fence_proxy_async_smem();
+        mbar_arrive(&sh.out_staged[h]);
+        if (r == 0) {
+          if (guarded_wait(&sh.out_staged[h], li & 1, abort_flag, wd, kSiteBwdFinal)) {
+            tma_store_3d(h ? &tm_dk : &tm_dv, region, 0, kb * 128, bh);
+            tma_store_commit();
+            bulk_wait_read_all();
+          }
+          mbar_arrive(&sh.out_free[h]);
+        }
+      }
       g += T;
     }
   } else {
@@ -642,6 +683,8 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     if (r == 0) tma_store_wait_all();
   }
 
+  // bulk stores issued by this thread must complete before the CTA exits
+  if (C::STAGE_OUT && (warp == 0 || warp == 4) && lane == 0) tma_store_wait_all();
   tc_fence_before();
   __syncthreads();
   if (warp == 13) {
@@ -652,6 +695,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 
 template <int D>
 cudaError_t launch_bwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                         const CUtensorMap& tdk, const CUtensorMap& tdv,
                          const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdPreParams& pre,
                          const BwdParams& p, const BwdPostParams& post, int BH, cudaStream_t stream) {
   using C = Bwd<D>;
@@ -699,7 +743,7 @@ cudaError_t launch_bwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
     pp.num_items = BH * p.num_kblocks;
     const int grid = pp.num_items < sm_count[dev & 63] ? pp.num_items : sm_count[dev & 63];
     prof_begin(kKindBwdMain, stream);
-    attn_bwd_kernel<D><<<grid, C::THREADS, C::SMEM, stream>>>(tq, tk, tv, tdo, tdq, pp);
+    attn_bwd_kernel<D><<<grid, C::THREADS, C::SMEM, stream>>>(tq, tk, tv, tdo, tdq, tdk, tdv, pp);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     prof_end(kKindBwdMain, stream);
   }
@@ -717,12 +761,13 @@ cudaError_t launch_bwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
 }  // namespace
 
 cudaError_t launch_bwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                       const CUtensorMap& tdk, const CUtensorMap& tdv,
                        const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdPreParams& pre,
                        const BwdParams& p, const BwdPostParams& post, int BH, cudaStream_t stream) {
   switch (d) {
-    case 32: return launch_bwd_d<32>(tq, tk, tv, tdo, tdq, pre, p, post, BH, stream);
-    case 64: return launch_bwd_d<64>(tq, tk, tv, tdo, tdq, pre, p, post, BH, stream);
-    case 128: return launch_bwd_d<128>(tq, tk, tv, tdo, tdq, pre, p, post, BH, stream);
+    case 32: return launch_bwd_d<32>(tq, tk, tv, tdk, tdv, tdo, tdq, pre, p, post, BH, stream);
+    case 64: return launch_bwd_d<64>(tq, tk, tv, tdk, tdv, tdo, tdq, pre, p, post, BH, stream);
+    case 128: return launch_bwd_d<128>(tq, tk, tv, tdk, tdv, tdo, tdq, pre, p, post, BH, stream);
     default: return cudaErrorInvalidValue;
   }
 }

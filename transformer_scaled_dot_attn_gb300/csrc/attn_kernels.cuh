@@ -136,7 +136,9 @@ cudaError_t launch_bwd_head(int d, const CUtensorMap& tq, const CUtensorMap& tk,
                             const CUtensorMap& tdv, const BwdHeadParams& p, cudaStream_t stream);
 
 // tdq: 2-D fp32 map over the dQ accumulator [BH*n_pad, d], box 32 x 128, 128-byte swizzle.
+// tdk, tdv: maps over the bf16 dK / dV outputs (the same shape of map as K's).
 cudaError_t launch_bwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                       const CUtensorMap& tdk, const CUtensorMap& tdv,
                        const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdPreParams& pre,
                        const BwdParams& p, const BwdPostParams& post, int BH, cudaStream_t stream);
 
