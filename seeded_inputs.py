@@ -130,6 +130,11 @@ def ragged_workloads() -> Iterator[Workload]:
         (2, 2, 200, 77, 32, False), (1, 2, 130, 300, 128, False),
         (1, 1, 255, 257, 128, True), (1, 1, 64, 1, 32, False),
         (3, 1, 300, 300, 32, True), (1, 1, 5, 400, 64, False),
+        # whole 128-key tiles, non-causal (the persistent forward): a partial
+        # second query tile, a query block whose second tile is empty, and a
+        # long ragged key sequence
+        (2, 3, 200, 256, 64, False), (1, 2, 130, 128, 32, False),
+        (1, 1, 384, 1024, 64, False), (1, 2, 100, 1100, 64, False),
     ]
     for i, (B, h, n, m, d, c) in enumerate(cases):
         yield _wl(f"ragged{i}_B{B}h{h}n{n}m{m}d{d}{'c' if c else ''}", B, h, n, m, d, c, 50 + i)

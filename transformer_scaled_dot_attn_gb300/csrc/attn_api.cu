@@ -245,7 +245,7 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
   if (lse != nullptr && (reinterpret_cast<uintptr_t>(lse) & 3u) != 0) return ATTN_ERR_INVALID_ARG;
   const long long BH = static_cast<long long>(B) * h;
   CUtensorMap tq, tk, tv, to;
-  const int bn = attn::fwd_key_tile(d_k, n);
+  const int bn = attn::fwd_key_tile(d_k, n, m, causal ? 1 : 0);
   if (!make_tile_map(&tq, q, BH, n, d_k) || !make_tile_map(&tk, k, BH, m, d_k, bn) ||
       !make_tile_map(&tv, v, BH, m, d_v, bn) || !make_tile_map(&to, o, BH, n, d_v))
     return ATTN_ERR_CUDA;

@@ -573,6 +573,443 @@ cudaError_t launch_fwd_cfg(const CUtensorMap& tq, const CUtensorMap& tk, const C
   return e;
 }
 
+// ---------------------------------------------------------------- persistent forward (d <= 64)
+//
+// One CTA per SM loops over work items (head, 256 query rows); items are
+// taken in launch order (causal: the blocks with the most key tiles first).
+// The two query tiles of an item are handled as in attn_fwd_kernel with P in
+// TMEM columns of its own. Across items: Q in two sets (the next item's Q
+// loads while the current one runs), one continuous K/V ring, and each query
+// tile's O epilogue (TMEM -> shared memory -> TMA store) overlaps the next
+// item's first score product, which only needs S to be free. The next item's
+// first P.V product waits until the epilogue has read O out of TMEM.
+// TMEM: S_0 S_1 [0,256), P_0 P_1 [256,384) (bf16 pairs), O_0 O_1 [384,384+2D).
+template <int D>
+struct FwdP {
+  static constexpr int NQ = 2, BN = 128;
+  static constexpr int ATOM = D;                          // one swizzle atom per row (D <= 64)
+  static constexpr uint32_t SWZ = (D == 64) ? 2u : 4u;
+  static constexpr uint32_t SBO = 8u * ATOM * 2u;
+  static constexpr uint32_t QTILE = 128u * D * 2u;
+  static constexpr uint32_t KTILE = BN * D * 2u;
+  static constexpr int STAGES = 4;
+  static constexpr uint32_t OFF_Q = 0;                    // 2 sets x NQ tiles
+  static constexpr uint32_t OFF_K = 2 * NQ * QTILE;
+  static constexpr uint32_t OFF_V = OFF_K + STAGES * KTILE;
+  static constexpr uint32_t SMEM = OFF_V + STAGES * KTILE + 1024;
+  static constexpr int THREADS = NQ * 128 + 128;          // softmax, producer, issuers, idle
+  static constexpr int PRODUCER = 4 * NQ, ISSUER = 4 * NQ + 1;
+  static constexpr int CHUNKS = BN / 32;
+  static constexpr uint32_t P_COLS = BN / 2;
+  __host__ __device__ static constexpr uint32_t tm_s(int g) { return g * BN; }
+  __host__ __device__ static constexpr uint32_t tm_p(int g) { return NQ * BN + g * P_COLS; }
+  __host__ __device__ static constexpr uint32_t tm_o(int g) { return NQ * (BN + P_COLS) + g * D; }
+  static_assert(NQ * (BN + P_COLS + D) <= 512, "TMEM columns");
+};
+
+struct FwdPShared {
+  uint64_t q_full[2], q_empty[2];
+  uint64_t kv_full[kMaxStages];
+  uint64_t kv_empty[2][kMaxStages];
+  uint64_t s_full[2], s_free[2], p_full[2], pv_done[2], o_full[2], o_free[2], o_staged[2];
+  uint64_t drain[2];
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+template <int D>
+__global__ void __launch_bounds__(FwdP<D>::THREADS, 1)
+attn_fwd_persist_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                        const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                        const FwdParams p, int BH, int items) {
+  using C = FwdP<D>;
+  constexpr int NQ = C::NQ, BN = C::BN;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) FwdPShared sh;
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  volatile int* abort_flag = &sh.abort_flag;
+  const Watchdog wd = p.wd;
+  // item -> (head, first query row); key tiles per query tile (0 past n)
+  auto item_of = [&](int it, int& bh, int& q0, int (&ntile)[2], int& nt, int& nq_valid) {
+    bh = it % BH;
+    const int y = it / BH;
+    const int qb = p.causal ? (p.num_qblocks - 1 - y) : y;
+    q0 = qb * (NQ * 128);
+    nt = 0;
+    nq_valid = 0;
+#pragma unroll
+    for (int g = 0; g < NQ; ++g) {
+      const int r0 = q0 + g * 128;
+      ntile[g] = (r0 < p.n) ? key_tiles<BN>(min(r0 + 127, p.n - 1), p.m, p.causal) : 0;
+      nt = max(nt, ntile[g]);
+      nq_valid += (r0 < p.n) ? 1 : 0;
+    }
+  };
+
+  if (tid == 0) {
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&sh.q_full[s], 1);
+      mbar_init(&sh.q_empty[s], NQ);
+    }
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(&sh.kv_full[s], 1);
+      for (int g = 0; g < NQ; ++g) mbar_init(&sh.kv_empty[g][s], 1);
+    }
+    for (int g = 0; g < NQ; ++g) {
+      mbar_init(&sh.s_full[g], 1);
+      mbar_init(&sh.s_free[g], 128);
+      mbar_init(&sh.p_full[g], 128);
+      mbar_init(&sh.pv_done[g], 1);
+      mbar_init(&sh.o_full[g], 1);
+      mbar_init(&sh.o_free[g], 128);
+      mbar_init(&sh.o_staged[g], 128);
+      mbar_init(&sh.drain[g], 1);
+    }
+    sh.abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == C::ISSUER) {
+    tmem_alloc<512>(&sh.tmem_base);
+    tmem_relinquish();
+  }
+  if (warp == C::PRODUCER && lane == 0) {
+    prefetch_tensormap(&tm_q);
+    prefetch_tensormap(&tm_k);
+    prefetch_tensormap(&tm_v);
+    prefetch_tensormap(&tm_o);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sh.tmem_base;
+
+  if (warp == C::PRODUCER) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      // per stage s, group g (bit g * 4 + s): `users` = the stage's last tile was
+      // used by group g; `uses` = parity of group g's uses of stage s so far
+      uint32_t users = 0, uses = 0, kv_filled = 0, kv_ph = 0, q_filled = 0, q_ph = 0;
+      int jj = 0;
+      bool ok = true;
+      for (int it = blockIdx.x, li = 0; ok && it < items; it += gridDim.x, ++li) {
+        int bh, q0, ntile[2], nt, nq_valid;
+        item_of(it, bh, q0, ntile, nt, nq_valid);
+        const int qs = li & 1;
+        if (li >= 2 && !(ok = guarded_wait(&sh.q_empty[qs], ((li >> 1) - 1) & 1, abort_flag, wd, kSiteKEmpty)))
+          break;
+        mbar_arrive_expect_tx(&sh.q_full[qs], nq_valid * C::QTILE);
+        for (int t = 0; t < nq_valid; ++t)
+          tma_load_3d(smem + C::OFF_Q + (qs * NQ + t) * C::QTILE, &tm_q, &sh.q_full[qs], 0, q0 + t * 128, bh);
+        q_filled |= 1u << qs;
+        q_ph = (q_ph & ~(1u << qs)) | (static_cast<uint32_t>((li >> 1) & 1) << qs);
+        for (int j = 0; ok && j < nt; ++j, ++jj) {
+          const int st = jj % C::STAGES;
+          // the stage's previous tile must be released by every query tile that used it
+#pragma unroll
+          for (int g = 0; g < NQ; ++g) {
+            const uint32_t bit = 1u << (g * 4 + st);
+            if (ok && (users & bit))
+              ok = guarded_wait(&sh.kv_empty[g][st], ((uses & bit) ? 1u : 0u) ^ 1u, abort_flag, wd, kSiteKEmpty);
+          }
+          if (!ok) break;
+          mbar_arrive_expect_tx(&sh.kv_full[st], 2 * C::KTILE);
+          kv_filled |= 1u << st;
+          kv_ph = (kv_ph & ~(1u << st)) | (static_cast<uint32_t>((jj / C::STAGES) & 1) << st);
+          tma_load_3d(smem + C::OFF_K + st * C::KTILE, &tm_k, &sh.kv_full[st], 0, j * BN, bh);
+          if (!(p.inject == 1 && jj == 0))  // test hook: this value tile never arrives
+            tma_load_3d(smem + C::OFF_V + st * C::KTILE, &tm_v, &sh.kv_full[st], 0, j * BN, bh);
+#pragma unroll
+          for (int g = 0; g < NQ; ++g) {
+            const uint32_t bit = 1u << (g * 4 + st);
+            if (j < ntile[g]) {
+              users |= bit;
+              uses ^= bit;
+            } else {
+              users &= ~bit;
+            }
+          }
+        }
+      }
+      // Let every copy this thread started land before shared memory is released.
+      for (int s = 0; s < 2; ++s)
+        if ((q_filled >> s) & 1u) drain_wait(&sh.q_full[s], (q_ph >> s) & 1u, wd);
+      for (int s = 0; s < C::STAGES; ++s)
+        if ((kv_filled >> s) & 1u) drain_wait(&sh.kv_full[s], (kv_ph >> s) & 1u, wd);
+    }
+  } else if (warp >= C::ISSUER) {
+    // ------------------------------------------------------------ MMA issuer of query tile g
+    const int g = warp - C::ISSUER;
+    if (lane == 0 && g < NQ) {
+      const uint32_t idesc_s = idesc_bf16_f32(128, BN, false, false) | (p.neg ? (1u << 13) : 0u);
+      const uint32_t idesc_o = idesc_bf16_f32(128, D, false, true);
+      const uint32_t sK = smem_u32(smem + C::OFF_K), sV = smem_u32(smem + C::OFF_V);
+      const uint32_t t_s = tmem + C::tm_s(g), t_p = tmem + C::tm_p(g), t_o = tmem + C::tm_o(g);
+      auto issue_s = [&](uint32_t sQ, int st) {
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k) {
+          const uint64_t da = smem_desc(sQ + k * 32, 16, C::SBO, C::SWZ);
+          const uint64_t db = smem_desc(sK + st * C::KTILE + k * 32, 16, C::SBO, C::SWZ);
+          mma_ss(t_s, da, db, idesc_s, k > 0 ? 1u : 0u);
+        }
+      };
+      auto issue_pv = [&](int st, bool acc) {
+#pragma unroll
+        for (int k = 0; k < BN / 16; ++k) {
+          const uint64_t db = smem_desc(sV + st * C::KTILE + k * 16 * C::ATOM * 2, C::KTILE, C::SBO, C::SWZ);
+          mma_ts(t_o, t_p + k * 8, db, idesc_o, (acc || k > 0) ? 1u : 0u);
+        }
+      };
+      bool ok = true;
+      int jj = 0, gt = 0, oc = 0;  // K/V tiles of earlier items, this tile's S count, items with output
+      for (int it = blockIdx.x, li = 0; ok && it < items; it += gridDim.x, ++li) {
+        int bh, q0, ntile[2], nt, nq_valid;
+        item_of(it, bh, q0, ntile, nt, nq_valid);
+        const int T = g == 0 ? ntile[0] : ntile[1];
+        if (T > 0) {
+          const uint32_t sQ = smem_u32(smem + C::OFF_Q) + ((li & 1) * NQ + g) * C::QTILE;
+          // S of this item's first tile: Q landed, K_0 landed, the softmax holds the previous S
+          ok = guarded_wait(&sh.q_full[li & 1], (li >> 1) & 1, abort_flag, wd, kSiteQFull) &&
+               guarded_wait(&sh.kv_full[jj % C::STAGES], (jj / C::STAGES) & 1, abort_flag, wd, kSiteKFull) &&
+               (gt == 0 || guarded_wait(&sh.s_free[g], (gt - 1) & 1, abort_flag, wd, kSiteSFull));
+          if (!ok) break;
+          tc_fence_after();
+          issue_s(sQ, jj % C::STAGES);
+          mma_commit(&sh.s_full[g]);
+          for (int j = 0; ok && j < T; ++j) {
+            const int st = (jj + j) % C::STAGES;
+            if (j + 1 < T) {
+              const int jn = jj + j + 1;
+              if (!(ok = guarded_wait(&sh.s_free[g], (gt + j) & 1, abort_flag, wd, kSiteSFull))) break;
+              if (!(ok = guarded_wait(&sh.kv_full[jn % C::STAGES], (jn / C::STAGES) & 1, abort_flag, wd, kSiteKFull)))
+                break;
+              tc_fence_after();
+              issue_s(sQ, jn % C::STAGES);
+              mma_commit(&sh.s_full[g]);
+            }
+            if (!(ok = guarded_wait(&sh.p_full[g], (gt + j) & 1, abort_flag, wd, kSitePFull))) break;
+            // the first P.V of an item overwrites O: the previous item's epilogue must have read it
+            if (j == 0 && oc >= 1 && !(ok = guarded_wait(&sh.o_free[g], (oc - 1) & 1, abort_flag, wd, kSiteOFull)))
+              break;
+            tc_fence_after();
+            issue_pv(st, j > 0);
+            mma_commit(&sh.pv_done[g]);
+            if (j == T - 1) mma_commit(&sh.o_full[g]);
+            mma_commit(&sh.kv_empty[g][st]);  // K and V of this tile are no longer read by this query tile
+          }
+          gt += T;
+          ++oc;
+        }
+        jj += nt;
+      }
+      // Every MMA this thread issued must finish before TMEM is released.
+      mma_commit(&sh.drain[g]);
+      drain_wait(&sh.drain[g], 0, wd);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ softmax of query tile g
+    const int g = warp >> 2;
+    const int r = tid & 127;
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t t_s = tmem + lane_base + C::tm_s(g);
+    const uint32_t t_p = tmem + lane_base + C::tm_p(g);
+    const uint32_t t_o = tmem + lane_base + C::tm_o(g);
+    const float c = p.c;
+    const uint64_t c2 = f2_pack(c, c);
+    bool ok = true;
+    int gt = 0, oc = 0;
+    // Q set whose O store thread 0 issued but has not yet seen read (-1: none).
+    // The wait for the store is deferred to the next item so that thread 0
+    // (and with it the group) is not held up by the store's latency.
+    int pending_q = -1;
+    auto release_pending = [&]() {
+      if (r == 0 && pending_q >= 0) {
+        bulk_wait_read_all();
+        mbar_arrive(&sh.q_empty[pending_q]);  // this Q tile may take a later item's rows
+        pending_q = -1;
+      }
+    };
+    for (int it = blockIdx.x, li = 0; ok && it < items; it += gridDim.x, ++li) {
+      int bh, q0, ntile[2], nt, nq_valid;
+      item_of(it, bh, q0, ntile, nt, nq_valid);
+      const int T = g == 0 ? ntile[0] : ntile[1];
+      const int qs = li & 1;
+      if (T == 0) {
+        release_pending();
+        // no rows of this item here: the Q set does not wait for this tile's output
+        if (r == 0) mbar_arrive(&sh.q_empty[qs]);
+        continue;
+      }
+      const int row = q0 + g * 128 + r;
+      const int lim = p.causal ? min(row + 1, p.m) : p.m;  // keys [0, lim) are visible
+      float m_used = 0.f, l = 0.f;
+      for (int j = 0; j < T; ++j) {
+        const int gj = gt + j;
+        ok = __all_sync(0xffffffffu, guarded_wait(&sh.s_full[g], gj & 1, abort_flag, wd, kSiteSFull));
+        if (!ok) break;
+        tc_fence_after();
+        if (j == 0) release_pending();
+        uint32_t s[C::CHUNKS][32];
+#pragma unroll
+        for (int q = 0; q < C::CHUNKS; ++q) tmem_ld32(t_s + q * 32, s[q]);
+        tmem_ld_wait();
+        tc_fence_before();
+        mbar_arrive(&sh.s_free[g]);  // S may be overwritten by the next score product
+        const int rem = lim - j * BN;
+        const bool masked = __any_sync(0xffffffffu, rem < BN);
+        if (masked) {
+#pragma unroll
+          for (int q = 0; q < C::CHUNKS; ++q)
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              if (q * 32 + i >= rem) s[q][i] = __float_as_uint(-INFINITY);
+        }
+        float mx4[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          mx4[u] = fmaxf(__uint_as_float(s[0][2 * u]), __uint_as_float(s[0][2 * u + 1]));
+#pragma unroll
+        for (int e = 8; e < BN; e += 8) {
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+            mx4[u] = max3(mx4[u], __uint_as_float(s[(e + 2 * u) >> 5][(e + 2 * u) & 31]),
+                          __uint_as_float(s[(e + 2 * u + 1) >> 5][(e + 2 * u + 1) & 31]));
+        }
+        const float m_new = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * c;
+        float alpha = 1.f;
+        bool rescale = false;
+        if (j == 0) {
+          m_used = m_new;
+        } else if (m_new > m_used + kRescaleThreshold) {
+          alpha = ex2(m_used - m_new);
+          m_used = m_new;
+          rescale = true;
+        }
+        const uint64_t nm2 = f2_pack(-m_used, -m_used);
+        if (gj >= 1) {
+          // the previous P.V (possibly the previous item's) still reads P until it completes
+          ok = __all_sync(0xffffffffu, guarded_wait(&sh.pv_done[g], (gj - 1) & 1, abort_flag, wd, kSitePFull));
+          if (!ok) break;
+          tc_fence_after();
+        }
+        uint64_t lsum2[2] = {0ull, 0ull};
+#pragma unroll
+        for (int q = 0; q < C::CHUNKS; ++q) {
+          uint32_t pk[16];
+          if (masked)
+            exp_chunk<true>(s[q], q * 32, rem, c2, nm2, lsum2, pk);
+          else
+            exp_chunk<false>(s[q], q * 32, rem, c2, nm2, lsum2, pk);
+          tmem_st16(t_p + q * 16, pk);
+        }
+        {
+          float a0, a1, b0, b1;
+          f2_unpack(lsum2[0], a0, a1);
+          f2_unpack(lsum2[1], b0, b1);
+          l = l * alpha + ((a0 + a1) + (b0 + b1));
+        }
+        tmem_st_wait();
+        if (j > 0 && __any_sync(0xffffffffu, rescale)) {
+#pragma unroll
+          for (int q = 0; q < D / 16; ++q) {
+            uint32_t o[16];
+            tmem_ld16(t_o + q * 16, o);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 16; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+            tmem_st16(t_o + q * 16, o);
+          }
+          tmem_st_wait();
+        }
+        tc_fence_before();
+        mbar_arrive(&sh.p_full[g]);
+      }
+      if (!ok) break;
+      // epilogue: O / l into the Q tile of this item (no MMA reads it once o_full
+      // completed), one thread stores it; rows past n are clipped by the map
+      ok = __all_sync(0xffffffffu, guarded_wait(&sh.o_full[g], oc & 1, abort_flag, wd, kSiteOFull));
+      if (!ok) break;
+      tc_fence_after();
+      const float inv_l = 1.f / l;
+      uint32_t w[D / 2];
+#pragma unroll
+      for (int q = 0; q < D / 16; ++q) {
+        uint32_t o[16];
+        tmem_ld16(t_o + q * 16, o);
+        tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          w[q * 8 + i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
+      }
+      tc_fence_before();
+      mbar_arrive(&sh.o_free[g]);  // the next item's first P.V may overwrite O
+      uint8_t* qtile = smem + C::OFF_Q + (qs * NQ + g) * C::QTILE;
+#pragma unroll
+      for (int ch = 0; ch < D / 8; ++ch) {
+        const int pc = (D == 64) ? (ch ^ (r & 7)) : (ch ^ ((r >> 1) & 3));
+        *reinterpret_cast<uint4*>(qtile + r * (D * 2) + (pc << 4)) =
+            make_uint4(w[4 * ch], w[4 * ch + 1], w[4 * ch + 2], w[4 * ch + 3]);
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(&sh.o_staged[g]);
+      if (r == 0) {
+        release_pending();  // the previous item's store, long done by now
+        if (guarded_wait(&sh.o_staged[g], oc & 1, abort_flag, wd, kSiteOFull)) {
+          tma_store_3d(&tm_o, qtile, 0, q0 + g * 128, bh);
+          tma_store_commit();
+        }
+        pending_q = qs;
+      }
+      if (row < p.n && p.lse != nullptr) p.lse[static_cast<size_t>(bh) * p.n + row] = (m_used + log2f(l)) * kLn2;
+      gt += T;
+      ++oc;
+    }
+    release_pending();
+    if (r == 0) tma_store_wait_all();  // stores must complete before the CTA exits
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == C::ISSUER) {
+    tc_fence_after();
+    tmem_dealloc<512>(tmem);
+  }
+}
+
+template <int D>
+cudaError_t launch_fwd_persist(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                               const CUtensorMap& to, FwdParams p, int BH, cudaStream_t stream) {
+  using C = FwdP<D>;
+  static std::once_flag once[64];
+  static int sm_count[64] = {0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  cudaError_t attr = cudaSuccess;
+  std::call_once(once[dev & 63], [&] {
+    attr = cudaFuncSetAttribute(attn_fwd_persist_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                static_cast<int>(C::SMEM));
+  });
+  if (attr != cudaSuccess) return attr;
+  if (sm_count[dev & 63] == 0) {
+    int c = 0;
+    if ((e = cudaDeviceGetAttribute(&c, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    sm_count[dev & 63] = c > 0 ? c : 1;
+  }
+  p.num_qblocks = (p.n + C::NQ * 128 - 1) / (C::NQ * 128);
+  const long long items_ll = static_cast<long long>(BH) * p.num_qblocks;
+  if (items_ll > 0x7fffffffLL) return cudaErrorInvalidValue;
+  const int items = static_cast<int>(items_ll);
+  const int grid = items < sm_count[dev & 63] ? items : sm_count[dev & 63];
+  prof_begin(kKindFwd, stream);
+  attn_fwd_persist_kernel<D><<<grid, C::THREADS, C::SMEM, stream>>>(tq, tk, tv, to, p, BH, items);
+  e = cudaGetLastError();
+  prof_end(kKindFwd, stream);
+  return e;
+}
+
 __global__ void exp2_probe_kernel(const float* x, float* y_poly, float* y_mufu, int n) {
   const int i = 2 * (blockIdx.x * blockDim.x + threadIdx.x);
   if (i >= n) return;
@@ -592,7 +1029,18 @@ __global__ void exp2_probe_kernel(const float* x, float* y_poly, float* y_mufu, 
 
 }  // namespace
 
-int fwd_key_tile(int d, int n) { return (d >= 128 || n > 256) ? 128 : 64; }
+// Which forward kernel runs (measured on GB300, see the launcher below).
+namespace {
+bool fwd_persistent(int d, int n, int m, int causal) {
+  (void)n;
+  return d <= 64 && !causal && (m % 128 == 0 || m >= 1024);
+}
+}  // namespace
+
+int fwd_key_tile(int d, int n, int m, int causal) {
+  if (fwd_persistent(d, n, m, causal)) return 128;
+  return (d >= 128 || n > 256) ? 128 : 64;
+}
 
 cudaError_t launch_exp2_probe(const float* x, float* y_poly, float* y_mufu, int n,
                               cudaStream_t stream) {
@@ -602,18 +1050,23 @@ cudaError_t launch_exp2_probe(const float* x, float* y_poly, float* y_mufu, int 
   return cudaGetLastError();
 }
 
-// Configuration: two 128-row query tiles per CTA. Key tiles of 128 (TMEM
-// 2 x (128 + D) columns, one CTA per SM) except for d <= 64 with n <= 256,
-// where 64-key tiles halve TMEM to 256 columns so two CTAs share an SM and
-// hide each other's prologue and epilogue latency (fwd_key_tile).
+// Configuration: two 128-row query tiles per item. Non-causal d <= 64 with
+// whole 128-key tiles (or long key sequences): the persistent kernel (P in
+// TMEM columns of its own, items overlapped). Otherwise one CTA per item:
+// 128-key tiles, or for d <= 64 with n <= 256 64-key tiles that halve TMEM to
+// 256 columns so two CTAs share an SM (ragged or causal short sequences
+// measured faster this way).
 cudaError_t launch_fwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const CUtensorMap& to, const FwdParams& p, int BH, cudaStream_t stream) {
-  const bool small_tiles = fwd_key_tile(d, p.n) == 64;
+  const bool persist = fwd_persistent(d, p.n, p.m, p.causal);
+  const bool small_tiles = fwd_key_tile(d, p.n, p.m, p.causal) == 64;
   switch (d) {
     case 32:
+      if (persist) return launch_fwd_persist<32>(tq, tk, tv, to, p, BH, stream);
       return small_tiles ? launch_fwd_cfg<32, 2, 64>(tq, tk, tv, to, p, BH, stream)
                          : launch_fwd_cfg<32, 2, 128>(tq, tk, tv, to, p, BH, stream);
     case 64:
+      if (persist) return launch_fwd_persist<64>(tq, tk, tv, to, p, BH, stream);
       return small_tiles ? launch_fwd_cfg<64, 2, 64>(tq, tk, tv, to, p, BH, stream)
                          : launch_fwd_cfg<64, 2, 128>(tq, tk, tv, to, p, BH, stream);
     case 128: return launch_fwd_cfg<128, 2, 128>(tq, tk, tv, to, p, BH, stream);

@@ -74,7 +74,7 @@ cudaError_t launch_exp2_probe(const float* x, float* y_poly, float* y_mufu, int 
 
 // Keys per tile the forward kernel streams for head size d and n queries
 // (the K/V TMA box height).
-int fwd_key_tile(int d, int n);
+int fwd_key_tile(int d, int n, int m, int causal);
 
 cudaError_t launch_fwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const CUtensorMap& to,
