@@ -56,11 +56,11 @@ def _load():
             lp = ctypes.POINTER(ctypes.c_long)
             L, I, D = ctypes.c_long, ctypes.c_int, ctypes.c_double
             lib.oracle_attn_weights.argtypes = [dp, dp, L, L, L, I, D, dp, dp]
-            lib.oracle_attn_fwd.argtypes = [dp, dp, dp, dp, dp, L, L, L, L, L, L, I, D, lp, L]
+            lib.oracle_attn_fwd.argtypes = [dp, dp, dp, dp, dp, L, L, L, L, L, L, I, D, lp, L, lp]
             lib.oracle_attn_bwd.argtypes = [dp, dp, dp, dp, dp, dp, dp, dp, dp,
-                                            L, L, L, L, L, L, I, D]
+                                            L, L, L, L, L, L, I, D, lp]
             lib.oracle_attn_bwd_rows.argtypes = [dp, dp, dp, dp, L, L, L, L, I, D, lp, L, dp,
-                                                 lp, L, dp, dp]
+                                                 lp, L, dp, dp, L]
             lib.oracle_attn_bwd_rows.restype = ctypes.c_int
             for f in (lib.oracle_attn_weights, lib.oracle_attn_fwd, lib.oracle_attn_bwd):
                 f.restype = ctypes.c_int
@@ -117,10 +117,22 @@ def weights(q, k, causal: bool, scale: float):
     return S, P
 
 
-def fwd(q, k, v, causal: bool, scale: float, rows: Optional[Sequence[int]] = None):
+def _lens(kv_len, B):
+    """Per-sequence real key counts as a C long array (None: no key padding)."""
+    if kv_len is None:
+        return None, None
+    a = np.ascontiguousarray(np.asarray(kv_len, dtype=np.int64).reshape(-1))
+    if a.size != B:
+        raise ValueError("kv_len needs one entry per sequence")
+    return a, a.ctypes.data_as(ctypes.POINTER(ctypes.c_long))
+
+
+def fwd(q, k, v, causal: bool, scale: float, rows: Optional[Sequence[int]] = None, kv_len=None):
     """O (fp64, shape of q with d_v) and lse ([..., n]) by eq. (1).
 
     With ``rows`` only those query rows are computed; the others are NaN.
+    ``kv_len`` (one entry per sequence b): only the first kv_len[b] keys of
+    sequence b are real, the rest are padding (masked).
     """
     Q, K, V = _as4(_f64(q)), _as4(_f64(k)), _as4(_f64(v))
     B, h, n, dk = Q.shape
@@ -134,16 +146,20 @@ def fwd(q, k, v, causal: bool, scale: float, rows: Optional[Sequence[int]] = Non
     if rows is not None:
         r = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
         nr = int(r.size)
+    lens, lens_p = _lens(kv_len, B)
     _check(_load().oracle_attn_fwd(
         _ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(lse), B, h, n, m, dk, dv, int(causal),
         float(scale), None if r is None else r.ctypes.data_as(ctypes.POINTER(ctypes.c_long)),
-        nr), "fwd")
+        nr, lens_p), "fwd")
     shape_o = tuple(np.shape(q)[:-1]) + (dv,)
     return O.reshape(shape_o), lse.reshape(shape_o[:-1])
 
 
-def bwd(q, k, v, dO, causal: bool, scale: float, need=("dq", "dk", "dv")):
-    """dQ, dK, dV of L = sum(dO * O) for O = Attention(q, k, v); also O and lse."""
+def bwd(q, k, v, dO, causal: bool, scale: float, need=("dq", "dk", "dv"), kv_len=None):
+    """dQ, dK, dV of L = sum(dO * O) for O = Attention(q, k, v); also O and lse.
+
+    ``kv_len``: per-sequence real key counts, as in ``fwd``.
+    """
     Q, K, V, G = _as4(_f64(q)), _as4(_f64(k)), _as4(_f64(v)), _as4(_f64(dO))
     B, h, n, dk = Q.shape
     m, dv = K.shape[2], V.shape[3]
@@ -154,9 +170,10 @@ def bwd(q, k, v, dO, causal: bool, scale: float, need=("dq", "dk", "dv")):
     dV = np.zeros((B, h, m, dv)) if "dv" in need else None
     O = np.empty((B, h, n, dv))
     lse = np.empty((B, h, n))
+    lens, lens_p = _lens(kv_len, B)
     _check(_load().oracle_attn_bwd(_ptr(Q), _ptr(K), _ptr(V), _ptr(G), _ptr(dQ), _ptr(dK),
                                    _ptr(dV), _ptr(O), _ptr(lse), B, h, n, m, dk, dv,
-                                   int(causal), float(scale)), "bwd")
+                                   int(causal), float(scale), lens_p), "bwd")
     lead_q = tuple(q.shape[:-2])
     lead_k = tuple(k.shape[:-2])
 
@@ -167,10 +184,11 @@ def bwd(q, k, v, dO, causal: bool, scale: float, need=("dq", "dk", "dv")):
             O.reshape(lead_q + (n, dv)), lse.reshape(lead_q + (n,)))
 
 
-def bwd_rows(q, k, v, dO, causal: bool, scale: float, qrows=(), krows=()):
+def bwd_rows(q, k, v, dO, causal: bool, scale: float, qrows=(), krows=(), kv_len=None):
     """Sampled backward of ONE head: (dQ[qrows], dK[krows], dV[krows]), fp64.
 
     q, dO: [n, d]; k, v: [m, d]. Key rows cost a full forward of the head.
+    ``kv_len``: the head's real key count (None: all m).
     """
     Q, K, V, G = _f64(q), _f64(k), _f64(v), _f64(dO)
     n, dk = Q.shape
@@ -184,5 +202,5 @@ def bwd_rows(q, k, v, dO, causal: bool, scale: float, qrows=(), krows=()):
     _check(_load().oracle_attn_bwd_rows(
         _ptr(Q), _ptr(K), _ptr(V), _ptr(G), n, m, dk, dv, int(causal), float(scale),
         qr.ctypes.data_as(lp), qr.size, _ptr(dQ), kr.ctypes.data_as(lp), kr.size, _ptr(dK),
-        _ptr(dV)), "bwd_rows")
+        _ptr(dV), -1 if kv_len is None else int(kv_len)), "bwd_rows")
     return dQ[: qr.size], dK[: kr.size], dV[: kr.size]

@@ -36,6 +36,11 @@
  *     j <= i, for any n and m.
  *   - lse_i = M_i + ln(l_i) = ln sum_j exp(s_ij), in natural-log units of the
  *     scaled score.
+ *   - key padding (variable-length batches; the <pad> positions of Figure 3):
+ *     sequence b has kv_len[b] real keys, the first ones; the others are
+ *     masked like illegal connections (weight exactly 0, no gradient). A row
+ *     that sees no key at all (kv_len[b] = 0) has O = 0, lse = -inf and zero
+ *     gradients (the empty sum).
  *
  * Layout: every tensor is a contiguous row-major [B, h, S, d] array of
  * doubles (lse is [B, h, n]). Built with -O2 -ffp-contract=off and without
@@ -58,6 +63,21 @@
 static long visible_keys(long i, long m, int causal) {
     if (!causal) return m;
     return (i + 1 < m) ? (i + 1) : m;
+}
+
+/* Keys visible to query i when only the first mb keys are real (key
+ * padding, mb <= m): the causal limit, cut at mb. */
+static long visible_padded(long i, long m, int causal, long mb) {
+    const long v = visible_keys(i, m, causal);
+    return v < mb ? v : mb;
+}
+
+/* Real keys of head bh: kv_len[b] for its sequence b = bh / h, clamped to
+ * [0, m]; all m without a length array. */
+static long head_keys(const long *kv_len, long bh, long h, long m) {
+    if (!kv_len) return m;
+    const long mb = kv_len[bh / h];
+    return mb < 0 ? 0 : (mb > m ? m : mb);
 }
 
 /* Step MatMul + Scale + Mask of Figure 2 for one query row:
@@ -83,6 +103,10 @@ static double softmax_row(double *s, long m) {
     double M = -INFINITY;
     for (long j = 0; j < m; ++j)
         if (s[j] > M) M = s[j];
+    if (M == -INFINITY) { /* no visible key: the empty sum */
+        for (long j = 0; j < m; ++j) s[j] = 0.0;
+        return -INFINITY;
+    }
     double l = 0.0;
     for (long j = 0; j < m; ++j) {
         s[j] = exp(s[j] - M);
@@ -138,7 +162,7 @@ int oracle_attn_weights(const double *Q, const double *K, long n, long m,
 int oracle_attn_fwd(const double *q, const double *k, const double *v,
                     double *o, double *lse, long B, long h, long n, long m,
                     long dk, long dv, int causal, double scale,
-                    const long *rows, long nrows) {
+                    const long *rows, long nrows, const long *kv_len) {
     if (check_dims(B, h, n, m, dk, dv) != ORACLE_OK) return ORACLE_ERR_ARG;
     const long heads = B * h;
     const long R = rows ? nrows : n;
@@ -161,7 +185,8 @@ int oracle_attn_fwd(const double *q, const double *k, const double *v,
                 const double *Q = q + bh * n * dk;
                 const double *K = k + bh * m * dk;
                 const double *V = v + bh * m * dv;
-                score_row(Q + i * dk, K, m, dk, scale, visible_keys(i, m, causal), row);
+                score_row(Q + i * dk, K, m, dk, scale,
+                          visible_padded(i, m, causal, head_keys(kv_len, bh, h, m)), row);
                 const double l = softmax_row(row, m);
                 weighted_sum(row, V, m, dv, o + (bh * n + i) * dv);
                 if (lse) lse[bh * n + i] = l;
@@ -179,10 +204,10 @@ int oracle_attn_fwd(const double *q, const double *k, const double *v,
  * row (m doubles) and oi (dv doubles) are scratch.
  */
 static void bwd_query_row(const double *Q, const double *K, const double *V,
-                          const double *dOi, long i, long m, long dk, long dv,
+                          const double *dOi, long i, long m, long mb, long dk, long dv,
                           int causal, double scale, double *row, double *oi,
                           double *lse_i, double *D_i, double *dqi) {
-    score_row(Q + i * dk, K, m, dk, scale, visible_keys(i, m, causal), row);
+    score_row(Q + i * dk, K, m, dk, scale, visible_padded(i, m, causal, mb), row);
     const double l = softmax_row(row, m);
     weighted_sum(row, V, m, dv, oi);
     double Di = 0.0;
@@ -212,12 +237,12 @@ static void bwd_query_row(const double *Q, const double *K, const double *V,
  */
 static void bwd_key_row(const double *Q, const double *kj, const double *vj,
                         const double *dO, const double *lse, const double *D,
-                        long j, long n, long m, long dk, long dv, int causal,
+                        long j, long n, long m, long mb, long dk, long dv, int causal,
                         double scale, double *dkj, double *dvj) {
     if (dkj) for (long c = 0; c < dk; ++c) dkj[c] = 0.0;
     if (dvj) for (long c = 0; c < dv; ++c) dvj[c] = 0.0;
     for (long i = 0; i < n; ++i) {
-        if (j >= visible_keys(i, m, causal)) continue; /* masked: P_ij = 0 */
+        if (j >= visible_padded(i, m, causal, mb)) continue; /* masked: P_ij = 0 */
         const double *qi = Q + i * dk;
         const double *dOi = dO + i * dv;
         double dot = 0.0;
@@ -249,7 +274,7 @@ int oracle_attn_bwd(const double *q, const double *k, const double *v,
                     const double *dO, double *dq, double *dk_out,
                     double *dv_out, double *o_out, double *lse_out, long B,
                     long h, long n, long m, long dk, long dv, int causal,
-                    double scale) {
+                    double scale, const long *kv_len) {
     if (check_dims(B, h, n, m, dk, dv) != ORACLE_OK) return ORACLE_ERR_ARG;
     const long heads = B * h;
     double *lse = (double *)malloc(sizeof(double) * (size_t)(heads * n + 1));
@@ -273,7 +298,8 @@ int oracle_attn_bwd(const double *q, const double *k, const double *v,
             for (long i = 0; i < n; ++i) {
                 if (!row || !oi) continue;
                 bwd_query_row(q + bh * n * dk, k + bh * m * dk, v + bh * m * dv,
-                              dO + (bh * n + i) * dv, i, m, dk, dv, causal, scale,
+                              dO + (bh * n + i) * dv, i, m, head_keys(kv_len, bh, h, m), dk, dv,
+                              causal, scale,
                               row, oi, &lse[bh * n + i], &D[bh * n + i],
                               dq ? dq + (bh * n + i) * dk : NULL);
                 if (o_out) memcpy(o_out + (bh * n + i) * dv, oi, sizeof(double) * (size_t)dv);
@@ -286,7 +312,8 @@ int oracle_attn_bwd(const double *q, const double *k, const double *v,
             for (long bh = 0; bh < heads; ++bh) {
                 for (long j = 0; j < m; ++j) {
                     bwd_key_row(q + bh * n * dk, k + (bh * m + j) * dk, v + (bh * m + j) * dv,
-                                dO + bh * n * dv, lse + bh * n, D + bh * n, j, n, m, dk, dv,
+                                dO + bh * n * dv, lse + bh * n, D + bh * n, j, n, m,
+                                head_keys(kv_len, bh, h, m), dk, dv,
                                 causal, scale, dk_out ? dk_out + (bh * m + j) * dk : NULL,
                                 dv_out ? dv_out + (bh * m + j) * dv : NULL);
                 }
@@ -311,13 +338,14 @@ int oracle_attn_bwd_rows(const double *q, const double *k, const double *v,
                          const double *dO, long n, long m, long dk, long dv,
                          int causal, double scale, const long *qrows, long nq,
                          double *dq_out, const long *krows, long nk,
-                         double *dk_out, double *dv_out) {
+                         double *dk_out, double *dv_out, long kv_len) {
     if (check_dims(1, 1, n, m, dk, dv) != ORACLE_OK || nq < 0 || nk < 0) return ORACLE_ERR_ARG;
     for (long r = 0; r < nq; ++r)
         if (qrows[r] < 0 || qrows[r] >= n) return ORACLE_ERR_ARG;
     for (long r = 0; r < nk; ++r)
         if (krows[r] < 0 || krows[r] >= m) return ORACLE_ERR_ARG;
     const long nall = nk > 0 ? n : 0;
+    const long mb = kv_len < 0 ? m : (kv_len > m ? m : kv_len); /* < 0: no key padding */
     double *lse = (double *)malloc(sizeof(double) * (size_t)(nall + 1));
     double *D = (double *)malloc(sizeof(double) * (size_t)(nall + 1));
     if (!lse || !D) {
@@ -339,19 +367,19 @@ int oracle_attn_bwd_rows(const double *q, const double *k, const double *v,
             if (!row || !oi) continue;
             double l, Di;
             const long i = qrows[r];
-            bwd_query_row(q, k, v, dO + i * dv, i, m, dk, dv, causal, scale, row, oi, &l, &Di,
+            bwd_query_row(q, k, v, dO + i * dv, i, m, mb, dk, dv, causal, scale, row, oi, &l, &Di,
                           dq_out + r * dk);
         }
 #pragma omp for schedule(dynamic, 16)
         for (long i = 0; i < nall; ++i) {
             if (!row || !oi) continue;
-            bwd_query_row(q, k, v, dO + i * dv, i, m, dk, dv, causal, scale, row, oi, &lse[i],
+            bwd_query_row(q, k, v, dO + i * dv, i, m, mb, dk, dv, causal, scale, row, oi, &lse[i],
                           &D[i], NULL);
         }
 #pragma omp for schedule(dynamic, 1)
         for (long r = 0; r < nk; ++r) {
             const long j = krows[r];
-            bwd_key_row(q, k + j * dk, v + j * dv, dO, lse, D, j, n, m, dk, dv, causal, scale,
+            bwd_key_row(q, k + j * dk, v + j * dv, dO, lse, D, j, n, m, mb, dk, dv, causal, scale,
                         dk_out + r * dk, dv_out + r * dv);
         }
         free(row);

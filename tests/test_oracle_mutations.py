@@ -26,8 +26,12 @@ MUTATIONS = {
                    "for (long c = 0; c < dv; ++c) dvj[c] += P * dOi[c] * (1.0 + 1e-3 * c);"),
     "dQ_transposed_operand": ("for (long c = 0; c < dk; ++c) dqi[c] += dS * kj[c];",
                               "for (long c = 0; c < dk; ++c) dqi[c] += dS * kj[dk - 1 - c];"),
-    "causal_mask_in_bwd_off_by_one": ("if (j >= visible_keys(i, m, causal)) continue;",
-                                      "if (j > visible_keys(i, m, causal)) continue;"),
+    "causal_mask_in_bwd_off_by_one": ("if (j >= visible_padded(i, m, causal, mb)) continue;",
+                                      "if (j > visible_padded(i, m, causal, mb)) continue;"),
+    "key_length_per_head": ("const long mb = kv_len[bh / h];", "const long mb = kv_len[bh % h];"),
+    "key_padding_off_by_one": ("return v < mb ? v : mb;", "return v < mb + 1 ? v : mb + 1;"),
+    "empty_row_not_zero": ("for (long j = 0; j < m; ++j) s[j] = 0.0;\n        return -INFINITY;",
+                           "for (long j = 0; j < m; ++j) s[j] = 1.0 / m;\n        return -INFINITY;"),
     "value_row_offset": ("const double *vj = V + j * dv;\n        for (long c = 0; c < dv; ++c) oi[c] += P[j] * vj[c];",
                          "const double *vj = V + (j > 0 ? j - 1 : 0) * dv;\n        for (long c = 0; c < dv; ++c) oi[c] += P[j] * vj[c];"),
 }
@@ -46,6 +50,9 @@ PIN_TESTS = [
     (pins.test_backward_sum_invariants, {"causal": True}),
     (pins.test_against_torch_cpu_fp64_library,
      {"causal": True, "n": 9, "m": 9, "dk": 16, "dv": 16}),
+    (pins.test_key_padding_equals_truncation, {"causal": True}),
+    (pins.test_key_padding_against_torch_masked_library, {}),
+    (pins.test_key_padding_empty_sequence_is_the_empty_sum, {}),
 ]
 
 
@@ -60,7 +67,7 @@ def test_planted_mistake_is_caught(name, tmp_path, monkeypatch):
     subprocess.run(["gcc", *oracle.CFLAGS, "-o", str(lib_path), str(mutated), "-lm"], check=True)
     real = oracle._load()
     lib = ctypes.CDLL(str(lib_path))
-    for fn in ("oracle_attn_weights", "oracle_attn_fwd", "oracle_attn_bwd"):
+    for fn in ("oracle_attn_weights", "oracle_attn_fwd", "oracle_attn_bwd", "oracle_attn_bwd_rows"):
         getattr(lib, fn).argtypes = getattr(real, fn).argtypes
         getattr(lib, fn).restype = ctypes.c_int
     lib.oracle_num_threads.restype = ctypes.c_int

@@ -298,3 +298,92 @@ def test_sampled_backward_rows_equal_full_backward(causal):
     np.testing.assert_array_equal(sq, dQ[qr])
     np.testing.assert_array_equal(sk, dK[kr])
     np.testing.assert_array_equal(sv, dV[kr])
+
+
+# ---------------------------------------------------------------- key padding
+#
+# Variable-length batches ("Attention Is All You Need" §5.1 batches sentences
+# of similar length; the <pad> positions of Figure 3): sequence b has kv_len[b]
+# real keys, the first ones, and the padding keys are masked.
+
+def _padding_case(seed=5, B=3, h=2, n=7, m=9, dk=5, dv=4):
+    g = torch.Generator().manual_seed(seed)
+    q = torch.randn(B, h, n, dk, dtype=torch.float64, generator=g).numpy()
+    k = torch.randn(B, h, m, dk, dtype=torch.float64, generator=g).numpy()
+    v = torch.randn(B, h, m, dv, dtype=torch.float64, generator=g).numpy()
+    dO = torch.randn(B, h, n, dv, dtype=torch.float64, generator=g).numpy()
+    return q, k, v, dO
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_key_padding_equals_truncation(causal):
+    """Padding keys j >= L of a sequence act as if the sequence had only L keys."""
+    q, k, v, dO = _padding_case()
+    lens = [9, 4, 1]
+    scale = 0.4
+    O, lse = oracle.fwd(q, k, v, causal, scale, kv_len=lens)
+    dQ, dK, dV, _, _ = oracle.bwd(q, k, v, dO, causal, scale, kv_len=lens)
+    for b, L in enumerate(lens):
+        Ob, lb = oracle.fwd(q[b:b + 1], k[b:b + 1, :, :L], v[b:b + 1, :, :L], causal, scale)
+        np.testing.assert_allclose(O[b], Ob[0], rtol=1e-13, atol=1e-14)
+        np.testing.assert_allclose(lse[b], lb[0], rtol=1e-13, atol=1e-14)
+        gq, gk, gv, _, _ = oracle.bwd(q[b:b + 1], k[b:b + 1, :, :L], v[b:b + 1, :, :L], dO[b:b + 1],
+                                      causal, scale)
+        np.testing.assert_allclose(dQ[b], gq[0], rtol=1e-12, atol=1e-14)
+        np.testing.assert_allclose(dK[b, :, :L], gk[0], rtol=1e-12, atol=1e-14)
+        np.testing.assert_allclose(dV[b, :, :L], gv[0], rtol=1e-12, atol=1e-14)
+        assert (dK[b, :, L:] == 0).all() and (dV[b, :, L:] == 0).all()
+
+
+def test_key_padding_against_torch_masked_library():
+    """torch CPU fp64 scaled_dot_product_attention with a boolean key mask."""
+    F = torch.nn.functional
+    q, k, v, dO = (torch.from_numpy(a).requires_grad_(i < 3) for i, a in enumerate(_padding_case(seed=9)))
+    lens = [2, 9, 6]
+    B, h, n, m = q.shape[0], q.shape[1], q.shape[2], k.shape[2]
+    keep = torch.arange(m)[None, :] < torch.tensor(lens)[:, None]       # [B, m]
+    mask = keep[:, None, None, :].expand(B, 1, n, m)
+    O_t = F.scaled_dot_product_attention(q, k, v, attn_mask=mask, scale=0.3)
+    O_t.backward(dO)
+    O, _ = oracle.fwd(q.detach(), k.detach(), v.detach(), False, 0.3, kv_len=lens)
+    dQ, dK, dV, _, _ = oracle.bwd(q.detach(), k.detach(), v.detach(), dO, False, 0.3, kv_len=lens)
+    np.testing.assert_allclose(O, O_t.detach().numpy(), rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(dQ, q.grad.numpy(), rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(dK, k.grad.numpy(), rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(dV, v.grad.numpy(), rtol=1e-10, atol=1e-12)
+
+
+def test_key_padding_values_do_not_matter():
+    """What sits in the padding keys and values cannot change any result."""
+    q, k, v, dO = _padding_case(seed=7)
+    lens = [5, 9, 3]
+    k2, v2 = k.copy(), v.copy()
+    for b, L in enumerate(lens):
+        k2[b, :, L:] = 1e3
+        v2[b, :, L:] = -7.0
+    a = oracle.fwd(q, k, v, True, 0.5, kv_len=lens)
+    b_ = oracle.fwd(q, k2, v2, True, 0.5, kv_len=lens)
+    np.testing.assert_array_equal(a[0], b_[0])
+    np.testing.assert_array_equal(a[1], b_[1])
+    ga = oracle.bwd(q, k, v, dO, True, 0.5, kv_len=lens)
+    gb = oracle.bwd(q, k2, v2, dO, True, 0.5, kv_len=lens)
+    np.testing.assert_array_equal(ga[0], gb[0])
+
+
+def test_key_padding_empty_sequence_is_the_empty_sum():
+    """A sequence without real keys: O = 0, lse = -inf, zero gradients (the reading for L = 0)."""
+    q, k, v, dO = _padding_case(seed=3)
+    lens = [0, 9, 0]
+    O, lse = oracle.fwd(q, k, v, False, 0.5, kv_len=lens)
+    dQ, dK, dV, _, _ = oracle.bwd(q, k, v, dO, False, 0.5, kv_len=lens)
+    for b in (0, 2):
+        assert (O[b] == 0).all() and np.isneginf(lse[b]).all()
+        assert (dQ[b] == 0).all() and (dK[b] == 0).all() and (dV[b] == 0).all()
+    assert np.isfinite(O[1]).all() and np.isfinite(lse[1]).all()
+    # sampled rows agree with the full backward under padding
+    sq, sk, sv = oracle.bwd_rows(q[1, 0], k[1, 0], v[1, 0], dO[1, 0], True, 0.5, [0, 6], [0, 3, 8],
+                                 kv_len=4)
+    fq, fk, fv, _, _ = oracle.bwd(q[1:2, :1], k[1:2, :1], v[1:2, :1], dO[1:2, :1], True, 0.5, kv_len=[4])
+    np.testing.assert_array_equal(sq, fq[0, 0][[0, 6]])
+    np.testing.assert_array_equal(sk, fk[0, 0][[0, 3, 8]])
+    np.testing.assert_array_equal(sv, fv[0, 0][[0, 3, 8]])
