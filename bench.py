@@ -31,7 +31,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
-from seeded_inputs import WORKLOADS, Workload  # noqa: E402
+from seeded_inputs import WORKLOADS, Workload, kv_lengths  # noqa: E402
 
 METRIC = "attention TFLOPS (bf16, fwd and bwd) and % of GB300 dense BF16 tensor peak"
 UNIT = "TFLOP/s"
@@ -274,12 +274,14 @@ def run_gpu(args, w: Workload, world, rank, local):
     ws_bytes = A.attn_bwd_workspace_bytes(w.B, w.h, w.n, w.m, w.d_k, w.d_v, w.causal)
     ws = torch.empty(max(ws_bytes, 16) // 4 + 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
+    lens = kv_lengths(w)  # key padding of a variable-length workload (None: none)
+    kvl = None if lens is None else torch.tensor(lens, dtype=torch.int32, device=dev)
 
     def step(i):
         q, k, v, do = sets[i % n_sets]
-        A.attn_fwd(q, k, v, causal=w.causal, scale=scale, out=o, lse=lse)
+        A.attn_fwd(q, k, v, causal=w.causal, scale=scale, out=o, lse=lse, kv_len=kvl)
         A.attn_bwd(q, k, v, o, lse, do, causal=w.causal, scale=scale, dq=dq, dk=dk, dv=dv,
-                   workspace=ws)
+                   workspace=ws, kv_len=kvl)
 
     # settle clocks, then the counted warm-up
     t_soak = time.time()
@@ -337,9 +339,9 @@ def run_gpu(args, w: Workload, world, rank, local):
     def e2e_step():
         for dst, src in zip(d_in, (hq, hk, hv, hdo)):
             dst.copy_(src, non_blocking=True)
-        A.attn_fwd(d_in[0], d_in[1], d_in[2], causal=w.causal, scale=scale, out=o, lse=lse)
+        A.attn_fwd(d_in[0], d_in[1], d_in[2], causal=w.causal, scale=scale, out=o, lse=lse, kv_len=kvl)
         A.attn_bwd(d_in[0], d_in[1], d_in[2], o, lse, d_in[3], causal=w.causal, scale=scale,
-                   dq=dq, dk=dk, dv=dv, workspace=ws)
+                   dq=dq, dk=dk, dv=dv, workspace=ws, kv_len=kvl)
         for dst, src in zip(outs_h, (o, dq, dk, dv)):
             dst.copy_(src, non_blocking=True)
 
@@ -403,21 +405,24 @@ def run_sweep(args, local):
     dev = torch.device("cuda", local)
     peaks, _ = load_peaks()
     out = {}
-    names = ["encoder", "encoder_sat", "decoder", "cross", "cross_h4_d128", "cross_h16_d32"]
+    names = ["encoder", "encoder_sat", "encoder_kpad", "decoder", "cross", "cross_h4_d128", "cross_h16_d32"]
     names += [f"long_n{n}_d{d}_{c}" for n in (1024, 4096, 16384) for d in (64, 128) for c in ("nc", "c")]
     for name in names:
         w = WORKLOADS[name]
         q, k, v, do = make_inputs(w, 99, dev)
-        o, lse = A.attn_fwd(q, k, v, causal=w.causal, scale=w.default_scale)
-        dq, dk, dv = A.attn_bwd(q, k, v, o, lse, do, causal=w.causal, scale=w.default_scale)
+        lens = kv_lengths(w)
+        kvl = None if lens is None else torch.tensor(lens, dtype=torch.int32, device=dev)
+        o, lse = A.attn_fwd(q, k, v, causal=w.causal, scale=w.default_scale, kv_len=kvl)
+        dq, dk, dv = A.attn_bwd(q, k, v, o, lse, do, causal=w.causal, scale=w.default_scale, kv_len=kvl)
         torch.cuda.synchronize()
         iters = max(3, min(50, int(2e12 / max(step_flops(w), 1))))
         A.attn_profile_enable(True)
         for kind in A.KERNEL_KINDS:
             A.attn_profile_read(kind)
         for _ in range(iters):
-            A.attn_fwd(q, k, v, causal=w.causal, scale=w.default_scale, out=o, lse=lse)
-            A.attn_bwd(q, k, v, o, lse, do, causal=w.causal, scale=w.default_scale, dq=dq, dk=dk, dv=dv)
+            A.attn_fwd(q, k, v, causal=w.causal, scale=w.default_scale, out=o, lse=lse, kv_len=kvl)
+            A.attn_bwd(q, k, v, o, lse, do, causal=w.causal, scale=w.default_scale, dq=dq, dk=dk, dv=dv,
+                       kv_len=kvl)
         torch.cuda.synchronize()
         A.attn_profile_enable(False)
         prof = {kind: A.attn_profile_read(kind) for kind in A.KERNEL_KINDS}
@@ -429,7 +434,7 @@ def run_sweep(args, local):
                      "fwd_frac_peak": round(ftf / peaks["bf16_tflops"], 3),
                      "bwd_us": round(b_ms * 1e3, 1), "bwd_tflops": round(btf, 1),
                      "bwd_frac_peak": round(btf / peaks["bf16_tflops"], 3), "iters": iters}
-        del q, k, v, do, o, lse, dq, dk, dv
+        del q, k, v, do, o, lse, dq, dk, dv, kvl
         torch.cuda.empty_cache()
     if A.attn_get_device_status() != A.ATTN_OK:
         raise RuntimeError("device watchdog fired in the sweep")

@@ -123,6 +123,29 @@ int attn_bwd_noalloc(const void* q, const void* k, const void* v, const void* o,
                      int d_k, int d_v, int causal, float scale, attn_stream_t stream);
 
 /*
+ * Key-padding variants (variable-length batches). The pages batch sentences
+ * of similar length (§5.1) and pad them (the <pad> positions of
+ * Figure 3); here sequence b of the batch has kv_len[b] real keys, the first
+ * ones, and the keys past them are masked like illegal connections: weight
+ * exactly 0, zero dK and dV rows. Query rows are all computed (a padded
+ * query row attends to the real keys; a caller drops it). With causal = 1
+ * both masks apply (key j visible to query i iff j <= i and j < kv_len[b]).
+ *   kv_len [B]   int32, device memory, 4-byte aligned, read by the kernels;
+ *                values are clamped to [0, m]. NULL = no padding (then the
+ *                calls equal attn_fwd / attn_bwd).
+ * A sequence with kv_len[b] = 0 has no visible key: its rows get O = 0,
+ * lse = -inf (the empty sum) and zero gradients. Everything else (arguments,
+ * layout, ownership, workspace, errors) is as in attn_fwd / attn_bwd.
+ */
+int attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
+                    const int* kv_len, int B, int h, int n, int m, int d_k, int d_v, int causal,
+                    float scale, attn_stream_t stream);
+int attn_bwd_varlen(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                    const void* dO, void* dq, void* dk, void* dv, const int* kv_len, int B, int h,
+                    int n, int m, int d_k, int d_v, int causal, float scale, void* workspace,
+                    size_t workspace_bytes, attn_stream_t stream);
+
+/*
  * Synchronises `stream`, then reports and clears the device-side error word of
  * the current device: ATTN_OK, or ATTN_ERR_TIMEOUT if any kernel's watchdog
  * fired since the last call. ATTN_ERR_CUDA if the synchronisation failed.

@@ -28,6 +28,7 @@ __all__ = [
     "normal_bf16",
     "workload_inputs",
     "ragged_workloads",
+    "kv_lengths",
 ]
 
 
@@ -45,6 +46,9 @@ class Workload:
     causal: bool
     cfg: int  # seed family: Q=1000+cfg, K=2000+cfg, V=3000+cfg, dO=4000+cfg
     q_mult: float = 1.0  # power-of-two multiplier applied before the bf16 cast
+    # key padding: 0 = none; else sequence b has kv_len[b] real keys, drawn
+    # uniformly from [kv_len_min, m] (seed 5000+cfg), see kv_lengths()
+    kv_len_min: int = 0
 
     @property
     def heads(self) -> int:
@@ -56,7 +60,16 @@ class Workload:
         return 1.0 / math.sqrt(self.d_k)
 
     def fwd_flops(self) -> float:
-        """Algorithmic forward FLOPs: 4*B*h*n*m*d_k, halved when causal."""
+        """Algorithmic forward FLOPs: 4*B*h*n*m*d_k, halved when causal.
+
+        With key padding (non-causal only) m is replaced by each sequence's
+        real key count: 4*h*n*d_k*sum_b kv_len[b].
+        """
+        lens = kv_lengths(self)
+        if lens is not None:
+            if self.causal:
+                raise ValueError("padded workloads are non-causal")
+            return 4.0 * self.h * self.n * self.d_k * float(sum(lens))
         f = 4.0 * self.B * self.h * self.n * self.m * self.d_k
         return f / 2 if self.causal else f
 
@@ -65,8 +78,8 @@ class Workload:
         return 2.5 * self.fwd_flops()
 
 
-def _wl(name, B, h, n, m, d, causal, cfg, q_mult=1.0) -> Workload:
-    return Workload(name, B, h, n, m, d, d, causal, cfg, q_mult)
+def _wl(name, B, h, n, m, d, causal, cfg, q_mult=1.0, kv_len_min=0) -> Workload:
+    return Workload(name, B, h, n, m, d, d, causal, cfg, q_mult, kv_len_min)
 
 
 def _build_table() -> Dict[str, Workload]:
@@ -79,6 +92,9 @@ def _build_table() -> Dict[str, Workload]:
         _wl("cross", 48, 16, 256, 320, 64, False, 4),
         _wl("cross_h4_d128", 48, 4, 256, 320, 128, False, 4),
         _wl("cross_h16_d32", 48, 16, 256, 320, 32, False, 4),
+        # variable-length batch (§5.1 batches sentences of similar length;
+        # <pad> keys of Figure 3): real key counts uniform in [128, 256]
+        _wl("encoder_kpad", 96, 8, 256, 256, 64, False, 6, kv_len_min=128),
     ]
     for n in (1024, 4096, 16384):
         for d in (64, 128):
@@ -138,3 +154,12 @@ def ragged_workloads() -> Iterator[Workload]:
     ]
     for i, (B, h, n, m, d, c) in enumerate(cases):
         yield _wl(f"ragged{i}_B{B}h{h}n{n}m{m}d{d}{'c' if c else ''}", B, h, n, m, d, c, 50 + i)
+
+
+def kv_lengths(w: Workload) -> Optional[List[int]]:
+    """Real keys per sequence of a padded workload (None: no key padding)."""
+    if w.kv_len_min <= 0:
+        return None
+    g = torch.Generator(device="cpu")
+    g.manual_seed(5000 + w.cfg)
+    return torch.randint(w.kv_len_min, w.m + 1, (w.B,), generator=g).tolist()

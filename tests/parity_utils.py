@@ -62,11 +62,12 @@ def ulp_ratio(gpu, ref) -> float:
     return float((np.abs(g - r) / bf16_ulp(r)).max())
 
 
-def d_term_bounds(q, k, v, dO, causal, scale, qrows=None, krows=None):
+def d_term_bounds(q, k, v, dO, causal, scale, qrows=None, krows=None, kv_len=None):
     """Bounds on |dQ| and |dK| errors caused by forming D_i from the bf16 O (see module doc).
 
     Full heads ([B,h,S,d] tensors) when qrows/krows are None; otherwise ONE head
-    ([S,d] tensors) and the bounds of the listed query / key rows.
+    ([S,d] tensors) and the bounds of the listed query / key rows; kv_len is
+    then that head's real key count (key padding).
     """
     import oracle
     u = 2.0 ** -8
@@ -81,13 +82,15 @@ def d_term_bounds(q, k, v, dO, causal, scale, qrows=None, krows=None):
         return bq, abs(scale) * PtdDq
     n = qa.shape[0]
     all_rows = list(range(n))
-    O, _ = oracle.fwd(qa, ka, va, causal, scale, rows=all_rows)
+    lens = None if kv_len is None else [kv_len]
+    O, _ = oracle.fwd(qa, ka, va, causal, scale, rows=all_rows, kv_len=lens)
     dD = u * (np.abs(da) * np.abs(O)).sum(axis=-1)
-    PK, _ = oracle.fwd(qa, ka, np.abs(ka), causal, scale, rows=list(qrows))
+    PK, _ = oracle.fwd(qa, ka, np.abs(ka), causal, scale, rows=list(qrows), kv_len=lens)
     bq = abs(scale) * dD[list(qrows), None] * PK[list(qrows)]
     bk = None
     if krows is not None and len(krows):
-        _, _, PtdDq = oracle.bwd_rows(qa, ka, ka, dD[:, None] * np.abs(qa), causal, scale, [], krows)
+        _, _, PtdDq = oracle.bwd_rows(qa, ka, ka, dD[:, None] * np.abs(qa), causal, scale, [], krows,
+                                      kv_len=kv_len)
         bk = abs(scale) * PtdDq
     return bq, bk
 

@@ -117,3 +117,19 @@ def test_binding_refuses_cpu_tensors(lib):
     q = torch.zeros(1, 1, 4, 64, dtype=torch.bfloat16)
     with pytest.raises(ValueError, match="CUDA"):
         A.attn_fwd(q, q, q)
+
+
+def test_varlen_argument_checks(lib):
+    """The key-padding entry points refuse a misaligned length array before any launch."""
+    vp = ctypes.c_void_p
+    f = ctypes.cast(vp(FAKE), ctypes.POINTER(ctypes.c_float))
+    st = lib.attn_fwd_varlen(vp(FAKE), vp(FAKE), vp(FAKE), vp(FAKE), f, vp(FAKE + 2), 1, 1, 8, 8, 64, 64,
+                             0, 0.125, None)
+    assert st == A.ATTN_ERR_INVALID_ARG
+    st = lib.attn_bwd_varlen(vp(FAKE), vp(FAKE), vp(FAKE), vp(FAKE), f, vp(FAKE), vp(FAKE), vp(FAKE),
+                             vp(FAKE), vp(FAKE + 2), 1, 1, 8, 8, 64, 64, 0, 0.125, vp(FAKE), 1 << 30, None)
+    assert st == A.ATTN_ERR_INVALID_ARG
+    # the same validation as the unpadded calls applies
+    st = lib.attn_fwd_varlen(vp(FAKE), vp(FAKE), vp(FAKE), vp(FAKE), f, vp(FAKE), 1, 1, 8, 8, 48, 48, 0,
+                             0.125, None)
+    assert st == A.ATTN_ERR_UNSUPPORTED

@@ -28,6 +28,8 @@ __all__ = [
     "attn_set_watchdog_ns", "attn_debug_inject", "attn_profile_enable", "attn_profile_read",
     "attn_debug_exp2", "attn_bwd_noalloc", "EXPORTED_SYMBOLS", "KERNEL_KINDS",
 ]
+# attn_fwd / attn_bwd take an optional ``kv_len`` (int32 CUDA tensor [B]: real
+# keys per sequence) and then call attn_fwd_varlen / attn_bwd_varlen.
 
 ATTN_OK = 0
 ATTN_ERR_INVALID_ARG = 1
@@ -39,7 +41,8 @@ ATTN_ERR_TIMEOUT = 4
 EXPORTED_SYMBOLS = (
     "attn_fwd", "attn_bwd", "attn_bwd_workspace_bytes", "attn_get_device_status",
     "attn_status_string", "attn_set_watchdog_ns", "attn_debug_inject", "attn_profile_enable",
-    "attn_profile_read", "attn_debug_exp2", "attn_bwd_noalloc",
+    "attn_profile_read", "attn_debug_exp2", "attn_bwd_noalloc", "attn_fwd_varlen",
+    "attn_bwd_varlen",
 )
 
 # Kernel kinds of attn_profile_read.
@@ -79,6 +82,11 @@ def load_library():
         lib.attn_bwd.argtypes = [vp, vp, vp, vp, fp, vp, vp, vp, vp, I, I, I, I, I, I, I, F,
                                  vp, SZ, vp]
         lib.attn_bwd.restype = I
+        lib.attn_fwd_varlen.argtypes = [vp, vp, vp, vp, fp, vp, I, I, I, I, I, I, I, F, vp]
+        lib.attn_fwd_varlen.restype = I
+        lib.attn_bwd_varlen.argtypes = [vp, vp, vp, vp, fp, vp, vp, vp, vp, vp, I, I, I, I, I, I, I, F,
+                                        vp, SZ, vp]
+        lib.attn_bwd_varlen.restype = I
         lib.attn_bwd_workspace_bytes.argtypes = [I, I, I, I, I, I, I]
         lib.attn_bwd_workspace_bytes.restype = SZ
         lib.attn_get_device_status.argtypes = [vp]
@@ -134,9 +142,23 @@ def _vptr(t):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
 
 
+def _check_lengths(kv_len, B, device):
+    import torch
+    if kv_len is None:
+        return None
+    _check_tensor("kv_len", kv_len, (B,), torch.int32)
+    if kv_len.device != device:
+        raise ValueError("kv_len must be on the device of q")
+    return _vptr(kv_len)
+
+
 def attn_fwd(q, k, v, causal: bool = False, scale: Optional[float] = None, out=None, lse=None,
-             need_lse: bool = True, stream=None) -> Tuple["torch.Tensor", Optional["torch.Tensor"]]:
-    """O, lse = attention(q, k, v) on the GPU. q [B,h,n,d], k/v [B,h,m,d], bf16."""
+             need_lse: bool = True, stream=None, kv_len=None) -> Tuple["torch.Tensor", Optional["torch.Tensor"]]:
+    """O, lse = attention(q, k, v) on the GPU. q [B,h,n,d], k/v [B,h,m,d], bf16.
+
+    kv_len (optional int32 CUDA tensor [B]): real keys per sequence; the keys
+    past them are padding and masked.
+    """
     import torch
     lib = load_library()
     if q.dim() != 4 or k.dim() != 4 or v.dim() != 4:
@@ -155,8 +177,13 @@ def attn_fwd(q, k, v, causal: bool = False, scale: Optional[float] = None, out=N
         lse = torch.empty((B, h, n), dtype=torch.float32, device=q.device)
     if lse is not None:
         _check_tensor("lse", lse, (B, h, n), torch.float32)
-    st = lib.attn_fwd(_vptr(q), _vptr(k), _vptr(v), _vptr(out), _fptr(lse), B, h, n, m, dk, dv,
-                      int(bool(causal)), float(scale), _stream_handle(stream))
+    lens = _check_lengths(kv_len, B, q.device)
+    if lens is None:
+        st = lib.attn_fwd(_vptr(q), _vptr(k), _vptr(v), _vptr(out), _fptr(lse), B, h, n, m, dk, dv,
+                          int(bool(causal)), float(scale), _stream_handle(stream))
+    else:
+        st = lib.attn_fwd_varlen(_vptr(q), _vptr(k), _vptr(v), _vptr(out), _fptr(lse), lens, B, h, n,
+                                 m, dk, dv, int(bool(causal)), float(scale), _stream_handle(stream))
     if st != ATTN_OK:
         raise AttnError(st, "attn_fwd")
     return out, lse
@@ -167,7 +194,7 @@ def attn_bwd_workspace_bytes(B, h, n, m, d_k, d_v, causal=False) -> int:
 
 
 def attn_bwd(q, k, v, o, lse, dO, causal: bool = False, scale: Optional[float] = None,
-             dq=None, dk=None, dv=None, workspace=None, stream=None):
+             dq=None, dk=None, dv=None, workspace=None, stream=None, kv_len=None):
     """dQ, dK, dV of sum(dO * O) for O = attention(q, k, v), from attn_fwd's O and lse."""
     import torch
     lib = load_library()
@@ -193,9 +220,16 @@ def attn_bwd(q, k, v, o, lse, dO, causal: bool = False, scale: Optional[float] =
         _check_tensor("workspace", workspace)
     ws_ptr = _vptr(workspace) if workspace is not None else None
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
-    st = lib.attn_bwd(_vptr(q), _vptr(k), _vptr(v), _vptr(o), _fptr(lse), _vptr(dO), _vptr(dq),
-                      _vptr(dk), _vptr(dv), B, h, n, m, d_k, d_v, int(bool(causal)), float(scale),
-                      ws_ptr, ws_bytes, _stream_handle(stream))
+    lens = _check_lengths(kv_len, B, q.device)
+    if lens is None:
+        st = lib.attn_bwd(_vptr(q), _vptr(k), _vptr(v), _vptr(o), _fptr(lse), _vptr(dO), _vptr(dq),
+                          _vptr(dk), _vptr(dv), B, h, n, m, d_k, d_v, int(bool(causal)), float(scale),
+                          ws_ptr, ws_bytes, _stream_handle(stream))
+    else:
+        st = lib.attn_bwd_varlen(_vptr(q), _vptr(k), _vptr(v), _vptr(o), _fptr(lse), _vptr(dO),
+                                 _vptr(dq), _vptr(dk), _vptr(dv), lens, B, h, n, m, d_k, d_v,
+                                 int(bool(causal)), float(scale), ws_ptr, ws_bytes,
+                                 _stream_handle(stream))
     if st != ATTN_OK:
         raise AttnError(st, "attn_bwd")
     return dq, dk, dv

@@ -234,8 +234,11 @@ int attn_debug_inject(int mode) {
   return ATTN_OK;
 }
 
-int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int h, int n,
-             int m, int d_k, int d_v, int causal, float scale, attn_stream_t stream) {
+// attn_fwd / attn_fwd_varlen: kv_len (device, B ints, or nullptr) are the real
+// keys of each sequence; the kernels clamp them to [0, m].
+static int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, const int* kv_len,
+                    int B, int h, int n, int m, int d_k, int d_v, int causal, float scale,
+                    attn_stream_t stream) {
   bool empty = false;
   int st = check_common(B, h, n, m, d_k, d_v, scale, &empty);
   if (st != ATTN_OK) return st;
@@ -261,6 +264,8 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
   p.c = static_cast<float>(std::fabs(static_cast<double>(scale)) * kLog2e);
   p.num_qblocks = 0;  // set by the launcher for its query-tile configuration
   p.inject = g_inject.exchange(0);
+  p.kv_len = kv_len;
+  p.h = h;
   p.wd.status = status;
   p.wd.budget_ns = g_watchdog_ns.load();
   cudaError_t e = attn::launch_fwd(d_k, tq, tk, tv, to, p, static_cast<int>(BH),
@@ -281,8 +286,9 @@ size_t attn_bwd_workspace_bytes(int B, int h, int n, int m, int d_k, int d_v, in
 
 // Short query sequences: the whole-head kernel (no scratch, one launch).
 static int bwd_head_path(const void* q, const void* k, const void* v, const void* o, const float* lse,
-                         const void* dO, void* dq, void* dk, void* dv, long long BH, int n, int m,
-                         int d, int causal, float scale, uint32_t* status, cudaStream_t stream) {
+                         const void* dO, void* dq, void* dk, void* dv, const int* kv_len, long long BH,
+                         int h, int n, int m, int d, int causal, float scale, uint32_t* status,
+                         cudaStream_t stream) {
   CUtensorMap tq, tk, tv, tdo, tdq, tdk, tdv;
   if (!make_tile_map(&tq, q, BH, n, d) || !make_tile_map(&tk, k, BH, m, d) ||
       !make_tile_map(&tv, v, BH, m, d) || !make_tile_map(&tdo, dO, BH, n, d) ||
@@ -303,16 +309,18 @@ static int bwd_head_path(const void* q, const void* k, const void* v, const void
   p.neg = scale < 0.f ? 1 : 0;
   p.c = static_cast<float>(std::fabs(static_cast<double>(scale)) * kLog2e);
   p.scale = scale;
+  p.kv_len = kv_len;
+  p.h = h;
   p.wd.status = status;
   p.wd.budget_ns = g_watchdog_ns.load();
   const cudaError_t e = attn::launch_bwd_head(d, tq, tk, tv, tdo, tdq, tdk, tdv, p, stream);
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
-int attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
-             const void* dO, void* dq, void* dk, void* dv, int B, int h, int n, int m, int d_k,
-             int d_v, int causal, float scale, void* workspace, size_t workspace_bytes,
-             attn_stream_t stream) {
+static int bwd_impl(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                    const void* dO, void* dq, void* dk, void* dv, const int* kv_len, int B, int h,
+                    int n, int m, int d_k, int d_v, int causal, float scale, void* workspace,
+                    size_t workspace_bytes, attn_stream_t stream) {
   bool empty = false;
   int st = check_common(B, h, n, m, d_k, d_v, scale, &empty);
   if (st != ATTN_OK) return st;
@@ -335,8 +343,8 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const f
   if (ws_need == 0) {
     uint32_t* status = nullptr;
     if (device_status_word(&status) != cudaSuccess) return ATTN_ERR_CUDA;
-    return bwd_head_path(q, k, v, o, lse, dO, dq, dk, dv, BH, n, m, d_k, causal, scale, status,
-                         reinterpret_cast<cudaStream_t>(stream));
+    return bwd_head_path(q, k, v, o, lse, dO, dq, dk, dv, kv_len, BH, h, n, m, d_k, causal, scale,
+                         status, reinterpret_cast<cudaStream_t>(stream));
   }
   if (!workspace || !aligned16(workspace) || workspace_bytes < ws_need) return ATTN_ERR_INVALID_ARG;
 
@@ -381,6 +389,8 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const f
   p.c = static_cast<float>(std::fabs(static_cast<double>(scale)) * kLog2e);
   p.scale = scale;
   p.num_kblocks = static_cast<int>((m + 127) / 128);
+  p.kv_len = kv_len;
+  p.h = h;
   p.wd.status = status;
   p.wd.budget_ns = g_watchdog_ns.load();
 
@@ -396,6 +406,35 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const f
   cudaError_t e = attn::launch_bwd(d_k, tq, tk, tv, tdk, tdv, tdo, tdq, pre, p, post, static_cast<int>(BH),
                                    reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int h, int n,
+             int m, int d_k, int d_v, int causal, float scale, attn_stream_t stream) {
+  return fwd_impl(q, k, v, o, lse, nullptr, B, h, n, m, d_k, d_v, causal, scale, stream);
+}
+
+int attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse, const int* kv_len,
+                    int B, int h, int n, int m, int d_k, int d_v, int causal, float scale,
+                    attn_stream_t stream) {
+  if ((reinterpret_cast<uintptr_t>(kv_len) & 3u) != 0) return ATTN_ERR_INVALID_ARG;
+  return fwd_impl(q, k, v, o, lse, kv_len, B, h, n, m, d_k, d_v, causal, scale, stream);
+}
+
+int attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+             const void* dO, void* dq, void* dk, void* dv, int B, int h, int n, int m, int d_k,
+             int d_v, int causal, float scale, void* workspace, size_t workspace_bytes,
+             attn_stream_t stream) {
+  return bwd_impl(q, k, v, o, lse, dO, dq, dk, dv, nullptr, B, h, n, m, d_k, d_v, causal, scale,
+                  workspace, workspace_bytes, stream);
+}
+
+int attn_bwd_varlen(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                    const void* dO, void* dq, void* dk, void* dv, const int* kv_len, int B, int h,
+                    int n, int m, int d_k, int d_v, int causal, float scale, void* workspace,
+                    size_t workspace_bytes, attn_stream_t stream) {
+  if ((reinterpret_cast<uintptr_t>(kv_len) & 3u) != 0) return ATTN_ERR_INVALID_ARG;
+  return bwd_impl(q, k, v, o, lse, dO, dq, dk, dv, kv_len, B, h, n, m, d_k, d_v, causal, scale,
+                  workspace, workspace_bytes, stream);
 }
 
 int attn_get_device_status(attn_stream_t stream) {
@@ -482,7 +521,8 @@ extern "C" int attn_bwd_noalloc(const void* q, const void* k, const void* v, con
   }
   if (status == nullptr) status = g_noalloc_status_ptr[dev];
   if (attn_bwd_workspace_bytes(B, h, n, m, d_k, d_v, causal) == 0)  // needs no scratch at all
-    return bwd_head_path(q, k, v, o, lse, dO, dq, dk, dv, BH, n, m, d_k, causal, scale, status, s);
+    return bwd_head_path(q, k, v, o, lse, dO, dq, dk, dv, nullptr, BH, h, n, m, d_k, causal, scale,
+                         status, s);
 
   const long long n_pad = round_up(n, 128);
   float* dq_acc = static_cast<float*>(g_noalloc_scratch_ptr[dev]);
@@ -522,6 +562,8 @@ extern "C" int attn_bwd_noalloc(const void* q, const void* k, const void* v, con
   p.c = static_cast<float>(std::fabs(static_cast<double>(scale)) * kLog2e);
   p.scale = scale;
   p.num_kblocks = static_cast<int>((m + 127) / 128);
+  p.kv_len = nullptr;
+  p.h = h;
   p.wd.status = status;
   p.wd.budget_ns = g_watchdog_ns.load();
 

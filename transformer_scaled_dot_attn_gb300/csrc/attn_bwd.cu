@@ -214,10 +214,13 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   // of an item: [i_start, n_qt) (causal: tiles wholly above the key tile see
   // none of its keys). All CTAs of a head walk the query tiles in the same
   // order, so the streamed Q and dO tiles come from DRAM once, then from L2.
+  // Key padding: a key tile wholly past the head's real keys has no query
+  // tiles (its dK, dV rows are zero).
   auto item_of = [&](int it, int& bh, int& kb, int& i_start, int& T) {
     kb = it / p.BH;
     bh = it - kb * p.BH;
     i_start = p.causal ? min(kb, n_qt) : 0;
+    if (kb * 128 >= head_keys(p.kv_len, bh, p.h, p.m)) i_start = n_qt;
     T = n_qt - i_start;
   };
 
@@ -466,6 +469,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       int bh, kb, i_start, T;
       item_of(it, bh, kb, i_start, T);
       const int key = kb * 128 + r;
+      const int mb = head_keys(p.kv_len, bh, p.h, p.m);  // real keys of this head
       // region h carried the previous item's dV / dK out: its TMA store must
       // have read it before dS (or this item's output) overwrites it
       if (C::STAGE_OUT && li >= 1) {
@@ -478,7 +482,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         const int q_row0 = (i_start + t) * 128;
         // queries [lo, hi) of this tile may attend to this key
         const int lo = p.causal ? max(0, key - q_row0) : 0;
-        const int hi = (key < p.m) ? min(128, p.n - q_row0) : 0;
+        const int hi = (key < mb) ? min(128, p.n - q_row0) : 0;
         const bool masked = __any_sync(0xffffffffu, lo > col0 || hi < col0 + 64);
         ok = __all_sync(0xffffffffu, guarded_wait(&sh.s_full, gt & 1, abort_flag, wd, kSiteBwdS) &&
                                          guarded_wait(&sh.qdo_full[st], (gt >> 1) & 1, abort_flag, wd, kSiteBwdLoad));

@@ -157,10 +157,15 @@ attn_bwd_head_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
   volatile int* abort_flag = &sh.abort_flag;
   const int NQT = (p.n + 127) / 128;  // 1 or 2
   const int NKT = (p.m + 127) / 128;
-  // query tiles [t_lo(kb), NQT) see key tile kb (causal: none wholly above the diagonal)
-  auto t_lo = [&](int kb) { return p.causal ? min(kb, NQT) : 0; };
-  // the last key tile that query tile t sees
-  auto last_kb = [&](int t) { return p.causal ? min(t, NKT - 1) : NKT - 1; };
+  // query tiles [t_lo(kb), NQT) see key tile kb (causal: none wholly above the
+  // diagonal; key padding: none if the tile lies past the head's mb real keys)
+  auto t_lo = [&](int kb, int mb) { return (kb * 128 >= mb) ? NQT : (p.causal ? min(kb, NQT) : 0); };
+  // the last key tile that reads query tile t's Q/dO slot (a key tile past the
+  // real keys reads none, but the slot is released on the head's last key tile)
+  auto last_kb = [&](int t, int mb) {
+    const int nk = mb > 0 ? (mb + 127) / 128 : 0;  // key tiles with real keys
+    return (nk == 0) ? -1 : (p.causal ? min(t, nk - 1) : nk - 1);
+  };
 
   if (tid == 0) {
     for (int s = 0; s < 2; ++s) {
@@ -277,12 +282,16 @@ attn_bwd_head_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
     bool ok = true;
     int g = 0, k = 0, ki = 0, li = 0;
     for (int bh = blockIdx.x; ok && bh < p.BH; bh += gridDim.x, ++li) {
+      const int mb = head_keys(p.kv_len, bh, p.h, p.m);  // real keys of this head
+      // dq_free is waited once per head, in order: before the head's first dQ
+      // product (key tile 0, query tile 0), or here for a head without real keys
+      if (mb == 0 && li >= 1 && !(ok = wait_all(&sh.dq_free, (li - 1) & 1, kSiteBwdDQ))) break;
       for (int kb = 0; ok && kb < NKT; ++kb, ++ki) {
         const int set = ki & 1;
         const uint32_t sK = smem_u32(smem + C::OFF_K + set * C::TILE);
         const uint32_t sV = smem_u32(smem + C::OFF_V + set * C::TILE);
         if (!(ok = wait_all(&sh.kv_full[set], (ki >> 1) & 1, kSiteBwdLoad))) break;
-        const int t0 = t_lo(kb), T = NQT - t0;
+        const int t0 = t_lo(kb, mb), T = NQT - t0;
         // acc_free is waited once per key tile, in order: below before the
         // first dV product, or here for a key tile without query tiles
         if (T == 0 && ki >= 1 && !(ok = wait_all(&sh.acc_free, (ki - 1) & 1, kSiteBwdFinal))) break;
@@ -346,7 +355,7 @@ attn_bwd_head_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
               mma_ss(tmem + C::TM_DQ + t * D, da, b_mn(sK, q), id_dq, (kb > 0 || q > 0) ? 1u : 0u);
             }
             mma_commit(&sh.ds_empty);
-            if (kb == last_kb(t)) mma_commit(&sh.slot_empty[slot]);  // no later product reads this slot
+            if (kb == last_kb(t, mb)) mma_commit(&sh.slot_empty[slot]);  // no later product reads this slot
           }
           __syncwarp();
           if (t + 1 < NQT) {
@@ -367,7 +376,12 @@ attn_bwd_head_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         g += T;
       }
       if (!ok) break;
-      if (lane == 0) mma_commit(&sh.dq_full);  // every dQ product of this head
+      if (lane == 0) {
+        // query tiles that no key tile read (a head without real keys) free their slots here
+        for (int t = 0; t < NQT; ++t)
+          if (last_kb(t, mb) < 0) mma_commit(&sh.slot_empty[(k + t) % C::NSLOT]);
+        mma_commit(&sh.dq_full);  // every dQ product of this head
+      }
       __syncwarp();
       k += NQT;
     }
@@ -433,9 +447,10 @@ attn_bwd_head_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
     bool ok = true;
     int g = 0, k = 0, ki = 0;
     for (int bh = blockIdx.x; ok && bh < p.BH; bh += gridDim.x) {
+      const int mb = head_keys(p.kv_len, bh, p.h, p.m);  // real keys of this head
       for (int kb = 0; ok && kb < NKT; ++kb, ++ki) {
         const int key = kb * 128 + r;
-        const int t0 = t_lo(kb), T = NQT - t0;
+        const int t0 = t_lo(kb, mb), T = NQT - t0;
         // region h carried the previous key tile's dV / dK out: its TMA store
         // must have read it before dS (or this key tile's output) overwrites it
         if (ki >= 1) {
@@ -448,7 +463,7 @@ attn_bwd_head_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
           const int q_row0 = t * 128;
           // queries [lo, hi) of this tile may attend to this key
           const int lo = p.causal ? max(0, key - q_row0) : 0;
-          const int hi = (key < p.m) ? min(128, p.n - q_row0) : 0;
+          const int hi = (key < mb) ? min(128, p.n - q_row0) : 0;
           const bool masked = __any_sync(0xffffffffu, lo > col0 || hi < col0 + 64);
           ok = __all_sync(0xffffffffu, guarded_wait(&sh.s_full, gt & 1, abort_flag, wd, kSiteBwdS) &&
                                            guarded_wait(&sh.stat_full[slot], (kk / C::NSLOT) & 1, abort_flag, wd,
@@ -576,14 +591,22 @@ attn_bwd_head_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
       if (!ok) break;
       tc_fence_after();
       uint8_t* stage = smem + C::OFF_STAGE;
+      // a head without real keys has no dQ product: its dQ is zero (TMEM
+      // still holds the previous head's)
+      const bool empty = head_keys(p.kv_len, bh, p.h, p.m) == 0;
       bool live = true;
       for (int t = 0; live && t < NQT; ++t, ++ns) {
         uint32_t w[D / 2];
 #pragma unroll
         for (int q = 0; q < D / 32; ++q) {
           uint32_t v[32];
-          tmem_ld32(tmem + lane_base + C::TM_DQ + t * D + q * 32, v);
-          tmem_ld_wait();
+          if (!empty) {
+            tmem_ld32(tmem + lane_base + C::TM_DQ + t * D + q * 32, v);
+            tmem_ld_wait();
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = 0u;
+          }
 #pragma unroll
           for (int i = 0; i < 16; ++i)
             w[q * 16 + i] = pack_bf16x2(__uint_as_float(v[2 * i]) * p.scale, __uint_as_float(v[2 * i + 1]) * p.scale);

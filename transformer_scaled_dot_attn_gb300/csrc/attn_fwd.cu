@@ -134,6 +134,17 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
+// A query row of a sequence without real keys (key padding with length 0):
+// O = 0 and lse = -inf, the empty sum. Written directly; this case is rare.
+template <int D>
+__device__ __forceinline__ void write_empty_row(const FwdParams& p, int bh, int row, int col0, int ncols,
+                                                bool write_lse) {
+  if (row >= p.n) return;
+  uint4* orow = reinterpret_cast<uint4*>(p.o + (static_cast<size_t>(bh) * p.n + row) * D + col0);
+  for (int c = 0; c < ncols / 8; ++c) orow[c] = make_uint4(0u, 0u, 0u, 0u);
+  if (write_lse && p.lse != nullptr) p.lse[static_cast<size_t>(bh) * p.n + row] = -INFINITY;
+}
+
 // Key tiles of BN needed by query rows up to r_hi (already clipped to n-1).
 template <int BN>
 __device__ __forceinline__ int key_tiles(int r_hi, int m, int causal) {
@@ -192,13 +203,15 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   volatile int* abort_flag = &sh.abort_flag;
   const Watchdog wd = p.wd;
 
-  // key tiles per query tile (0 for tiles past n); nondecreasing in g
+  // real keys of this head (key padding), key tiles per query tile (0 for
+  // tiles past n or without real keys); nondecreasing in g
+  const int mb = head_keys(p.kv_len, bh, p.h, p.m);
   int ntile[NQ];
   int nt = 0, nq_valid = 0;
 #pragma unroll
   for (int g = 0; g < NQ; ++g) {
     const int r0 = q0 + g * 128;
-    ntile[g] = (r0 < p.n) ? key_tiles<BN>(min(r0 + 127, p.n - 1), p.m, p.causal) : 0;
+    ntile[g] = (r0 < p.n && mb > 0) ? key_tiles<BN>(min(r0 + 127, p.n - 1), mb, p.causal) : 0;
     nt = max(nt, ntile[g]);
     nq_valid += (r0 < p.n) ? 1 : 0;
   }
@@ -367,7 +380,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     const uint32_t t_s = tmem + lane_base + C::tm_s(g) + h * C::COLS;
     const uint32_t t_p = tmem + lane_base + C::tm_p(g) + h * (C::COLS / 2);
     const uint32_t t_o = tmem + lane_base + C::tm_o(g) + h * C::OCOLS;
-    const int lim = (p.causal ? min(row + 1, p.m) : p.m) - h * C::COLS;  // visible keys, from column h*COLS
+    const int lim = (p.causal ? min(row + 1, mb) : mb) - h * C::COLS;  // visible keys, from column h*COLS
     const float c = p.c;
     const uint64_t c2 = f2_pack(c, c);
     float m_used = 0.f, l = 0.f;
@@ -479,6 +492,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       mbar_arrive(&sh.p_full[g]);
       if (C::SPLIT == 1 && !ok) break;
     }
+    if (mb == 0) write_empty_row<D>(p, bh, row, h * C::OCOLS, C::OCOLS, h == 0);
     if (my_tiles > 0) {
       ok = __all_sync(0xffffffffu, guarded_wait(&sh.o_full[g], 0, abort_flag, wd, kSiteOFull)) && ok;
       if (C::SPLIT == 2) {
@@ -632,17 +646,19 @@ attn_fwd_persist_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
   volatile int* abort_flag = &sh.abort_flag;
   const Watchdog wd = p.wd;
   // item -> (head, first query row); key tiles per query tile (0 past n)
-  auto item_of = [&](int it, int& bh, int& q0, int (&ntile)[2], int& nt, int& nq_valid) {
+  // item -> (head, first query row, real keys of the head)
+  auto item_of = [&](int it, int& bh, int& q0, int& mb, int (&ntile)[2], int& nt, int& nq_valid) {
     bh = it % BH;
     const int y = it / BH;
     const int qb = p.causal ? (p.num_qblocks - 1 - y) : y;
     q0 = qb * (NQ * 128);
+    mb = head_keys(p.kv_len, bh, p.h, p.m);
     nt = 0;
     nq_valid = 0;
 #pragma unroll
     for (int g = 0; g < NQ; ++g) {
       const int r0 = q0 + g * 128;
-      ntile[g] = (r0 < p.n) ? key_tiles<BN>(min(r0 + 127, p.n - 1), p.m, p.causal) : 0;
+      ntile[g] = (r0 < p.n && mb > 0) ? key_tiles<BN>(min(r0 + 127, p.n - 1), mb, p.causal) : 0;
       nt = max(nt, ntile[g]);
       nq_valid += (r0 < p.n) ? 1 : 0;
     }
@@ -694,14 +710,20 @@ attn_fwd_persist_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
       int jj = 0;
       bool ok = true;
       for (int it = blockIdx.x, li = 0; ok && it < items; it += gridDim.x, ++li) {
-        int bh, q0, ntile[2], nt, nq_valid;
-        item_of(it, bh, q0, ntile, nt, nq_valid);
+        int bh, q0, mb, ntile[2], nt, nq_valid;
+        item_of(it, bh, q0, mb, ntile, nt, nq_valid);
         const int qs = li & 1;
         if (li >= 2 && !(ok = guarded_wait(&sh.q_empty[qs], ((li >> 1) - 1) & 1, abort_flag, wd, kSiteKEmpty)))
           break;
-        mbar_arrive_expect_tx(&sh.q_full[qs], nq_valid * C::QTILE);
-        for (int t = 0; t < nq_valid; ++t)
-          tma_load_3d(smem + C::OFF_Q + (qs * NQ + t) * C::QTILE, &tm_q, &sh.q_full[qs], 0, q0 + t * 128, bh);
+        if (nt > 0) {
+          mbar_arrive_expect_tx(&sh.q_full[qs], nq_valid * C::QTILE);
+          for (int t = 0; t < nq_valid; ++t)
+            tma_load_3d(smem + C::OFF_Q + (qs * NQ + t) * C::QTILE, &tm_q, &sh.q_full[qs], 0, q0 + t * 128, bh);
+        } else {
+          // no key tile (a sequence without real keys): no MMA reads Q, so none
+          // is loaded, but the set's phase still completes
+          mbar_arrive(&sh.q_full[qs]);
+        }
         q_filled |= 1u << qs;
         q_ph = (q_ph & ~(1u << qs)) | (static_cast<uint32_t>((li >> 1) & 1) << qs);
         for (int j = 0; ok && j < nt; ++j, ++jj) {
@@ -764,8 +786,8 @@ attn_fwd_persist_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
       bool ok = true;
       int jj = 0, gt = 0, oc = 0;  // K/V tiles of earlier items, this tile's S count, items with output
       for (int it = blockIdx.x, li = 0; ok && it < items; it += gridDim.x, ++li) {
-        int bh, q0, ntile[2], nt, nq_valid;
-        item_of(it, bh, q0, ntile, nt, nq_valid);
+        int bh, q0, mb, ntile[2], nt, nq_valid;
+        item_of(it, bh, q0, mb, ntile, nt, nq_valid);
         const int T = g == 0 ? ntile[0] : ntile[1];
         if (T > 0) {
           const uint32_t sQ = smem_u32(smem + C::OFF_Q) + ((li & 1) * NQ + g) * C::QTILE;
@@ -832,18 +854,19 @@ attn_fwd_persist_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
       }
     };
     for (int it = blockIdx.x, li = 0; ok && it < items; it += gridDim.x, ++li) {
-      int bh, q0, ntile[2], nt, nq_valid;
-      item_of(it, bh, q0, ntile, nt, nq_valid);
+      int bh, q0, mb, ntile[2], nt, nq_valid;
+      item_of(it, bh, q0, mb, ntile, nt, nq_valid);
       const int T = g == 0 ? ntile[0] : ntile[1];
       const int qs = li & 1;
       if (T == 0) {
+        if (mb == 0) write_empty_row<D>(p, bh, q0 + g * 128 + r, 0, D, true);
         release_pending();
         // no rows of this item here: the Q set does not wait for this tile's output
         if (r == 0) mbar_arrive(&sh.q_empty[qs]);
         continue;
       }
       const int row = q0 + g * 128 + r;
-      const int lim = p.causal ? min(row + 1, p.m) : p.m;  // keys [0, lim) are visible
+      const int lim = p.causal ? min(row + 1, mb) : mb;  // keys [0, lim) are visible
       float m_used = 0.f, l = 0.f;
       for (int j = 0; j < T; ++j) {
         const int gj = gt + j;

@@ -49,6 +49,13 @@ __device__ __forceinline__ bool guarded_wait(uint64_t* bar, uint32_t parity, vol
   }
 }
 
+// Key padding: real keys of head bh, kv_len[b] for its sequence b = bh / h
+// clamped to [0, m]; all m without a length array.
+__device__ __forceinline__ int head_keys(const int* kv_len, int bh, int h, int m) {
+  if (kv_len == nullptr) return m;
+  return min(max(__ldg(kv_len + bh / h), 0), m);
+}
+
 // Profiling hooks (implemented with the C ABI): bracket one kernel launch
 // with CUDA events on `stream` when profiling is enabled; no-ops otherwise.
 enum KernelKind : int { kKindFwd = 0, kKindBwdPre = 1, kKindBwdMain = 2, kKindBwdPost = 3, kNumKinds = 4 };
@@ -66,6 +73,8 @@ struct FwdParams {
   float c;            // |scale| * log2(e)
   int num_qblocks;    // query blocks (set by the launcher)
   int inject;         // test hook: 1 = skip the first value-tile load
+  const int* kv_len;  // [B] real keys per sequence (key padding) or nullptr
+  int h;              // heads per sequence (kv_len is indexed by bh / h)
   Watchdog wd;
 };
 
@@ -105,6 +114,8 @@ struct BwdParams {
   int num_kblocks;          // ceil(m / 128)
   int BH;                   // heads (set by the launcher)
   int num_items;            // BH * num_kblocks work items (set by the launcher)
+  const int* kv_len;        // [B] real keys per sequence (key padding) or nullptr
+  int h;                    // heads per sequence
   Watchdog wd;
 };
 
@@ -127,6 +138,8 @@ struct BwdHeadParams {
   int causal, neg;
   float c;                  // |scale| * log2(e)
   float scale;              // signed scale, applied to dQ and dK
+  const int* kv_len;        // [B] real keys per sequence (key padding) or nullptr
+  int h;                    // heads per sequence
   Watchdog wd;
 };
 bool bwd_head_supported(int n, int d);
