@@ -462,7 +462,9 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 #pragma unroll
       for (int q = 0; q < C::CHUNKS; ++q) {
         uint32_t pk[16];
-        if (masked)
+        // masked scores already hold -inf, and 2^(-inf * c - m) = 0 for c > 0;
+        // only c = 0 (scale 0) needs the explicit mask (-inf * 0 is NaN)
+        if (masked && c == 0.f)
           exp_chunk<true>(s[q], q * 32, rem, c2, nm2, lsum2, pk);
         else
           exp_chunk<false>(s[q], q * 32, rem, c2, nm2, lsum2, pk);
@@ -921,7 +923,9 @@ attn_fwd_persist_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
 #pragma unroll
         for (int q = 0; q < C::CHUNKS; ++q) {
           uint32_t pk[16];
-          if (masked)
+          // masked scores already hold -inf, and 2^(-inf * c - m) = 0 for c > 0;
+          // only c = 0 (scale 0) needs the explicit mask (-inf * 0 is NaN)
+          if (masked && c == 0.f)
             exp_chunk<true>(s[q], q * 32, rem, c2, nm2, lsum2, pk);
           else
             exp_chunk<false>(s[q], q * 32, rem, c2, nm2, lsum2, pk);
