@@ -24,6 +24,7 @@ CASES = [
     (4, 2, 200, 256, 64, True, [256, 7, 0, 128]),       # per-item fwd, whole-head bwd, causal
     (3, 2, 130, 300, 32, False, [300, 64, 0]),          # ragged m, d = 32
     (2, 2, 384, 1024, 64, False, [1000, 513]),          # persistent fwd, general bwd
+    (3, 2, 256, 512, 32, False, [0, 300, 512]),         # persistent fwd (later tiles speculative)
     (3, 1, 300, 300, 64, True, [300, 150, 1]),          # general bwd, causal
     (2, 2, 200, 320, 128, False, [320, 0]),             # d = 128: per-item fwd, general bwd
 ]

@@ -62,6 +62,26 @@ def test_fwd_bwd_match_oracle(w):
     assert_close("dV", dv, rdv, grad=True)
 
 
+@pytest.mark.parametrize("d", [32, 64])
+@pytest.mark.parametrize("mult,first_big", [(4.0, 1), (16.0, 1), (64.0, 1), (64.0, 3), (0.25, 1)])
+def test_scores_that_grow_after_the_first_key_tile(d, mult, first_big):
+    """Later key tiles with much larger scores than the first (keys scaled by a
+    power of two, exact in bf16): the forward that exponentiates later tiles
+    against the first tile's row maximum must notice the growth (weights far
+    above 1, or infinite for mult = 64) and move to the new maximum; mult < 1
+    makes the later tiles' weights vanish instead."""
+    n, m = 256, 512
+    q = normal_bf16((1, 2, n, d), 1101)
+    k = normal_bf16((1, 2, m, d), 1102)
+    v = normal_bf16((1, 2, m, d), 1103)
+    k[:, :, first_big * 128:, :] *= mult
+    scale = default_scale(d)
+    o, lse = run_fwd(q, k, v, False, scale)
+    ro, rlse = oracle.fwd(q, k, v, False, scale)
+    assert_close("O", o, ro)
+    assert_close("lse", lse, rlse)
+
+
 @pytest.mark.parametrize("scale", [0.0, 1.0, -0.2, 0.03])
 @pytest.mark.parametrize("causal", [False, True])
 def test_scale_values(scale, causal):
@@ -86,6 +106,21 @@ def test_scale_values(scale, causal):
     assert_close("dQ", dq, rdq, grad=True, rel_l2=rel, extra=bq)
     assert_close("dK", dk, rdk, grad=True, rel_l2=rel, extra=bk)
     assert_close("dV", dv, rdv, grad=True, rel_l2=rel)
+
+
+@pytest.mark.parametrize("scale", [0.0, 1.0, -0.2, 0.03])
+@pytest.mark.parametrize("m", [256, 640])
+def test_scale_values_persistent_forward(scale, m):
+    """The same scales through the persistent forward (non-causal, whole 128-key
+    tiles): m = 256 takes every tile's maximum, m = 640 exponentiates its later
+    tiles against the running reference (scale = 1 saturates the softmax, so the
+    scores there often outgrow the first tile's maximum)."""
+    w = _small("sp", 1, 2, 256, m, 64, False, 8)
+    q, k, v = workload_inputs(w)
+    o, lse = run_fwd(q, k, v, False, scale)
+    ro, rlse = oracle.fwd(q, k, v, False, scale)
+    assert_close("O", o, ro)
+    assert_close("lse", lse, rlse)
 
 
 def test_worked_example_weights_on_gpu():

@@ -43,6 +43,11 @@ namespace {
 using namespace sm103;
 
 constexpr float kLn2 = 0.69314718055994530942f;
+// Speculative exponentials (persistent forward): a tile is exponentiated against
+// the running reference without taking its own maximum first; a tile row whose
+// weights sum above 2^8 is redone against its maximum. So no weight exceeds
+// 2^8, the same bound the lazy rescale (threshold kRescaleThreshold = 8) keeps.
+constexpr float kSpecLimitSum = 256.f;
 // A stale running max is kept while new scores exceed it by at most 8 in
 // log2 units (p <= 256), so most tiles skip the O rescale. Exact after the
 // final division by the row sum.
@@ -166,11 +171,14 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, const
 }
 
 // p = 2^(s*c - m) for one 32-column chunk of a row held in registers; packs
-// the bf16 weights and adds the fp32 weights into lsum2. MASKED: columns at
-// or past `rem` (keys this row may not see) get weight exactly 0.
+// the bf16 weights and adds them, as rounded, into lsum: the row sum l is the
+// sum of the weights the P.V product applies, so O / l is an exact convex
+// combination of value rows (a row dominated by one key returns that value
+// row even when the reference m lags the row maximum). MASKED: columns at or
+// past `rem` (keys this row may not see) get weight exactly 0.
 template <bool MASKED>
 __device__ __forceinline__ void exp_chunk(const uint32_t (&s)[32], int col0, int rem, uint64_t c2,
-                                          uint64_t nm2, uint64_t (&lsum2)[2], uint32_t (&pk)[16]) {
+                                          uint64_t nm2, float (&lsum)[4], uint32_t (&pk)[16]) {
 #pragma unroll
   for (int i = 0; i < 16; ++i) {
     const uint64_t x2 = fma2(f2_pack(__uint_as_float(s[2 * i]), __uint_as_float(s[2 * i + 1])), c2, nm2);
@@ -181,8 +189,8 @@ __device__ __forceinline__ void exp_chunk(const uint32_t (&s)[32], int col0, int
       if (col0 + 2 * i + 1 >= rem) x1 = -INFINITY;
     }
     const uint64_t p2 = f2_pack(ex2(x0), ex2(x1));
-    lsum2[i & 1] = add2(lsum2[i & 1], p2);
     pk[i] = pack_bf16x2_pair(p2);
+    acc_bf16x2(lsum[(i & 1) * 2], lsum[(i & 1) * 2 + 1], pk[i]);
   }
 }
 
@@ -458,24 +466,21 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         ok = __all_sync(0xffffffffu, guarded_wait(&sh.pv_done[g], (j - 1) & 1, abort_flag, wd, kSitePFull)) && ok;
         tc_fence_after();
       }
-      uint64_t lsum2[2] = {0ull, 0ull};
+      float lsum[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int q = 0; q < C::CHUNKS; ++q) {
         uint32_t pk[16];
         // masked scores already hold -inf, and 2^(-inf * c - m) = 0 for c > 0;
         // only c = 0 (scale 0) needs the explicit mask (-inf * 0 is NaN)
         if (masked && c == 0.f)
-          exp_chunk<true>(s[q], q * 32, rem, c2, nm2, lsum2, pk);
+          exp_chunk<true>(s[q], q * 32, rem, c2, nm2, lsum, pk);
         else
-          exp_chunk<false>(s[q], q * 32, rem, c2, nm2, lsum2, pk);
+          exp_chunk<false>(s[q], q * 32, rem, c2, nm2, lsum, pk);
         tmem_st16(t_p + q * 16, pk);
       }
       if (TURNS) mbar_arrive(&sh.exp_turn[g ^ 1]);  // the other group's turn
       {
-        float a0, a1, b0, b1;
-        f2_unpack(lsum2[0], a0, a1);
-        f2_unpack(lsum2[1], b0, b1);
-        l = l * alpha + ((a0 + a1) + (b0 + b1));
+        l = l * alpha + ((lsum[0] + lsum[1]) + (lsum[2] + lsum[3]));
       }
       tmem_st_wait();
       if (j > 0 && __any_sync(0xffffffffu, rescale)) {
@@ -615,6 +620,10 @@ struct FwdP {
   static constexpr uint32_t SMEM = OFF_V + STAGES * KTILE + 1024;
   static constexpr int THREADS = NQ * 128 + 128;          // softmax, producer, issuers, idle
   static constexpr int PRODUCER = 4 * NQ, ISSUER = 4 * NQ + 1;
+  // setmaxnreg split of the 384 x 168 registers the CTA is launched with: the
+  // softmax keeps a tile's scores and its packed weights in registers at once
+  static constexpr int REG_SOFTMAX = 224, REG_OTHER = 56;
+  static_assert(NQ * 128 * REG_SOFTMAX + 128 * REG_OTHER <= 384 * 168, "register split");
   static constexpr int CHUNKS = BN / 32;
   static constexpr uint32_t P_COLS = BN / 2;
   __host__ __device__ static constexpr uint32_t tm_s(int g) { return g * BN; }
@@ -633,7 +642,7 @@ struct FwdPShared {
   int abort_flag;
 };
 
-template <int D>
+template <int D, bool SPEC>
 __global__ void __launch_bounds__(FwdP<D>::THREADS, 1)
 attn_fwd_persist_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                         const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
@@ -705,6 +714,7 @@ attn_fwd_persist_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
 
   if (warp == C::PRODUCER) {
     // ------------------------------------------------------------ TMA producer
+    if constexpr (SPEC) reg_dealloc<C::REG_OTHER>();
     if (lane == 0) {
       // per stage s, group g (bit g * 4 + s): `users` = the stage's last tile was
       // used by group g; `uses` = parity of group g's uses of stage s so far
@@ -764,6 +774,7 @@ attn_fwd_persist_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
     }
   } else if (warp >= C::ISSUER) {
     // ------------------------------------------------------------ MMA issuer of query tile g
+    if constexpr (SPEC) reg_dealloc<C::REG_OTHER>();
     const int g = warp - C::ISSUER;
     if (lane == 0 && g < NQ) {
       const uint32_t idesc_s = idesc_bf16_f32(128, BN, false, false) | (p.neg ? (1u << 13) : 0u);
@@ -834,6 +845,7 @@ attn_fwd_persist_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
     __syncwarp();
   } else {
     // ------------------------------------------------------------ softmax of query tile g
+    if constexpr (SPEC) reg_alloc<C::REG_SOFTMAX>();
     const int g = warp >> 2;
     const int r = tid & 127;
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
@@ -870,88 +882,197 @@ attn_fwd_persist_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
       const int row = q0 + g * 128 + r;
       const int lim = p.causal ? min(row + 1, mb) : mb;  // keys [0, lim) are visible
       float m_used = 0.f, l = 0.f;
-      for (int j = 0; j < T; ++j) {
-        const int gj = gt + j;
-        ok = __all_sync(0xffffffffu, guarded_wait(&sh.s_full[g], gj & 1, abort_flag, wd, kSiteSFull));
-        if (!ok) break;
-        tc_fence_after();
-        if (j == 0) release_pending();
-        uint32_t s[C::CHUNKS][32];
-#pragma unroll
-        for (int q = 0; q < C::CHUNKS; ++q) tmem_ld32(t_s + q * 32, s[q]);
-        tmem_ld_wait();
-        tc_fence_before();
-        mbar_arrive(&sh.s_free[g]);  // S may be overwritten by the next score product
-        const int rem = lim - j * BN;
-        const bool masked = __any_sync(0xffffffffu, rem < BN);
-        if (masked) {
-#pragma unroll
-          for (int q = 0; q < C::CHUNKS; ++q)
-#pragma unroll
-            for (int i = 0; i < 32; ++i)
-              if (q * 32 + i >= rem) s[q][i] = __float_as_uint(-INFINITY);
-        }
-        float mx4[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u)
-          mx4[u] = fmaxf(__uint_as_float(s[0][2 * u]), __uint_as_float(s[0][2 * u + 1]));
-#pragma unroll
-        for (int e = 8; e < BN; e += 8) {
-#pragma unroll
-          for (int u = 0; u < 4; ++u)
-            mx4[u] = max3(mx4[u], __uint_as_float(s[(e + 2 * u) >> 5][(e + 2 * u) & 31]),
-                          __uint_as_float(s[(e + 2 * u + 1) >> 5][(e + 2 * u + 1) & 31]));
-        }
-        const float m_new = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * c;
-        float alpha = 1.f;
-        bool rescale = false;
-        if (j == 0) {
-          m_used = m_new;
-        } else if (m_new > m_used + kRescaleThreshold) {
-          alpha = ex2(m_used - m_new);
-          m_used = m_new;
-          rescale = true;
-        }
-        const uint64_t nm2 = f2_pack(-m_used, -m_used);
-        if (gj >= 1) {
-          // the previous P.V (possibly the previous item's) still reads P until it completes
-          ok = __all_sync(0xffffffffu, guarded_wait(&sh.pv_done[g], (gj - 1) & 1, abort_flag, wd, kSitePFull));
+      if constexpr (SPEC) {
+        for (int j = 0; j < T; ++j) {
+          const int gj = gt + j;
+          ok = __all_sync(0xffffffffu, guarded_wait(&sh.s_full[g], gj & 1, abort_flag, wd, kSiteSFull));
           if (!ok) break;
           tc_fence_after();
-        }
-        uint64_t lsum2[2] = {0ull, 0ull};
-#pragma unroll
-        for (int q = 0; q < C::CHUNKS; ++q) {
-          uint32_t pk[16];
-          // masked scores already hold -inf, and 2^(-inf * c - m) = 0 for c > 0;
-          // only c = 0 (scale 0) needs the explicit mask (-inf * 0 is NaN)
-          if (masked && c == 0.f)
-            exp_chunk<true>(s[q], q * 32, rem, c2, nm2, lsum2, pk);
-          else
-            exp_chunk<false>(s[q], q * 32, rem, c2, nm2, lsum2, pk);
-          tmem_st16(t_p + q * 16, pk);
-        }
-        {
-          float a0, a1, b0, b1;
-          f2_unpack(lsum2[0], a0, a1);
-          f2_unpack(lsum2[1], b0, b1);
-          l = l * alpha + ((a0 + a1) + (b0 + b1));
-        }
-        tmem_st_wait();
-        if (j > 0 && __any_sync(0xffffffffu, rescale)) {
-#pragma unroll
-          for (int q = 0; q < D / 16; ++q) {
-            uint32_t o[16];
-            tmem_ld16(t_o + q * 16, o);
-            tmem_ld_wait();
-#pragma unroll
-            for (int i = 0; i < 16; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-            tmem_st16(t_o + q * 16, o);
+          if (j == 0) release_pending();
+          uint32_t s[C::CHUNKS][32];
+  #pragma unroll
+          for (int q = 0; q < C::CHUNKS; ++q) tmem_ld32(t_s + q * 32, s[q]);
+          tmem_ld_wait();
+          tc_fence_before();
+          mbar_arrive(&sh.s_free[g]);  // S may be overwritten by the next score product
+          const int rem = lim - j * BN;
+          const bool masked = __any_sync(0xffffffffu, rem < BN);
+          if (masked) {
+  #pragma unroll
+            for (int q = 0; q < C::CHUNKS; ++q)
+  #pragma unroll
+              for (int i = 0; i < 32; ++i)
+                if (q * 32 + i >= rem) s[q][i] = __float_as_uint(-INFINITY);
+          }
+          // Row maximum of the tile (scaled, log2 units).
+          auto tile_max = [&]() {
+            float mx4[4];
+  #pragma unroll
+            for (int u = 0; u < 4; ++u)
+              mx4[u] = fmaxf(__uint_as_float(s[0][2 * u]), __uint_as_float(s[0][2 * u + 1]));
+  #pragma unroll
+            for (int e = 8; e < BN; e += 8) {
+  #pragma unroll
+              for (int u = 0; u < 4; ++u)
+                mx4[u] = max3(mx4[u], __uint_as_float(s[(e + 2 * u) >> 5][(e + 2 * u) & 31]),
+                              __uint_as_float(s[(e + 2 * u + 1) >> 5][(e + 2 * u + 1) & 31]));
+            }
+            return fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * c;
+          };
+          // The first two tiles of an item take their row maximum (lazy rescale
+          // as in attn_fwd_kernel). From the third tile on, a tile is
+          // exponentiated against the running reference without a maximum pass;
+          // a tile sum above kSpecLimitSum shows that the scores grew, and only
+          // then is the tile's maximum taken and the row moved to it.
+          const bool spec = j >= 2;
+          float alpha = 1.f;
+          bool rescale = false;
+          if (!spec) {
+            const float m_new = tile_max();
+            if (j == 0) {
+              m_used = m_new;
+            } else if (m_new > m_used + kRescaleThreshold) {
+              alpha = ex2(m_used - m_new);
+              m_used = m_new;
+              rescale = true;
+            }
+          }
+          uint32_t pk[C::CHUNKS][16];
+          float lsum[4];
+          // weights of the tile against m_used into pk; returns their sum
+          auto exps = [&]() {
+            const uint64_t nm2 = f2_pack(-m_used, -m_used);
+            lsum[0] = lsum[1] = lsum[2] = lsum[3] = 0.f;
+  #pragma unroll
+            for (int q = 0; q < C::CHUNKS; ++q) {
+              // masked scores already hold -inf, and 2^(-inf * c - m) = 0 for c > 0;
+              // only c = 0 (scale 0) needs the explicit mask (-inf * 0 is NaN)
+              if (masked && c == 0.f)
+                exp_chunk<true>(s[q], q * 32, rem, c2, nm2, lsum, pk[q]);
+              else
+                exp_chunk<false>(s[q], q * 32, rem, c2, nm2, lsum, pk[q]);
+            }
+            return (lsum[0] + lsum[1]) + (lsum[2] + lsum[3]);
+          };
+          // the weights are computed while the previous P.V still runs, then stored
+          float l_tile = exps();
+          if (spec) {
+            const bool grew = !(l_tile <= kSpecLimitSum);  // also catches inf / NaN
+            if (__any_sync(0xffffffffu, grew)) {
+              if (grew) {
+                const float m_new = tile_max();
+                alpha = ex2(m_used - m_new);
+                m_used = m_new;
+                rescale = true;
+              }
+              l_tile = exps();  // unchanged for the rows that did not grow
+            }
+          }
+          if (gj >= 1) {
+            // the previous P.V (possibly the previous item's) still reads P until it completes
+            ok = __all_sync(0xffffffffu, guarded_wait(&sh.pv_done[g], (gj - 1) & 1, abort_flag, wd, kSitePFull));
+            if (!ok) break;
+            tc_fence_after();
+          }
+  #pragma unroll
+          for (int q = 0; q < C::CHUNKS; ++q) tmem_st16(t_p + q * 16, pk[q]);
+          l = l * alpha + l_tile;
+          if (j > 0 && __any_sync(0xffffffffu, rescale)) {
+  #pragma unroll
+            for (int q = 0; q < D / 16; ++q) {
+              uint32_t o[16];
+              tmem_ld16(t_o + q * 16, o);
+              tmem_ld_wait();
+  #pragma unroll
+              for (int i = 0; i < 16; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+              tmem_st16(t_o + q * 16, o);
+            }
           }
           tmem_st_wait();
+          tc_fence_before();
+          mbar_arrive(&sh.p_full[g]);
         }
-        tc_fence_before();
-        mbar_arrive(&sh.p_full[g]);
+      } else {
+        for (int j = 0; j < T; ++j) {
+          const int gj = gt + j;
+          ok = __all_sync(0xffffffffu, guarded_wait(&sh.s_full[g], gj & 1, abort_flag, wd, kSiteSFull));
+          if (!ok) break;
+          tc_fence_after();
+          if (j == 0) release_pending();
+          uint32_t s[C::CHUNKS][32];
+  #pragma unroll
+          for (int q = 0; q < C::CHUNKS; ++q) tmem_ld32(t_s + q * 32, s[q]);
+          tmem_ld_wait();
+          tc_fence_before();
+          mbar_arrive(&sh.s_free[g]);  // S may be overwritten by the next score product
+          const int rem = lim - j * BN;
+          const bool masked = __any_sync(0xffffffffu, rem < BN);
+          if (masked) {
+  #pragma unroll
+            for (int q = 0; q < C::CHUNKS; ++q)
+  #pragma unroll
+              for (int i = 0; i < 32; ++i)
+                if (q * 32 + i >= rem) s[q][i] = __float_as_uint(-INFINITY);
+          }
+          float mx4[4];
+  #pragma unroll
+          for (int u = 0; u < 4; ++u)
+            mx4[u] = fmaxf(__uint_as_float(s[0][2 * u]), __uint_as_float(s[0][2 * u + 1]));
+  #pragma unroll
+          for (int e = 8; e < BN; e += 8) {
+  #pragma unroll
+            for (int u = 0; u < 4; ++u)
+              mx4[u] = max3(mx4[u], __uint_as_float(s[(e + 2 * u) >> 5][(e + 2 * u) & 31]),
+                            __uint_as_float(s[(e + 2 * u + 1) >> 5][(e + 2 * u + 1) & 31]));
+          }
+          const float m_new = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * c;
+          float alpha = 1.f;
+          bool rescale = false;
+          if (j == 0) {
+            m_used = m_new;
+          } else if (m_new > m_used + kRescaleThreshold) {
+            alpha = ex2(m_used - m_new);
+            m_used = m_new;
+            rescale = true;
+          }
+          const uint64_t nm2 = f2_pack(-m_used, -m_used);
+          if (gj >= 1) {
+            // the previous P.V (possibly the previous item's) still reads P until it completes
+            ok = __all_sync(0xffffffffu, guarded_wait(&sh.pv_done[g], (gj - 1) & 1, abort_flag, wd, kSitePFull));
+            if (!ok) break;
+            tc_fence_after();
+          }
+          float lsum[4] = {0.f, 0.f, 0.f, 0.f};
+  #pragma unroll
+          for (int q = 0; q < C::CHUNKS; ++q) {
+            uint32_t pk[16];
+            // masked scores already hold -inf, and 2^(-inf * c - m) = 0 for c > 0;
+            // only c = 0 (scale 0) needs the explicit mask (-inf * 0 is NaN)
+            if (masked && c == 0.f)
+              exp_chunk<true>(s[q], q * 32, rem, c2, nm2, lsum, pk);
+            else
+              exp_chunk<false>(s[q], q * 32, rem, c2, nm2, lsum, pk);
+            tmem_st16(t_p + q * 16, pk);
+          }
+          {
+            l = l * alpha + ((lsum[0] + lsum[1]) + (lsum[2] + lsum[3]));
+          }
+          tmem_st_wait();
+          if (j > 0 && __any_sync(0xffffffffu, rescale)) {
+  #pragma unroll
+            for (int q = 0; q < D / 16; ++q) {
+              uint32_t o[16];
+              tmem_ld16(t_o + q * 16, o);
+              tmem_ld_wait();
+  #pragma unroll
+              for (int i = 0; i < 16; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+              tmem_st16(t_o + q * 16, o);
+            }
+            tmem_st_wait();
+          }
+          tc_fence_before();
+          mbar_arrive(&sh.p_full[g]);
+        }
       }
       if (!ok) break;
       // epilogue: O / l into the Q tile of this item (no MMA reads it once o_full
@@ -1005,9 +1126,9 @@ attn_fwd_persist_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
   }
 }
 
-template <int D>
-cudaError_t launch_fwd_persist(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                               const CUtensorMap& to, FwdParams p, int BH, cudaStream_t stream) {
+template <int D, bool SPEC>
+cudaError_t launch_fwd_persist_cfg(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                                   const CUtensorMap& to, FwdParams p, int BH, cudaStream_t stream) {
   using C = FwdP<D>;
   static std::once_flag once[64];
   static int sm_count[64] = {0};
@@ -1016,11 +1137,19 @@ cudaError_t launch_fwd_persist(const CUtensorMap& tq, const CUtensorMap& tk, con
   if (e != cudaSuccess) return e;
   cudaError_t attr = cudaSuccess;
   std::call_once(once[dev & 63], [&] {
-    attr = cudaFuncSetAttribute(attn_fwd_persist_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    attr = cudaFuncSetAttribute(attn_fwd_persist_kernel<D, SPEC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 static_cast<int>(C::SMEM));
   });
   if (attr != cudaSuccess) return attr;
   if (sm_count[dev & 63] == 0) {
+    if (SPEC) {
+      // setmaxnreg.inc waits until registers are free: the split must fit in the
+      // registers the CTA is launched with, or the kernel would never proceed.
+      cudaFuncAttributes fa;
+      if ((e = cudaFuncGetAttributes(&fa, attn_fwd_persist_kernel<D, SPEC>)) != cudaSuccess) return e;
+      if (fa.numRegs * C::THREADS < C::NQ * 128 * C::REG_SOFTMAX + 128 * C::REG_OTHER)
+        return cudaErrorInvalidConfiguration;
+    }
     int c = 0;
     if ((e = cudaDeviceGetAttribute(&c, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
     sm_count[dev & 63] = c > 0 ? c : 1;
@@ -1031,10 +1160,20 @@ cudaError_t launch_fwd_persist(const CUtensorMap& tq, const CUtensorMap& tk, con
   const int items = static_cast<int>(items_ll);
   const int grid = items < sm_count[dev & 63] ? items : sm_count[dev & 63];
   prof_begin(kKindFwd, stream);
-  attn_fwd_persist_kernel<D><<<grid, C::THREADS, C::SMEM, stream>>>(tq, tk, tv, to, p, BH, items);
+  attn_fwd_persist_kernel<D, SPEC><<<grid, C::THREADS, C::SMEM, stream>>>(tq, tk, tv, to, p, BH, items);
   e = cudaGetLastError();
   prof_end(kKindFwd, stream);
   return e;
+}
+
+// Speculative exponentials pay off from the third key tile of an item on;
+// with at most two (m <= 256) every tile takes its maximum and no register
+// split is needed.
+template <int D>
+cudaError_t launch_fwd_persist(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                               const CUtensorMap& to, const FwdParams& p, int BH, cudaStream_t stream) {
+  if (p.m > 2 * FwdP<D>::BN) return launch_fwd_persist_cfg<D, true>(tq, tk, tv, to, p, BH, stream);
+  return launch_fwd_persist_cfg<D, false>(tq, tk, tv, to, p, BH, stream);
 }
 
 __global__ void exp2_probe_kernel(const float* x, float* y_poly, float* y_mufu, int n) {
