@@ -14,6 +14,11 @@ Functions:
   fwd(q, k, v, causal, scale, rows=None)   -> (O, lse)                 (eq. (1))
   bwd(q, k, v, dO, causal, scale)          -> (dQ, dK, dV, O, lse)     (derivative of eq. (1))
   bwd_rows(q, k, v, dO, causal, scale, qrows, krows) -> sampled rows of one head
+
+Optional masks on fwd / bwd / bwd_rows: ``kv_len`` (key padding, per
+sequence) and ``window=(wl, wr)`` (restricted self-attention, §4 and Table 1:
+key j visible to query i only if i - wl <= j <= i + wr; a negative side is
+open; None = no window).
 """
 from __future__ import annotations
 
@@ -56,11 +61,12 @@ def _load():
             lp = ctypes.POINTER(ctypes.c_long)
             L, I, D = ctypes.c_long, ctypes.c_int, ctypes.c_double
             lib.oracle_attn_weights.argtypes = [dp, dp, L, L, L, I, D, dp, dp]
-            lib.oracle_attn_fwd.argtypes = [dp, dp, dp, dp, dp, L, L, L, L, L, L, I, D, lp, L, lp]
+            lib.oracle_attn_fwd.argtypes = [dp, dp, dp, dp, dp, L, L, L, L, L, L, I, D, lp, L, lp,
+                                            L, L]
             lib.oracle_attn_bwd.argtypes = [dp, dp, dp, dp, dp, dp, dp, dp, dp,
-                                            L, L, L, L, L, L, I, D, lp]
+                                            L, L, L, L, L, L, I, D, lp, L, L]
             lib.oracle_attn_bwd_rows.argtypes = [dp, dp, dp, dp, L, L, L, L, I, D, lp, L, dp,
-                                                 lp, L, dp, dp, L]
+                                                 lp, L, dp, dp, L, L, L]
             lib.oracle_attn_bwd_rows.restype = ctypes.c_int
             for f in (lib.oracle_attn_weights, lib.oracle_attn_fwd, lib.oracle_attn_bwd):
                 f.restype = ctypes.c_int
@@ -117,6 +123,14 @@ def weights(q, k, causal: bool, scale: float):
     return S, P
 
 
+def _window(window):
+    """(wl, wr) as C longs; None -> (-1, -1), no window."""
+    if window is None:
+        return -1, -1
+    wl, wr = window
+    return int(wl), int(wr)
+
+
 def _lens(kv_len, B):
     """Per-sequence real key counts as a C long array (None: no key padding)."""
     if kv_len is None:
@@ -127,7 +141,8 @@ def _lens(kv_len, B):
     return a, a.ctypes.data_as(ctypes.POINTER(ctypes.c_long))
 
 
-def fwd(q, k, v, causal: bool, scale: float, rows: Optional[Sequence[int]] = None, kv_len=None):
+def fwd(q, k, v, causal: bool, scale: float, rows: Optional[Sequence[int]] = None, kv_len=None,
+        window=None):
     """O (fp64, shape of q with d_v) and lse ([..., n]) by eq. (1).
 
     With ``rows`` only those query rows are computed; the others are NaN.
@@ -150,12 +165,12 @@ def fwd(q, k, v, causal: bool, scale: float, rows: Optional[Sequence[int]] = Non
     _check(_load().oracle_attn_fwd(
         _ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(lse), B, h, n, m, dk, dv, int(causal),
         float(scale), None if r is None else r.ctypes.data_as(ctypes.POINTER(ctypes.c_long)),
-        nr, lens_p), "fwd")
+        nr, lens_p, *_window(window)), "fwd")
     shape_o = tuple(np.shape(q)[:-1]) + (dv,)
     return O.reshape(shape_o), lse.reshape(shape_o[:-1])
 
 
-def bwd(q, k, v, dO, causal: bool, scale: float, need=("dq", "dk", "dv"), kv_len=None):
+def bwd(q, k, v, dO, causal: bool, scale: float, need=("dq", "dk", "dv"), kv_len=None, window=None):
     """dQ, dK, dV of L = sum(dO * O) for O = Attention(q, k, v); also O and lse.
 
     ``kv_len``: per-sequence real key counts, as in ``fwd``.
@@ -173,7 +188,7 @@ def bwd(q, k, v, dO, causal: bool, scale: float, need=("dq", "dk", "dv"), kv_len
     lens, lens_p = _lens(kv_len, B)
     _check(_load().oracle_attn_bwd(_ptr(Q), _ptr(K), _ptr(V), _ptr(G), _ptr(dQ), _ptr(dK),
                                    _ptr(dV), _ptr(O), _ptr(lse), B, h, n, m, dk, dv,
-                                   int(causal), float(scale), lens_p), "bwd")
+                                   int(causal), float(scale), lens_p, *_window(window)), "bwd")
     lead_q = tuple(q.shape[:-2])
     lead_k = tuple(k.shape[:-2])
 
@@ -184,7 +199,7 @@ def bwd(q, k, v, dO, causal: bool, scale: float, need=("dq", "dk", "dv"), kv_len
             O.reshape(lead_q + (n, dv)), lse.reshape(lead_q + (n,)))
 
 
-def bwd_rows(q, k, v, dO, causal: bool, scale: float, qrows=(), krows=(), kv_len=None):
+def bwd_rows(q, k, v, dO, causal: bool, scale: float, qrows=(), krows=(), kv_len=None, window=None):
     """Sampled backward of ONE head: (dQ[qrows], dK[krows], dV[krows]), fp64.
 
     q, dO: [n, d]; k, v: [m, d]. Key rows cost a full forward of the head.
@@ -202,5 +217,5 @@ def bwd_rows(q, k, v, dO, causal: bool, scale: float, qrows=(), krows=(), kv_len
     _check(_load().oracle_attn_bwd_rows(
         _ptr(Q), _ptr(K), _ptr(V), _ptr(G), n, m, dk, dv, int(causal), float(scale),
         qr.ctypes.data_as(lp), qr.size, _ptr(dQ), kr.ctypes.data_as(lp), kr.size, _ptr(dK),
-        _ptr(dV), -1 if kv_len is None else int(kv_len)), "bwd_rows")
+        _ptr(dV), -1 if kv_len is None else int(kv_len), *_window(window)), "bwd_rows")
     return dQ[: qr.size], dK[: kr.size], dV[: kr.size]

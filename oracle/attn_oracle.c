@@ -41,6 +41,12 @@
  *     masked like illegal connections (weight exactly 0, no gradient). A row
  *     that sees no key at all (kv_len[b] = 0) has O = 0, lse = -inf and zero
  *     gradients (the empty sum).
+ *   - restricted self-attention (§4, Table 1: a neighbourhood of size r
+ *     around the output position): key j is visible to query i only if
+ *     i - wl <= j <= i + wr; wl = wr = (r - 1) / 2 for an odd r centred on i.
+ *     A negative wl or wr leaves that side open. The window combines with the
+ *     causal mask and with key padding (all conditions must hold); a row left
+ *     with no visible key is the empty sum, as above.
  *
  * Layout: every tensor is a contiguous row-major [B, h, S, d] array of
  * doubles (lse is [B, h, n]). Built with -O2 -ffp-contract=off and without
@@ -72,6 +78,17 @@ static long visible_padded(long i, long m, int causal, long mb) {
     return v < mb ? v : mb;
 }
 
+/* The keys [lo, hi) visible to query i: the causal and padding limit above,
+ * narrowed to the window i - wl <= j <= i + wr (a negative side is open).
+ * hi <= lo means no key is visible. */
+static void key_range(long i, long m, int causal, long mb, long wl, long wr,
+                      long *lo, long *hi) {
+    long h = visible_padded(i, m, causal, mb);
+    if (wr >= 0 && i + wr + 1 < h) h = i + wr + 1;
+    *lo = (wl >= 0 && i - wl > 0) ? i - wl : 0;
+    *hi = h;
+}
+
 /* Real keys of head bh: kv_len[b] for its sequence b = bh / h, clamped to
  * [0, m]; all m without a length array. */
 static long head_keys(const long *kv_len, long bh, long h, long m) {
@@ -83,9 +100,9 @@ static long head_keys(const long *kv_len, long bh, long h, long m) {
 /* Step MatMul + Scale + Mask of Figure 2 for one query row:
  * s_j = scale * sum_c q_c k_jc for visible j, and -inf for masked j. */
 static void score_row(const double *qi, const double *K, long m, long dk,
-                      double scale, long visible, double *s) {
+                      double scale, long lo, long hi, double *s) {
     for (long j = 0; j < m; ++j) {
-        if (j >= visible) {
+        if (j < lo || j >= hi) {
             s[j] = -INFINITY;
             continue;
         }
@@ -144,7 +161,7 @@ int oracle_attn_weights(const double *Q, const double *K, long n, long m,
     double *row = (double *)malloc(sizeof(double) * (size_t)m);
     if (!row) return ORACLE_ERR_NOMEM;
     for (long i = 0; i < n; ++i) {
-        score_row(Q + i * dk, K, m, dk, scale, visible_keys(i, m, causal), row);
+        score_row(Q + i * dk, K, m, dk, scale, 0, visible_keys(i, m, causal), row);
         if (s_out) memcpy(s_out + i * m, row, sizeof(double) * (size_t)m);
         softmax_row(row, m);
         if (p_out) memcpy(p_out + i * m, row, sizeof(double) * (size_t)m);
@@ -162,7 +179,7 @@ int oracle_attn_weights(const double *Q, const double *K, long n, long m,
 int oracle_attn_fwd(const double *q, const double *k, const double *v,
                     double *o, double *lse, long B, long h, long n, long m,
                     long dk, long dv, int causal, double scale,
-                    const long *rows, long nrows, const long *kv_len) {
+                    const long *rows, long nrows, const long *kv_len, long wl, long wr) {
     if (check_dims(B, h, n, m, dk, dv) != ORACLE_OK) return ORACLE_ERR_ARG;
     const long heads = B * h;
     const long R = rows ? nrows : n;
@@ -185,8 +202,9 @@ int oracle_attn_fwd(const double *q, const double *k, const double *v,
                 const double *Q = q + bh * n * dk;
                 const double *K = k + bh * m * dk;
                 const double *V = v + bh * m * dv;
-                score_row(Q + i * dk, K, m, dk, scale,
-                          visible_padded(i, m, causal, head_keys(kv_len, bh, h, m)), row);
+                long lo, hi;
+                key_range(i, m, causal, head_keys(kv_len, bh, h, m), wl, wr, &lo, &hi);
+                score_row(Q + i * dk, K, m, dk, scale, lo, hi, row);
                 const double l = softmax_row(row, m);
                 weighted_sum(row, V, m, dv, o + (bh * n + i) * dv);
                 if (lse) lse[bh * n + i] = l;
@@ -204,10 +222,12 @@ int oracle_attn_fwd(const double *q, const double *k, const double *v,
  * row (m doubles) and oi (dv doubles) are scratch.
  */
 static void bwd_query_row(const double *Q, const double *K, const double *V,
-                          const double *dOi, long i, long m, long mb, long dk, long dv,
-                          int causal, double scale, double *row, double *oi,
-                          double *lse_i, double *D_i, double *dqi) {
-    score_row(Q + i * dk, K, m, dk, scale, visible_padded(i, m, causal, mb), row);
+                          const double *dOi, long i, long m, long mb, long wl, long wr,
+                          long dk, long dv, int causal, double scale, double *row,
+                          double *oi, double *lse_i, double *D_i, double *dqi) {
+    long lo, hi;
+    key_range(i, m, causal, mb, wl, wr, &lo, &hi);
+    score_row(Q + i * dk, K, m, dk, scale, lo, hi, row);
     const double l = softmax_row(row, m);
     weighted_sum(row, V, m, dv, oi);
     double Di = 0.0;
@@ -237,12 +257,14 @@ static void bwd_query_row(const double *Q, const double *K, const double *V,
  */
 static void bwd_key_row(const double *Q, const double *kj, const double *vj,
                         const double *dO, const double *lse, const double *D,
-                        long j, long n, long m, long mb, long dk, long dv, int causal,
-                        double scale, double *dkj, double *dvj) {
+                        long j, long n, long m, long mb, long wl, long wr, long dk, long dv,
+                        int causal, double scale, double *dkj, double *dvj) {
     if (dkj) for (long c = 0; c < dk; ++c) dkj[c] = 0.0;
     if (dvj) for (long c = 0; c < dv; ++c) dvj[c] = 0.0;
     for (long i = 0; i < n; ++i) {
-        if (j >= visible_padded(i, m, causal, mb)) continue; /* masked: P_ij = 0 */
+        long lo, hi;
+        key_range(i, m, causal, mb, wl, wr, &lo, &hi);
+        if (j < lo || j >= hi) continue; /* masked: P_ij = 0 */
         const double *qi = Q + i * dk;
         const double *dOi = dO + i * dv;
         double dot = 0.0;
@@ -274,7 +296,7 @@ int oracle_attn_bwd(const double *q, const double *k, const double *v,
                     const double *dO, double *dq, double *dk_out,
                     double *dv_out, double *o_out, double *lse_out, long B,
                     long h, long n, long m, long dk, long dv, int causal,
-                    double scale, const long *kv_len) {
+                    double scale, const long *kv_len, long wl, long wr) {
     if (check_dims(B, h, n, m, dk, dv) != ORACLE_OK) return ORACLE_ERR_ARG;
     const long heads = B * h;
     double *lse = (double *)malloc(sizeof(double) * (size_t)(heads * n + 1));
@@ -298,8 +320,8 @@ int oracle_attn_bwd(const double *q, const double *k, const double *v,
             for (long i = 0; i < n; ++i) {
                 if (!row || !oi) continue;
                 bwd_query_row(q + bh * n * dk, k + bh * m * dk, v + bh * m * dv,
-                              dO + (bh * n + i) * dv, i, m, head_keys(kv_len, bh, h, m), dk, dv,
-                              causal, scale,
+                              dO + (bh * n + i) * dv, i, m, head_keys(kv_len, bh, h, m), wl, wr,
+                              dk, dv, causal, scale,
                               row, oi, &lse[bh * n + i], &D[bh * n + i],
                               dq ? dq + (bh * n + i) * dk : NULL);
                 if (o_out) memcpy(o_out + (bh * n + i) * dv, oi, sizeof(double) * (size_t)dv);
@@ -313,7 +335,7 @@ int oracle_attn_bwd(const double *q, const double *k, const double *v,
                 for (long j = 0; j < m; ++j) {
                     bwd_key_row(q + bh * n * dk, k + (bh * m + j) * dk, v + (bh * m + j) * dv,
                                 dO + bh * n * dv, lse + bh * n, D + bh * n, j, n, m,
-                                head_keys(kv_len, bh, h, m), dk, dv,
+                                head_keys(kv_len, bh, h, m), wl, wr, dk, dv,
                                 causal, scale, dk_out ? dk_out + (bh * m + j) * dk : NULL,
                                 dv_out ? dv_out + (bh * m + j) * dv : NULL);
                 }
@@ -338,7 +360,7 @@ int oracle_attn_bwd_rows(const double *q, const double *k, const double *v,
                          const double *dO, long n, long m, long dk, long dv,
                          int causal, double scale, const long *qrows, long nq,
                          double *dq_out, const long *krows, long nk,
-                         double *dk_out, double *dv_out, long kv_len) {
+                         double *dk_out, double *dv_out, long kv_len, long wl, long wr) {
     if (check_dims(1, 1, n, m, dk, dv) != ORACLE_OK || nq < 0 || nk < 0) return ORACLE_ERR_ARG;
     for (long r = 0; r < nq; ++r)
         if (qrows[r] < 0 || qrows[r] >= n) return ORACLE_ERR_ARG;
@@ -367,20 +389,20 @@ int oracle_attn_bwd_rows(const double *q, const double *k, const double *v,
             if (!row || !oi) continue;
             double l, Di;
             const long i = qrows[r];
-            bwd_query_row(q, k, v, dO + i * dv, i, m, mb, dk, dv, causal, scale, row, oi, &l, &Di,
-                          dq_out + r * dk);
+            bwd_query_row(q, k, v, dO + i * dv, i, m, mb, wl, wr, dk, dv, causal, scale, row, oi,
+                          &l, &Di, dq_out + r * dk);
         }
 #pragma omp for schedule(dynamic, 16)
         for (long i = 0; i < nall; ++i) {
             if (!row || !oi) continue;
-            bwd_query_row(q, k, v, dO + i * dv, i, m, mb, dk, dv, causal, scale, row, oi, &lse[i],
-                          &D[i], NULL);
+            bwd_query_row(q, k, v, dO + i * dv, i, m, mb, wl, wr, dk, dv, causal, scale, row, oi,
+                          &lse[i], &D[i], NULL);
         }
 #pragma omp for schedule(dynamic, 1)
         for (long r = 0; r < nk; ++r) {
             const long j = krows[r];
-            bwd_key_row(q, k + j * dk, v + j * dv, dO, lse, D, j, n, m, mb, dk, dv, causal, scale,
-                        dk_out + r * dk, dv_out + r * dv);
+            bwd_key_row(q, k + j * dk, v + j * dv, dO, lse, D, j, n, m, mb, wl, wr, dk, dv, causal,
+                        scale, dk_out + r * dk, dv_out + r * dv);
         }
         free(row);
         free(oi);

@@ -26,8 +26,13 @@ MUTATIONS = {
                    "for (long c = 0; c < dv; ++c) dvj[c] += P * dOi[c] * (1.0 + 1e-3 * c);"),
     "dQ_transposed_operand": ("for (long c = 0; c < dk; ++c) dqi[c] += dS * kj[c];",
                               "for (long c = 0; c < dk; ++c) dqi[c] += dS * kj[dk - 1 - c];"),
-    "causal_mask_in_bwd_off_by_one": ("if (j >= visible_padded(i, m, causal, mb)) continue;",
-                                      "if (j > visible_padded(i, m, causal, mb)) continue;"),
+    "causal_mask_in_bwd_off_by_one": ("if (j < lo || j >= hi) continue;", "if (j < lo || j > hi) continue;"),
+    "window_right_off_by_one": ("if (wr >= 0 && i + wr + 1 < h) h = i + wr + 1;",
+                                "if (wr >= 0 && i + wr < h) h = i + wr;"),
+    "window_left_off_by_one": ("*lo = (wl >= 0 && i - wl > 0) ? i - wl : 0;",
+                               "*lo = (wl >= 0 && i - wl + 1 > 0) ? i - wl + 1 : 0;"),
+    "window_sides_swapped": ("*lo = (wl >= 0 && i - wl > 0) ? i - wl : 0;",
+                             "*lo = (wr >= 0 && i - wr > 0) ? i - wr : 0;"),
     "key_length_per_head": ("const long mb = kv_len[bh / h];", "const long mb = kv_len[bh % h];"),
     "key_padding_off_by_one": ("return v < mb ? v : mb;", "return v < mb + 1 ? v : mb + 1;"),
     "empty_row_not_zero": ("for (long j = 0; j < m; ++j) s[j] = 0.0;\n        return -INFINITY;",
@@ -53,6 +58,9 @@ PIN_TESTS = [
     (pins.test_key_padding_equals_truncation, {"causal": True}),
     (pins.test_key_padding_against_torch_masked_library, {}),
     (pins.test_key_padding_empty_sequence_is_the_empty_sum, {}),
+    (pins.test_window_of_one_position_returns_own_value, {}),
+    (pins.test_window_against_torch_masked_library, {"wl": 2, "wr": 3, "causal": False, "lens": None}),
+    (pins.test_window_rows_without_keys_are_the_empty_sum, {}),
 ]
 
 

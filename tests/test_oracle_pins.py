@@ -387,3 +387,149 @@ def test_key_padding_empty_sequence_is_the_empty_sum():
     np.testing.assert_array_equal(sq, fq[0, 0][[0, 6]])
     np.testing.assert_array_equal(sk, fk[0, 0][[0, 3, 8]])
     np.testing.assert_array_equal(sv, fv[0, 0][[0, 3, 8]])
+
+
+# ---------------------------------------------------------------- restricted self-attention (§4, Table 1)
+
+def _window_case(seed=21, B=2, h=2, n=11, m=11, d=6):
+    rng = np.random.default_rng(seed)
+    q = rng.standard_normal((B, h, n, d))
+    k = rng.standard_normal((B, h, m, d))
+    v = rng.standard_normal((B, h, m, d))
+    dO = rng.standard_normal((B, h, n, d))
+    return q, k, v, dO
+
+
+def _band(n, m, wl, wr, causal=False, lens=None, B=1):
+    """Boolean [B, n, m] mask written out from the definition: i - wl <= j <= i + wr."""
+    i = np.arange(n)[:, None]
+    j = np.arange(m)[None, :]
+    keep = np.ones((n, m), dtype=bool)
+    if wl >= 0:
+        keep &= j >= i - wl
+    if wr >= 0:
+        keep &= j <= i + wr
+    if causal:
+        keep &= j <= i
+    keep = np.broadcast_to(keep, (B, n, m)).copy()
+    if lens is not None:
+        for b, L in enumerate(lens):
+            keep[b, :, L:] = False
+    return keep
+
+
+def test_window_wider_than_the_sequence_is_no_window():
+    """A window reaching past both ends changes nothing, bit for bit."""
+    q, k, v, dO = _window_case()
+    for causal in (False, True):
+        a = oracle.fwd(q, k, v, causal, 0.5)
+        b = oracle.fwd(q, k, v, causal, 0.5, window=(11, 11))
+        c = oracle.fwd(q, k, v, causal, 0.5, window=(-1, 40))
+        for x in (b, c):
+            np.testing.assert_array_equal(a[0], x[0])
+            np.testing.assert_array_equal(a[1], x[1])
+        ga = oracle.bwd(q, k, v, dO, causal, 0.5)
+        gb = oracle.bwd(q, k, v, dO, causal, 0.5, window=(20, 20))
+        for x, y in zip(ga[:3], gb[:3]):
+            np.testing.assert_array_equal(x, y)
+
+
+def test_window_of_one_position_returns_own_value():
+    """r = 1 (wl = wr = 0): query i sees only key i, so O_i = v_i, lse_i = s_ii,
+    dQ = dK = 0 (a single weight of 1 has zero derivative) and dV_i = dO_i."""
+    q, k, v, dO = _window_case(seed=5)
+    scale = 0.8
+    O, lse = oracle.fwd(q, k, v, False, scale, window=(0, 0))
+    np.testing.assert_allclose(O, v, rtol=0, atol=1e-15)
+    np.testing.assert_allclose(lse, scale * (q * k).sum(-1), rtol=1e-14, atol=1e-14)
+    dQ, dK, dV, _, _ = oracle.bwd(q, k, v, dO, False, scale, window=(0, 0))
+    np.testing.assert_allclose(dQ, 0.0, atol=1e-14)
+    np.testing.assert_allclose(dK, 0.0, atol=1e-14)
+    np.testing.assert_allclose(dV, dO, rtol=1e-14, atol=1e-14)
+
+
+@pytest.mark.parametrize("wl,wr,causal,lens", [(2, 3, False, None), (4, -1, False, None), (-1, 1, False, None),
+                                               (3, 3, True, None), (2, 5, False, [7, 11])])
+def test_window_against_torch_masked_library(wl, wr, causal, lens):
+    """torch CPU fp64 scaled_dot_product_attention (+ autograd) with the band written
+    out as a boolean mask, asymmetric windows, one open side, causal, key padding."""
+    F = torch.nn.functional
+    q, k, v, dO = (torch.from_numpy(a).requires_grad_(i < 3) for i, a in enumerate(_window_case(seed=wl + 7)))
+    B, h, n, m = q.shape[0], q.shape[1], q.shape[2], k.shape[2]
+    mask = torch.from_numpy(_band(n, m, wl, wr, causal, lens, B))[:, None]
+    O_t = F.scaled_dot_product_attention(q, k, v, attn_mask=mask, scale=0.6)
+    O_t.backward(dO)
+    O, _ = oracle.fwd(q.detach(), k.detach(), v.detach(), causal, 0.6, kv_len=lens, window=(wl, wr))
+    dQ, dK, dV, _, _ = oracle.bwd(q.detach(), k.detach(), v.detach(), dO, causal, 0.6, kv_len=lens,
+                                  window=(wl, wr))
+    np.testing.assert_allclose(O, O_t.detach().numpy(), rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(dQ, q.grad.numpy(), rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(dK, k.grad.numpy(), rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(dV, v.grad.numpy(), rtol=1e-10, atol=1e-12)
+
+
+def test_causal_window_is_the_left_window():
+    """The causal mask is the window's right side at 0: (causal, wl, any wr) = (not causal, wl, 0)."""
+    q, k, v, dO = _window_case(seed=8)
+    a = oracle.bwd(q, k, v, dO, True, 0.4, window=(3, 6))
+    b = oracle.bwd(q, k, v, dO, False, 0.4, window=(3, 0))
+    for x, y in zip(a, b):
+        np.testing.assert_array_equal(x, y)
+
+
+def test_window_rows_without_keys_are_the_empty_sum():
+    """n > m: rows whose window lies wholly past the last key see nothing (O = 0,
+    lse = -inf) and pass no gradient; the other rows are untouched by them."""
+    q, k, v, dO = _window_case(seed=4, n=14, m=6)
+    wl, wr = 2, 1
+    O, lse = oracle.fwd(q, k, v, False, 0.5, window=(wl, wr))
+    empty = np.arange(14) - wl > 5
+    assert (O[:, :, empty] == 0).all() and np.isneginf(lse[:, :, empty]).all()
+    assert np.isfinite(lse[:, :, ~empty]).all()
+    dQ, dK, dV, _, _ = oracle.bwd(q, k, v, dO, False, 0.5, window=(wl, wr))
+    assert (dQ[:, :, empty] == 0).all()
+    dO2 = dO.copy()
+    dO2[:, :, empty] = 5.0  # upstream gradient of the empty rows cannot reach K or V
+    _, dK2, dV2, _, _ = oracle.bwd(q, k, v, dO2, False, 0.5, window=(wl, wr))
+    np.testing.assert_array_equal(dK, dK2)
+    np.testing.assert_array_equal(dV, dV2)
+
+
+def test_window_backward_matches_central_differences():
+    """Brute force for the banded backward on a tiny head."""
+    rng = np.random.default_rng(77)
+    n, m, dk, dv = 6, 7, 3, 2
+    q = rng.standard_normal((1, 1, n, dk))
+    k = rng.standard_normal((1, 1, m, dk))
+    v = rng.standard_normal((1, 1, m, dv))
+    dO = rng.standard_normal((1, 1, n, dv))
+    win, scale = (1, 2), 0.9
+    dQ, dK, dV, _, _ = oracle.bwd(q, k, v, dO, False, scale, window=win)
+
+    def loss(qq, kk, vv):
+        O, _ = oracle.fwd(qq, kk, vv, False, scale, window=win)
+        return float((dO * O).sum())
+
+    eps = 1e-6
+    for name, x, g in (("q", q, dQ), ("k", k, dK), ("v", v, dV)):
+        num = np.zeros_like(x)
+        for idx in np.ndindex(x.shape):
+            xp, xm = x.copy(), x.copy()
+            xp[idx] += eps
+            xm[idx] -= eps
+            a = {"q": q, "k": k, "v": v}
+            b = dict(a)
+            a[name], b[name] = xp, xm
+            num[idx] = (loss(a["q"], a["k"], a["v"]) - loss(b["q"], b["k"], b["v"])) / (2 * eps)
+        assert np.abs(num - g).max() <= 1e-8 * max(1.0, np.abs(g).max()), name
+
+
+def test_window_sampled_rows_match_full_backward():
+    q, k, v, dO = _window_case(seed=12, B=1, h=1, n=13, m=13)
+    win = (2, 4)
+    sq, sk, sv = oracle.bwd_rows(q[0, 0], k[0, 0], v[0, 0], dO[0, 0], False, 0.5, [0, 7, 12], [1, 6, 12],
+                                 kv_len=10, window=win)
+    fq, fk, fv, _, _ = oracle.bwd(q, k, v, dO, False, 0.5, kv_len=[10], window=win)
+    np.testing.assert_array_equal(sq, fq[0, 0][[0, 7, 12]])
+    np.testing.assert_array_equal(sk, fk[0, 0][[1, 6, 12]])
+    np.testing.assert_array_equal(sv, fv[0, 0][[1, 6, 12]])
