@@ -146,6 +146,31 @@ int attn_bwd_varlen(const void* q, const void* k, const void* v, const void* o, 
                     size_t workspace_bytes, attn_stream_t stream);
 
 /*
+ * Restricted self-attention ("Attention Is All You Need" §4 and Table 1: each
+ * output position attends to a neighbourhood of size r centred on it, cost
+ * O(r n d)), together with the other masks. Key j is visible to query i iff
+ *   i - window_left <= j <= i + window_right   (a negative side is open),
+ *   j <= i                                     when causal = 1,
+ *   j < kv_len[b]                              when kv_len is not NULL.
+ * A centred neighbourhood of odd size r is window_left = window_right =
+ * (r - 1) / 2; causal local attention is causal = 1 with window_left = w.
+ * Positions are the row indices of Q and K (top-left aligned, as for the
+ * causal mask). A row left without a visible key is the empty sum: O = 0,
+ * lse = -inf, zero gradients. Key tiles that no row of a query tile sees are
+ * neither loaded nor multiplied, in the forward and the backward. With both
+ * window sides negative the calls equal attn_fwd_varlen / attn_bwd_varlen.
+ * Everything else (arguments, layout, ownership, workspace size, errors) is
+ * as in attn_fwd / attn_bwd and the key-padding variants.
+ */
+int attn_fwd_masked(const void* q, const void* k, const void* v, void* o, float* lse,
+                    const int* kv_len, int B, int h, int n, int m, int d_k, int d_v, int causal,
+                    int window_left, int window_right, float scale, attn_stream_t stream);
+int attn_bwd_masked(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                    const void* dO, void* dq, void* dk, void* dv, const int* kv_len, int B, int h,
+                    int n, int m, int d_k, int d_v, int causal, int window_left, int window_right,
+                    float scale, void* workspace, size_t workspace_bytes, attn_stream_t stream);
+
+/*
  * Synchronises `stream`, then reports and clears the device-side error word of
  * the current device: ATTN_OK, or ATTN_ERR_TIMEOUT if any kernel's watchdog
  * fired since the last call. ATTN_ERR_CUDA if the synchronisation failed.

@@ -62,35 +62,37 @@ def ulp_ratio(gpu, ref) -> float:
     return float((np.abs(g - r) / bf16_ulp(r)).max())
 
 
-def d_term_bounds(q, k, v, dO, causal, scale, qrows=None, krows=None, kv_len=None):
+def d_term_bounds(q, k, v, dO, causal, scale, qrows=None, krows=None, kv_len=None, window=None):
     """Bounds on |dQ| and |dK| errors caused by forming D_i from the bf16 O (see module doc).
 
     Full heads ([B,h,S,d] tensors) when qrows/krows are None; otherwise ONE head
     ([S,d] tensors) and the bounds of the listed query / key rows; kv_len is
-    then that head's real key count (key padding).
+    then that head's real key count (key padding). kv_len (per sequence, full
+    heads) and window (left, right) are the masks of the call checked.
     """
     import oracle
     u = 2.0 ** -8
     qa, ka, va, da = to64(q), to64(k), to64(v), to64(dO)
     if qrows is None:
-        O, _ = oracle.fwd(qa, ka, va, causal, scale)
-        PK, _ = oracle.fwd(qa, ka, np.abs(ka), causal, scale)
+        O, _ = oracle.fwd(qa, ka, va, causal, scale, kv_len=kv_len, window=window)
+        PK, _ = oracle.fwd(qa, ka, np.abs(ka), causal, scale, kv_len=kv_len, window=window)
         dD = u * (np.abs(da) * np.abs(O)).sum(axis=-1)
         bq = abs(scale) * dD[..., None] * PK
         # dK bound: P^T (|dD| |q|), i.e. the dV of a backward whose upstream gradient is |dD| |q|
-        _, _, PtdDq, _, _ = oracle.bwd(qa, ka, ka, dD[..., None] * np.abs(qa), causal, scale)
+        _, _, PtdDq, _, _ = oracle.bwd(qa, ka, ka, dD[..., None] * np.abs(qa), causal, scale, kv_len=kv_len,
+                                       window=window)
         return bq, abs(scale) * PtdDq
     n = qa.shape[0]
     all_rows = list(range(n))
     lens = None if kv_len is None else [kv_len]
-    O, _ = oracle.fwd(qa, ka, va, causal, scale, rows=all_rows, kv_len=lens)
+    O, _ = oracle.fwd(qa, ka, va, causal, scale, rows=all_rows, kv_len=lens, window=window)
     dD = u * (np.abs(da) * np.abs(O)).sum(axis=-1)
-    PK, _ = oracle.fwd(qa, ka, np.abs(ka), causal, scale, rows=list(qrows), kv_len=lens)
+    PK, _ = oracle.fwd(qa, ka, np.abs(ka), causal, scale, rows=list(qrows), kv_len=lens, window=window)
     bq = abs(scale) * dD[list(qrows), None] * PK[list(qrows)]
     bk = None
     if krows is not None and len(krows):
         _, _, PtdDq = oracle.bwd_rows(qa, ka, ka, dD[:, None] * np.abs(qa), causal, scale, [], krows,
-                                      kv_len=kv_len)
+                                      kv_len=kv_len, window=window)
         bk = abs(scale) * PtdDq
     return bq, bk
 

@@ -29,7 +29,9 @@ __all__ = [
     "attn_debug_exp2", "attn_bwd_noalloc", "EXPORTED_SYMBOLS", "KERNEL_KINDS",
 ]
 # attn_fwd / attn_bwd take an optional ``kv_len`` (int32 CUDA tensor [B]: real
-# keys per sequence) and then call attn_fwd_varlen / attn_bwd_varlen.
+# keys per sequence) and an optional ``window`` = (left, right) (restricted
+# self-attention: query i sees keys i - left .. i + right, None or a negative
+# side = open); with either they call attn_fwd_masked / attn_bwd_masked.
 
 ATTN_OK = 0
 ATTN_ERR_INVALID_ARG = 1
@@ -42,7 +44,7 @@ EXPORTED_SYMBOLS = (
     "attn_fwd", "attn_bwd", "attn_bwd_workspace_bytes", "attn_get_device_status",
     "attn_status_string", "attn_set_watchdog_ns", "attn_debug_inject", "attn_profile_enable",
     "attn_profile_read", "attn_debug_exp2", "attn_bwd_noalloc", "attn_fwd_varlen",
-    "attn_bwd_varlen",
+    "attn_bwd_varlen", "attn_fwd_masked", "attn_bwd_masked",
 )
 
 # Kernel kinds of attn_profile_read.
@@ -87,6 +89,11 @@ def load_library():
         lib.attn_bwd_varlen.argtypes = [vp, vp, vp, vp, fp, vp, vp, vp, vp, vp, I, I, I, I, I, I, I, F,
                                         vp, SZ, vp]
         lib.attn_bwd_varlen.restype = I
+        lib.attn_fwd_masked.argtypes = [vp, vp, vp, vp, fp, vp, I, I, I, I, I, I, I, I, I, F, vp]
+        lib.attn_fwd_masked.restype = I
+        lib.attn_bwd_masked.argtypes = [vp, vp, vp, vp, fp, vp, vp, vp, vp, vp, I, I, I, I, I, I, I, I, I,
+                                        F, vp, SZ, vp]
+        lib.attn_bwd_masked.restype = I
         lib.attn_bwd_workspace_bytes.argtypes = [I, I, I, I, I, I, I]
         lib.attn_bwd_workspace_bytes.restype = SZ
         lib.attn_get_device_status.argtypes = [vp]
@@ -152,12 +159,26 @@ def _check_lengths(kv_len, B, device):
     return _vptr(kv_len)
 
 
+def _window(window):
+    """(left, right) as C ints, -1 for an open side; None when there is no window."""
+    if window is None:
+        return None
+    wl, wr = window
+    wl = -1 if wl is None or int(wl) < 0 else int(wl)
+    wr = -1 if wr is None or int(wr) < 0 else int(wr)
+    if wl > 0x7fffffff or wr > 0x7fffffff:
+        raise ValueError("window sides must fit in int32")
+    return None if (wl < 0 and wr < 0) else (wl, wr)
+
+
 def attn_fwd(q, k, v, causal: bool = False, scale: Optional[float] = None, out=None, lse=None,
-             need_lse: bool = True, stream=None, kv_len=None) -> Tuple["torch.Tensor", Optional["torch.Tensor"]]:
+             need_lse: bool = True, stream=None, kv_len=None,
+             window=None) -> Tuple["torch.Tensor", Optional["torch.Tensor"]]:
     """O, lse = attention(q, k, v) on the GPU. q [B,h,n,d], k/v [B,h,m,d], bf16.
 
     kv_len (optional int32 CUDA tensor [B]): real keys per sequence; the keys
     past them are padding and masked.
+    window (optional (left, right)): query i sees only keys i - left .. i + right.
     """
     import torch
     lib = load_library()
@@ -178,7 +199,12 @@ def attn_fwd(q, k, v, causal: bool = False, scale: Optional[float] = None, out=N
     if lse is not None:
         _check_tensor("lse", lse, (B, h, n), torch.float32)
     lens = _check_lengths(kv_len, B, q.device)
-    if lens is None:
+    win = _window(window)
+    if win is not None:
+        st = lib.attn_fwd_masked(_vptr(q), _vptr(k), _vptr(v), _vptr(out), _fptr(lse), lens, B, h, n,
+                                 m, dk, dv, int(bool(causal)), win[0], win[1], float(scale),
+                                 _stream_handle(stream))
+    elif lens is None:
         st = lib.attn_fwd(_vptr(q), _vptr(k), _vptr(v), _vptr(out), _fptr(lse), B, h, n, m, dk, dv,
                           int(bool(causal)), float(scale), _stream_handle(stream))
     else:
@@ -194,8 +220,9 @@ def attn_bwd_workspace_bytes(B, h, n, m, d_k, d_v, causal=False) -> int:
 
 
 def attn_bwd(q, k, v, o, lse, dO, causal: bool = False, scale: Optional[float] = None,
-             dq=None, dk=None, dv=None, workspace=None, stream=None, kv_len=None):
-    """dQ, dK, dV of sum(dO * O) for O = attention(q, k, v), from attn_fwd's O and lse."""
+             dq=None, dk=None, dv=None, workspace=None, stream=None, kv_len=None, window=None):
+    """dQ, dK, dV of sum(dO * O) for O = attention(q, k, v), from attn_fwd's O and lse
+    (the same causal, kv_len and window as the forward)."""
     import torch
     lib = load_library()
     B, h, n, d_k = q.shape
@@ -221,7 +248,13 @@ def attn_bwd(q, k, v, o, lse, dO, causal: bool = False, scale: Optional[float] =
     ws_ptr = _vptr(workspace) if workspace is not None else None
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     lens = _check_lengths(kv_len, B, q.device)
-    if lens is None:
+    win = _window(window)
+    if win is not None:
+        st = lib.attn_bwd_masked(_vptr(q), _vptr(k), _vptr(v), _vptr(o), _fptr(lse), _vptr(dO),
+                                 _vptr(dq), _vptr(dk), _vptr(dv), lens, B, h, n, m, d_k, d_v,
+                                 int(bool(causal)), win[0], win[1], float(scale), ws_ptr, ws_bytes,
+                                 _stream_handle(stream))
+    elif lens is None:
         st = lib.attn_bwd(_vptr(q), _vptr(k), _vptr(v), _vptr(o), _fptr(lse), _vptr(dO), _vptr(dq),
                           _vptr(dk), _vptr(dv), B, h, n, m, d_k, d_v, int(bool(causal)), float(scale),
                           ws_ptr, ws_bytes, _stream_handle(stream))

@@ -234,10 +234,17 @@ int attn_debug_inject(int mode) {
   return ATTN_OK;
 }
 
-// attn_fwd / attn_fwd_varlen: kv_len (device, B ints, or nullptr) are the real
-// keys of each sequence; the kernels clamp them to [0, m].
+// A window side: negative or reaching past every position is open (-1).
+static int window_side(int w, int n, int m) {
+  if (w < 0) return -1;
+  return (static_cast<long long>(w) >= static_cast<long long>(n) + m) ? -1 : w;
+}
+
+// attn_fwd / attn_fwd_varlen / attn_fwd_masked: kv_len (device, B ints, or
+// nullptr) are the real keys of each sequence, which the kernels clamp to
+// [0, m]; wl / wr the restricted-attention window (-1: open side).
 static int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, const int* kv_len,
-                    int B, int h, int n, int m, int d_k, int d_v, int causal, float scale,
+                    int B, int h, int n, int m, int d_k, int d_v, int causal, int wl, int wr, float scale,
                     attn_stream_t stream) {
   bool empty = false;
   int st = check_common(B, h, n, m, d_k, d_v, scale, &empty);
@@ -248,7 +255,9 @@ static int fwd_impl(const void* q, const void* k, const void* v, void* o, float*
   if (lse != nullptr && (reinterpret_cast<uintptr_t>(lse) & 3u) != 0) return ATTN_ERR_INVALID_ARG;
   const long long BH = static_cast<long long>(B) * h;
   CUtensorMap tq, tk, tv, to;
-  const int bn = attn::fwd_key_tile(d_k, n, m, causal ? 1 : 0);
+  wl = window_side(wl, n, m);
+  wr = window_side(wr, n, m);
+  const int bn = attn::fwd_key_tile(d_k, n, m, causal ? 1 : 0, wl >= 0 || wr >= 0);
   if (!make_tile_map(&tq, q, BH, n, d_k) || !make_tile_map(&tk, k, BH, m, d_k, bn) ||
       !make_tile_map(&tv, v, BH, m, d_v, bn) || !make_tile_map(&to, o, BH, n, d_v))
     return ATTN_ERR_CUDA;
@@ -266,6 +275,8 @@ static int fwd_impl(const void* q, const void* k, const void* v, void* o, float*
   p.inject = g_inject.exchange(0);
   p.kv_len = kv_len;
   p.h = h;
+  p.wl = wl;
+  p.wr = wr;
   p.wd.status = status;
   p.wd.budget_ns = g_watchdog_ns.load();
   cudaError_t e = attn::launch_fwd(d_k, tq, tk, tv, to, p, static_cast<int>(BH),
@@ -287,8 +298,8 @@ size_t attn_bwd_workspace_bytes(int B, int h, int n, int m, int d_k, int d_v, in
 // Short query sequences: the whole-head kernel (no scratch, one launch).
 static int bwd_head_path(const void* q, const void* k, const void* v, const void* o, const float* lse,
                          const void* dO, void* dq, void* dk, void* dv, const int* kv_len, long long BH,
-                         int h, int n, int m, int d, int causal, float scale, uint32_t* status,
-                         cudaStream_t stream) {
+                         int h, int n, int m, int d, int causal, int wl, int wr, float scale,
+                         uint32_t* status, cudaStream_t stream) {
   CUtensorMap tq, tk, tv, tdo, tdq, tdk, tdv;
   if (!make_tile_map(&tq, q, BH, n, d) || !make_tile_map(&tk, k, BH, m, d) ||
       !make_tile_map(&tv, v, BH, m, d) || !make_tile_map(&tdo, dO, BH, n, d) ||
@@ -311,6 +322,8 @@ static int bwd_head_path(const void* q, const void* k, const void* v, const void
   p.scale = scale;
   p.kv_len = kv_len;
   p.h = h;
+  p.wl = wl;
+  p.wr = wr;
   p.wd.status = status;
   p.wd.budget_ns = g_watchdog_ns.load();
   const cudaError_t e = attn::launch_bwd_head(d, tq, tk, tv, tdo, tdq, tdk, tdv, p, stream);
@@ -319,11 +332,13 @@ static int bwd_head_path(const void* q, const void* k, const void* v, const void
 
 static int bwd_impl(const void* q, const void* k, const void* v, const void* o, const float* lse,
                     const void* dO, void* dq, void* dk, void* dv, const int* kv_len, int B, int h,
-                    int n, int m, int d_k, int d_v, int causal, float scale, void* workspace,
+                    int n, int m, int d_k, int d_v, int causal, int wl, int wr, float scale, void* workspace,
                     size_t workspace_bytes, attn_stream_t stream) {
   bool empty = false;
   int st = check_common(B, h, n, m, d_k, d_v, scale, &empty);
   if (st != ATTN_OK) return st;
+  wl = window_side(wl, n, m);
+  wr = window_side(wr, n, m);
   if (!k || !v || !dk || !dv) return ATTN_ERR_INVALID_ARG;
   if (!aligned16(k) || !aligned16(v) || !aligned16(dk) || !aligned16(dv)) return ATTN_ERR_INVALID_ARG;
   const long long BH = static_cast<long long>(B) * h;
@@ -343,7 +358,7 @@ static int bwd_impl(const void* q, const void* k, const void* v, const void* o, 
   if (ws_need == 0) {
     uint32_t* status = nullptr;
     if (device_status_word(&status) != cudaSuccess) return ATTN_ERR_CUDA;
-    return bwd_head_path(q, k, v, o, lse, dO, dq, dk, dv, kv_len, BH, h, n, m, d_k, causal, scale,
+    return bwd_head_path(q, k, v, o, lse, dO, dq, dk, dv, kv_len, BH, h, n, m, d_k, causal, wl, wr, scale,
                          status, reinterpret_cast<cudaStream_t>(stream));
   }
   if (!workspace || !aligned16(workspace) || workspace_bytes < ws_need) return ATTN_ERR_INVALID_ARG;
@@ -391,6 +406,8 @@ static int bwd_impl(const void* q, const void* k, const void* v, const void* o, 
   p.num_kblocks = static_cast<int>((m + 127) / 128);
   p.kv_len = kv_len;
   p.h = h;
+  p.wl = wl;
+  p.wr = wr;
   p.wd.status = status;
   p.wd.budget_ns = g_watchdog_ns.load();
 
@@ -410,21 +427,29 @@ static int bwd_impl(const void* q, const void* k, const void* v, const void* o, 
 
 int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int h, int n,
              int m, int d_k, int d_v, int causal, float scale, attn_stream_t stream) {
-  return fwd_impl(q, k, v, o, lse, nullptr, B, h, n, m, d_k, d_v, causal, scale, stream);
+  return fwd_impl(q, k, v, o, lse, nullptr, B, h, n, m, d_k, d_v, causal, -1, -1, scale, stream);
 }
 
 int attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse, const int* kv_len,
                     int B, int h, int n, int m, int d_k, int d_v, int causal, float scale,
                     attn_stream_t stream) {
   if ((reinterpret_cast<uintptr_t>(kv_len) & 3u) != 0) return ATTN_ERR_INVALID_ARG;
-  return fwd_impl(q, k, v, o, lse, kv_len, B, h, n, m, d_k, d_v, causal, scale, stream);
+  return fwd_impl(q, k, v, o, lse, kv_len, B, h, n, m, d_k, d_v, causal, -1, -1, scale, stream);
+}
+
+int attn_fwd_masked(const void* q, const void* k, const void* v, void* o, float* lse, const int* kv_len,
+                    int B, int h, int n, int m, int d_k, int d_v, int causal, int window_left,
+                    int window_right, float scale, attn_stream_t stream) {
+  if ((reinterpret_cast<uintptr_t>(kv_len) & 3u) != 0) return ATTN_ERR_INVALID_ARG;
+  return fwd_impl(q, k, v, o, lse, kv_len, B, h, n, m, d_k, d_v, causal, window_left, window_right, scale,
+                  stream);
 }
 
 int attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
              const void* dO, void* dq, void* dk, void* dv, int B, int h, int n, int m, int d_k,
              int d_v, int causal, float scale, void* workspace, size_t workspace_bytes,
              attn_stream_t stream) {
-  return bwd_impl(q, k, v, o, lse, dO, dq, dk, dv, nullptr, B, h, n, m, d_k, d_v, causal, scale,
+  return bwd_impl(q, k, v, o, lse, dO, dq, dk, dv, nullptr, B, h, n, m, d_k, d_v, causal, -1, -1, scale,
                   workspace, workspace_bytes, stream);
 }
 
@@ -433,8 +458,17 @@ int attn_bwd_varlen(const void* q, const void* k, const void* v, const void* o, 
                     int n, int m, int d_k, int d_v, int causal, float scale, void* workspace,
                     size_t workspace_bytes, attn_stream_t stream) {
   if ((reinterpret_cast<uintptr_t>(kv_len) & 3u) != 0) return ATTN_ERR_INVALID_ARG;
-  return bwd_impl(q, k, v, o, lse, dO, dq, dk, dv, kv_len, B, h, n, m, d_k, d_v, causal, scale,
+  return bwd_impl(q, k, v, o, lse, dO, dq, dk, dv, kv_len, B, h, n, m, d_k, d_v, causal, -1, -1, scale,
                   workspace, workspace_bytes, stream);
+}
+
+int attn_bwd_masked(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                    const void* dO, void* dq, void* dk, void* dv, const int* kv_len, int B, int h,
+                    int n, int m, int d_k, int d_v, int causal, int window_left, int window_right,
+                    float scale, void* workspace, size_t workspace_bytes, attn_stream_t stream) {
+  if ((reinterpret_cast<uintptr_t>(kv_len) & 3u) != 0) return ATTN_ERR_INVALID_ARG;
+  return bwd_impl(q, k, v, o, lse, dO, dq, dk, dv, kv_len, B, h, n, m, d_k, d_v, causal, window_left,
+                  window_right, scale, workspace, workspace_bytes, stream);
 }
 
 int attn_get_device_status(attn_stream_t stream) {
@@ -521,7 +555,7 @@ extern "C" int attn_bwd_noalloc(const void* q, const void* k, const void* v, con
   }
   if (status == nullptr) status = g_noalloc_status_ptr[dev];
   if (attn_bwd_workspace_bytes(B, h, n, m, d_k, d_v, causal) == 0)  // needs no scratch at all
-    return bwd_head_path(q, k, v, o, lse, dO, dq, dk, dv, nullptr, BH, h, n, m, d_k, causal, scale,
+    return bwd_head_path(q, k, v, o, lse, dO, dq, dk, dv, nullptr, BH, h, n, m, d_k, causal, -1, -1, scale,
                          status, s);
 
   const long long n_pad = round_up(n, 128);
@@ -564,6 +598,8 @@ extern "C" int attn_bwd_noalloc(const void* q, const void* k, const void* v, con
   p.num_kblocks = static_cast<int>((m + 127) / 128);
   p.kv_len = nullptr;
   p.h = h;
+  p.wl = -1;
+  p.wr = -1;
   p.wd.status = status;
   p.wd.budget_ns = g_watchdog_ns.load();
 

@@ -85,7 +85,9 @@ __global__ void __launch_bounds__(256) attn_bwd_pre_kernel(const BwdPreParams p)
   for (int off = LPR / 2; off > 0; off >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off, LPR);
   if (row < total && sub == 0) {
     p.Dsum[row] = valid ? dot : 0.f;
-    p.lse2[row] = valid ? p.lse[static_cast<size_t>(bh) * p.n + i] * kLog2e : INFINITY;
+    // rows past n and rows that saw no key (lse = -inf) get lse2 = +inf: weight 0
+    const float lse = valid ? p.lse[static_cast<size_t>(bh) * p.n + i] : -INFINITY;
+    p.lse2[row] = (lse > -INFINITY) ? lse * kLog2e : INFINITY;
   }
 }
 
@@ -211,17 +213,25 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   // Work item it = (key tile kb, head bh), key-tile major, so that under the
   // causal mask the items with the most query tiles come first. Every CTA
   // takes items it = blockIdx.x, blockIdx.x + gridDim.x, ...; the query tiles
-  // of an item: [i_start, n_qt) (causal: tiles wholly above the key tile see
-  // none of its keys). All CTAs of a head walk the query tiles in the same
-  // order, so the streamed Q and dO tiles come from DRAM once, then from L2.
-  // Key padding: a key tile wholly past the head's real keys has no query
-  // tiles (its dK, dV rows are zero).
+  // of an item: [i_start, i_start + T), those with a row that sees one of
+  // its keys (causal: none wholly above the key tile; a window: only those
+  // near it). All CTAs of a head walk the query tiles in the same order, so
+  // the streamed Q and dO tiles come from DRAM once, then from L2. Key
+  // padding: a key tile wholly past the head's real keys has no query tiles
+  // (its dK, dV rows are zero).
   auto item_of = [&](int it, int& bh, int& kb, int& i_start, int& T) {
     kb = it / p.BH;
     bh = it - kb * p.BH;
-    i_start = p.causal ? min(kb, n_qt) : 0;
-    if (kb * 128 >= head_keys(p.kv_len, bh, p.h, p.m)) i_start = n_qt;
-    T = n_qt - i_start;
+    const int mb = head_keys(p.kv_len, bh, p.h, p.m);
+    i_start = n_qt;
+    T = 0;
+    const int k0 = kb * 128;
+    if (k0 >= mb) return;
+    int qlo, qhi;
+    query_range(k0, min(k0 + 127, mb - 1), p.n, p.causal, p.wl, p.wr, qlo, qhi);
+    if (qhi <= qlo) return;
+    i_start = qlo / 128;
+    T = (qhi + 127) / 128 - i_start;
   };
 
   if (tid == 0) {
@@ -470,6 +480,8 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       item_of(it, bh, kb, i_start, T);
       const int key = kb * 128 + r;
       const int mb = head_keys(p.kv_len, bh, p.h, p.m);  // real keys of this head
+      int qlo, qhi;  // query rows that see this key
+      query_range(key, key, p.n, p.causal, p.wl, p.wr, qlo, qhi);
       // region h carried the previous item's dV / dK out: its TMA store must
       // have read it before dS (or this item's output) overwrites it
       if (C::STAGE_OUT && li >= 1) {
@@ -481,8 +493,8 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         const int st = gt & 1;
         const int q_row0 = (i_start + t) * 128;
         // queries [lo, hi) of this tile may attend to this key
-        const int lo = p.causal ? max(0, key - q_row0) : 0;
-        const int hi = (key < mb) ? min(128, p.n - q_row0) : 0;
+        const int lo = max(0, qlo - q_row0);
+        const int hi = (key < mb) ? min(128, qhi - q_row0) : 0;
         const bool masked = __any_sync(0xffffffffu, lo > col0 || hi < col0 + 64);
         ok = __all_sync(0xffffffffu, guarded_wait(&sh.s_full, gt & 1, abort_flag, wd, kSiteBwdS) &&
                                          guarded_wait(&sh.qdo_full[st], (gt >> 1) & 1, abort_flag, wd, kSiteBwdLoad));

@@ -157,14 +157,46 @@ attn_bwd_head_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
   volatile int* abort_flag = &sh.abort_flag;
   const int NQT = (p.n + 127) / 128;  // 1 or 2
   const int NKT = (p.m + 127) / 128;
-  // query tiles [t_lo(kb), NQT) see key tile kb (causal: none wholly above the
-  // diagonal; key padding: none if the tile lies past the head's mb real keys)
-  auto t_lo = [&](int kb, int mb) { return (kb * 128 >= mb) ? NQT : (p.causal ? min(kb, NQT) : 0); };
-  // the last key tile that reads query tile t's Q/dO slot (a key tile past the
-  // real keys reads none, but the slot is released on the head's last key tile)
-  auto last_kb = [&](int t, int mb) {
-    const int nk = mb > 0 ? (mb + 127) / 128 : 0;  // key tiles with real keys
-    return (nk == 0) ? -1 : (p.causal ? min(t, nk - 1) : nk - 1);
+  // query tiles [t0, t1) hold a row that sees some key of key tile kb (causal:
+  // none wholly above the diagonal; key padding: none past the head's mb real
+  // keys; a window: only those near the tile); t0 = t1 = NQT when none does
+  auto q_tiles = [&](int kb, int mb, int& t0, int& t1) {
+    const int k0 = kb * 128;
+    t0 = t1 = NQT;
+    if (k0 >= mb) return;
+    int qlo, qhi;
+    query_range(k0, min(k0 + 127, mb - 1), p.n, p.causal, p.wl, p.wr, qlo, qhi);
+    if (qhi <= qlo) return;
+    t0 = qlo / 128;
+    t1 = (qhi + 127) / 128;
+  };
+  // The key tiles that read query tile t: both ends of [t0, t1) above are
+  // nondecreasing in kb, so those key tiles are the run [first, last] with
+  // first = the smallest kb whose t1 exceeds t and last = the largest kb whose
+  // t0 is at most t (found by bisection); first > last: no key tile reads t,
+  // and the tile's Q/dO slot is released and its dQ written as zero at the
+  // head's end. Returns first in f and last in l, both -1 when there is none.
+  auto kb_span = [&](int t, int mb, int& f, int& l) {
+    int lo = 0, hi = NKT;  // first kb with t1 > t
+    while (lo < hi) {
+      const int mid = (lo + hi) >> 1;
+      int a, b;
+      q_tiles(mid, mb, a, b);
+      if (b > t) hi = mid;
+      else lo = mid + 1;
+    }
+    f = lo;
+    lo = -1;
+    hi = NKT - 1;  // last kb with t0 <= t
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      int a, b;
+      q_tiles(mid, mb, a, b);
+      if (a <= t) lo = mid;
+      else hi = mid - 1;
+    }
+    l = lo;
+    if (f > l) f = l = -1;
   };
 
   if (tid == 0) {
@@ -284,14 +316,19 @@ attn_bwd_head_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
     for (int bh = blockIdx.x; ok && bh < p.BH; bh += gridDim.x, ++li) {
       const int mb = head_keys(p.kv_len, bh, p.h, p.m);  // real keys of this head
       // dq_free is waited once per head, in order: before the head's first dQ
-      // product (key tile 0, query tile 0), or here for a head without real keys
-      if (mb == 0 && li >= 1 && !(ok = wait_all(&sh.dq_free, (li - 1) & 1, kSiteBwdDQ))) break;
+      // product, or at the head's end when it has none
+      bool dq_waited = (li == 0);
+      int f0, l0, f1 = -1, l1 = -1;  // key tiles reading query tiles 0 and 1
+      kb_span(0, mb, f0, l0);
+      if (NQT > 1) kb_span(1, mb, f1, l1);
       for (int kb = 0; ok && kb < NKT; ++kb, ++ki) {
         const int set = ki & 1;
         const uint32_t sK = smem_u32(smem + C::OFF_K + set * C::TILE);
         const uint32_t sV = smem_u32(smem + C::OFF_V + set * C::TILE);
         if (!(ok = wait_all(&sh.kv_full[set], (ki >> 1) & 1, kSiteBwdLoad))) break;
-        const int t0 = t_lo(kb, mb), T = NQT - t0;
+        int t0, t1;
+        q_tiles(kb, mb, t0, t1);
+        const int T = t1 - t0;
         // acc_free is waited once per key tile, in order: below before the
         // first dV product, or here for a key tile without query tiles
         if (T == 0 && ki >= 1 && !(ok = wait_all(&sh.acc_free, (ki - 1) & 1, kSiteBwdFinal))) break;
@@ -307,7 +344,7 @@ attn_bwd_head_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
           }
           __syncwarp();
         }
-        for (int t = t0; ok && t < NQT; ++t) {
+        for (int t = t0; ok && t < t1; ++t) {
           const int gt = g + (t - t0);
           const int kk = k + t, slot = kk % C::NSLOT;
           const uint32_t q_off = slot * C::TILE;
@@ -328,7 +365,7 @@ attn_bwd_head_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
           }
           __syncwarp();
           // next S^T while the compute warps form dS
-          if (t + 1 < NQT) {
+          if (t + 1 < t1) {
             const int kn = kk + 1;
             if (!(ok = wait_all(&sh.qdo_full[kn % C::NSLOT], (kn / C::NSLOT) & 1, kSiteBwdLoad))) break;
             if (lane == 0) {
@@ -339,7 +376,11 @@ attn_bwd_head_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
           }
           if (!(ok = wait_all(&sh.ds_full, gt & 1, kSiteBwdDS))) break;
           // the head's first dQ product overwrites the previous head's dQ
-          if (kb == 0 && t == 0 && li >= 1 && !(ok = wait_all(&sh.dq_free, (li - 1) & 1, kSiteBwdDQ))) break;
+          if (!dq_waited) {
+            if (!(ok = wait_all(&sh.dq_free, (li - 1) & 1, kSiteBwdDQ))) break;
+            dq_waited = true;
+          }
+          const bool dq_acc = kb > (t ? f1 : f0);  // query tile t's first dQ product starts it
           if (lane == 0) {
             tc_fence_after();
             // dK += dS^T Q : A = dS^T (K-major over queries), B = Q (MN-major)
@@ -352,13 +393,13 @@ attn_bwd_head_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
 #pragma unroll
             for (int q = 0; q < 8; ++q) {
               const uint64_t da = smem_desc(sDS + q * 16 * 128, C::DS_REGION, 1024, 2);
-              mma_ss(tmem + C::TM_DQ + t * D, da, b_mn(sK, q), id_dq, (kb > 0 || q > 0) ? 1u : 0u);
+              mma_ss(tmem + C::TM_DQ + t * D, da, b_mn(sK, q), id_dq, (dq_acc || q > 0) ? 1u : 0u);
             }
             mma_commit(&sh.ds_empty);
-            if (kb == last_kb(t, mb)) mma_commit(&sh.slot_empty[slot]);  // no later product reads this slot
+            if (kb == (t ? l1 : l0)) mma_commit(&sh.slot_empty[slot]);  // no later product reads this slot
           }
           __syncwarp();
-          if (t + 1 < NQT) {
+          if (t + 1 < t1) {
             const int kn = kk + 1;
             if (lane == 0) {
               issue_kmajor(tmem + C::TM_DP, sV, sDO + (kn % C::NSLOT) * C::TILE, id_dp);
@@ -376,10 +417,11 @@ attn_bwd_head_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         g += T;
       }
       if (!ok) break;
+      if (!dq_waited && !(ok = wait_all(&sh.dq_free, (li - 1) & 1, kSiteBwdDQ))) break;
       if (lane == 0) {
         // query tiles that no key tile read (a head without real keys) free their slots here
         for (int t = 0; t < NQT; ++t)
-          if (last_kb(t, mb) < 0) mma_commit(&sh.slot_empty[(k + t) % C::NSLOT]);
+          if ((t ? l1 : l0) < 0) mma_commit(&sh.slot_empty[(k + t) % C::NSLOT]);
         mma_commit(&sh.dq_full);  // every dQ product of this head
       }
       __syncwarp();
@@ -423,7 +465,9 @@ attn_bwd_head_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
                 dsum = fmaf(x.y, y.y, dsum);
               }
             }
-            lse2 = p.lse[static_cast<size_t>(bh) * p.n + row] * kLog2eH;
+            // a row that saw no key (lse = -inf, O = 0) keeps lse2 = +inf: weight 0
+            const float lse = p.lse[static_cast<size_t>(bh) * p.n + row];
+            if (lse > -INFINITY) lse2 = lse * kLog2eH;
           }
           stat[slot * 256 + r] = -lse2;
           stat[slot * 256 + 128 + r] = dsum;
@@ -450,20 +494,24 @@ attn_bwd_head_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
       const int mb = head_keys(p.kv_len, bh, p.h, p.m);  // real keys of this head
       for (int kb = 0; ok && kb < NKT; ++kb, ++ki) {
         const int key = kb * 128 + r;
-        const int t0 = t_lo(kb, mb), T = NQT - t0;
+        int t0, t1;
+        q_tiles(kb, mb, t0, t1);
+        const int T = t1 - t0;
+        int qlo, qhi;  // query rows that see this key
+        query_range(key, key, p.n, p.causal, p.wl, p.wr, qlo, qhi);
         // region h carried the previous key tile's dV / dK out: its TMA store
         // must have read it before dS (or this key tile's output) overwrites it
         if (ki >= 1) {
           ok = __all_sync(0xffffffffu, guarded_wait(&sh.out_free[h], (ki - 1) & 1, abort_flag, wd, kSiteBwdFinal));
           if (!ok) break;
         }
-        for (int t = t0; t < NQT; ++t) {
+        for (int t = t0; t < t1; ++t) {
           const int gt = g + (t - t0);
           const int kk = k + t, slot = kk % C::NSLOT;
           const int q_row0 = t * 128;
           // queries [lo, hi) of this tile may attend to this key
-          const int lo = p.causal ? max(0, key - q_row0) : 0;
-          const int hi = (key < mb) ? min(128, p.n - q_row0) : 0;
+          const int lo = max(0, qlo - q_row0);
+          const int hi = (key < mb) ? min(128, qhi - q_row0) : 0;
           const bool masked = __any_sync(0xffffffffu, lo > col0 || hi < col0 + 64);
           ok = __all_sync(0xffffffffu, guarded_wait(&sh.s_full, gt & 1, abort_flag, wd, kSiteBwdS) &&
                                            guarded_wait(&sh.stat_full[slot], (kk / C::NSLOT) & 1, abort_flag, wd,
@@ -591,11 +639,15 @@ attn_bwd_head_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
       if (!ok) break;
       tc_fence_after();
       uint8_t* stage = smem + C::OFF_STAGE;
-      // a head without real keys has no dQ product: its dQ is zero (TMEM
-      // still holds the previous head's)
-      const bool empty = head_keys(p.kv_len, bh, p.h, p.m) == 0;
+      const int mb = head_keys(p.kv_len, bh, p.h, p.m);
       bool live = true;
       for (int t = 0; live && t < NQT; ++t, ++ns) {
+        // a query tile that no key tile reads (a head without real keys, rows
+        // whose windows miss every key) has no dQ product: its dQ is zero
+        // (TMEM still holds an earlier head's)
+        int f, l;
+        kb_span(t, mb, f, l);
+        const bool empty = f < 0;
         uint32_t w[D / 2];
 #pragma unroll
         for (int q = 0; q < D / 32; ++q) {

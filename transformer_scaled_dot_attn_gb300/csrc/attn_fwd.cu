@@ -57,14 +57,6 @@ constexpr uint32_t tmem_cols_for(uint32_t c) {
   return c <= 32 ? 32 : c <= 64 ? 64 : c <= 128 ? 128 : c <= 256 ? 256 : 512;
 }
 
-// Build option: 2 gives each query row two softmax threads (half of the key
-// columns each) in the one-CTA-per-SM configurations. On GB300 it measured
-// slower than one thread per row (the exchange of row maxima costs more than
-// the shorter rows save), so the default is 1.
-#ifndef ATTN_FWD_SPLIT
-#define ATTN_FWD_SPLIT 1
-#endif
-
 template <int D, int NQ, int BN>
 struct Fwd {
   // P in TMEM columns of its own (see above)
@@ -86,18 +78,13 @@ struct Fwd {
   static constexpr uint32_t OFF_V = OFF_K + STAGES * KTILE;
   static constexpr uint32_t TMEM_COLS = tmem_cols_for(NQ * (BN + P_COLS + D));
   static constexpr int MIN_BLOCKS = (TMEM_COLS <= 256 && OFF_V + STAGES * KTILE + 1024 <= 110u * 1024u) ? 2 : 1;
-  // Threads per query row (see ATTN_FWD_SPLIT): with SPLIT = 2 two
-  // warpgroups share each query tile, one thread per row and half of the key
-  // columns each. Only with one CTA per SM, for the registers.
-  static constexpr int SPLIT = (ATTN_FWD_SPLIT == 2 && MIN_BLOCKS == 1) ? 2 : 1;
-  static constexpr int COLS = BN / SPLIT;                 // key columns per softmax thread
-  static constexpr int OCOLS = D / SPLIT;                 // O columns per softmax thread
-  // two threads per row: partial row maxima [key tile parity][query tile][half][row]
-  // and partial row sums [query tile][half][row], in fp32
-  static constexpr uint32_t OFF_MAX = OFF_V + STAGES * KTILE;
-  static constexpr uint32_t OFF_SUM = OFF_MAX + (SPLIT == 2 ? 2u * NQ * 2u * 128u * 4u : 0u);
-  static constexpr uint32_t SMEM = OFF_SUM + (SPLIT == 2 ? NQ * 2u * 128u * 4u : 0u) + 1024;  // + alignment slack
-  static constexpr int SOFT_WARPS = 4 * NQ * SPLIT;
+  // One softmax thread per query row (a variant with two threads per row,
+  // half of the key columns each, measured slower on GB300: exchanging the
+  // row maxima cost more than the shorter rows saved).
+  static constexpr int COLS = BN;                         // key columns per softmax thread
+  static constexpr int OCOLS = D;                         // O columns per softmax thread
+  static constexpr uint32_t SMEM = OFF_V + STAGES * KTILE + 1024;  // + alignment slack
+  static constexpr int SOFT_WARPS = 4 * NQ;
   // Softmax warpgroups, then one warpgroup with the producer, the NQ issuer
   // warps and idle padding, so that setmaxnreg can move registers from it to
   // the softmax warpgroups.
@@ -109,7 +96,7 @@ struct Fwd {
   static_assert(REG_SOFTMAX * SOFT_WARPS * 32 + REG_OTHER * 128 <= THREADS * REG_LAUNCH,
                 "register split exceeds the launch allocation");
   // a single CTA per SM with one thread per row has registers enough without a split
-  static constexpr bool REG_SPLIT = (MIN_BLOCKS == 2 || SPLIT == 2);
+  static constexpr bool REG_SPLIT = (MIN_BLOCKS == 2);
   static constexpr int PRODUCER = SOFT_WARPS, ISSUER = SOFT_WARPS + 1;  // issuers: ISSUER .. ISSUER + NQ - 1
   static constexpr int CHUNKS = COLS / 32;                // 32-column TMEM loads per row
   __host__ __device__ static constexpr uint32_t tm_s(int g) { return g * BN; }
@@ -175,9 +162,9 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, const
 // sum of the weights the P.V product applies, so O / l is an exact convex
 // combination of value rows (a row dominated by one key returns that value
 // row even when the reference m lags the row maximum). MASKED: columns at or
-// past `rem` (keys this row may not see) get weight exactly 0.
+// past `rem` or before `rlo` (keys this row may not see) get weight exactly 0.
 template <bool MASKED>
-__device__ __forceinline__ void exp_chunk(const uint32_t (&s)[32], int col0, int rem, uint64_t c2,
+__device__ __forceinline__ void exp_chunk(const uint32_t (&s)[32], int col0, int rlo, int rem, uint64_t c2,
                                           uint64_t nm2, float (&lsum)[4], uint32_t (&pk)[16]) {
 #pragma unroll
   for (int i = 0; i < 16; ++i) {
@@ -185,8 +172,8 @@ __device__ __forceinline__ void exp_chunk(const uint32_t (&s)[32], int col0, int
     float x0, x1;
     f2_unpack(x2, x0, x1);
     if (MASKED) {
-      if (col0 + 2 * i >= rem) x0 = -INFINITY;
-      if (col0 + 2 * i + 1 >= rem) x1 = -INFINITY;
+      if (col0 + 2 * i >= rem || col0 + 2 * i < rlo) x0 = -INFINITY;
+      if (col0 + 2 * i + 1 >= rem || col0 + 2 * i + 1 < rlo) x1 = -INFINITY;
     }
     const uint64_t p2 = f2_pack(ex2(x0), ex2(x1));
     pk[i] = pack_bf16x2_pair(p2);
@@ -211,18 +198,30 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   volatile int* abort_flag = &sh.abort_flag;
   const Watchdog wd = p.wd;
 
-  // real keys of this head (key padding), key tiles per query tile (0 for
-  // tiles past n or without real keys); nondecreasing in g
+  // real keys of this head (key padding); per query tile g the key tiles
+  // [jlo[g], jlo[g] + ntile[g]) that hold a key some row of the tile sees
+  // (ntile 0 for tiles past n or without a visible key); the CTA loads the
+  // union [jlo_cta, jlo_cta + nt) through its ring
   const int mb = head_keys(p.kv_len, bh, p.h, p.m);
-  int ntile[NQ];
-  int nt = 0, nq_valid = 0;
+  int ntile[NQ], jlo[NQ];
+  int nt = 0, nq_valid = 0, jlo_cta = 0x7fffffff, jhi_cta = 0;
 #pragma unroll
   for (int g = 0; g < NQ; ++g) {
-    const int r0 = q0 + g * 128;
-    ntile[g] = (r0 < p.n && mb > 0) ? key_tiles<BN>(min(r0 + 127, p.n - 1), mb, p.causal) : 0;
-    nt = max(nt, ntile[g]);
+    const int r0 = q0 + g * 128, r1 = min(r0 + 127, p.n - 1);
+    int lo0, hi0, lo1, hi1;
+    key_range(r0, mb, p.causal, p.wl, p.wr, lo0, hi0);  // row bounds are nondecreasing in the row
+    key_range(r1, mb, p.causal, p.wl, p.wr, lo1, hi1);
+    const bool any = r0 < p.n && hi1 > lo0;
+    jlo[g] = any ? lo0 / BN : 0;
+    ntile[g] = any ? (hi1 + BN - 1) / BN - jlo[g] : 0;
+    if (ntile[g] > 0) {
+      jlo_cta = min(jlo_cta, jlo[g]);
+      jhi_cta = max(jhi_cta, jlo[g] + ntile[g]);
+    }
     nq_valid += (r0 < p.n) ? 1 : 0;
   }
+  if (jhi_cta > 0) nt = jhi_cta - jlo_cta;
+  else jlo_cta = 0;
 
   if (tid == 0) {
     mbar_init(&sh.q_full, 1);
@@ -232,15 +231,15 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     }
     for (int g = 0; g < NQ; ++g) {
       mbar_init(&sh.s_full[g], 1);
-      mbar_init(&sh.p_full[g], 128 * C::SPLIT);
+      mbar_init(&sh.p_full[g], 128);
       mbar_init(&sh.o_full[g], 1);
       mbar_init(&sh.drain[g], 1);
-      mbar_init(&sh.s_free[g], 128 * C::SPLIT);
+      mbar_init(&sh.s_free[g], 128);
       mbar_init(&sh.pv_done[g], 1);
     }
-    for (int g = 0; g < NQ; ++g) mbar_init(&sh.o_staged[g], 128 * C::SPLIT);
-    mbar_init(&sh.exp_turn[0], 128 * C::SPLIT);
-    mbar_init(&sh.exp_turn[1], 128 * C::SPLIT);
+    for (int g = 0; g < NQ; ++g) mbar_init(&sh.o_staged[g], 128);
+    mbar_init(&sh.exp_turn[0], 128);
+    mbar_init(&sh.exp_turn[1], 128);
     sh.abort_flag = 0;
     fence_mbar_init();
   }
@@ -271,16 +270,24 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           tma_load_3d(smem + C::OFF_Q + t * C::QTILE + a * C::QBOX, &tm_q, &sh.q_full, a * C::ATOM,
                       q0 + t * 128, bh);
       bool ok = true;
-      for (int j = 0; ok && j < nt; ++j) {
-        const int st = j % C::STAGES;
-        const uint32_t ph = (j / C::STAGES) & 1;
-        // the stage's previous tile (j - STAGES) must be released by every
-        // query tile that used it
-        if (j >= C::STAGES) {
+      for (int jj = 0; ok && jj < nt; ++jj) {
+        // ring position jj holds key tile j; query tile g reads ring positions
+        // [a, a + ntile[g]) with a = jlo[g] - jlo_cta
+        const int j = jlo_cta + jj;
+        const int st = jj % C::STAGES;
+        const uint32_t ph = (jj / C::STAGES) & 1;
+        // the stage's previous tile (ring position x = jj - STAGES) must be
+        // released by every query tile that read it; it was that tile's use
+        // number (x - a) / STAGES of the stage
+        if (jj >= C::STAGES) {
+          const int x = jj - C::STAGES;
 #pragma unroll
-          for (int g = 0; g < NQ; ++g)
-            if (ok && ntile[g] > j - C::STAGES)
-              ok = guarded_wait(&sh.kv_empty[g][st], ph ^ 1, abort_flag, wd, kSiteKEmpty);
+          for (int g = 0; g < NQ; ++g) {
+            const int a = jlo[g] - jlo_cta;
+            if (ok && ntile[g] > 0 && x >= a && x < a + ntile[g])
+              ok = guarded_wait(&sh.kv_empty[g][st], static_cast<uint32_t>((x - a) / C::STAGES) & 1u, abort_flag,
+                                wd, kSiteKEmpty);
+          }
           if (!ok) break;
         }
         mbar_arrive_expect_tx(&sh.kv_full[st], 2 * C::KTILE);
@@ -289,7 +296,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         for (int a = 0; a < C::NATOM; ++a)
           tma_load_3d(smem + C::OFF_K + st * C::KTILE + a * C::KBOX, &tm_k, &sh.kv_full[st],
                       a * C::ATOM, j * BN, bh);
-        if (p.inject == 1 && j == 0) continue;  // test hook: this value tile never arrives
+        if (p.inject == 1 && jj == 0) continue;  // test hook: this value tile never arrives
         for (int a = 0; a < C::NATOM; ++a)
           tma_load_3d(smem + C::OFF_V + st * C::KTILE + a * C::KBOX, &tm_v, &sh.kv_full[st],
                       a * C::ATOM, j * BN, bh);
@@ -303,10 +310,13 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     // ------------------------------------------------------------ MMA issuer of query tile g
     if (C::REG_SPLIT) reg_dealloc<C::REG_OTHER>();
     const int g = warp - C::ISSUER;
-    int T = 0;
+    int T = 0, a = 0;  // key tiles of this query tile, ring position of its first
 #pragma unroll
     for (int gg = 0; gg < NQ; ++gg)
-      if (gg == g) T = ntile[gg];
+      if (gg == g) {
+        T = ntile[gg];
+        a = jlo[gg] - jlo_cta;
+      }
     if (lane == 0 && T > 0) {
       const uint32_t idesc_s = idesc_bf16_f32(128, BN, false, false) | (p.neg ? (1u << 13) : 0u);
       const uint32_t idesc_o = idesc_bf16_f32(128, D, false, true);
@@ -330,17 +340,18 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           mma_ts(t_o, t_p + k * 8, db, idesc_o, (acc || k > 0) ? 1u : 0u);
         }
       };
+      // this query tile's key tile j (0-based among its T) sits at ring position a + j
       bool ok = guarded_wait(&sh.q_full, 0, abort_flag, wd, kSiteQFull) &&
-                guarded_wait(&sh.kv_full[0], 0, abort_flag, wd, kSiteKFull);
+                guarded_wait(&sh.kv_full[a % C::STAGES], (a / C::STAGES) & 1, abort_flag, wd, kSiteKFull);
       if (ok) {
-        issue_s(0);
+        issue_s(a % C::STAGES);
         mma_commit(&sh.s_full[g]);
       }
       for (int j = 0; ok && j < T; ++j) {
-        const int st = j % C::STAGES;
+        const int st = (a + j) % C::STAGES;
         if (C::SEP_P && j + 1 < T) {
           // S_g(j+1) as soon as the softmax holds S_g(j) in registers
-          const int jn = j + 1, stn = jn % C::STAGES;
+          const int jn = a + j + 1, stn = jn % C::STAGES;
           if (!(ok = guarded_wait(&sh.s_free[g], j & 1, abort_flag, wd, kSiteSFull))) break;
           if (!(ok = guarded_wait(&sh.kv_full[stn], (jn / C::STAGES) & 1, abort_flag, wd, kSiteKFull))) break;
           tc_fence_after();
@@ -354,7 +365,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         if (j == T - 1) mma_commit(&sh.o_full[g]);
         mma_commit(&sh.kv_empty[g][st]);  // K_j and V_j are no longer read by this tile
         if (!C::SEP_P && j + 1 < T) {
-          const int jn = j + 1, stn = jn % C::STAGES;
+          const int jn = a + j + 1, stn = jn % C::STAGES;
           if (!(ok = guarded_wait(&sh.kv_full[stn], (jn / C::STAGES) & 1, abort_flag, wd, kSiteKFull))) break;
           issue_s(stn);
           mma_commit(&sh.s_full[g]);
@@ -367,33 +378,28 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     __syncwarp();
   } else {
     // ------------------------------------------------------------ softmax groups
-    // Query tile g, column half h: the thread owns row r of the tile (TMEM
-    // lane r) and key columns [h*COLS, (h+1)*COLS) of every key tile. The two
-    // halves of a row combine their row maxima and row sums through shared
-    // memory and a named barrier of the two warps that share those lanes.
+    // Query tile g: the thread owns row r of the tile (TMEM lane r).
     if (C::REG_SPLIT) reg_alloc<C::REG_SOFTMAX>();
-    const int g = warp / (4 * C::SPLIT);
-    const int h = (warp >> 2) % C::SPLIT;
+    const int g = warp / 4;
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;
     const int row = q0 + g * 128 + r;
-    const uint32_t pair_bar = 1 + g * 4 + quarter;      // named barrier of the two halves
-    float* part_max = reinterpret_cast<float*>(smem + C::OFF_MAX);
-    float* part_sum = reinterpret_cast<float*>(smem + C::OFF_SUM);
-    int my_tiles = 0;
+    int my_tiles = 0, my_jlo = 0;
 #pragma unroll
     for (int gg = 0; gg < NQ; ++gg)
-      if (gg == g) my_tiles = ntile[gg];
+      if (gg == g) {
+        my_tiles = ntile[gg];
+        my_jlo = jlo[gg];
+      }
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
-    const uint32_t t_s = tmem + lane_base + C::tm_s(g) + h * C::COLS;
-    const uint32_t t_p = tmem + lane_base + C::tm_p(g) + h * (C::COLS / 2);
-    const uint32_t t_o = tmem + lane_base + C::tm_o(g) + h * C::OCOLS;
-    const int lim = (p.causal ? min(row + 1, mb) : mb) - h * C::COLS;  // visible keys, from column h*COLS
+    const uint32_t t_s = tmem + lane_base + C::tm_s(g);
+    const uint32_t t_p = tmem + lane_base + C::tm_p(g);
+    const uint32_t t_o = tmem + lane_base + C::tm_o(g);
+    int klo, khi;  // visible keys [klo, khi) of this row
+    key_range(row, mb, p.causal, p.wl, p.wr, klo, khi);
     const float c = p.c;
     const uint64_t c2 = f2_pack(c, c);
-    float m_used = 0.f, l = 0.f;
-    // Failures are not acted on at once where the two halves must meet at a
-    // named barrier: they are voted on at the next one, so both leave together.
+    float m_used = -INFINITY, l = 0.f;
     bool ok = true;
     // With two query tiles and P aliasing S, the exponentials of tile 0 and
     // tile 1 take turns (0, 1, 0, 1, ... per key tile), so that one group's
@@ -401,14 +407,16 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     // computing at once and then both waiting for the tensor cores. Group 0
     // waits for group 1's previous turn, group 1 for group 0's turn on the
     // same key tile, each only while the other group still has that tile.
-    constexpr bool TURNS = (NQ == 2) && !C::SEP_P;
+    // (Both groups must start at the same key tile: not with a window.)
+    const bool turns = (NQ == 2) && !C::SEP_P && p.wl < 0 && p.wr < 0;
     int other_tiles = 0;
 #pragma unroll
     for (int gg = 0; gg < NQ; ++gg)
-      if (TURNS && gg == (g ^ 1)) other_tiles = ntile[gg];
-    if (TURNS && g == 1) mbar_arrive(&sh.exp_turn[0]);  // group 0 goes first
+      if (gg == (g ^ 1)) other_tiles = ntile[gg];
+    if (turns && g == 1) mbar_arrive(&sh.exp_turn[0]);  // group 0 goes first
     for (int j = 0; j < my_tiles; ++j) {
-      ok = __all_sync(0xffffffffu, guarded_wait(&sh.s_full[g], j & 1, abort_flag, wd, kSiteSFull)) && ok;
+      ok = __all_sync(0xffffffffu, guarded_wait(&sh.s_full[g], j & 1, abort_flag, wd, kSiteSFull));
+      if (!ok) break;
       tc_fence_after();
       uint32_t s[C::CHUNKS][32];
 #pragma unroll
@@ -418,14 +426,16 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         tc_fence_before();
         mbar_arrive(&sh.s_free[g]);  // S_g may be overwritten by S_g(j+1)
       }
-      const int rem = lim - j * BN;  // visible keys of this row among this thread's columns
-      const bool masked = __any_sync(0xffffffffu, rem < C::COLS);
+      // this row sees the tile's columns [rlo, rem) (key tile my_jlo + j)
+      const int k0 = (my_jlo + j) * BN;
+      const int rem = khi - k0, rlo = klo - k0;
+      const bool masked = __any_sync(0xffffffffu, rem < C::COLS || rlo > 0);
       if (masked) {
 #pragma unroll
         for (int q = 0; q < C::CHUNKS; ++q)
 #pragma unroll
           for (int i = 0; i < 32; ++i)
-            if (q * 32 + i >= rem) s[q][i] = __float_as_uint(-INFINITY);
+            if (q * 32 + i >= rem || q * 32 + i < rlo) s[q][i] = __float_as_uint(-INFINITY);
       }
       // row max: four chains of 3-input max, seeded with columns 0..7; every
       // later step covers 8 columns, ending exactly at COLS
@@ -440,30 +450,28 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           mx4[u] = max3(mx4[u], __uint_as_float(s[(e + 2 * u) >> 5][(e + 2 * u) & 31]),
                         __uint_as_float(s[(e + 2 * u + 1) >> 5][(e + 2 * u + 1) & 31]));
       }
-      float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
-      if (C::SPLIT == 2) {
-        part_max[(((j & 1) * NQ + g) * 2 + h) * 128 + r] = mx;
-        if (named_bar_or(pair_bar, 64, !ok || *abort_flag != 0)) break;
-        mx = fmaxf(mx, part_max[(((j & 1) * NQ + g) * 2 + (h ^ 1)) * 128 + r]);
-      } else if (!ok) {
-        break;
-      }
-      const float m_new = mx * c;
+      const float m_new = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * c;
       float alpha = 1.f;
       bool rescale = false;
       if (j == 0) {
         m_used = m_new;
       } else if (m_new > m_used + kRescaleThreshold) {
+        // (from -inf, a row whose window starts in this tile: alpha = 0, O and l are 0)
         alpha = ex2(m_used - m_new);
         m_used = m_new;
         rescale = true;
       }
-      const uint64_t nm2 = f2_pack(-m_used, -m_used);
-      if (TURNS && (g == 0 ? (j == 0 || j - 1 < other_tiles) : j < other_tiles))
-        ok = __all_sync(0xffffffffu, guarded_wait(&sh.exp_turn[g], j & 1, abort_flag, wd, kSiteExpTurn)) && ok;
+      // a row with no visible key so far keeps the reference 0 (its weights are 0)
+      const float m_ref = (m_used == -INFINITY) ? 0.f : m_used;
+      const uint64_t nm2 = f2_pack(-m_ref, -m_ref);
+      if (turns && (g == 0 ? (j == 0 || j - 1 < other_tiles) : j < other_tiles)) {
+        ok = __all_sync(0xffffffffu, guarded_wait(&sh.exp_turn[g], j & 1, abort_flag, wd, kSiteExpTurn));
+        if (!ok) break;
+      }
       if (C::SEP_P && j > 0) {
         // PV_g(j-1) still reads P_g until it completes
-        ok = __all_sync(0xffffffffu, guarded_wait(&sh.pv_done[g], (j - 1) & 1, abort_flag, wd, kSitePFull)) && ok;
+        ok = __all_sync(0xffffffffu, guarded_wait(&sh.pv_done[g], (j - 1) & 1, abort_flag, wd, kSitePFull));
+        if (!ok) break;
         tc_fence_after();
       }
       float lsum[4] = {0.f, 0.f, 0.f, 0.f};
@@ -473,15 +481,13 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         // masked scores already hold -inf, and 2^(-inf * c - m) = 0 for c > 0;
         // only c = 0 (scale 0) needs the explicit mask (-inf * 0 is NaN)
         if (masked && c == 0.f)
-          exp_chunk<true>(s[q], q * 32, rem, c2, nm2, lsum, pk);
+          exp_chunk<true>(s[q], q * 32, rlo, rem, c2, nm2, lsum, pk);
         else
-          exp_chunk<false>(s[q], q * 32, rem, c2, nm2, lsum, pk);
+          exp_chunk<false>(s[q], q * 32, rlo, rem, c2, nm2, lsum, pk);
         tmem_st16(t_p + q * 16, pk);
       }
-      if (TURNS) mbar_arrive(&sh.exp_turn[g ^ 1]);  // the other group's turn
-      {
-        l = l * alpha + ((lsum[0] + lsum[1]) + (lsum[2] + lsum[3]));
-      }
+      if (turns) mbar_arrive(&sh.exp_turn[g ^ 1]);  // the other group's turn
+      l = l * alpha + ((lsum[0] + lsum[1]) + (lsum[2] + lsum[3]));
       tmem_st_wait();
       if (j > 0 && __any_sync(0xffffffffu, rescale)) {
 #pragma unroll
@@ -497,21 +503,16 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       }
       tc_fence_before();
       mbar_arrive(&sh.p_full[g]);
-      if (C::SPLIT == 1 && !ok) break;
     }
-    if (mb == 0) write_empty_row<D>(p, bh, row, h * C::OCOLS, C::OCOLS, h == 0);
-    if (my_tiles > 0) {
-      ok = __all_sync(0xffffffffu, guarded_wait(&sh.o_full[g], 0, abort_flag, wd, kSiteOFull)) && ok;
-      if (C::SPLIT == 2) {
-        // a loop left early on a vote leaves both halves here together
-        part_sum[(g * 2 + h) * 128 + r] = l;
-        const bool failed = named_bar_or(pair_bar, 64, !ok || *abort_flag != 0);
-        l += part_sum[(g * 2 + (h ^ 1)) * 128 + r];
-        ok = !failed;
-      }
+    // a query tile without a visible key (a sequence without real keys, or a
+    // window past the keys): its rows are the empty sum
+    if (my_tiles == 0) write_empty_row<D>(p, bh, row, 0, D, true);
+    if (ok && my_tiles > 0) {
+      ok = __all_sync(0xffffffffu, guarded_wait(&sh.o_full[g], 0, abort_flag, wd, kSiteOFull));
       if (ok) {
         tc_fence_after();
-        const float inv_l = 1.f / l;
+        // a row that saw no key (l = 0) is the empty sum: O = 0, lse = -inf
+        const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
         // O leaves through the shared-memory tile of Q_g (no MMA reads it any
         // more once o_full completed), written in the TMA map's swizzled layout
         // and stored by one thread; rows past n are clipped by the map.
@@ -527,26 +528,26 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             pk[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
 #pragma unroll
           for (int u = 0; u < 2; ++u) {
-            const int c = (h * C::OCOLS + q * 16) / 8 + u;  // 16-byte chunk of the row
+            const int cc = (q * 16) / 8 + u;                 // 16-byte chunk of the row
             constexpr int CPA = C::ATOM / 8;                 // chunks per swizzle atom row
-            const int a = c / CPA, ca = c % CPA;
+            const int at = cc / CPA, ca = cc % CPA;
             const int pc = (C::ATOM == 64) ? (ca ^ (r & 7)) : (ca ^ ((r >> 1) & 3));
-            *reinterpret_cast<uint4*>(qtile + a * C::QBOX + r * (C::ATOM * 2) + (pc << 4)) =
+            *reinterpret_cast<uint4*>(qtile + at * C::QBOX + r * (C::ATOM * 2) + (pc << 4)) =
                 make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
           }
         }
         fence_proxy_async_smem();
         mbar_arrive(&sh.o_staged[g]);
-        if (h == 0 && r == 0) {
+        if (r == 0) {
           if (guarded_wait(&sh.o_staged[g], 0, abort_flag, wd, kSiteOFull)) {
-            for (int a = 0; a < C::NATOM; ++a)
-              tma_store_3d(&tm_o, qtile + a * C::QBOX, a * C::ATOM, q0 + g * 128, bh);
+            for (int at = 0; at < C::NATOM; ++at)
+              tma_store_3d(&tm_o, qtile + at * C::QBOX, at * C::ATOM, q0 + g * 128, bh);
             tma_store_commit();
             tma_store_wait_all();  // before the CTA (and its shared memory) goes away
           }
         }
-        if (row < p.n && h == 0 && p.lse != nullptr)
-          p.lse[static_cast<size_t>(bh) * p.n + row] = (m_used + log2f(l)) * kLn2;
+        if (row < p.n && p.lse != nullptr)
+          p.lse[static_cast<size_t>(bh) * p.n + row] = (l > 0.f) ? (m_used + log2f(l)) * kLn2 : -INFINITY;
       }
     }
   }
@@ -948,9 +949,9 @@ attn_fwd_persist_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
               // masked scores already hold -inf, and 2^(-inf * c - m) = 0 for c > 0;
               // only c = 0 (scale 0) needs the explicit mask (-inf * 0 is NaN)
               if (masked && c == 0.f)
-                exp_chunk<true>(s[q], q * 32, rem, c2, nm2, lsum, pk[q]);
+                exp_chunk<true>(s[q], q * 32, 0, rem, c2, nm2, lsum, pk[q]);
               else
-                exp_chunk<false>(s[q], q * 32, rem, c2, nm2, lsum, pk[q]);
+                exp_chunk<false>(s[q], q * 32, 0, rem, c2, nm2, lsum, pk[q]);
             }
             return (lsum[0] + lsum[1]) + (lsum[2] + lsum[3]);
           };
@@ -1049,9 +1050,9 @@ attn_fwd_persist_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
             // masked scores already hold -inf, and 2^(-inf * c - m) = 0 for c > 0;
             // only c = 0 (scale 0) needs the explicit mask (-inf * 0 is NaN)
             if (masked && c == 0.f)
-              exp_chunk<true>(s[q], q * 32, rem, c2, nm2, lsum, pk);
+              exp_chunk<true>(s[q], q * 32, 0, rem, c2, nm2, lsum, pk);
             else
-              exp_chunk<false>(s[q], q * 32, rem, c2, nm2, lsum, pk);
+              exp_chunk<false>(s[q], q * 32, 0, rem, c2, nm2, lsum, pk);
             tmem_st16(t_p + q * 16, pk);
           }
           {
@@ -1197,14 +1198,16 @@ __global__ void exp2_probe_kernel(const float* x, float* y_poly, float* y_mufu, 
 
 // Which forward kernel runs (measured on GB300, see the launcher below).
 namespace {
-bool fwd_persistent(int d, int n, int m, int causal) {
+// The persistent kernel handles neither the causal mask nor a window (the
+// per-item kernel skips their masked key tiles per query tile).
+bool fwd_persistent(int d, int n, int m, int causal, bool windowed) {
   (void)n;
-  return d <= 64 && !causal && (m % 128 == 0 || m >= 1024);
+  return d <= 64 && !causal && !windowed && (m % 128 == 0 || m >= 1024);
 }
 }  // namespace
 
-int fwd_key_tile(int d, int n, int m, int causal) {
-  if (fwd_persistent(d, n, m, causal)) return 128;
+int fwd_key_tile(int d, int n, int m, int causal, bool windowed) {
+  if (fwd_persistent(d, n, m, causal, windowed)) return 128;
   return (d >= 128 || n > 256) ? 128 : 64;
 }
 
@@ -1224,8 +1227,9 @@ cudaError_t launch_exp2_probe(const float* x, float* y_poly, float* y_mufu, int 
 // measured faster this way).
 cudaError_t launch_fwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const CUtensorMap& to, const FwdParams& p, int BH, cudaStream_t stream) {
-  const bool persist = fwd_persistent(d, p.n, p.m, p.causal);
-  const bool small_tiles = fwd_key_tile(d, p.n, p.m, p.causal) == 64;
+  const bool windowed = p.wl >= 0 || p.wr >= 0;
+  const bool persist = fwd_persistent(d, p.n, p.m, p.causal, windowed);
+  const bool small_tiles = fwd_key_tile(d, p.n, p.m, p.causal, windowed) == 64;
   switch (d) {
     case 32:
       if (persist) return launch_fwd_persist<32>(tq, tk, tv, to, p, BH, stream);

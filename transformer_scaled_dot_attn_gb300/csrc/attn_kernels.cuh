@@ -56,6 +56,30 @@ __device__ __forceinline__ int head_keys(const int* kv_len, int bh, int h, int m
   return min(max(__ldg(kv_len + bh / h), 0), m);
 }
 
+// Keys [lo, hi) visible to query row i of a head with mb real keys: the
+// causal mask (j <= i), key padding (j < mb) and the restricted-attention
+// window i - wl <= j <= i + wr (a side given as -1 is open; the host clamps
+// both to [-1, n + m]). hi <= lo: the row sees no key.
+__device__ __forceinline__ void key_range(int i, int mb, int causal, int wl, int wr, int& lo, int& hi) {
+  int h = mb;
+  if (causal) h = min(h, i + 1);
+  if (wr >= 0) h = min(h, i + wr + 1);
+  lo = (wl >= 0) ? max(0, i - wl) : 0;
+  hi = h;
+}
+
+// Query rows [lo, hi) that see some key of [k0, k1] (k1 < mb), the transpose
+// of key_range for a key tile: rows i with i - wl <= k1, and i >= k0 when
+// causal, and i + wr >= k0.
+__device__ __forceinline__ void query_range(int k0, int k1, int n, int causal, int wl, int wr, int& lo,
+                                            int& hi) {
+  int l = 0;
+  if (causal) l = max(l, k0);
+  if (wr >= 0) l = max(l, k0 - wr);
+  lo = l;
+  hi = (wl >= 0) ? min(n, k1 + wl + 1) : n;
+}
+
 // Profiling hooks (implemented with the C ABI): bracket one kernel launch
 // with CUDA events on `stream` when profiling is enabled; no-ops otherwise.
 enum KernelKind : int { kKindFwd = 0, kKindBwdPre = 1, kKindBwdMain = 2, kKindBwdPost = 3, kNumKinds = 4 };
@@ -75,6 +99,7 @@ struct FwdParams {
   int inject;         // test hook: 1 = skip the first value-tile load
   const int* kv_len;  // [B] real keys per sequence (key padding) or nullptr
   int h;              // heads per sequence (kv_len is indexed by bh / h)
+  int wl, wr;         // window: query i sees keys i - wl .. i + wr (-1: open side)
   Watchdog wd;
 };
 
@@ -83,7 +108,7 @@ cudaError_t launch_exp2_probe(const float* x, float* y_poly, float* y_mufu, int 
 
 // Keys per tile the forward kernel streams for head size d and n queries
 // (the K/V TMA box height).
-int fwd_key_tile(int d, int n, int m, int causal);
+int fwd_key_tile(int d, int n, int m, int causal, bool windowed);
 
 cudaError_t launch_fwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const CUtensorMap& to,
@@ -116,6 +141,7 @@ struct BwdParams {
   int num_items;            // BH * num_kblocks work items (set by the launcher)
   const int* kv_len;        // [B] real keys per sequence (key padding) or nullptr
   int h;                    // heads per sequence
+  int wl, wr;               // window (see FwdParams)
   Watchdog wd;
 };
 
@@ -140,6 +166,7 @@ struct BwdHeadParams {
   float scale;              // signed scale, applied to dQ and dK
   const int* kv_len;        // [B] real keys per sequence (key padding) or nullptr
   int h;                    // heads per sequence
+  int wl, wr;               // window (see FwdParams)
   Watchdog wd;
 };
 bool bwd_head_supported(int n, int d);
