@@ -227,7 +227,7 @@ def oracle_sample(w: Workload, target_s: float):
     def run(heads):
         q, k, v, do = workload_inputs(w, with_grad=True, heads=heads)
         t0 = time.perf_counter()
-        oracle.bwd(q, k, v, do, w.causal, w.default_scale)
+        oracle.bwd(q, k, v, do, w.causal, w.default_scale, window=w.window)
         return time.perf_counter() - t0
 
     probe = 1
@@ -279,9 +279,9 @@ def run_gpu(args, w: Workload, world, rank, local):
 
     def step(i):
         q, k, v, do = sets[i % n_sets]
-        A.attn_fwd(q, k, v, causal=w.causal, scale=scale, out=o, lse=lse, kv_len=kvl)
+        A.attn_fwd(q, k, v, causal=w.causal, scale=scale, out=o, lse=lse, kv_len=kvl, window=w.window)
         A.attn_bwd(q, k, v, o, lse, do, causal=w.causal, scale=scale, dq=dq, dk=dk, dv=dv,
-                   workspace=ws, kv_len=kvl)
+                   workspace=ws, kv_len=kvl, window=w.window)
 
     # settle clocks, then the counted warm-up
     t_soak = time.time()
@@ -339,9 +339,10 @@ def run_gpu(args, w: Workload, world, rank, local):
     def e2e_step():
         for dst, src in zip(d_in, (hq, hk, hv, hdo)):
             dst.copy_(src, non_blocking=True)
-        A.attn_fwd(d_in[0], d_in[1], d_in[2], causal=w.causal, scale=scale, out=o, lse=lse, kv_len=kvl)
+        A.attn_fwd(d_in[0], d_in[1], d_in[2], causal=w.causal, scale=scale, out=o, lse=lse, kv_len=kvl,
+                   window=w.window)
         A.attn_bwd(d_in[0], d_in[1], d_in[2], o, lse, d_in[3], causal=w.causal, scale=scale,
-                   dq=dq, dk=dk, dv=dv, workspace=ws, kv_len=kvl)
+                   dq=dq, dk=dk, dv=dv, workspace=ws, kv_len=kvl, window=w.window)
         for dst, src in zip(outs_h, (o, dq, dk, dv)):
             dst.copy_(src, non_blocking=True)
 
@@ -407,22 +408,25 @@ def run_sweep(args, local):
     out = {}
     names = ["encoder", "encoder_sat", "encoder_kpad", "decoder", "cross", "cross_h4_d128", "cross_h16_d32"]
     names += [f"long_n{n}_d{d}_{c}" for n in (1024, 4096, 16384) for d in (64, 128) for c in ("nc", "c")]
+    names += ["long_n16384_d64_band257", "long_n16384_d64_local256"]
     for name in names:
         w = WORKLOADS[name]
         q, k, v, do = make_inputs(w, 99, dev)
         lens = kv_lengths(w)
         kvl = None if lens is None else torch.tensor(lens, dtype=torch.int32, device=dev)
-        o, lse = A.attn_fwd(q, k, v, causal=w.causal, scale=w.default_scale, kv_len=kvl)
-        dq, dk, dv = A.attn_bwd(q, k, v, o, lse, do, causal=w.causal, scale=w.default_scale, kv_len=kvl)
+        o, lse = A.attn_fwd(q, k, v, causal=w.causal, scale=w.default_scale, kv_len=kvl, window=w.window)
+        dq, dk, dv = A.attn_bwd(q, k, v, o, lse, do, causal=w.causal, scale=w.default_scale, kv_len=kvl,
+                                window=w.window)
         torch.cuda.synchronize()
         iters = max(3, min(50, int(2e12 / max(step_flops(w), 1))))
         A.attn_profile_enable(True)
         for kind in A.KERNEL_KINDS:
             A.attn_profile_read(kind)
         for _ in range(iters):
-            A.attn_fwd(q, k, v, causal=w.causal, scale=w.default_scale, out=o, lse=lse, kv_len=kvl)
+            A.attn_fwd(q, k, v, causal=w.causal, scale=w.default_scale, out=o, lse=lse, kv_len=kvl,
+                       window=w.window)
             A.attn_bwd(q, k, v, o, lse, do, causal=w.causal, scale=w.default_scale, dq=dq, dk=dk, dv=dv,
-                       kv_len=kvl)
+                       kv_len=kvl, window=w.window)
         torch.cuda.synchronize()
         A.attn_profile_enable(False)
         prof = {kind: A.attn_profile_read(kind) for kind in A.KERNEL_KINDS}
@@ -459,7 +463,8 @@ def main():
     world, rank, local = dist_setup()
     w = WORKLOADS[args.workload]
     config = {"workload": f"{w.name}: B={w.B}, h={w.h}, n={w.n}, m={w.m}, d_k=d_v={w.d_k}, "
-                          f"causal={w.causal}" + (f", Q x {w.q_mult:g}" if w.q_mult != 1 else ""),
+                          f"causal={w.causal}" + (f", Q x {w.q_mult:g}" if w.q_mult != 1 else "")
+                          + (f", window={w.window}" if w.window is not None else ""),
               "global_batch": w.B * world, "seq_len": w.n, "kv_len": w.m, "heads": w.h,
               "head_dim": w.d_k, "causal": w.causal, "parallelism": f"replicas x{world} (independent batches)",
               "step": "attn_fwd + attn_bwd"}

@@ -17,8 +17,9 @@ base model h=8, d_k=d_v=64 (§3.2.2), big model h=16 with d_model=1024
 from __future__ import annotations
 
 import dataclasses
+import functools
 import math
-from typing import Dict, Iterator, List, Optional
+from typing import Dict, Iterator, List, Optional, Tuple
 
 import torch
 
@@ -49,6 +50,9 @@ class Workload:
     # key padding: 0 = none; else sequence b has kv_len[b] real keys, drawn
     # uniformly from [kv_len_min, m] (seed 5000+cfg), see kv_lengths()
     kv_len_min: int = 0
+    # restricted self-attention (§4, Table 1): query i sees keys
+    # i - window[0] .. i + window[1] (-1: open side); None = no window
+    window: Optional[Tuple[int, int]] = None
 
     @property
     def heads(self) -> int:
@@ -63,9 +67,14 @@ class Workload:
         """Algorithmic forward FLOPs: 4*B*h*n*m*d_k, halved when causal.
 
         With key padding (non-causal only) m is replaced by each sequence's
-        real key count: 4*h*n*d_k*sum_b kv_len[b].
+        real key count: 4*h*n*d_k*sum_b kv_len[b]. With a window the count is
+        4*d_k per visible (query, key) pair, the pairs counted exactly.
         """
         lens = kv_lengths(self)
+        if self.window is not None:
+            per_seq = [visible_pairs(self.n, self.m, self.causal, self.window, L)
+                       for L in (lens if lens is not None else [self.m] * self.B)]
+            return 4.0 * self.h * self.d_k * float(sum(per_seq))
         if lens is not None:
             if self.causal:
                 raise ValueError("padded workloads are non-causal")
@@ -78,8 +87,25 @@ class Workload:
         return 2.5 * self.fwd_flops()
 
 
-def _wl(name, B, h, n, m, d, causal, cfg, q_mult=1.0, kv_len_min=0) -> Workload:
-    return Workload(name, B, h, n, m, d, d, causal, cfg, q_mult, kv_len_min)
+def _wl(name, B, h, n, m, d, causal, cfg, q_mult=1.0, kv_len_min=0, window=None) -> Workload:
+    return Workload(name, B, h, n, m, d, d, causal, cfg, q_mult, kv_len_min, window)
+
+
+@functools.lru_cache(maxsize=None)
+def visible_pairs(n: int, m: int, causal: bool, window, mb: int) -> int:
+    """Number of (query, key) pairs with key j visible to query i: j < mb,
+    j <= i when causal, i - window[0] <= j <= i + window[1] (negative: open)."""
+    total = 0
+    wl, wr = window if window is not None else (-1, -1)
+    for i in range(n):
+        hi = mb
+        if causal:
+            hi = min(hi, i + 1)
+        if wr >= 0:
+            hi = min(hi, i + wr + 1)
+        lo = max(0, i - wl) if wl >= 0 else 0
+        total += max(0, hi - lo)
+    return total
 
 
 def _build_table() -> Dict[str, Workload]:
@@ -101,6 +127,11 @@ def _build_table() -> Dict[str, Workload]:
             for causal in (False, True):
                 tag = "c" if causal else "nc"
                 t.append(_wl(f"long_n{n}_d{d}_{tag}", 4, 16, n, n, d, causal, 5))
+    # restricted self-attention (§4, Table 1: a neighbourhood of size r around
+    # each position): r = 257 centred, and causal local attention over the
+    # 256 previous positions, on the long-sequence shape
+    t.append(_wl("long_n16384_d64_band257", 4, 16, 16384, 16384, 64, False, 9, window=(128, 128)))
+    t.append(_wl("long_n16384_d64_local256", 4, 16, 16384, 16384, 64, True, 9, window=(256, -1)))
     return {w.name: w for w in t}
 
 

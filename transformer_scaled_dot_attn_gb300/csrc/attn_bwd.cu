@@ -188,7 +188,9 @@ __device__ __forceinline__ void drain_wait_b(uint64_t* bar, uint32_t parity, con
   }
 }
 
-template <int D>
+// WIN: a restricted-attention window is set (otherwise both sides are open at
+// compile time and the tile ranges reduce to the causal / padding ones).
+template <int D, bool WIN>
 __global__ void __launch_bounds__(512, 1)
 attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -197,6 +199,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   using C = Bwd<D>;
   extern __shared__ uint8_t smem_raw[];
   const Watchdog wd = p.wd;
+  const int wl = WIN ? p.wl : -1, wr = WIN ? p.wr : -1;
   // The tiles need 1024-byte alignment (128-byte swizzle atoms). The kernel
   // declares no static shared memory, so the dynamic window starts aligned in
   // practice; if it ever did not leave room, report it and do nothing.
@@ -228,7 +231,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     const int k0 = kb * 128;
     if (k0 >= mb) return;
     int qlo, qhi;
-    query_range(k0, min(k0 + 127, mb - 1), p.n, p.causal, p.wl, p.wr, qlo, qhi);
+    query_range(k0, min(k0 + 127, mb - 1), p.n, p.causal, wl, wr, qlo, qhi);
     if (qhi <= qlo) return;
     i_start = qlo / 128;
     T = (qhi + 127) / 128 - i_start;
@@ -481,7 +484,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       const int key = kb * 128 + r;
       const int mb = head_keys(p.kv_len, bh, p.h, p.m);  // real keys of this head
       int qlo, qhi;  // query rows that see this key
-      query_range(key, key, p.n, p.causal, p.wl, p.wr, qlo, qhi);
+      query_range(key, key, p.n, p.causal, wl, wr, qlo, qhi);
       // region h carried the previous item's dV / dK out: its TMA store must
       // have read it before dS (or this item's output) overwrites it
       if (C::STAGE_OUT && li >= 1) {
@@ -709,7 +712,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   }
 }
 
-template <int D>
+template <int D, bool WIN>
 cudaError_t launch_bwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                          const CUtensorMap& tdk, const CUtensorMap& tdv,
                          const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdPreParams& pre,
@@ -721,7 +724,7 @@ cudaError_t launch_bwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
   if (e != cudaSuccess) return e;
   cudaError_t attr = cudaSuccess;
   std::call_once(once[dev & 63], [&] {
-    attr = cudaFuncSetAttribute(attn_bwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    attr = cudaFuncSetAttribute(attn_bwd_kernel<D, WIN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 static_cast<int>(C::SMEM));
   });
   if (attr != cudaSuccess) return attr;
@@ -731,7 +734,7 @@ cudaError_t launch_bwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
     static int regs_per_thread[64] = {0};
     if (regs_per_thread[dev & 63] == 0) {
       cudaFuncAttributes fa;
-      if ((e = cudaFuncGetAttributes(&fa, attn_bwd_kernel<D>)) != cudaSuccess) return e;
+      if ((e = cudaFuncGetAttributes(&fa, attn_bwd_kernel<D, WIN>)) != cudaSuccess) return e;
       regs_per_thread[dev & 63] = fa.numRegs;
     }
     const int need = 128 * (2 * C::REG_COMPUTE + C::REG_DQ + C::REG_OTHER);  // four warpgroups
@@ -759,7 +762,7 @@ cudaError_t launch_bwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
     pp.num_items = BH * p.num_kblocks;
     const int grid = pp.num_items < sm_count[dev & 63] ? pp.num_items : sm_count[dev & 63];
     prof_begin(kKindBwdMain, stream);
-    attn_bwd_kernel<D><<<grid, C::THREADS, C::SMEM, stream>>>(tq, tk, tv, tdo, tdq, tdk, tdv, pp);
+    attn_bwd_kernel<D, WIN><<<grid, C::THREADS, C::SMEM, stream>>>(tq, tk, tv, tdo, tdq, tdk, tdv, pp);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     prof_end(kKindBwdMain, stream);
   }
@@ -780,12 +783,17 @@ cudaError_t launch_bwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, cons
                        const CUtensorMap& tdk, const CUtensorMap& tdv,
                        const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdPreParams& pre,
                        const BwdParams& p, const BwdPostParams& post, int BH, cudaStream_t stream) {
+  const bool win = p.wl >= 0 || p.wr >= 0;
+#define ATTN_BWD_CFG(D_)                                                                   \
+  (win ? launch_bwd_d<D_, true>(tq, tk, tv, tdk, tdv, tdo, tdq, pre, p, post, BH, stream) \
+       : launch_bwd_d<D_, false>(tq, tk, tv, tdk, tdv, tdo, tdq, pre, p, post, BH, stream))
   switch (d) {
-    case 32: return launch_bwd_d<32>(tq, tk, tv, tdk, tdv, tdo, tdq, pre, p, post, BH, stream);
-    case 64: return launch_bwd_d<64>(tq, tk, tv, tdk, tdv, tdo, tdq, pre, p, post, BH, stream);
-    case 128: return launch_bwd_d<128>(tq, tk, tv, tdk, tdv, tdo, tdq, pre, p, post, BH, stream);
+    case 32: return ATTN_BWD_CFG(32);
+    case 64: return ATTN_BWD_CFG(64);
+    case 128: return ATTN_BWD_CFG(128);
     default: return cudaErrorInvalidValue;
   }
+#undef ATTN_BWD_CFG
 }
 
 }  // namespace attn

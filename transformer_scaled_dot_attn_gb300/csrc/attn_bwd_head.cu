@@ -137,7 +137,29 @@ __device__ __forceinline__ void p_block(const uint32_t (&s)[32], const float* ne
   }
 }
 
-template <int D>
+// The key tiles [x, y] that read query tile t of a head with mb real keys
+// (x = y = -1: none; then the tile's Q/dO slot is released and its dQ written
+// as zero at the head's end). The rows that see any key are a prefix of the
+// head (i < mb + wl with a left window, all rows otherwise, none when mb = 0),
+// and the keys seen by consecutive such rows overlap, so the tile's rows see
+// the one run of keys [lo(q0), hi(q_last)) with q_last its last such row; the
+// key tiles meeting that run are exactly the key tiles whose query-tile range
+// (query_range over the key tile) contains t.
+__device__ __forceinline__ int2 key_tile_span(int t, int mb, int n, int causal, int wl, int wr) {
+  const int q0 = t * 128;
+  int q1 = min(q0 + 127, n - 1);
+  if (wl >= 0) q1 = min(q1, mb + wl - 1);
+  if (mb <= 0 || q1 < q0) return make_int2(-1, -1);
+  int lo, hi, lo1, hi1;
+  key_range(q0, mb, causal, wl, wr, lo, hi);
+  key_range(q1, mb, causal, wl, wr, lo1, hi1);
+  if (hi1 <= lo) return make_int2(-1, -1);
+  return make_int2(lo / 128, (hi1 - 1) / 128);
+}
+
+// WIN: a restricted-attention window is set (otherwise both sides are open at
+// compile time and the tile ranges reduce to the causal / padding ones).
+template <int D, bool WIN>
 __global__ void __launch_bounds__(512, 1)
 attn_bwd_head_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -146,6 +168,7 @@ attn_bwd_head_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
   using C = BwdHead<D>;
   extern __shared__ uint8_t smem_raw[];
   const Watchdog wd = p.wd;
+  const int wl = WIN ? p.wl : -1, wr = WIN ? p.wr : -1;
   const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
   if (pad + C::PAYLOAD > C::SMEM) {
     if (threadIdx.x == 0) atomicCAS(wd.status, 0u, kDevLayout);
@@ -165,38 +188,15 @@ attn_bwd_head_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
     t0 = t1 = NQT;
     if (k0 >= mb) return;
     int qlo, qhi;
-    query_range(k0, min(k0 + 127, mb - 1), p.n, p.causal, p.wl, p.wr, qlo, qhi);
+    query_range(k0, min(k0 + 127, mb - 1), p.n, p.causal, wl, wr, qlo, qhi);
     if (qhi <= qlo) return;
     t0 = qlo / 128;
     t1 = (qhi + 127) / 128;
   };
-  // The key tiles that read query tile t: both ends of [t0, t1) above are
-  // nondecreasing in kb, so those key tiles are the run [first, last] with
-  // first = the smallest kb whose t1 exceeds t and last = the largest kb whose
-  // t0 is at most t (found by bisection); first > last: no key tile reads t,
-  // and the tile's Q/dO slot is released and its dQ written as zero at the
-  // head's end. Returns first in f and last in l, both -1 when there is none.
   auto kb_span = [&](int t, int mb, int& f, int& l) {
-    int lo = 0, hi = NKT;  // first kb with t1 > t
-    while (lo < hi) {
-      const int mid = (lo + hi) >> 1;
-      int a, b;
-      q_tiles(mid, mb, a, b);
-      if (b > t) hi = mid;
-      else lo = mid + 1;
-    }
-    f = lo;
-    lo = -1;
-    hi = NKT - 1;  // last kb with t0 <= t
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      int a, b;
-      q_tiles(mid, mb, a, b);
-      if (a <= t) lo = mid;
-      else hi = mid - 1;
-    }
-    l = lo;
-    if (f > l) f = l = -1;
+    const int2 r = key_tile_span(t, mb, p.n, p.causal, wl, wr);
+    f = r.x;
+    l = r.y;
   };
 
   if (tid == 0) {
@@ -498,7 +498,7 @@ attn_bwd_head_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         q_tiles(kb, mb, t0, t1);
         const int T = t1 - t0;
         int qlo, qhi;  // query rows that see this key
-        query_range(key, key, p.n, p.causal, p.wl, p.wr, qlo, qhi);
+        query_range(key, key, p.n, p.causal, wl, wr, qlo, qhi);
         // region h carried the previous key tile's dV / dK out: its TMA store
         // must have read it before dS (or this key tile's output) overwrites it
         if (ki >= 1) {
@@ -699,7 +699,7 @@ attn_bwd_head_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
   }
 }
 
-template <int D>
+template <int D, bool WIN>
 cudaError_t launch_bwd_head_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                               const CUtensorMap& tdo, const CUtensorMap& tdq, const CUtensorMap& tdk,
                               const CUtensorMap& tdv, const BwdHeadParams& p, cudaStream_t stream) {
@@ -710,7 +710,7 @@ cudaError_t launch_bwd_head_d(const CUtensorMap& tq, const CUtensorMap& tk, cons
   if (e != cudaSuccess) return e;
   cudaError_t attr = cudaSuccess;
   std::call_once(once[dev & 63], [&] {
-    attr = cudaFuncSetAttribute(attn_bwd_head_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    attr = cudaFuncSetAttribute(attn_bwd_head_kernel<D, WIN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 static_cast<int>(C::SMEM));
   });
   if (attr != cudaSuccess) return attr;
@@ -718,7 +718,7 @@ cudaError_t launch_bwd_head_d(const CUtensorMap& tq, const CUtensorMap& tk, cons
   static int sm_count[64] = {0};
   if (regs_per_thread[dev & 63] == 0) {
     cudaFuncAttributes fa;
-    if ((e = cudaFuncGetAttributes(&fa, attn_bwd_head_kernel<D>)) != cudaSuccess) return e;
+    if ((e = cudaFuncGetAttributes(&fa, attn_bwd_head_kernel<D, WIN>)) != cudaSuccess) return e;
     regs_per_thread[dev & 63] = fa.numRegs;
   }
   // setmaxnreg.inc waits until registers are free: the split must fit in the
@@ -732,7 +732,7 @@ cudaError_t launch_bwd_head_d(const CUtensorMap& tq, const CUtensorMap& tk, cons
   }
   const int grid = p.BH < sm_count[dev & 63] ? p.BH : sm_count[dev & 63];
   prof_begin(kKindBwdMain, stream);
-  attn_bwd_head_kernel<D><<<grid, C::THREADS, C::SMEM, stream>>>(tq, tk, tv, tdo, tdq, tdk, tdv, p);
+  attn_bwd_head_kernel<D, WIN><<<grid, C::THREADS, C::SMEM, stream>>>(tq, tk, tv, tdo, tdq, tdk, tdv, p);
   e = cudaGetLastError();
   prof_end(kKindBwdMain, stream);
   return e;
@@ -745,9 +745,14 @@ bool bwd_head_supported(int n, int d) { return n >= 1 && n <= 256 && (d == 32 ||
 cudaError_t launch_bwd_head(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                             const CUtensorMap& tdo, const CUtensorMap& tdq, const CUtensorMap& tdk,
                             const CUtensorMap& tdv, const BwdHeadParams& p, cudaStream_t stream) {
+  const bool win = p.wl >= 0 || p.wr >= 0;
   switch (d) {
-    case 32: return launch_bwd_head_d<32>(tq, tk, tv, tdo, tdq, tdk, tdv, p, stream);
-    case 64: return launch_bwd_head_d<64>(tq, tk, tv, tdo, tdq, tdk, tdv, p, stream);
+    case 32:
+      return win ? launch_bwd_head_d<32, true>(tq, tk, tv, tdo, tdq, tdk, tdv, p, stream)
+                 : launch_bwd_head_d<32, false>(tq, tk, tv, tdo, tdq, tdk, tdv, p, stream);
+    case 64:
+      return win ? launch_bwd_head_d<64, true>(tq, tk, tv, tdo, tdq, tdk, tdv, p, stream)
+                 : launch_bwd_head_d<64, false>(tq, tk, tv, tdo, tdq, tdk, tdv, p, stream);
     default: return cudaErrorInvalidValue;
   }
 }

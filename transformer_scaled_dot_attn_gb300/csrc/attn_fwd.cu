@@ -91,7 +91,7 @@ struct Fwd {
   static_assert(NQ + 1 <= 4, "producer and issuers share one warpgroup");
   static constexpr int THREADS = SOFT_WARPS * 32 + 128;
   static constexpr int REG_LAUNCH = (65536 / (THREADS * MIN_BLOCKS)) / 8 * 8;
-  static constexpr int REG_OTHER = (MIN_BLOCKS == 2) ? 48 : 96;
+  static constexpr int REG_OTHER = (MIN_BLOCKS == 2) ? 40 : 96;
   static constexpr int REG_SOFTMAX = ((THREADS * REG_LAUNCH - 128 * REG_OTHER) / (SOFT_WARPS * 32)) / 8 * 8;
   static_assert(REG_SOFTMAX * SOFT_WARPS * 32 + REG_OTHER * 128 <= THREADS * REG_LAUNCH,
                 "register split exceeds the launch allocation");
@@ -181,7 +181,9 @@ __device__ __forceinline__ void exp_chunk(const uint32_t (&s)[32], int col0, int
   }
 }
 
-template <int D, int NQ, int BN>
+// WIN: a restricted-attention window is set (otherwise both sides are open at
+// compile time, and the tile ranges reduce to the causal / padding ones).
+template <int D, int NQ, int BN, bool WIN>
 __global__ void __launch_bounds__(Fwd<D, NQ, BN>::THREADS, Fwd<D, NQ, BN>::MIN_BLOCKS)
 attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
@@ -197,6 +199,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   const int q0 = qb * (NQ * 128);
   volatile int* abort_flag = &sh.abort_flag;
   const Watchdog wd = p.wd;
+  const int wl = WIN ? p.wl : -1, wr = WIN ? p.wr : -1;
 
   // real keys of this head (key padding); per query tile g the key tiles
   // [jlo[g], jlo[g] + ntile[g]) that hold a key some row of the tile sees
@@ -209,8 +212,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   for (int g = 0; g < NQ; ++g) {
     const int r0 = q0 + g * 128, r1 = min(r0 + 127, p.n - 1);
     int lo0, hi0, lo1, hi1;
-    key_range(r0, mb, p.causal, p.wl, p.wr, lo0, hi0);  // row bounds are nondecreasing in the row
-    key_range(r1, mb, p.causal, p.wl, p.wr, lo1, hi1);
+    key_range(r0, mb, p.causal, wl, wr, lo0, hi0);  // row bounds are nondecreasing in the row
+    key_range(r1, mb, p.causal, wl, wr, lo1, hi1);
     const bool any = r0 < p.n && hi1 > lo0;
     jlo[g] = any ? lo0 / BN : 0;
     ntile[g] = any ? (hi1 + BN - 1) / BN - jlo[g] : 0;
@@ -396,7 +399,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     const uint32_t t_p = tmem + lane_base + C::tm_p(g);
     const uint32_t t_o = tmem + lane_base + C::tm_o(g);
     int klo, khi;  // visible keys [klo, khi) of this row
-    key_range(row, mb, p.causal, p.wl, p.wr, klo, khi);
+    key_range(row, mb, p.causal, wl, wr, klo, khi);
     const float c = p.c;
     const uint64_t c2 = f2_pack(c, c);
     float m_used = -INFINITY, l = 0.f;
@@ -408,15 +411,15 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     // waits for group 1's previous turn, group 1 for group 0's turn on the
     // same key tile, each only while the other group still has that tile.
     // (Both groups must start at the same key tile: not with a window.)
-    const bool turns = (NQ == 2) && !C::SEP_P && p.wl < 0 && p.wr < 0;
+    constexpr bool turns = (NQ == 2) && !C::SEP_P && !WIN;
     int other_tiles = 0;
 #pragma unroll
     for (int gg = 0; gg < NQ; ++gg)
       if (gg == (g ^ 1)) other_tiles = ntile[gg];
     if (turns && g == 1) mbar_arrive(&sh.exp_turn[0]);  // group 0 goes first
     for (int j = 0; j < my_tiles; ++j) {
-      ok = __all_sync(0xffffffffu, guarded_wait(&sh.s_full[g], j & 1, abort_flag, wd, kSiteSFull));
-      if (!ok) break;
+      // a failed wait is acted on at the end of the iteration
+      ok = __all_sync(0xffffffffu, guarded_wait(&sh.s_full[g], j & 1, abort_flag, wd, kSiteSFull)) && ok;
       tc_fence_after();
       uint32_t s[C::CHUNKS][32];
 #pragma unroll
@@ -464,14 +467,11 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       // a row with no visible key so far keeps the reference 0 (its weights are 0)
       const float m_ref = (m_used == -INFINITY) ? 0.f : m_used;
       const uint64_t nm2 = f2_pack(-m_ref, -m_ref);
-      if (turns && (g == 0 ? (j == 0 || j - 1 < other_tiles) : j < other_tiles)) {
-        ok = __all_sync(0xffffffffu, guarded_wait(&sh.exp_turn[g], j & 1, abort_flag, wd, kSiteExpTurn));
-        if (!ok) break;
-      }
+      if (turns && (g == 0 ? (j == 0 || j - 1 < other_tiles) : j < other_tiles))
+        ok = __all_sync(0xffffffffu, guarded_wait(&sh.exp_turn[g], j & 1, abort_flag, wd, kSiteExpTurn)) && ok;
       if (C::SEP_P && j > 0) {
         // PV_g(j-1) still reads P_g until it completes
-        ok = __all_sync(0xffffffffu, guarded_wait(&sh.pv_done[g], (j - 1) & 1, abort_flag, wd, kSitePFull));
-        if (!ok) break;
+        ok = __all_sync(0xffffffffu, guarded_wait(&sh.pv_done[g], (j - 1) & 1, abort_flag, wd, kSitePFull)) && ok;
         tc_fence_after();
       }
       float lsum[4] = {0.f, 0.f, 0.f, 0.f};
@@ -503,6 +503,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       }
       tc_fence_before();
       mbar_arrive(&sh.p_full[g]);
+      if (!ok) break;
     }
     // a query tile without a visible key (a sequence without real keys, or a
     // window past the keys): its rows are the empty sum
@@ -560,7 +561,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   }
 }
 
-template <int D, int NQ, int BN>
+template <int D, int NQ, int BN, bool WIN>
 cudaError_t launch_fwd_cfg(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                            const CUtensorMap& to, FwdParams p, int BH, cudaStream_t stream) {
   using C = Fwd<D, NQ, BN>;
@@ -570,7 +571,7 @@ cudaError_t launch_fwd_cfg(const CUtensorMap& tq, const CUtensorMap& tk, const C
   if (e != cudaSuccess) return e;
   cudaError_t attr = cudaSuccess;
   std::call_once(once[dev & 63], [&] {
-    attr = cudaFuncSetAttribute(attn_fwd_kernel<D, NQ, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    attr = cudaFuncSetAttribute(attn_fwd_kernel<D, NQ, BN, WIN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 static_cast<int>(C::SMEM));
   });
   if (attr != cudaSuccess) return attr;
@@ -580,7 +581,7 @@ cudaError_t launch_fwd_cfg(const CUtensorMap& tq, const CUtensorMap& tk, const C
     static int regs_per_thread[64] = {0};
     if (regs_per_thread[dev & 63] == 0) {
       cudaFuncAttributes fa;
-      if ((e = cudaFuncGetAttributes(&fa, attn_fwd_kernel<D, NQ, BN>)) != cudaSuccess) return e;
+      if ((e = cudaFuncGetAttributes(&fa, attn_fwd_kernel<D, NQ, BN, WIN>)) != cudaSuccess) return e;
       regs_per_thread[dev & 63] = fa.numRegs;
     }
     if (regs_per_thread[dev & 63] * C::THREADS < C::SOFT_WARPS * 32 * C::REG_SOFTMAX + 128 * C::REG_OTHER)
@@ -589,7 +590,7 @@ cudaError_t launch_fwd_cfg(const CUtensorMap& tq, const CUtensorMap& tk, const C
   p.num_qblocks = (p.n + NQ * 128 - 1) / (NQ * 128);
   dim3 grid(static_cast<unsigned>(BH), static_cast<unsigned>(p.num_qblocks));
   prof_begin(kKindFwd, stream);
-  attn_fwd_kernel<D, NQ, BN><<<grid, C::THREADS, C::SMEM, stream>>>(tq, tk, tv, to, p);
+  attn_fwd_kernel<D, NQ, BN, WIN><<<grid, C::THREADS, C::SMEM, stream>>>(tq, tk, tv, to, p);
   e = cudaGetLastError();
   prof_end(kKindFwd, stream);
   return e;
@@ -1230,18 +1231,20 @@ cudaError_t launch_fwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, cons
   const bool windowed = p.wl >= 0 || p.wr >= 0;
   const bool persist = fwd_persistent(d, p.n, p.m, p.causal, windowed);
   const bool small_tiles = fwd_key_tile(d, p.n, p.m, p.causal, windowed) == 64;
+#define ATTN_FWD_CFG(D_, BN_)                                                  \
+  (windowed ? launch_fwd_cfg<D_, 2, BN_, true>(tq, tk, tv, to, p, BH, stream) \
+            : launch_fwd_cfg<D_, 2, BN_, false>(tq, tk, tv, to, p, BH, stream))
   switch (d) {
     case 32:
       if (persist) return launch_fwd_persist<32>(tq, tk, tv, to, p, BH, stream);
-      return small_tiles ? launch_fwd_cfg<32, 2, 64>(tq, tk, tv, to, p, BH, stream)
-                         : launch_fwd_cfg<32, 2, 128>(tq, tk, tv, to, p, BH, stream);
+      return small_tiles ? ATTN_FWD_CFG(32, 64) : ATTN_FWD_CFG(32, 128);
     case 64:
       if (persist) return launch_fwd_persist<64>(tq, tk, tv, to, p, BH, stream);
-      return small_tiles ? launch_fwd_cfg<64, 2, 64>(tq, tk, tv, to, p, BH, stream)
-                         : launch_fwd_cfg<64, 2, 128>(tq, tk, tv, to, p, BH, stream);
-    case 128: return launch_fwd_cfg<128, 2, 128>(tq, tk, tv, to, p, BH, stream);
+      return small_tiles ? ATTN_FWD_CFG(64, 64) : ATTN_FWD_CFG(64, 128);
+    case 128: return ATTN_FWD_CFG(128, 128);
     default: return cudaErrorInvalidValue;
   }
+#undef ATTN_FWD_CFG
 }
 
 }  // namespace attn
