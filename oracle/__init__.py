@@ -14,6 +14,7 @@ Functions:
   fwd(q, k, v, causal, scale, rows=None)   -> (O, lse)                 (eq. (1))
   bwd(q, k, v, dO, causal, scale)          -> (dQ, dK, dV, O, lse)     (derivative of eq. (1))
   bwd_rows(q, k, v, dO, causal, scale, qrows, krows) -> sampled rows of one head
+  decode(q, k, v, scale, kv_len=None)      -> (O, lse) of one decoding step (§3, KV cache)
 
 Optional masks on fwd / bwd / bwd_rows: ``kv_len`` (key padding, per
 sequence) and ``window=(wl, wr)`` (restricted self-attention, §4 and Table 1:
@@ -197,6 +198,42 @@ def bwd(q, k, v, dO, causal: bool, scale: float, need=("dq", "dk", "dv"), kv_len
 
     return (shp(dQ, lead_q, n, dk), shp(dK, lead_k, m, dk), shp(dV, lead_k, m, dv),
             O.reshape(lead_q + (n, dv)), lse.reshape(lead_q + (n,)))
+
+
+def decode(q, k, v, scale: float, kv_len=None):
+    """One incremental decoding step (§3: the decoder emits one symbol at a time,
+    each step attending to the positions produced so far, itself included).
+
+    q: [B, h, n, d] are the queries of the n newest positions of each sequence,
+    k / v: [B, h, m, d] its cached keys and values, of which the first L_b =
+    kv_len[b] (all m without kv_len) are real. Query i stands at position
+    L_b - n + i and sees keys j <= L_b - n + i: the decoder's causal mask aligned
+    to the end of the cache. Written with the masks above, per sequence: key
+    padding L_b and the window's right side L_b - n. Returns (O, lse).
+    """
+    Q, K, V = _as4(_f64(q)), _as4(_f64(k)), _as4(_f64(v))
+    B, h, n, _ = Q.shape
+    m = K.shape[2]
+    lens = [m] * B if kv_len is None else [int(x) for x in np.asarray(kv_len).reshape(-1)]
+    if len(lens) != B:
+        raise ValueError("kv_len needs one entry per sequence")
+    O = np.empty(Q.shape[:3] + (V.shape[3],))
+    lse = np.empty(Q.shape[:3])
+    for b, L in enumerate(lens):
+        L = min(max(L, 0), m)
+        if L >= n:
+            O[b:b + 1], lse[b:b + 1] = fwd(Q[b:b + 1], K[b:b + 1], V[b:b + 1], False, scale, kv_len=[L],
+                                           window=(-1, L - n))
+        else:
+            # fewer cached positions than new queries: the first n - L queries
+            # stand before the cache starts and see nothing (the empty sum)
+            i0 = n - L
+            O[b, :, :i0] = 0.0
+            lse[b, :, :i0] = -np.inf
+            if L > 0:
+                O[b:b + 1, :, i0:], lse[b:b + 1, :, i0:] = fwd(Q[b:b + 1, :, i0:], K[b:b + 1], V[b:b + 1], True,
+                                                               scale, kv_len=[L])
+    return O, lse
 
 
 def bwd_rows(q, k, v, dO, causal: bool, scale: float, qrows=(), krows=(), kv_len=None, window=None):

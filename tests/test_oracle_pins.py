@@ -533,3 +533,55 @@ def test_window_sampled_rows_match_full_backward():
     np.testing.assert_array_equal(sq, fq[0, 0][[0, 7, 12]])
     np.testing.assert_array_equal(sk, fk[0, 0][[1, 6, 12]])
     np.testing.assert_array_equal(sv, fv[0, 0][[1, 6, 12]])
+
+
+# ---------------------------------------------------------------- incremental decoding (§3)
+
+@pytest.mark.parametrize("n,lens", [(1, None), (4, None), (3, [9, 17, 4]), (5, [2, 17, 0])])
+def test_decode_step_equals_last_rows_of_full_causal_pass(n, lens):
+    """A decoding step over the cache gives exactly the last n rows of the decoder's
+    causal self-attention over the whole sequence (the reason a cache works): the
+    n newest queries attend to everything cached up to and including themselves."""
+    rng = np.random.default_rng(n + 31)
+    B, h, m, d = 3, 2, 17, 5
+    q_full = rng.standard_normal((B, h, m, d))
+    k = rng.standard_normal((B, h, m, d))
+    v = rng.standard_normal((B, h, m, d))
+    Ls = [m] * B if lens is None else lens
+    q_new = np.zeros((B, h, n, d))
+    for b, L in enumerate(Ls):
+        for i in range(n):
+            pos = L - n + i
+            if pos >= 0:
+                q_new[b, :, i] = q_full[b, :, pos]
+    O, lse = oracle.decode(q_new, k, v, 0.45, kv_len=lens)
+    for b, L in enumerate(Ls):
+        if L == 0:
+            assert (O[b] == 0).all() and np.isneginf(lse[b]).all()
+            continue
+        Of, lf = oracle.fwd(q_full[b:b + 1, :, :L], k[b:b + 1, :, :L], v[b:b + 1, :, :L], True, 0.45)
+        for i in range(n):
+            pos = L - n + i
+            if pos < 0:
+                assert (O[b, :, i] == 0).all() and np.isneginf(lse[b, :, i]).all()
+            else:
+                np.testing.assert_allclose(O[b, :, i], Of[0, :, pos], rtol=1e-13, atol=1e-14)
+                np.testing.assert_allclose(lse[b, :, i], lf[0, :, pos], rtol=1e-13, atol=1e-14)
+
+
+def test_decode_against_torch_with_bottom_right_mask():
+    """torch fp64 SDPA with the cache mask written out: query i of n sees key j iff j <= L - n + i, j < L."""
+    F = torch.nn.functional
+    rng = np.random.default_rng(5)
+    B, h, n, m, d = 2, 3, 4, 13, 8
+    q = torch.from_numpy(rng.standard_normal((B, h, n, d)))
+    k = torch.from_numpy(rng.standard_normal((B, h, m, d)))
+    v = torch.from_numpy(rng.standard_normal((B, h, m, d)))
+    lens = [13, 7]
+    mask = torch.zeros(B, 1, n, m, dtype=torch.bool)
+    for b, L in enumerate(lens):
+        for i in range(n):
+            mask[b, 0, i, : L - n + i + 1] = True
+    ref = F.scaled_dot_product_attention(q, k, v, attn_mask=mask, scale=0.3)
+    O, _ = oracle.decode(q, k, v, 0.3, kv_len=lens)
+    np.testing.assert_allclose(O, ref.numpy(), rtol=1e-12, atol=1e-12)
