@@ -204,17 +204,49 @@ int attn_debug_exp2(const float* x, float* y_poly, float* y_mufu, int n, attn_st
 
 /*
  * Per-kernel device timing, for profiling. While enabled (on != 0), every
- * kernel that attn_fwd / attn_bwd launches is bracketed by two CUDA events
- * recorded on the caller's stream. attn_profile_read synchronises the
- * recorded events, adds their elapsed times into per-kind totals, and returns
- * and clears the totals of one kind:
+ * kernel that attn_fwd / attn_bwd / attn_decode launch is bracketed by two
+ * CUDA events recorded on the caller's stream. attn_profile_read synchronises
+ * the recorded events, adds their elapsed times into per-kind totals, and
+ * returns and clears the totals of one kind:
  *   kind 0 forward, 1 backward pre-pass (D, padded lse, dQ clear),
- *   kind 2 backward main kernel, 3 backward dQ conversion.
+ *   kind 2 backward main kernel, 3 backward dQ conversion,
+ *   kind 4 decoding step (per key chunk), 5 decoding merge of the chunks.
  * launches / total_ms may be NULL. Returns ATTN_OK, ATTN_ERR_INVALID_ARG for an
  * unknown kind, or ATTN_ERR_CUDA. Enabling costs two event records per launch.
  */
 int attn_profile_enable(int on);
 int attn_profile_read(int kind, int* launches, double* total_ms);
+
+/*
+ * One incremental decoding step with a key/value cache ("Attention Is All You
+ * Need" §3: the decoder emits one symbol at a time; each step attends to every
+ * position produced so far, itself included). Sequence b has L_b = kv_len[b]
+ * cached positions (all m when kv_len is NULL; clamped to [0, m]); its n
+ * newest positions, L_b - n .. L_b - 1, are the queries: query i sees the keys
+ * j <= L_b - n + i (the decoder's causal mask aligned to the end of the cache;
+ * a query before the cache start, when L_b < n, sees nothing and is the empty
+ * sum: O = 0, lse = -inf).
+ *   q    [B, h, n, d_k]  bf16, device, 16-byte aligned; 1 <= n <= 16
+ *   k, v [B, h, m, d]    bf16, device, 16-byte aligned: the caches, capacity m
+ *   o    [B, h, n, d_v]  bf16 out;  lse [B, h, n] fp32 out (natural log) or NULL
+ *   kv_len [B]           int32, device, 4-byte aligned, or NULL
+ *   scale                multiplies q.k (1/sqrt(d_k) for eq. (1)); finite
+ *   workspace            caller-owned device memory of at least
+ *                        attn_decode_workspace_bytes(B, h, n, m, d_k, d_v)
+ *                        bytes, 16-byte aligned (fp32 partial results of the
+ *                        key chunks); every byte the step reads it writes first
+ * The keys of each head are split into chunks processed by separate CTAs on
+ * the FP32 pipes (the step reads each cached element once and is bound by
+ * HBM); a second kernel merges the chunks. d_k = d_v in {32, 64, 128}.
+ * Returns ATTN_OK, ATTN_ERR_INVALID_ARG (null or misaligned pointer, n outside
+ * [1, 16], m < 1, short workspace, non-finite scale), ATTN_ERR_UNSUPPORTED
+ * (d_k != d_v, other head sizes, B*h too large) or ATTN_ERR_CUDA. B*h = 0:
+ * ATTN_OK, nothing launched. Asynchronous on `stream`, like attn_fwd.
+ */
+size_t attn_decode_workspace_bytes(int B, int h, int n, int m, int d_k, int d_v);
+int attn_decode(const void* q, const void* k, const void* v, void* o, float* lse, const int* kv_len,
+                int B, int h, int n, int m, int d_k, int d_v, float scale, void* workspace,
+                size_t workspace_bytes, attn_stream_t stream);
 
 #ifdef __cplusplus
 }

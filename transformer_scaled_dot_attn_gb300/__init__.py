@@ -26,7 +26,8 @@ __all__ = [
     "ATTN_ERR_TIMEOUT", "load_library", "library_path", "attn_fwd", "attn_bwd",
     "attn_bwd_workspace_bytes", "attn_get_device_status", "attn_status_string",
     "attn_set_watchdog_ns", "attn_debug_inject", "attn_profile_enable", "attn_profile_read",
-    "attn_debug_exp2", "attn_bwd_noalloc", "EXPORTED_SYMBOLS", "KERNEL_KINDS",
+    "attn_debug_exp2", "attn_bwd_noalloc", "attn_decode", "attn_decode_workspace_bytes",
+    "EXPORTED_SYMBOLS", "KERNEL_KINDS",
 ]
 # attn_fwd / attn_bwd take an optional ``kv_len`` (int32 CUDA tensor [B]: real
 # keys per sequence) and an optional ``window`` = (left, right) (restricted
@@ -44,11 +45,11 @@ EXPORTED_SYMBOLS = (
     "attn_fwd", "attn_bwd", "attn_bwd_workspace_bytes", "attn_get_device_status",
     "attn_status_string", "attn_set_watchdog_ns", "attn_debug_inject", "attn_profile_enable",
     "attn_profile_read", "attn_debug_exp2", "attn_bwd_noalloc", "attn_fwd_varlen",
-    "attn_bwd_varlen", "attn_fwd_masked", "attn_bwd_masked",
+    "attn_bwd_varlen", "attn_fwd_masked", "attn_bwd_masked", "attn_decode_workspace_bytes", "attn_decode",
 )
 
 # Kernel kinds of attn_profile_read.
-KERNEL_KINDS = {"fwd": 0, "bwd_pre": 1, "bwd_main": 2, "bwd_post": 3}
+KERNEL_KINDS = {"fwd": 0, "bwd_pre": 1, "bwd_main": 2, "bwd_post": 3, "decode": 4, "decode_merge": 5}
 
 _lock = threading.Lock()
 _lib = None
@@ -94,6 +95,10 @@ def load_library():
         lib.attn_bwd_masked.argtypes = [vp, vp, vp, vp, fp, vp, vp, vp, vp, vp, I, I, I, I, I, I, I, I, I,
                                         F, vp, SZ, vp]
         lib.attn_bwd_masked.restype = I
+        lib.attn_decode_workspace_bytes.argtypes = [I, I, I, I, I, I]
+        lib.attn_decode_workspace_bytes.restype = SZ
+        lib.attn_decode.argtypes = [vp, vp, vp, vp, fp, vp, I, I, I, I, I, I, F, vp, SZ, vp]
+        lib.attn_decode.restype = I
         lib.attn_bwd_workspace_bytes.argtypes = [I, I, I, I, I, I, I]
         lib.attn_bwd_workspace_bytes.restype = SZ
         lib.attn_get_device_status.argtypes = [vp]
@@ -266,6 +271,46 @@ def attn_bwd(q, k, v, o, lse, dO, causal: bool = False, scale: Optional[float] =
     if st != ATTN_OK:
         raise AttnError(st, "attn_bwd")
     return dq, dk, dv
+
+
+def attn_decode_workspace_bytes(B, h, n, m, d_k, d_v) -> int:
+    return int(load_library().attn_decode_workspace_bytes(B, h, n, m, d_k, d_v))
+
+
+def attn_decode(q, k, v, kv_len=None, scale: Optional[float] = None, out=None, lse=None,
+                need_lse: bool = True, workspace=None, stream=None):
+    """One decoding step: q [B,h,n,d] (the n newest positions, n <= 16) against the
+    caches k, v [B,h,m,d]; kv_len (optional int32 CUDA [B]) cached positions per
+    sequence (default m). Query i sees keys j <= L - n + i. Returns (O, lse)."""
+    import torch
+    lib = load_library()
+    if q.dim() != 4 or k.dim() != 4 or v.dim() != 4:
+        raise ValueError("q, k, v must be [B, h, S, d]")
+    B, h, n, dk = q.shape
+    m, dv = k.shape[2], v.shape[3]
+    _check_tensor("q", q, dtype=torch.bfloat16)
+    _check_tensor("k", k, (B, h, m, dk), torch.bfloat16)
+    _check_tensor("v", v, (B, h, m, dv), torch.bfloat16)
+    if scale is None:
+        scale = 1.0 / math.sqrt(dk)
+    if out is None:
+        out = torch.empty((B, h, n, dv), dtype=torch.bfloat16, device=q.device)
+    _check_tensor("out", out, (B, h, n, dv), torch.bfloat16)
+    if need_lse and lse is None:
+        lse = torch.empty((B, h, n), dtype=torch.float32, device=q.device)
+    if lse is not None:
+        _check_tensor("lse", lse, (B, h, n), torch.float32)
+    lens = _check_lengths(kv_len, B, q.device)
+    need = attn_decode_workspace_bytes(B, h, n, m, dk, dv)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16) // 4 + 4, dtype=torch.float32, device=q.device)
+    _check_tensor("workspace", workspace)
+    st = lib.attn_decode(_vptr(q), _vptr(k), _vptr(v), _vptr(out), _fptr(lse), lens, B, h, n, m, dk, dv,
+                         float(scale), _vptr(workspace), workspace.numel() * workspace.element_size(),
+                         _stream_handle(stream))
+    if st != ATTN_OK:
+        raise AttnError(st, "attn_decode")
+    return out, lse
 
 
 def attn_get_device_status(stream=None) -> int:

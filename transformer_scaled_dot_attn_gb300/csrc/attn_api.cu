@@ -136,8 +136,8 @@ std::mutex g_prof_mu;
 std::vector<EventPair> g_prof_pending;  // recorded, not yet read
 std::vector<EventPair> g_prof_free;     // created, reusable
 EventPair g_prof_open[attn::kNumKinds];  // begun, waiting for prof_end
-double g_prof_ms[attn::kNumKinds] = {0, 0, 0, 0};
-int g_prof_count[attn::kNumKinds] = {0, 0, 0, 0};
+double g_prof_ms[attn::kNumKinds] = {};
+int g_prof_count[attn::kNumKinds] = {};
 
 // Moves every pending pair's elapsed time into the per-kind totals.
 cudaError_t prof_drain_locked() {
@@ -469,6 +469,52 @@ int attn_bwd_masked(const void* q, const void* k, const void* v, const void* o, 
   if ((reinterpret_cast<uintptr_t>(kv_len) & 3u) != 0) return ATTN_ERR_INVALID_ARG;
   return bwd_impl(q, k, v, o, lse, dO, dq, dk, dv, kv_len, B, h, n, m, d_k, d_v, causal, window_left,
                   window_right, scale, workspace, workspace_bytes, stream);
+}
+
+size_t attn_decode_workspace_bytes(int B, int h, int n, int m, int d_k, int d_v) {
+  (void)d_v;
+  if (B <= 0 || h <= 0 || n <= 0 || m <= 0 || d_k <= 0) return 0;
+  const long long BH = static_cast<long long>(B) * h;
+  int splits = 1, chunk = 0;
+  attn::decode_split(BH, m, &splits, &chunk);
+  return static_cast<size_t>(BH * splits * n * (static_cast<long long>(d_k) + 2) * 4);
+}
+
+int attn_decode(const void* q, const void* k, const void* v, void* o, float* lse, const int* kv_len, int B, int h,
+                int n, int m, int d_k, int d_v, float scale, void* workspace, size_t workspace_bytes,
+                attn_stream_t stream) {
+  if (B < 0 || h < 0 || m < 1 || n < 1 || n > attn::kDecMaxN || !std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
+  if (d_k != d_v || (d_k != 32 && d_k != 64 && d_k != 128)) return ATTN_ERR_UNSUPPORTED;
+  const long long BH = static_cast<long long>(B) * h;
+  if (BH > 65535) return ATTN_ERR_UNSUPPORTED;  // grid y
+  if (BH == 0) return ATTN_OK;
+  if (!q || !k || !v || !o || !workspace) return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(workspace))
+    return ATTN_ERR_INVALID_ARG;
+  if ((lse != nullptr && (reinterpret_cast<uintptr_t>(lse) & 3u) != 0) ||
+      (reinterpret_cast<uintptr_t>(kv_len) & 3u) != 0)
+    return ATTN_ERR_INVALID_ARG;
+  if (workspace_bytes < attn_decode_workspace_bytes(B, h, n, m, d_k, d_v)) return ATTN_ERR_INVALID_ARG;
+  CUtensorMap tk, tv;
+  if (!make_tile_map(&tk, k, BH, m, d_k, 64) || !make_tile_map(&tv, v, BH, m, d_v, 64)) return ATTN_ERR_CUDA;
+  uint32_t* status = nullptr;
+  if (device_status_word(&status) != cudaSuccess) return ATTN_ERR_CUDA;
+  attn::DecParams p{};
+  p.q = static_cast<const __nv_bfloat16*>(q);
+  p.o = static_cast<__nv_bfloat16*>(o);
+  p.lse = lse;
+  p.part = static_cast<float*>(workspace);
+  p.kv_len = kv_len;
+  p.h = h;
+  p.n = n;
+  p.m = m;
+  attn::decode_split(BH, m, &p.splits, &p.chunk);
+  p.c = static_cast<float>(static_cast<double>(scale) * kLog2e);
+  p.wd.status = status;
+  p.wd.budget_ns = g_watchdog_ns.load();
+  const cudaError_t e = attn::launch_decode(d_k, tk, tv, p, static_cast<int>(BH),
+                                            reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
 int attn_get_device_status(attn_stream_t stream) {

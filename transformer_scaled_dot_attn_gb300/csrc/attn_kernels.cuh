@@ -82,7 +82,10 @@ __device__ __forceinline__ void query_range(int k0, int k1, int n, int causal, i
 
 // Profiling hooks (implemented with the C ABI): bracket one kernel launch
 // with CUDA events on `stream` when profiling is enabled; no-ops otherwise.
-enum KernelKind : int { kKindFwd = 0, kKindBwdPre = 1, kKindBwdMain = 2, kKindBwdPost = 3, kNumKinds = 4 };
+enum KernelKind : int {
+  kKindFwd = 0, kKindBwdPre = 1, kKindBwdMain = 2, kKindBwdPost = 3, kKindDecode = 4, kKindDecodeMerge = 5,
+  kNumKinds = 6
+};
 void prof_begin(int kind, cudaStream_t stream);
 void prof_end(int kind, cudaStream_t stream);
 
@@ -181,5 +184,26 @@ cudaError_t launch_bwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, cons
                        const CUtensorMap& tdk, const CUtensorMap& tdv,
                        const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdPreParams& pre,
                        const BwdParams& p, const BwdPostParams& post, int BH, cudaStream_t stream);
+
+// ---------------------------------------------------------------- decoding
+
+constexpr int kDecMaxN = 16;  // new queries per sequence in one decoding step
+
+struct DecParams {
+  const __nv_bfloat16* q;   // [BH, n, d]
+  __nv_bfloat16* o;         // [BH, n, d]
+  float* lse;               // [BH, n] or nullptr
+  float* part;              // [BH, splits, n, d + 2] fp32: partial O, max, sum (log2 units)
+  const int* kv_len;        // [B] cached positions per sequence or nullptr (all m)
+  int h, n, m;              // heads per sequence, new queries, cache capacity
+  int splits, chunk;        // key chunks per head and keys per chunk (set by decode_split)
+  float c;                  // scale * log2(e)
+  Watchdog wd;
+};
+// Key chunks of a decoding step over BH heads with capacity m.
+void decode_split(long long BH, int m, int* splits, int* chunk);
+// tk, tv: maps over the caches [BH, m, d] with 64-row boxes.
+cudaError_t launch_decode(int d, const CUtensorMap& tk, const CUtensorMap& tv, const DecParams& p, int BH,
+                          cudaStream_t stream);
 
 }  // namespace attn
