@@ -445,6 +445,57 @@ def run_sweep(args, local):
     return out
 
 
+def run_decode_sweep(args, local):
+    """Throughput of one decoding step (attn_decode, split keys + merge) per decoding workload.
+
+    HBM-bound: bytes = the caches K and V read once (B*h*m*d*2 each) plus q and
+    o; FLOPs = 4*d per visible (query, key) pair. Rank 0, N=1 only.
+    """
+    import torch
+    import transformer_scaled_dot_attn_gb300 as A
+    from seeded_inputs import DECODE_WORKLOADS
+    dev = torch.device("cuda", local)
+    peaks, _ = load_peaks()
+    out = {}
+    for name, (B, h, n, m, d) in DECODE_WORKLOADS.items():
+        g = torch.Generator(device=dev)
+        g.manual_seed(7)
+        # inputs larger than L2: rotate enough cache copies between steps
+        one = 2 * B * h * m * d * 2
+        nsets = max(1, min(4, -(-3 * (129 << 20) // one)))
+        sets = [(torch.randn(B, h, n, d, device=dev, generator=g).bfloat16(),
+                 torch.randn(B, h, m, d, device=dev, generator=g).bfloat16(),
+                 torch.randn(B, h, m, d, device=dev, generator=g).bfloat16()) for _ in range(nsets)]
+        ws = torch.empty(A.attn_decode_workspace_bytes(B, h, n, m, d, d) // 4 + 4, dtype=torch.float32, device=dev)
+        o = torch.empty(B, h, n, d, dtype=torch.bfloat16, device=dev)
+        lse = torch.empty(B, h, n, dtype=torch.float32, device=dev)
+        for i in range(3):
+            A.attn_decode(*sets[i % nsets], out=o, lse=lse, workspace=ws)
+        torch.cuda.synchronize()
+        iters = 40
+        A.attn_profile_enable(True)
+        for kind in A.KERNEL_KINDS:
+            A.attn_profile_read(kind)
+        for i in range(iters):
+            A.attn_decode(*sets[i % nsets], out=o, lse=lse, workspace=ws)
+        torch.cuda.synchronize()
+        A.attn_profile_enable(False)
+        c1, ms1 = A.attn_profile_read("decode")
+        c2, ms2 = A.attn_profile_read("decode_merge")
+        us = (ms1 + ms2) / max(c1, 1) * 1e3
+        nbytes = 2 * B * h * m * d * 2 + 2 * B * h * n * d * 2 + 4 * B * h * n
+        pairs = B * h * sum(m - n + i + 1 for i in range(n))
+        out[name] = {"us": round(us, 1), "merge_us": round(ms2 / max(c2, 1) * 1e3, 1),
+                     "gbs": round(nbytes / (us * 1e-6) / 1e9, 1),
+                     "hbm_frac": round(nbytes / (us * 1e-6) / 1e9 / peaks["hbm_gbs"], 3),
+                     "tflops": round(4.0 * d * pairs / (us * 1e-6) / 1e12, 2)}
+        del sets, ws, o, lse
+        torch.cuda.empty_cache()
+    if A.attn_get_device_status() != A.ATTN_OK:
+        raise RuntimeError("device watchdog fired in the decoding sweep")
+    return out
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -494,9 +545,10 @@ def main():
         return
 
     res = run_gpu(args, w, world, rank, local)
-    sweep = None
+    sweep = decode_sweep = None
     if world == 1 and not args.no_sweep:
         sweep = run_sweep(args, local)
+        decode_sweep = run_decode_sweep(args, local)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         tf, t, heads, threads = oracle_sample(w, args.cpu_seconds)
@@ -518,6 +570,8 @@ def main():
     }
     if sweep is not None:
         line["sweep"] = sweep
+    if decode_sweep is not None:
+        line["decode_sweep"] = decode_sweep
     print(json.dumps(line), flush=True)
 
 

@@ -30,6 +30,7 @@ __all__ = [
     "workload_inputs",
     "ragged_workloads",
     "kv_lengths",
+    "DECODE_WORKLOADS",
 ]
 
 
@@ -136,6 +137,17 @@ def _build_table() -> Dict[str, Workload]:
 
 
 WORKLOADS: Dict[str, Workload] = _build_table()
+
+
+# One incremental decoding step (§3: one output symbol per step) over a
+# key/value cache: (B sequences, h heads, n new positions, m cached positions,
+# d). B = 64 stands for a batch of 16 sentences with beam 4 (§6.1 beam size);
+# n = 4 for four positions per step; the big model's h = 16 heads of d = 64.
+DECODE_WORKLOADS: Dict[str, Tuple[int, int, int, int, int]] = {
+    "decode_b64_h16_n1_m4096_d64": (64, 16, 1, 4096, 64),
+    "decode_b64_h16_n4_m4096_d64": (64, 16, 4, 4096, 64),
+    "decode_b16_h16_n1_m16384_d128": (16, 16, 1, 16384, 128),
+}
 
 
 def normal_bf16(shape, seed: int, mult: float = 1.0, device: str = "cpu") -> torch.Tensor:

@@ -74,6 +74,23 @@ __device__ __forceinline__ void drain_wait_dec(uint64_t* bar, uint32_t parity, c
   }
 }
 
+// Bounded wait on a TMA phase that polls without a suspend hint: the step has
+// no other work to hand the issue slots to, and a suspended thread resumes late.
+__device__ __forceinline__ bool spin_wait_dec(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                              const Watchdog& wd, uint32_t site) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (*abort_flag) return false;
+    if (global_timer_ns() - t0 > wd.budget_ns) {
+      *abort_flag = 1;
+      atomicCAS(wd.status, 0u, kDevTimeout | site);
+      return false;
+    }
+  }
+  return true;
+}
+
 __device__ __forceinline__ float warp_max(float x) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
@@ -90,11 +107,14 @@ __device__ __forceinline__ float2 bf16x2_to_f2(uint32_t w) {
   return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
 }
 
-template <int D>
+// NQ: queries the kernel is compiled for (n <= NQ; the smallest power of two
+// that holds n), so that loops over the queries carry no idle iterations.
+template <int D, int NQ>
 __global__ void __launch_bounds__(kDecThreads)
 attn_decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                    const DecParams p) {
   using C = Dec<D>;
+  constexpr int NU = (NQ + 3) / 4;  // queries per warp in the weight phase
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t full[C::STAGES];
   __shared__ int abort_word;
@@ -150,22 +170,27 @@ attn_decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
     for (int t = 0; t < C::STAGES && t < ntiles; ++t) load(t);
 
   // running maximum and sum of query i = warp + 4 u, held by every lane of that warp
-  float mrun[kDecMaxN / 4], lrun[kDecMaxN / 4];
+  float mrun[NU], lrun[NU];
 #pragma unroll
-  for (int u = 0; u < kDecMaxN / 4; ++u) {
+  for (int u = 0; u < NU; ++u) {
     mrun[u] = -INFINITY;
     lrun[u] = 0.f;
   }
-  // P.V accumulators: columns 2 cp, 2 cp + 1 of every query, over key group kg
+  // P.V accumulators: columns 2 cp, 2 cp + 1 of every query, over key group kg;
+  // the value pair sits in 16-byte chunk cc of its row, which the swizzle
+  // moves by the row's index mod 8 (the same 8 offsets for every 8 rows)
   const int cp = tid % C::CP, kg = tid / C::CP;
-  float acc[kDecMaxN][2];
+  float acc[NQ][2];
 #pragma unroll
-  for (int i = 0; i < kDecMaxN; ++i) acc[i][0] = acc[i][1] = 0.f;
+  for (int i = 0; i < NQ; ++i) acc[i][0] = acc[i][1] = 0.f;
+  uint32_t voff[8];
+#pragma unroll
+  for (int u = 0; u < 8; ++u) voff[u] = dec_off<D>(u, cp / 4) + (cp % 4) * 4 - u * (C::ATOM * 2);
 
   int t = 0;
   for (; t < ntiles; ++t) {
     const int st = t % C::STAGES;
-    const bool ok = guarded_wait(&full[st], (t / C::STAGES) & 1, abort_flag, wd, kSiteKFull);
+    const bool ok = spin_wait_dec(&full[st], (t / C::STAGES) & 1, abort_flag, wd, kSiteKFull);
     if (__syncthreads_or(!ok)) break;
     const uint8_t* sK = smem + C::OFF_K + st * C::TILE;
     const uint8_t* sV = smem + C::OFF_V + st * C::TILE;
@@ -198,7 +223,7 @@ attn_decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
     __syncthreads();
     // exact running maximum and the weights, one warp per query
 #pragma unroll
-    for (int u = 0; u < kDecMaxN / 4; ++u) {
+    for (int u = 0; u < NU; ++u) {
       const int i = warp + 4 * u;
       if (i < n) {
         const float s0 = sS[i * kDecTK + lane], s1 = sS[i * kDecTK + lane + 32];
@@ -214,26 +239,35 @@ attn_decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
       }
     }
     __syncthreads();
-    // P.V over this thread's key group
+    // P.V over this thread's key group, four keys at a time (rows past n
+    // hold weight 0 and contribute nothing)
 #pragma unroll
-    for (int i = 0; i < kDecMaxN; ++i)
-      if (i < n) {
-        const float a = sA[i];
-        acc[i][0] *= a;
-        acc[i][1] *= a;
+    for (int i = 0; i < NQ; ++i) {
+      const float a = (i < n) ? sA[i] : 1.f;
+      acc[i][0] *= a;
+      acc[i][1] *= a;
+    }
+#pragma unroll
+    for (int j4 = 0; j4 < C::KPG; j4 += 4) {
+      const int j0 = kg * C::KPG + j4;
+      float2 vf[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int j = j0 + e;
+        vf[e] = bf16x2_to_f2(*reinterpret_cast<const uint32_t*>(sV + j * (C::ATOM * 2) + voff[j & 7]));
       }
-#pragma unroll 4
-    for (int jj = 0; jj < C::KPG; ++jj) {
-      const int j = kg * C::KPG + jj;
-      const uint32_t vv = *reinterpret_cast<const uint32_t*>(sV + dec_off<D>(j, cp / 4) + (cp % 4) * 4);
-      const float2 vf = bf16x2_to_f2(vv);
 #pragma unroll
-      for (int i = 0; i < kDecMaxN; ++i)
-        if (i < n) {
-          const float pw = sS[i * kDecTK + j];
-          acc[i][0] = fmaf(pw, vf.x, acc[i][0]);
-          acc[i][1] = fmaf(pw, vf.y, acc[i][1]);
-        }
+      for (int i = 0; i < NQ; ++i) {
+        const float4 pw = *reinterpret_cast<const float4*>(sS + i * kDecTK + j0);
+        acc[i][0] = fmaf(pw.x, vf[0].x, acc[i][0]);
+        acc[i][1] = fmaf(pw.x, vf[0].y, acc[i][1]);
+        acc[i][0] = fmaf(pw.y, vf[1].x, acc[i][0]);
+        acc[i][1] = fmaf(pw.y, vf[1].y, acc[i][1]);
+        acc[i][0] = fmaf(pw.z, vf[2].x, acc[i][0]);
+        acc[i][1] = fmaf(pw.z, vf[2].y, acc[i][1]);
+        acc[i][0] = fmaf(pw.w, vf[3].x, acc[i][0]);
+        acc[i][1] = fmaf(pw.w, vf[3].y, acc[i][1]);
+      }
     }
     __syncthreads();  // stage st and the weights are free again
     if (tid == 0 && t + C::STAGES < ntiles) {
@@ -252,7 +286,7 @@ attn_decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
   }
   // combine the key groups' accumulators
 #pragma unroll
-  for (int i = 0; i < kDecMaxN; ++i)
+  for (int i = 0; i < NQ; ++i)
     if (i < n) {
       sR[(kg * kDecMaxN + i) * D + 2 * cp] = acc[i][0];
       sR[(kg * kDecMaxN + i) * D + 2 * cp + 1] = acc[i][1];
@@ -266,7 +300,7 @@ attn_decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
     part[i * (D + 2) + c] = o;
   }
 #pragma unroll
-  for (int u = 0; u < kDecMaxN / 4; ++u) {
+  for (int u = 0; u < NU; ++u) {
     const int i = warp + 4 * u;
     if (i < n && lane == 0) {
       part[i * (D + 2) + D] = mrun[u];
@@ -319,9 +353,9 @@ __global__ void __launch_bounds__(128) attn_decode_merge_kernel(const DecParams 
   if (lane == 0 && p.lse != nullptr) p.lse[row] = (l > 0.f) ? (M + log2f(l)) * kDecLn2 : -INFINITY;
 }
 
-template <int D>
-cudaError_t launch_decode_d(const CUtensorMap& tk, const CUtensorMap& tv, const DecParams& p, int BH,
-                            cudaStream_t stream) {
+template <int D, int NQ>
+cudaError_t launch_decode_step(const CUtensorMap& tk, const CUtensorMap& tv, const DecParams& p, int BH,
+                               cudaStream_t stream) {
   using C = Dec<D>;
   static std::once_flag once[64];
   int dev = 0;
@@ -329,15 +363,28 @@ cudaError_t launch_decode_d(const CUtensorMap& tk, const CUtensorMap& tv, const 
   if (e != cudaSuccess) return e;
   cudaError_t attr = cudaSuccess;
   std::call_once(once[dev & 63], [&] {
-    attr = cudaFuncSetAttribute(attn_decode_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    attr = cudaFuncSetAttribute(attn_decode_kernel<D, NQ>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 static_cast<int>(C::SMEM));
   });
   if (attr != cudaSuccess) return attr;
   prof_begin(kKindDecode, stream);
-  attn_decode_kernel<D><<<dim3(static_cast<unsigned>(p.splits), static_cast<unsigned>(BH)), kDecThreads, C::SMEM,
-                          stream>>>(tk, tv, p);
+  attn_decode_kernel<D, NQ><<<dim3(static_cast<unsigned>(p.splits), static_cast<unsigned>(BH)), kDecThreads,
+                              C::SMEM, stream>>>(tk, tv, p);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   prof_end(kKindDecode, stream);
+  return cudaSuccess;
+}
+
+template <int D>
+cudaError_t launch_decode_d(const CUtensorMap& tk, const CUtensorMap& tv, const DecParams& p, int BH,
+                            cudaStream_t stream) {
+  cudaError_t e;
+  if (p.n <= 1) e = launch_decode_step<D, 1>(tk, tv, p, BH, stream);
+  else if (p.n <= 2) e = launch_decode_step<D, 2>(tk, tv, p, BH, stream);
+  else if (p.n <= 4) e = launch_decode_step<D, 4>(tk, tv, p, BH, stream);
+  else if (p.n <= 8) e = launch_decode_step<D, 8>(tk, tv, p, BH, stream);
+  else e = launch_decode_step<D, 16>(tk, tv, p, BH, stream);
+  if (e != cudaSuccess) return e;
   const long long rows = static_cast<long long>(BH) * p.n;
   prof_begin(kKindDecodeMerge, stream);
   attn_decode_merge_kernel<D><<<static_cast<unsigned>((rows + 3) / 4), 128, 0, stream>>>(p, rows);
@@ -350,8 +397,9 @@ cudaError_t launch_decode_d(const CUtensorMap& tk, const CUtensorMap& tv, const 
 
 void decode_split(long long BH, int m, int* splits, int* chunk) {
   const int tiles = (m + kDecTK - 1) / kDecTK;
-  // about 1024 CTAs over the whole batch, each at least one tile
-  long long want = (1024 + BH - 1) / (BH > 0 ? BH : 1);
+  // about 4096 CTAs over the whole batch (enough loads in flight per SM to
+  // cover the HBM latency), each at least one tile
+  long long want = (4096 + BH - 1) / (BH > 0 ? BH : 1);
   if (want < 1) want = 1;
   if (want > tiles) want = tiles;
   const int per = static_cast<int>((tiles + want - 1) / want);  // tiles per chunk
