@@ -15,6 +15,7 @@ Functions:
   bwd(q, k, v, dO, causal, scale)          -> (dQ, dK, dV, O, lse)     (derivative of eq. (1))
   bwd_rows(q, k, v, dO, causal, scale, qrows, krows) -> sampled rows of one head
   decode(q, k, v, scale, kv_len=None)      -> (O, lse) of one decoding step (§3, KV cache)
+  project_qkv / project_out / multi_head   -> the projections around eq. (1) (§3.2.2)
 
 Optional masks on fwd / bwd / bwd_rows: ``kv_len`` (key padding, per
 sequence) and ``window=(wl, wr)`` (restricted self-attention, §4 and Table 1:
@@ -234,6 +235,41 @@ def decode(q, k, v, scale: float, kv_len=None):
                 O[b:b + 1, :, i0:], lse[b:b + 1, :, i0:] = fwd(Q[b:b + 1, :, i0:], K[b:b + 1], V[b:b + 1], True,
                                                                scale, kv_len=[L])
     return O, lse
+
+
+def project_qkv(x_q, x_kv, w_qkv, h: int, d: int):
+    """The multi-head projections of §3.2.2: Q = x_q W^Q, K = x_kv W^K, V = x_kv W^V.
+
+    x_q: [B, n, d_model], x_kv: [B, m, d_model]; w_qkv: [d_model, 3 h d], the
+    column blocks W^Q | W^K | W^V, head i's d columns at i d within each (the
+    pages' W_i^Q in R^{d_model x d_k}). Returns q [B, h, n, d], k, v [B, h, m, d] (fp64).
+    """
+    Xq, Xkv, W = _f64(x_q), _f64(x_kv), _f64(w_qkv)
+    hd = h * d
+    if W.shape != (Xq.shape[-1], 3 * hd):
+        raise ValueError("w_qkv must be [d_model, 3 h d]")
+
+    def heads(Y):  # [B, S, h d] -> [B, h, S, d]
+        B, S, _ = Y.shape
+        return np.ascontiguousarray(Y.reshape(B, S, h, d).transpose(0, 2, 1, 3))
+
+    return heads(Xq @ W[:, :hd]), heads(Xkv @ W[:, hd:2 * hd]), heads(Xkv @ W[:, 2 * hd:])
+
+
+def project_out(o, w_o):
+    """Concat(head_1, ..., head_h) W^O (§3.2.2): o [B, h, n, d], w_o [h d, d_model] -> [B, n, d_model]."""
+    O, W = _f64(o), _f64(w_o)
+    B, h, n, d = O.shape
+    if W.shape[0] != h * d:
+        raise ValueError("w_o must be [h d, d_model]")
+    return O.transpose(0, 2, 1, 3).reshape(B, n, h * d) @ W
+
+
+def multi_head(x_q, x_kv, w_qkv, w_o, h: int, d: int, causal: bool = False, scale=None):
+    """MultiHead(Q, K, V) = Concat(head_1..head_h) W^O, head_i = Attention(Q W_i^Q, K W_i^K, V W_i^V)."""
+    q, k, v = project_qkv(x_q, x_kv, w_qkv, h, d)
+    O, _ = fwd(q, k, v, causal, 1.0 / np.sqrt(d) if scale is None else scale)
+    return project_out(O, w_o)
 
 
 def bwd_rows(q, k, v, dO, causal: bool, scale: float, qrows=(), krows=(), kv_len=None, window=None):

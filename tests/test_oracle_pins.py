@@ -585,3 +585,48 @@ def test_decode_against_torch_with_bottom_right_mask():
     ref = F.scaled_dot_product_attention(q, k, v, attn_mask=mask, scale=0.3)
     O, _ = oracle.decode(q, k, v, 0.3, kv_len=lens)
     np.testing.assert_allclose(O, ref.numpy(), rtol=1e-12, atol=1e-12)
+
+
+# ---------------------------------------------------------------- multi-head projections (§3.2.2)
+
+def test_multi_head_shapes_and_weight_count_of_the_close_reading():
+    """The close reading's walk-through: a 10-token sentence, d_model 512, h = 8 heads of 64:
+    each head projects 10 x 512 to 10 x 64, weights are 10 x 10, the heads concatenate back to
+    10 x 512, and the sublayer holds four 512 x 512 matrices = 1,048,576 weights."""
+    rng = np.random.default_rng(0)
+    h, d, dm = 8, 64, 512
+    x = rng.standard_normal((1, 10, dm))
+    w_qkv = rng.standard_normal((dm, 3 * h * d)) / np.sqrt(dm)
+    w_o = rng.standard_normal((h * d, dm)) / np.sqrt(dm)
+    q, k, v = oracle.project_qkv(x, x, w_qkv, h, d)
+    assert q.shape == k.shape == v.shape == (1, h, 10, d)
+    S, P = oracle.weights(q[0, 0], k[0, 0], False, 1 / 8)
+    assert P.shape == (10, 10)
+    y = oracle.multi_head(x, x, w_qkv, w_o, h, d)
+    assert y.shape == (1, 10, dm)
+    assert w_qkv.size + w_o.size == 1_048_576
+
+
+@pytest.mark.parametrize("causal,n,m", [(False, 7, 7), (True, 9, 9), (False, 5, 11)])
+def test_multi_head_against_torch_library(causal, n, m):
+    """torch fp64 multi_head_attention_forward (no biases, no dropout) as an independent routine;
+    its in_proj_weight [3E, E] is the transpose of the pages' [d_model, 3 h d] orientation."""
+    F = torch.nn.functional
+    rng = np.random.default_rng(n * 7 + m)
+    h, d = 4, 8
+    E = h * d
+    xq = rng.standard_normal((2, n, E))
+    xkv = xq if n == m else rng.standard_normal((2, m, E))  # self- or cross-attention
+    w_qkv = rng.standard_normal((E, 3 * E)) / np.sqrt(E)
+    w_o = rng.standard_normal((E, E)) / np.sqrt(E)
+    mask = None
+    if causal:
+        mask = torch.triu(torch.full((n, m), float("-inf"), dtype=torch.float64), diagonal=1)
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a))
+    ref, _ = F.multi_head_attention_forward(
+        t(xq).transpose(0, 1), t(xkv).transpose(0, 1), t(xkv).transpose(0, 1), E, h,
+        in_proj_weight=t(w_qkv.T), in_proj_bias=None, bias_k=None, bias_v=None, add_zero_attn=False,
+        dropout_p=0.0, out_proj_weight=t(w_o.T), out_proj_bias=None, training=False,
+        need_weights=False, attn_mask=mask)
+    y = oracle.multi_head(xq, xkv, w_qkv, w_o, h, d, causal=causal)
+    np.testing.assert_allclose(y, ref.transpose(0, 1).numpy(), rtol=1e-11, atol=1e-12)
