@@ -204,13 +204,14 @@ int attn_debug_exp2(const float* x, float* y_poly, float* y_mufu, int n, attn_st
 
 /*
  * Per-kernel device timing, for profiling. While enabled (on != 0), every
- * kernel that attn_fwd / attn_bwd / attn_decode launch is bracketed by two
+ * kernel that attn_fwd / attn_bwd / attn_decode / the projections launch is bracketed by two
  * CUDA events recorded on the caller's stream. attn_profile_read synchronises
  * the recorded events, adds their elapsed times into per-kind totals, and
  * returns and clears the totals of one kind:
  *   kind 0 forward, 1 backward pre-pass (D, padded lse, dQ clear),
  *   kind 2 backward main kernel, 3 backward dQ conversion,
- *   kind 4 decoding step (per key chunk), 5 decoding merge of the chunks.
+ *   kind 4 decoding step (per key chunk), 5 decoding merge of the chunks,
+ *   kind 6 projection GEMM (attn_qkv_projection, attn_out_projection).
  * launches / total_ms may be NULL. Returns ATTN_OK, ATTN_ERR_INVALID_ARG for an
  * unknown kind, or ATTN_ERR_CUDA. Enabling costs two event records per launch.
  */
@@ -243,6 +244,32 @@ int attn_profile_read(int kind, int* launches, double* total_ms);
  * (d_k != d_v, other head sizes, B*h too large) or ATTN_ERR_CUDA. B*h = 0:
  * ATTN_OK, nothing launched. Asynchronous on `stream`, like attn_fwd.
  */
+/*
+ * The multi-head projections around eq. (1) ("Attention Is All You Need"
+ * §3.2.2: head_i = Attention(Q W_i^Q, K W_i^K, V W_i^V), MultiHead =
+ * Concat(head_1, ..., head_h) W^O), as tcgen05 GEMMs (bf16 operands, fp32
+ * accumulation, bf16 results) that read and write the [B, h, S, d] layout of
+ * attn_fwd directly: the head split and the concatenation are tensor maps,
+ * no transposed copy is made.
+ *
+ * attn_qkv_projection: Q = x_q W^Q, K = x_kv W^K, V = x_kv W^V.
+ *   x_q  [B, n, d_model], x_kv [B, m, d_model]  bf16, device, 16-byte aligned
+ *        (self-attention: pass the same pointer and n = m; one fused GEMM)
+ *   w_qkv [d_model, 3 h d] bf16: the column blocks W^Q | W^K | W^V in the
+ *        pages' orientation (x W); head i's d columns at i d within each block
+ *   q [B, h, n, d], k, v [B, h, m, d]  bf16 out
+ * attn_out_projection: y = Concat(heads) W^O.
+ *   o [B, h, n, d] bf16 (attn_fwd's O), w_o [h d, d_model] bf16, y [B, n, d_model] bf16 out.
+ * Requirements: d in {64, 128}; d_model a multiple of 64; for the QKV
+ * projection h d a multiple of 128. Returns ATTN_OK, ATTN_ERR_INVALID_ARG
+ * (null or misaligned pointer, negative size), ATTN_ERR_UNSUPPORTED (other
+ * shapes) or ATTN_ERR_CUDA. Asynchronous on `stream`; profiling kind 6.
+ */
+int attn_qkv_projection(const void* x_q, const void* x_kv, const void* w_qkv, void* q, void* k, void* v, int B,
+                        int n, int m, int d_model, int h, int d, attn_stream_t stream);
+int attn_out_projection(const void* o, const void* w_o, void* y, int B, int n, int d_model, int h, int d,
+                        attn_stream_t stream);
+
 size_t attn_decode_workspace_bytes(int B, int h, int n, int m, int d_k, int d_v);
 int attn_decode(const void* q, const void* k, const void* v, void* o, float* lse, const int* kv_len,
                 int B, int h, int n, int m, int d_k, int d_v, float scale, void* workspace,

@@ -27,6 +27,7 @@ __all__ = [
     "attn_bwd_workspace_bytes", "attn_get_device_status", "attn_status_string",
     "attn_set_watchdog_ns", "attn_debug_inject", "attn_profile_enable", "attn_profile_read",
     "attn_debug_exp2", "attn_bwd_noalloc", "attn_decode", "attn_decode_workspace_bytes",
+    "attn_qkv_projection", "attn_out_projection",
     "EXPORTED_SYMBOLS", "KERNEL_KINDS",
 ]
 # attn_fwd / attn_bwd take an optional ``kv_len`` (int32 CUDA tensor [B]: real
@@ -46,10 +47,11 @@ EXPORTED_SYMBOLS = (
     "attn_status_string", "attn_set_watchdog_ns", "attn_debug_inject", "attn_profile_enable",
     "attn_profile_read", "attn_debug_exp2", "attn_bwd_noalloc", "attn_fwd_varlen",
     "attn_bwd_varlen", "attn_fwd_masked", "attn_bwd_masked", "attn_decode_workspace_bytes", "attn_decode",
+    "attn_qkv_projection", "attn_out_projection",
 )
 
 # Kernel kinds of attn_profile_read.
-KERNEL_KINDS = {"fwd": 0, "bwd_pre": 1, "bwd_main": 2, "bwd_post": 3, "decode": 4, "decode_merge": 5}
+KERNEL_KINDS = {"fwd": 0, "bwd_pre": 1, "bwd_main": 2, "bwd_post": 3, "decode": 4, "decode_merge": 5, "proj": 6}
 
 _lock = threading.Lock()
 _lib = None
@@ -99,6 +101,10 @@ def load_library():
         lib.attn_decode_workspace_bytes.restype = SZ
         lib.attn_decode.argtypes = [vp, vp, vp, vp, fp, vp, I, I, I, I, I, I, F, vp, SZ, vp]
         lib.attn_decode.restype = I
+        lib.attn_qkv_projection.argtypes = [vp, vp, vp, vp, vp, vp, I, I, I, I, I, I, vp]
+        lib.attn_qkv_projection.restype = I
+        lib.attn_out_projection.argtypes = [vp, vp, vp, I, I, I, I, I, vp]
+        lib.attn_out_projection.restype = I
         lib.attn_bwd_workspace_bytes.argtypes = [I, I, I, I, I, I, I]
         lib.attn_bwd_workspace_bytes.restype = SZ
         lib.attn_get_device_status.argtypes = [vp]
@@ -311,6 +317,53 @@ def attn_decode(q, k, v, kv_len=None, scale: Optional[float] = None, out=None, l
     if st != ATTN_OK:
         raise AttnError(st, "attn_decode")
     return out, lse
+
+
+def attn_qkv_projection(x_q, x_kv, w_qkv, h: int, d: int, q=None, k=None, v=None, stream=None):
+    """Q = x_q W^Q, K = x_kv W^K, V = x_kv W^V into [B, h, S, d] (§3.2.2).
+
+    x_q [B, n, d_model], x_kv [B, m, d_model] (the same tensor for
+    self-attention), w_qkv [d_model, 3 h d] (W^Q | W^K | W^V), all bf16 CUDA."""
+    import torch
+    lib = load_library()
+    if x_q.dim() != 3 or x_kv.dim() != 3:
+        raise ValueError("x_q, x_kv must be [B, S, d_model]")
+    B, n, dm = x_q.shape
+    m = x_kv.shape[1]
+    _check_tensor("x_q", x_q, dtype=torch.bfloat16)
+    _check_tensor("x_kv", x_kv, (B, m, dm), torch.bfloat16)
+    _check_tensor("w_qkv", w_qkv, (dm, 3 * h * d), torch.bfloat16)
+    q = torch.empty((B, h, n, d), dtype=torch.bfloat16, device=x_q.device) if q is None else q
+    k = torch.empty((B, h, m, d), dtype=torch.bfloat16, device=x_q.device) if k is None else k
+    v = torch.empty((B, h, m, d), dtype=torch.bfloat16, device=x_q.device) if v is None else v
+    _check_tensor("q", q, (B, h, n, d), torch.bfloat16)
+    _check_tensor("k", k, (B, h, m, d), torch.bfloat16)
+    _check_tensor("v", v, (B, h, m, d), torch.bfloat16)
+    st = lib.attn_qkv_projection(_vptr(x_q), _vptr(x_kv), _vptr(w_qkv), _vptr(q), _vptr(k), _vptr(v),
+                                 B, n, m, dm, h, d, _stream_handle(stream))
+    if st != ATTN_OK:
+        raise AttnError(st, "attn_qkv_projection")
+    return q, k, v
+
+
+def attn_out_projection(o, w_o, y=None, stream=None):
+    """y = Concat(head_1..h) W^O from o [B, h, n, d] and w_o [h d, d_model], bf16 CUDA (§3.2.2)."""
+    import torch
+    lib = load_library()
+    if o.dim() != 4:
+        raise ValueError("o must be [B, h, n, d]")
+    B, h, n, d = o.shape
+    _check_tensor("o", o, dtype=torch.bfloat16)
+    if w_o.dim() != 2 or w_o.shape[0] != h * d:
+        raise ValueError("w_o must be [h d, d_model]")
+    dm = w_o.shape[1]
+    _check_tensor("w_o", w_o, (h * d, dm), torch.bfloat16)
+    y = torch.empty((B, n, dm), dtype=torch.bfloat16, device=o.device) if y is None else y
+    _check_tensor("y", y, (B, n, dm), torch.bfloat16)
+    st = lib.attn_out_projection(_vptr(o), _vptr(w_o), _vptr(y), B, n, dm, h, d, _stream_handle(stream))
+    if st != ATTN_OK:
+        raise AttnError(st, "attn_out_projection")
+    return y
 
 
 def attn_get_device_status(stream=None) -> int:

@@ -87,6 +87,21 @@ bool make_tile_map(CUtensorMap* map, const void* base, long long BH, long long S
   return r == CUDA_SUCCESS;
 }
 
+// 3-D map over a row-major bf16 array [d2][d1][d0] (d0 fastest): box =
+// (64, box1, 1), 128-byte swizzle. Out-of-bounds reads are zero, stores clip.
+bool make_map3(CUtensorMap* map, const void* base, long long d0, long long d1, long long d2, int box1) {
+  EncodeTiledFn enc = encode_fn();
+  if (enc == nullptr) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(d0), static_cast<cuuint64_t>(d1), static_cast<cuuint64_t>(d2)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(d0) * 2, static_cast<cuuint64_t>(d0 * d1) * 2};
+  cuuint32_t box[3] = {64u, static_cast<cuuint32_t>(box1), 1u};
+  cuuint32_t estr[3] = {1u, 1u, 1u};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 // 2-D map over the fp32 dQ accumulator [rows, d]: box = (32 columns, 128 rows),
 // 128-byte swizzle (the layout the backward kernel stages its dQ tile in).
 bool make_dq_map(CUtensorMap* map, const float* base, long long rows, int d) {
@@ -515,6 +530,104 @@ int attn_decode(const void* q, const void* k, const void* v, void* o, float* lse
   const cudaError_t e = attn::launch_decode(d_k, tk, tv, p, static_cast<int>(BH),
                                             reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+// Checks shared by the projections: head sizes 64 / 128 (whole 64-column
+// boxes per head), widths that are multiples of the 64-column boxes.
+static int check_proj(int B, int n, int d_model, int h, int d) {
+  if (B < 0 || n < 0 || d_model < 1 || h < 1) return ATTN_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+  if (d_model % 64 != 0) return ATTN_ERR_UNSUPPORTED;
+  const long long hd = static_cast<long long>(h) * d;
+  if (hd > 0x3fffffff || static_cast<long long>(B) * h > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
+  return ATTN_OK;
+}
+
+int attn_qkv_projection(const void* x_q, const void* x_kv, const void* w_qkv, void* q, void* k, void* v, int B,
+                        int n, int m, int d_model, int h, int d, attn_stream_t stream) {
+  int st = check_proj(B, n, d_model, h, d);
+  if (st != ATTN_OK) return st;
+  if (m < 0) return ATTN_ERR_INVALID_ARG;
+  if ((static_cast<long long>(h) * d) % 128 != 0) return ATTN_ERR_UNSUPPORTED;  // tiles never straddle Q | K | V
+  if (B == 0 || (n == 0 && m == 0)) return ATTN_OK;
+  if (!x_q || !x_kv || !w_qkv || !q || !k || !v) return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(x_q) || !aligned16(x_kv) || !aligned16(w_qkv) || !aligned16(q) || !aligned16(k) || !aligned16(v))
+    return ATTN_ERR_INVALID_ARG;
+  const long long BH = static_cast<long long>(B) * h, hd = static_cast<long long>(h) * d;
+  uint32_t* status = nullptr;
+  if (device_status_word(&status) != cudaSuccess) return ATTN_ERR_CUDA;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  CUtensorMap tw, tq, tk, tv;
+  if (!make_map3(&tw, w_qkv, 3 * hd, d_model, 1, 64)) return ATTN_ERR_CUDA;
+  if ((n > 0 && !make_tile_map(&tq, q, BH, n, d)) || (m > 0 && (!make_tile_map(&tk, k, BH, m, d) ||
+                                                               !make_tile_map(&tv, v, BH, m, d))))
+    return ATTN_ERR_CUDA;
+  attn::ProjParams p{};
+  p.mode = 0;
+  p.B = B;
+  p.K = d_model;
+  p.h = h;
+  p.d = d;
+  p.wd.status = status;
+  p.wd.budget_ns = g_watchdog_ns.load();
+  const bool fused = x_q == x_kv && n == m;
+  if (fused) {
+    // self-attention: one GEMM against all of W^Q | W^K | W^V
+    CUtensorMap tx;
+    if (!make_map3(&tx, x_q, d_model, n, B, 128)) return ATTN_ERR_CUDA;
+    p.S = n;
+    p.N = static_cast<int>(3 * hd);
+    p.n_base = 0;
+    return attn::launch_proj(tx, tw, tq, tk, tv, p, s) == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+  }
+  // cross-attention: Q from x_q, K and V from x_kv
+  if (n > 0) {
+    CUtensorMap tx;
+    if (!make_map3(&tx, x_q, d_model, n, B, 128)) return ATTN_ERR_CUDA;
+    p.S = n;
+    p.N = static_cast<int>(hd);
+    p.n_base = 0;
+    if (attn::launch_proj(tx, tw, tq, tq, tq, p, s) != cudaSuccess) return ATTN_ERR_CUDA;
+  }
+  if (m > 0) {
+    CUtensorMap tx;
+    if (!make_map3(&tx, x_kv, d_model, m, B, 128)) return ATTN_ERR_CUDA;
+    p.S = m;
+    p.N = static_cast<int>(2 * hd);
+    p.n_base = static_cast<int>(hd);
+    if (attn::launch_proj(tx, tw, tk, tk, tv, p, s) != cudaSuccess) return ATTN_ERR_CUDA;
+  }
+  return ATTN_OK;
+}
+
+int attn_out_projection(const void* o, const void* w_o, void* y, int B, int n, int d_model, int h, int d,
+                        attn_stream_t stream) {
+  int st = check_proj(B, n, d_model, h, d);
+  if (st != ATTN_OK) return st;
+  if (B == 0 || n == 0) return ATTN_OK;
+  if (!o || !w_o || !y) return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(o) || !aligned16(w_o) || !aligned16(y)) return ATTN_ERR_INVALID_ARG;
+  const long long BH = static_cast<long long>(B) * h, hd = static_cast<long long>(h) * d;
+  uint32_t* status = nullptr;
+  if (device_status_word(&status) != cudaSuccess) return ATTN_ERR_CUDA;
+  CUtensorMap to, tw, ty;
+  if (!make_tile_map(&to, o, BH, n, d) || !make_map3(&tw, w_o, d_model, hd, 1, 64) ||
+      !make_map3(&ty, y, d_model, n, B, 128))
+    return ATTN_ERR_CUDA;
+  attn::ProjParams p{};
+  p.mode = 1;
+  p.B = B;
+  p.S = n;
+  p.K = static_cast<int>(hd);
+  p.N = d_model;
+  p.h = h;
+  p.d = d;
+  p.n_base = 0;
+  p.wd.status = status;
+  p.wd.budget_ns = g_watchdog_ns.load();
+  return attn::launch_proj(to, tw, ty, ty, ty, p, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? ATTN_OK
+             : ATTN_ERR_CUDA;
 }
 
 int attn_get_device_status(attn_stream_t stream) {

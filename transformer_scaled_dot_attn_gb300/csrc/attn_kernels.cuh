@@ -84,7 +84,7 @@ __device__ __forceinline__ void query_range(int k0, int k1, int n, int causal, i
 // with CUDA events on `stream` when profiling is enabled; no-ops otherwise.
 enum KernelKind : int {
   kKindFwd = 0, kKindBwdPre = 1, kKindBwdMain = 2, kKindBwdPost = 3, kKindDecode = 4, kKindDecodeMerge = 5,
-  kNumKinds = 6
+  kKindProj = 6, kNumKinds = 7
 };
 void prof_begin(int kind, cudaStream_t stream);
 void prof_end(int kind, cudaStream_t stream);
@@ -205,5 +205,23 @@ void decode_split(long long BH, int m, int* splits, int* chunk);
 // tk, tv: maps over the caches [BH, m, d] with 64-row boxes.
 cudaError_t launch_decode(int d, const CUtensorMap& tk, const CUtensorMap& tv, const DecParams& p, int BH,
                           cudaStream_t stream);
+
+// ---------------------------------------------------------------- projections
+
+struct ProjParams {
+  int mode;        // 0: A = token rows x [B, S, K] (map (K, S, B)), output scattered to Q | K | V
+                   //    [B, h, S, d]; 1: A = O [B, h, S, d] (K = h d), output Y [B, S, N]
+  int B, S, K, N;  // sequences, tokens per sequence, reduction, output columns of this launch
+  int h, d;        // heads and head size of the [B, h, S, d] side
+  int n_base;      // mode 0: first column of W (and of Q | K | V) this launch computes
+  int tiles_s;     // set by the launcher
+  int num_tiles;   // set by the launcher
+  Watchdog wd;
+};
+// ta: A map (mode 0: (K, S, B), box (64, 128, 1); mode 1: O's (d, S, B h) map);
+// tb: W map (Ntot, K, 1), box (64, 64, 1); to0..to2: Q, K, V maps (mode 0) or
+// the Y map (N, S, B) in to0 (mode 1). 128-byte swizzle everywhere.
+cudaError_t launch_proj(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& to0,
+                        const CUtensorMap& to1, const CUtensorMap& to2, ProjParams p, cudaStream_t stream);
 
 }  // namespace attn
