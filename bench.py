@@ -496,6 +496,65 @@ def run_decode_sweep(args, local):
     return out
 
 
+def run_proj_sweep(args, local):
+    """Throughput of the multi-head projections (tensor-bound GEMMs): the QKV
+    projection (fused for self-attention) and the output projection, FLOPs
+    2 * tokens * d_model * (columns), bytes = operands read once + results. Rank 0, N=1 only."""
+    import torch
+    import transformer_scaled_dot_attn_gb300 as A
+    from seeded_inputs import PROJ_WORKLOADS
+    dev = torch.device("cuda", local)
+    peaks, _ = load_peaks()
+    out = {}
+    for name, (B, n, m, dm, h, d) in PROJ_WORKLOADS.items():
+        g = torch.Generator(device=dev)
+        g.manual_seed(11)
+        hd = h * d
+        xq = torch.randn(B, n, dm, device=dev, generator=g).bfloat16()
+        xkv = xq if n == m and "self" in name else torch.randn(B, m, dm, device=dev, generator=g).bfloat16()
+        w = (torch.randn(dm, 3 * hd, device=dev, generator=g) / dm ** 0.5).bfloat16()
+        wo = (torch.randn(hd, dm, device=dev, generator=g) / hd ** 0.5).bfloat16()
+        q = torch.empty(B, h, n, d, dtype=torch.bfloat16, device=dev)
+        k = torch.empty(B, h, m, d, dtype=torch.bfloat16, device=dev)
+        v = torch.empty_like(k)
+        y = torch.empty(B, n, dm, dtype=torch.bfloat16, device=dev)
+        res = {}
+        for kind in ("qkv", "out"):
+            def call():
+                if kind == "qkv":
+                    A.attn_qkv_projection(xq, xkv, w, h, d, q=q, k=k, v=v)
+                else:
+                    A.attn_out_projection(q, wo, y=y)
+            for _ in range(3):
+                call()
+            torch.cuda.synchronize()
+            A.attn_profile_enable(True)
+            A.attn_profile_read("proj")
+            iters = 30
+            for _ in range(iters):
+                call()
+            torch.cuda.synchronize()
+            A.attn_profile_enable(False)
+            c, ms = A.attn_profile_read("proj")
+            us = ms / iters * 1e3  # a cross-attention QKV projection is two launches per call
+            if kind == "qkv":
+                flops = 2.0 * B * n * dm * hd + 2.0 * B * m * dm * 2 * hd
+                nbytes = 2 * (B * n * dm + (0 if xkv is xq else B * m * dm) + dm * 3 * hd + B * n * hd + 2 * B * m * hd)
+            else:
+                flops = 2.0 * B * n * hd * dm
+                nbytes = 2 * (B * n * hd + hd * dm + B * n * dm)
+            tf = flops / (us * 1e-6) / 1e12
+            res[kind] = {"us": round(us, 1), "launches_per_call": round(c / iters, 2), "tflops": round(tf, 1),
+                         "frac_peak": round(tf / peaks["bf16_tflops"], 3),
+                         "gbs": round(nbytes / (us * 1e-6) / 1e9, 1)}
+        out[name] = res
+        del xq, xkv, w, wo, q, k, v, y
+        torch.cuda.empty_cache()
+    if A.attn_get_device_status() != A.ATTN_OK:
+        raise RuntimeError("device watchdog fired in the projection sweep")
+    return out
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -545,10 +604,11 @@ def main():
         return
 
     res = run_gpu(args, w, world, rank, local)
-    sweep = decode_sweep = None
+    sweep = decode_sweep = proj_sweep = None
     if world == 1 and not args.no_sweep:
         sweep = run_sweep(args, local)
         decode_sweep = run_decode_sweep(args, local)
+        proj_sweep = run_proj_sweep(args, local)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         tf, t, heads, threads = oracle_sample(w, args.cpu_seconds)
@@ -572,6 +632,8 @@ def main():
         line["sweep"] = sweep
     if decode_sweep is not None:
         line["decode_sweep"] = decode_sweep
+    if proj_sweep is not None:
+        line["proj_sweep"] = proj_sweep
     print(json.dumps(line), flush=True)
 
 

@@ -31,6 +31,7 @@ __all__ = [
     "ragged_workloads",
     "kv_lengths",
     "DECODE_WORKLOADS",
+    "PROJ_WORKLOADS",
 ]
 
 
@@ -147,6 +148,16 @@ DECODE_WORKLOADS: Dict[str, Tuple[int, int, int, int, int]] = {
     "decode_b64_h16_n1_m4096_d64": (64, 16, 1, 4096, 64),
     "decode_b64_h16_n4_m4096_d64": (64, 16, 4, 4096, 64),
     "decode_b16_h16_n1_m16384_d128": (16, 16, 1, 16384, 128),
+}
+
+
+# The projections around eq. (1) (§3.2.2): (B, n query tokens, m key tokens,
+# d_model, h, d). The base model's encoder self-attention batch and the big
+# model's encoder-decoder attention (queries from 256 decoder tokens, keys and
+# values from 320 encoder tokens).
+PROJ_WORKLOADS: Dict[str, Tuple[int, int, int, int, int, int]] = {
+    "proj_base_self_b96_n256": (96, 256, 256, 512, 8, 64),
+    "proj_big_cross_b48_n256_m320": (48, 256, 320, 1024, 16, 64),
 }
 
 
