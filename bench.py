@@ -567,9 +567,15 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--soak-seconds", type=float, default=1.0,
                     help="untimed steps before the warm-up so clocks settle (0 for profiler runs)")
+    ap.add_argument("--only", choices=("decode", "proj"),
+                    help="run only the decoding or the projection sweep and print it (for profiling)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.only is not None:
+        fn = run_decode_sweep if args.only == "decode" else run_proj_sweep
+        print(json.dumps({args.only: fn(args, 0)}), flush=True)
+        return
     world, rank, local = dist_setup()
     w = WORKLOADS[args.workload]
     config = {"workload": f"{w.name}: B={w.B}, h={w.h}, n={w.n}, m={w.m}, d_k=d_v={w.d_k}, "
