@@ -29,15 +29,15 @@ constexpr int kPStages = 5;
 constexpr uint32_t kPATile = kPM * kPK * 2;         // 16 KB
 constexpr uint32_t kPBBox = kPK * 64 * 2;           // 8 KB: 64 reduction rows x 64 columns
 constexpr uint32_t kPStage = kPATile + 2 * kPBBox;  // 32 KB
-constexpr uint32_t kPOffOut = kPStages * kPStage;   // staging: 2 x [128 rows x 64 columns] bf16
+constexpr uint32_t kPOffOut = kPStages * kPStage;   // staging: 2 tiles x 2 x [128 rows x 64 columns] bf16
 constexpr uint32_t kPOutBox = kPM * 64 * 2;         // 16 KB
-constexpr uint32_t kPSmem = kPOffOut + 2 * kPOutBox + 1024;
+constexpr uint32_t kPSmem = kPOffOut + 4 * kPOutBox + 1024;
 constexpr int kPThreads = 256;
 
 struct ProjShared {
   uint64_t full[kPStages], empty[kPStages];
   uint64_t acc_full[2], acc_free[2];
-  uint64_t staged, stage_free;
+  uint64_t staged, stage_free[2];
   uint64_t drain;
   uint32_t tmem_base;
   int abort_flag;
@@ -85,7 +85,8 @@ attn_proj_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant
       mbar_init(&sh.acc_free[i], 128);
     }
     mbar_init(&sh.staged, 128);
-    mbar_init(&sh.stage_free, 1);
+    mbar_init(&sh.stage_free[0], 1);
+    mbar_init(&sh.stage_free[1], 1);
     mbar_init(&sh.drain, 1);
     sh.abort_flag = 0;
     fence_mbar_init();
@@ -185,11 +186,13 @@ attn_proj_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant
       const int buf = tc & 1;
       bool ok = __all_sync(0xffffffffu, guarded_wait(&sh.acc_full[buf], static_cast<uint32_t>((tc / 2) & 1),
                                                      abort_flag, wd, kSiteOFull));
-      // the previous tile's stores must have read the staging tiles
-      if (ok && tc >= 1)
-        ok = __all_sync(0xffffffffu, guarded_wait(&sh.stage_free, static_cast<uint32_t>((tc - 1) & 1), abort_flag,
-                                                  wd, kSiteOFull));
+      // staging set sb (of two) was last used by tile tc - 2: its stores must have read it
+      const int sb = tc & 1;
+      if (ok && tc >= 2)
+        ok = __all_sync(0xffffffffu, guarded_wait(&sh.stage_free[sb], static_cast<uint32_t>((tc / 2 - 1) & 1),
+                                                  abort_flag, wd, kSiteOFull));
       if (!ok) break;
+      uint8_t* tstage = stage + sb * 2 * kPOutBox;
       tc_fence_after();
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
@@ -201,7 +204,7 @@ attn_proj_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant
           tc_fence_before();
           mbar_arrive(&sh.acc_free[buf]);  // the MMAs of a later tile may overwrite this accumulator
         }
-        uint8_t* box = stage + half * kPOutBox;
+        uint8_t* box = tstage + half * kPOutBox;
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
           const uint32_t* f = v[c >> 2] + (c & 3) * 8;
@@ -225,15 +228,17 @@ attn_proj_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant
               const int gc = p.n_base + c, hd = p.h * p.d;
               const int which = gc / hd, within = gc - which * hd;
               const CUtensorMap* map = which == 0 ? &tm_o0 : (which == 1 ? &tm_o1 : &tm_o2);
-              tma_store_3d(map, stage + half * kPOutBox, within % p.d, s0, b * p.h + within / p.d);
+              tma_store_3d(map, tstage + half * kPOutBox, within % p.d, s0, b * p.h + within / p.d);
             } else {
-              tma_store_3d(&tm_o0, stage + half * kPOutBox, c, s0, b);
+              tma_store_3d(&tm_o0, tstage + half * kPOutBox, c, s0, b);
             }
           }
           tma_store_commit();
-          bulk_wait_read_all();
         }
-        mbar_arrive(&sh.stage_free);
+        // the previous tile's stores (the other staging set) have read their source
+        // once every group but this tile's has: that set may be written again
+        bulk_wait_read_but_last();
+        if (tc >= 1) mbar_arrive(&sh.stage_free[sb ^ 1]);
       }
     }
     if (r == 0) tma_store_wait_all();  // stores must complete before the CTA exits
