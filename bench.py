@@ -499,7 +499,9 @@ def run_decode_sweep(args, local):
 def run_proj_sweep(args, local):
     """Throughput of the multi-head projections (tensor-bound GEMMs): the QKV
     projection (fused for self-attention) and the output projection, FLOPs
-    2 * tokens * d_model * (columns), bytes = operands read once + results. Rank 0, N=1 only."""
+    2 * tokens * d_model * (columns), bytes = operands read once + results; and
+    their backward (input and weight gradients: twice the FLOPs; all launches of
+    a call, the split reduction included). Rank 0, N=1 only."""
     import torch
     import transformer_scaled_dot_attn_gb300 as A
     from seeded_inputs import PROJ_WORKLOADS
@@ -518,13 +520,30 @@ def run_proj_sweep(args, local):
         k = torch.empty(B, h, m, d, dtype=torch.bfloat16, device=dev)
         v = torch.empty_like(k)
         y = torch.empty(B, n, dm, dtype=torch.bfloat16, device=dev)
+        gq = torch.randn(B, h, n, d, device=dev, generator=g).bfloat16()
+        gk = torch.randn(B, h, m, d, device=dev, generator=g).bfloat16()
+        gv = torch.randn(B, h, m, d, device=dev, generator=g).bfloat16()
+        gy = torch.randn(B, n, dm, device=dev, generator=g).bfloat16()
+        dxq = torch.empty(B, n, dm, dtype=torch.bfloat16, device=dev)
+        dxkv = dxq if xkv is xq else torch.empty(B, m, dm, dtype=torch.bfloat16, device=dev)
+        dw = torch.empty(dm, 3 * hd, dtype=torch.bfloat16, device=dev)
+        d_o = torch.empty(B, h, n, d, dtype=torch.bfloat16, device=dev)
+        dwo = torch.empty(hd, dm, dtype=torch.bfloat16, device=dev)
+        ws = torch.empty(max(A.attn_qkv_projection_bwd_workspace_bytes(B, n, m, dm, h, d),
+                             A.attn_out_projection_bwd_workspace_bytes(B, n, dm, h, d), 16),
+                         dtype=torch.uint8, device=dev)
         res = {}
-        for kind in ("qkv", "out"):
+        for kind in ("qkv", "out", "qkv_bwd", "out_bwd"):
             def call():
                 if kind == "qkv":
                     A.attn_qkv_projection(xq, xkv, w, h, d, q=q, k=k, v=v)
-                else:
+                elif kind == "out":
                     A.attn_out_projection(q, wo, y=y)
+                elif kind == "qkv_bwd":
+                    A.attn_qkv_projection_bwd(xq, xkv, w, gq, gk, gv, dx_q=dxq, dx_kv=dxkv, dw_qkv=dw,
+                                              workspace=ws)
+                else:
+                    A.attn_out_projection_bwd(q, wo, gy, d_o=d_o, dw_o=dwo, workspace=ws)
             for _ in range(3):
                 call()
             torch.cuda.synchronize()
@@ -537,18 +556,27 @@ def run_proj_sweep(args, local):
             A.attn_profile_enable(False)
             c, ms = A.attn_profile_read("proj")
             us = ms / iters * 1e3  # a cross-attention QKV projection is two launches per call
+            xkv_b = 0 if xkv is xq else B * m * dm
             if kind == "qkv":
                 flops = 2.0 * B * n * dm * hd + 2.0 * B * m * dm * 2 * hd
-                nbytes = 2 * (B * n * dm + (0 if xkv is xq else B * m * dm) + dm * 3 * hd + B * n * hd + 2 * B * m * hd)
-            else:
+                nbytes = 2 * (B * n * dm + xkv_b + dm * 3 * hd + B * n * hd + 2 * B * m * hd)
+            elif kind == "out":
                 flops = 2.0 * B * n * hd * dm
                 nbytes = 2 * (B * n * hd + hd * dm + B * n * dm)
+            elif kind == "qkv_bwd":
+                flops = 2 * (2.0 * B * n * dm * hd + 2.0 * B * m * dm * 2 * hd)
+                # reads x, W, dQ, dK, dV; writes dx and dW
+                nbytes = 2 * (B * n * dm + xkv_b + dm * 3 * hd + B * n * hd + 2 * B * m * hd +
+                              B * n * dm + xkv_b + dm * 3 * hd)
+            else:
+                flops = 2 * 2.0 * B * n * hd * dm
+                nbytes = 2 * (B * n * hd + hd * dm + B * n * dm + B * n * hd + hd * dm)
             tf = flops / (us * 1e-6) / 1e12
             res[kind] = {"us": round(us, 1), "launches_per_call": round(c / iters, 2), "tflops": round(tf, 1),
                          "frac_peak": round(tf / peaks["bf16_tflops"], 3),
                          "gbs": round(nbytes / (us * 1e-6) / 1e9, 1)}
         out[name] = res
-        del xq, xkv, w, wo, q, k, v, y
+        del xq, xkv, w, wo, q, k, v, y, gq, gk, gv, gy, dxq, dxkv, dw, d_o, dwo, ws
         torch.cuda.empty_cache()
     if A.attn_get_device_status() != A.ATTN_OK:
         raise RuntimeError("device watchdog fired in the projection sweep")

@@ -211,7 +211,7 @@ int attn_debug_exp2(const float* x, float* y_poly, float* y_mufu, int n, attn_st
  *   kind 0 forward, 1 backward pre-pass (D, padded lse, dQ clear),
  *   kind 2 backward main kernel, 3 backward dQ conversion,
  *   kind 4 decoding step (per key chunk), 5 decoding merge of the chunks,
- *   kind 6 projection GEMM (attn_qkv_projection, attn_out_projection).
+ *   kind 6 projection GEMM (attn_qkv_projection, attn_out_projection and their _bwd).
  * launches / total_ms may be NULL. Returns ATTN_OK, ATTN_ERR_INVALID_ARG for an
  * unknown kind, or ATTN_ERR_CUDA. Enabling costs two event records per launch.
  */
@@ -269,6 +269,40 @@ int attn_qkv_projection(const void* x_q, const void* x_kv, const void* w_qkv, vo
                         int n, int m, int d_model, int h, int d, attn_stream_t stream);
 int attn_out_projection(const void* o, const void* w_o, void* y, int B, int n, int d_model, int h, int d,
                         attn_stream_t stream);
+
+/*
+ * Backward of the projections above (for y = x W and an upstream gradient dy:
+ * dx = dy W^T, dW = x^T dy), as tcgen05 GEMMs with fp32 accumulation and bf16
+ * results. The weight gradients reduce over every token: they run in token
+ * splits whose fp32 partial sums go to the caller's workspace and are added in
+ * split order by a second kernel (deterministic).
+ *
+ * attn_qkv_projection_bwd: given dq [B, h, n, d], dk, dv [B, h, m, d] (bf16,
+ * e.g. from attn_bwd), the inputs x_q, x_kv and w_qkv of attn_qkv_projection:
+ *   dx_q  [B, n, d_model] = Concat(dq) (W^Q)^T              bf16 out
+ *   dx_kv [B, m, d_model] = Concat(dk) (W^K)^T + Concat(dv) (W^V)^T
+ *   dw_qkv [d_model, 3 h d] = x_q^T Concat(dq) | x_kv^T Concat(dk) | x_kv^T Concat(dv)
+ *   Self-attention (x_q == x_kv, n == m) with dx_q == dx_kv: dx_q receives the
+ *   whole input gradient dx = Concat(dq | dk | dv) W_qkv^T (one GEMM), and the
+ *   weight gradient is one GEMM as well.
+ *   workspace: at least attn_qkv_projection_bwd_workspace_bytes(...) bytes,
+ *   device, 16-byte aligned (fp32 partials; every byte read is written first).
+ * attn_out_projection_bwd: given dy [B, n, d_model] and o, w_o of attn_out_projection:
+ *   d_o [B, h, n, d] = dy (W^O)^T in attn_fwd's layout (the dO of attn_bwd)   bf16 out
+ *   dw_o [h d, d_model] = Concat(o)^T dy                                     bf16 out
+ *   workspace: attn_out_projection_bwd_workspace_bytes(...) bytes, as above.
+ * Same shape requirements and return codes as the forward projections; a short
+ * workspace is ATTN_ERR_INVALID_ARG. Asynchronous on `stream`; profiling kind 6.
+ */
+size_t attn_qkv_projection_bwd_workspace_bytes(int B, int n, int m, int d_model, int h, int d);
+int attn_qkv_projection_bwd(const void* x_q, const void* x_kv, const void* w_qkv, const void* dq, const void* dk,
+                            const void* dv, void* dx_q, void* dx_kv, void* dw_qkv, int B, int n, int m,
+                            int d_model, int h, int d, void* workspace, size_t workspace_bytes,
+                            attn_stream_t stream);
+size_t attn_out_projection_bwd_workspace_bytes(int B, int n, int d_model, int h, int d);
+int attn_out_projection_bwd(const void* o, const void* w_o, const void* dy, void* d_o, void* dw_o, int B, int n,
+                            int d_model, int h, int d, void* workspace, size_t workspace_bytes,
+                            attn_stream_t stream);
 
 size_t attn_decode_workspace_bytes(int B, int h, int n, int m, int d_k, int d_v);
 int attn_decode(const void* q, const void* k, const void* v, void* o, float* lse, const int* kv_len,

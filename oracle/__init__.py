@@ -265,6 +265,41 @@ def project_out(o, w_o):
     return O.transpose(0, 2, 1, 3).reshape(B, n, h * d) @ W
 
 
+def project_qkv_bwd(x_q, x_kv, w_qkv, dq, dk, dv):
+    """Gradients of project_qkv for upstream gradients dq [B, h, n, d], dk, dv [B, h, m, d].
+
+    The projections are linear, y = x W, so dx = dy W^T and dW = sum over the
+    batch's tokens of x^T dy, with the head split undone (Concat of the heads'
+    columns, §3.2.2). Returns dx_q [B, n, d_model], dx_kv [B, m, d_model] and
+    dw_qkv [d_model, 3 h d] (fp64).
+    """
+    Xq, Xkv, W = _f64(x_q), _f64(x_kv), _f64(w_qkv)
+    Gq, Gk, Gv = _f64(dq), _f64(dk), _f64(dv)
+    B, h, n, d = Gq.shape
+    hd = h * d
+
+    def concat(G):  # [B, h, S, d] -> [B, S, h d]
+        b, hh, S, dd = G.shape
+        return G.transpose(0, 2, 1, 3).reshape(b, S, hh * dd)
+
+    Cq, Ck, Cv = concat(Gq), concat(Gk), concat(Gv)
+    dx_q = Cq @ W[:, :hd].T
+    dx_kv = Ck @ W[:, hd:2 * hd].T + Cv @ W[:, 2 * hd:].T
+    dw = np.concatenate([np.einsum("bsc,bsj->cj", Xq, Cq), np.einsum("bsc,bsj->cj", Xkv, Ck),
+                         np.einsum("bsc,bsj->cj", Xkv, Cv)], axis=1)
+    return dx_q, dx_kv, dw
+
+
+def project_out_bwd(o, w_o, dy):
+    """Gradients of project_out for dy [B, n, d_model]: d_o = dy (W^O)^T back in the
+    [B, h, n, d] layout, dw_o = sum over tokens of Concat(o)^T dy [h d, d_model] (fp64)."""
+    O, W, G = _f64(o), _f64(w_o), _f64(dy)
+    B, h, n, d = O.shape
+    C = O.transpose(0, 2, 1, 3).reshape(B, n, h * d)
+    d_o = (G @ W.T).reshape(B, n, h, d).transpose(0, 2, 1, 3)
+    return np.ascontiguousarray(d_o), np.einsum("bsj,bsc->jc", C, G)
+
+
 def multi_head(x_q, x_kv, w_qkv, w_o, h: int, d: int, causal: bool = False, scale=None):
     """MultiHead(Q, K, V) = Concat(head_1..head_h) W^O, head_i = Attention(Q W_i^Q, K W_i^K, V W_i^V)."""
     q, k, v = project_qkv(x_q, x_kv, w_qkv, h, d)

@@ -100,3 +100,90 @@ def test_projection_argument_checks():
     wo = torch.zeros(512, 100, dtype=torch.bfloat16, device=DEV)
     with pytest.raises(A.AttnError):
         A.attn_out_projection(o, wo)  # d_model = 100: not a multiple of 64
+
+
+# ---------------------------------------------------------------- backward (dx = dy W^T, dW = x^T dy)
+
+QKV_BWD_CASES = [
+    # (B, n, m, d_model, h, d, self-attention, one input gradient for self-attention)
+    (2, 256, 256, 512, 8, 64, True, True),      # base model: dx and dW one GEMM each
+    (2, 256, 256, 512, 8, 64, True, False),     # same inputs, dx_q and dx_kv apart
+    (2, 200, 320, 512, 8, 64, False, False),    # cross-attention, ragged sequences
+    (3, 130, 130, 512, 4, 128, True, True),     # d = 128
+    (1, 77, 300, 1024, 16, 64, False, False),   # big model width
+    (2, 64, 0, 256, 2, 64, False, False),       # no keys: dW^K = dW^V = 0
+]
+
+
+@pytest.mark.parametrize("case", range(len(QKV_BWD_CASES)))
+def test_qkv_projection_bwd_matches_oracle(case):
+    B, n, m, dm, h, d, self_attn, fused = QKV_BWD_CASES[case]
+    xq = normal_bf16((B, n, dm), 3700 + case)
+    xkv = xq if self_attn else normal_bf16((B, m, dm), 3710 + case)
+    w = _weights(dm, 3 * h * d, 3720 + case)
+    gq = normal_bf16((B, h, n, d), 3730 + case)
+    gk = normal_bf16((B, h, m, d), 3740 + case)
+    gv = normal_bf16((B, h, m, d), 3750 + case)
+    xq_d = xq.to(DEV)
+    xkv_d = xq_d if self_attn else xkv.to(DEV)
+    dx_kv = None if fused else torch.empty((B, m, dm), dtype=torch.bfloat16, device=DEV)
+    dxq, dxkv, dw = A.attn_qkv_projection_bwd(xq_d, xkv_d, w.to(DEV), gq.to(DEV), gk.to(DEV), gv.to(DEV),
+                                              dx_kv=dx_kv)
+    assert A.attn_get_device_status() == A.ATTN_OK
+    rq, rkv, rw = oracle.project_qkv_bwd(xq, xkv, w, gq, gk, gv)
+    if self_attn and fused:
+        assert dxkv.data_ptr() == dxq.data_ptr()
+        assert_close("dx", dxq.cpu(), rq + rkv)
+    else:
+        if n > 0:
+            assert_close("dx_q", dxq.cpu(), rq)
+        if m > 0:
+            assert_close("dx_kv", dxkv.cpu(), rkv)
+    assert_close("dW_qkv", dw.cpu(), rw)
+    if m == 0:
+        assert not dw[:, h * d:].any()
+
+
+OUT_BWD_CASES = [
+    # (B, n, h, d, d_model)
+    (2, 256, 8, 64, 512),
+    (3, 200, 4, 128, 512),
+    (2, 130, 8, 64, 576),     # a last column tile of 64 (dO reduction and dW^O columns)
+    (1, 300, 16, 64, 1024),
+]
+
+
+@pytest.mark.parametrize("case", range(len(OUT_BWD_CASES)))
+def test_out_projection_bwd_matches_oracle(case):
+    B, n, h, d, dm = OUT_BWD_CASES[case]
+    o = normal_bf16((B, h, n, d), 3800 + case)
+    w = _weights(h * d, dm, 3810 + case)
+    gy = normal_bf16((B, n, dm), 3820 + case)
+    d_o, dw = A.attn_out_projection_bwd(o.to(DEV), w.to(DEV), gy.to(DEV))
+    assert A.attn_get_device_status() == A.ATTN_OK
+    r_o, r_w = oracle.project_out_bwd(o, w, gy)
+    assert_close("dO", d_o.cpu(), r_o)
+    assert_close("dW_o", dw.cpu(), r_w)
+
+
+def test_projection_bwd_is_deterministic():
+    """The weight gradients add their token splits in a fixed order: two runs agree bit for bit."""
+    B, n, h, d, dm = 4, 256, 8, 64, 512
+    o = normal_bf16((B, h, n, d), 3900).to(DEV)
+    w = _weights(h * d, dm, 3901).to(DEV)
+    gy = normal_bf16((B, n, dm), 3902).to(DEV)
+    a = A.attn_out_projection_bwd(o, w, gy)[1].clone()
+    b = A.attn_out_projection_bwd(o, w, gy)[1]
+    assert torch.equal(a, b)
+
+
+def test_projection_bwd_rejects_a_short_workspace():
+    B, n, h, d, dm = 2, 128, 4, 64, 256
+    o = normal_bf16((B, h, n, d), 3910).to(DEV)
+    w = _weights(h * d, dm, 3911).to(DEV)
+    gy = normal_bf16((B, n, dm), 3912).to(DEV)
+    need = A.attn_out_projection_bwd_workspace_bytes(B, n, dm, h, d)
+    assert need > 0
+    short = torch.empty(need - 16, dtype=torch.uint8, device=DEV)
+    with pytest.raises(A.AttnError):
+        A.attn_out_projection_bwd(o, w, gy, workspace=short)

@@ -630,3 +630,68 @@ def test_multi_head_against_torch_library(causal, n, m):
         need_weights=False, attn_mask=mask)
     y = oracle.multi_head(xq, xkv, w_qkv, w_o, h, d, causal=causal)
     np.testing.assert_allclose(y, ref.transpose(0, 1).numpy(), rtol=1e-11, atol=1e-12)
+
+
+# ---------------------------------------------------------------- projection gradients (§3.2.2, differentiated)
+
+def _proj_case(seed, B=2, n=5, m=7, h=2, d=4, dm=8):
+    rng = np.random.default_rng(seed)
+    xq = rng.standard_normal((B, n, dm))
+    xkv = rng.standard_normal((B, m, dm))
+    w_qkv = rng.standard_normal((dm, 3 * h * d))
+    w_o = rng.standard_normal((h * d, dm))
+    gq = rng.standard_normal((B, h, n, d))
+    gk = rng.standard_normal((B, h, m, d))
+    gv = rng.standard_normal((B, h, m, d))
+    o = rng.standard_normal((B, h, n, d))
+    gy = rng.standard_normal((B, n, dm))
+    return xq, xkv, w_qkv, w_o, gq, gk, gv, o, gy
+
+
+def test_projection_gradients_match_finite_differences():
+    """For L = <dq, Q> + <dk, K> + <dv, V> (and <dy, Y>) the oracle's gradients are the derivatives
+    of its own forward projections: a central difference along a random direction of (x, W) equals
+    <grad, direction> (the maps are linear, so only rounding separates the two)."""
+    xq, xkv, w_qkv, w_o, gq, gk, gv, o, gy = _proj_case(11)
+    h, d = gq.shape[1], gq.shape[3]
+    rng = np.random.default_rng(12)
+    ux, uk, uw = (rng.standard_normal(a.shape) for a in (xq, xkv, w_qkv))
+
+    def loss(a, b, w):
+        q, k, v = oracle.project_qkv(a, b, w, h, d)
+        return float((gq * q).sum() + (gk * k).sum() + (gv * v).sum())
+
+    eps = 1e-3
+    fd = (loss(xq + eps * ux, xkv + eps * uk, w_qkv + eps * uw) -
+          loss(xq - eps * ux, xkv - eps * uk, w_qkv - eps * uw)) / (2 * eps)
+    dxq, dxkv, dw = oracle.project_qkv_bwd(xq, xkv, w_qkv, gq, gk, gv)
+    an = float((dxq * ux).sum() + (dxkv * uk).sum() + (dw * uw).sum())
+    assert abs(fd - an) <= 1e-8 * max(1.0, abs(an))
+
+    uo, uwo = rng.standard_normal(o.shape), rng.standard_normal(w_o.shape)
+    lo = lambda a, w: float((gy * oracle.project_out(a, w)).sum())
+    fd = (lo(o + eps * uo, w_o + eps * uwo) - lo(o - eps * uo, w_o - eps * uwo)) / (2 * eps)
+    d_o, dwo = oracle.project_out_bwd(o, w_o, gy)
+    an = float((d_o * uo).sum() + (dwo * uwo).sum())
+    assert abs(fd - an) <= 1e-8 * max(1.0, abs(an))
+
+
+def test_projection_gradients_against_torch_autograd():
+    """torch fp64 autograd of the same products (an independent routine): the head split of
+    x W (reshape to heads) and the concatenation Concat(o) W^O, differentiated by the library."""
+    xq, xkv, w_qkv, w_o, gq, gk, gv, o, gy = _proj_case(21, B=3, n=6, m=4, h=3, d=2, dm=5)
+    B, h, n, d = gq.shape
+    m = gk.shape[2]
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).requires_grad_(True)
+    Xq, Xkv, W, O, Wo = t(xq), t(xkv), t(w_qkv), t(o), t(w_o)
+    hd = h * d
+    split = lambda Y, S: Y.reshape(Y.shape[0], S, h, d).transpose(1, 2)
+    q, k, v = split(Xq @ W[:, :hd], n), split(Xkv @ W[:, hd:2 * hd], m), split(Xkv @ W[:, 2 * hd:], m)
+    y = O.transpose(1, 2).reshape(B, n, hd) @ Wo
+    L = (q * torch.from_numpy(gq)).sum() + (k * torch.from_numpy(gk)).sum() + (v * torch.from_numpy(gv)).sum() \
+        + (y * torch.from_numpy(gy)).sum()
+    L.backward()
+    dxq, dxkv, dw = oracle.project_qkv_bwd(xq, xkv, w_qkv, gq, gk, gv)
+    d_o, dwo = oracle.project_out_bwd(o, w_o, gy)
+    for got, ref in ((dxq, Xq.grad), (dxkv, Xkv.grad), (dw, W.grad), (d_o, O.grad), (dwo, Wo.grad)):
+        np.testing.assert_allclose(got, ref.numpy(), rtol=1e-12, atol=1e-12)

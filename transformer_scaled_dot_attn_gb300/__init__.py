@@ -27,7 +27,8 @@ __all__ = [
     "attn_bwd_workspace_bytes", "attn_get_device_status", "attn_status_string",
     "attn_set_watchdog_ns", "attn_debug_inject", "attn_profile_enable", "attn_profile_read",
     "attn_debug_exp2", "attn_bwd_noalloc", "attn_decode", "attn_decode_workspace_bytes",
-    "attn_qkv_projection", "attn_out_projection",
+    "attn_qkv_projection", "attn_out_projection", "attn_qkv_projection_bwd", "attn_out_projection_bwd",
+    "attn_qkv_projection_bwd_workspace_bytes", "attn_out_projection_bwd_workspace_bytes",
     "EXPORTED_SYMBOLS", "KERNEL_KINDS",
 ]
 # attn_fwd / attn_bwd take an optional ``kv_len`` (int32 CUDA tensor [B]: real
@@ -47,7 +48,8 @@ EXPORTED_SYMBOLS = (
     "attn_status_string", "attn_set_watchdog_ns", "attn_debug_inject", "attn_profile_enable",
     "attn_profile_read", "attn_debug_exp2", "attn_bwd_noalloc", "attn_fwd_varlen",
     "attn_bwd_varlen", "attn_fwd_masked", "attn_bwd_masked", "attn_decode_workspace_bytes", "attn_decode",
-    "attn_qkv_projection", "attn_out_projection",
+    "attn_qkv_projection", "attn_out_projection", "attn_qkv_projection_bwd_workspace_bytes",
+    "attn_qkv_projection_bwd", "attn_out_projection_bwd_workspace_bytes", "attn_out_projection_bwd",
 )
 
 # Kernel kinds of attn_profile_read.
@@ -105,6 +107,14 @@ def load_library():
         lib.attn_qkv_projection.restype = I
         lib.attn_out_projection.argtypes = [vp, vp, vp, I, I, I, I, I, vp]
         lib.attn_out_projection.restype = I
+        lib.attn_qkv_projection_bwd_workspace_bytes.argtypes = [I, I, I, I, I, I]
+        lib.attn_qkv_projection_bwd_workspace_bytes.restype = SZ
+        lib.attn_qkv_projection_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, I, I, I, I, I, I, vp, SZ, vp]
+        lib.attn_qkv_projection_bwd.restype = I
+        lib.attn_out_projection_bwd_workspace_bytes.argtypes = [I, I, I, I, I]
+        lib.attn_out_projection_bwd_workspace_bytes.restype = SZ
+        lib.attn_out_projection_bwd.argtypes = [vp, vp, vp, vp, vp, I, I, I, I, I, vp, SZ, vp]
+        lib.attn_out_projection_bwd.restype = I
         lib.attn_bwd_workspace_bytes.argtypes = [I, I, I, I, I, I, I]
         lib.attn_bwd_workspace_bytes.restype = SZ
         lib.attn_get_device_status.argtypes = [vp]
@@ -364,6 +374,83 @@ def attn_out_projection(o, w_o, y=None, stream=None):
     if st != ATTN_OK:
         raise AttnError(st, "attn_out_projection")
     return y
+
+
+def attn_qkv_projection_bwd_workspace_bytes(B, n, m, d_model, h, d) -> int:
+    return int(load_library().attn_qkv_projection_bwd_workspace_bytes(B, n, m, d_model, h, d))
+
+
+def attn_out_projection_bwd_workspace_bytes(B, n, d_model, h, d) -> int:
+    return int(load_library().attn_out_projection_bwd_workspace_bytes(B, n, d_model, h, d))
+
+
+def attn_qkv_projection_bwd(x_q, x_kv, w_qkv, dq, dk, dv, dx_q=None, dx_kv=None, dw_qkv=None, workspace=None,
+                            stream=None):
+    """Gradients of attn_qkv_projection: dx_q, dx_kv [B, S, d_model] and dw_qkv [d_model, 3 h d]
+    from dq [B, h, n, d], dk, dv [B, h, m, d] (bf16 CUDA). Self-attention (x_q is x_kv) with
+    dx_kv omitted: dx_q is the whole input gradient and dx_kv is returned as the same tensor."""
+    import torch
+    lib = load_library()
+    if dq.dim() != 4 or dk.dim() != 4:
+        raise ValueError("dq, dk, dv must be [B, h, S, d]")
+    B, h, n, d = dq.shape
+    m = dk.shape[2]
+    dm = x_q.shape[2]
+    _check_tensor("x_q", x_q, (B, n, dm), torch.bfloat16)
+    _check_tensor("x_kv", x_kv, (B, m, dm), torch.bfloat16)
+    _check_tensor("w_qkv", w_qkv, (dm, 3 * h * d), torch.bfloat16)
+    _check_tensor("dq", dq, (B, h, n, d), torch.bfloat16)
+    _check_tensor("dk", dk, (B, h, m, d), torch.bfloat16)
+    _check_tensor("dv", dv, (B, h, m, d), torch.bfloat16)
+    dev = dq.device
+    self_attn = x_q.data_ptr() == x_kv.data_ptr() and n == m
+    if dx_q is None:
+        dx_q = torch.empty((B, n, dm), dtype=torch.bfloat16, device=dev)
+    if dx_kv is None:
+        dx_kv = dx_q if self_attn else torch.empty((B, m, dm), dtype=torch.bfloat16, device=dev)
+    if dw_qkv is None:
+        dw_qkv = torch.empty((dm, 3 * h * d), dtype=torch.bfloat16, device=dev)
+    _check_tensor("dx_q", dx_q, (B, n, dm), torch.bfloat16)
+    _check_tensor("dx_kv", dx_kv, (B, m, dm), torch.bfloat16)
+    _check_tensor("dw_qkv", dw_qkv, (dm, 3 * h * d), torch.bfloat16)
+    need = lib.attn_qkv_projection_bwd_workspace_bytes(B, n, m, dm, h, d)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+    st = lib.attn_qkv_projection_bwd(_vptr(x_q), _vptr(x_kv), _vptr(w_qkv), _vptr(dq), _vptr(dk), _vptr(dv),
+                                     _vptr(dx_q), _vptr(dx_kv), _vptr(dw_qkv), B, n, m, dm, h, d,
+                                     _vptr(workspace), workspace.numel() * workspace.element_size(),
+                                     _stream_handle(stream))
+    if st != ATTN_OK:
+        raise AttnError(st, "attn_qkv_projection_bwd")
+    return dx_q, dx_kv, dw_qkv
+
+
+def attn_out_projection_bwd(o, w_o, dy, d_o=None, dw_o=None, workspace=None, stream=None):
+    """Gradients of attn_out_projection: d_o [B, h, n, d] (attn_fwd's layout) and
+    dw_o [h d, d_model] from dy [B, n, d_model] (bf16 CUDA)."""
+    import torch
+    lib = load_library()
+    if o.dim() != 4:
+        raise ValueError("o must be [B, h, n, d]")
+    B, h, n, d = o.shape
+    dm = w_o.shape[1]
+    _check_tensor("o", o, (B, h, n, d), torch.bfloat16)
+    _check_tensor("w_o", w_o, (h * d, dm), torch.bfloat16)
+    _check_tensor("dy", dy, (B, n, dm), torch.bfloat16)
+    dev = o.device
+    d_o = torch.empty((B, h, n, d), dtype=torch.bfloat16, device=dev) if d_o is None else d_o
+    dw_o = torch.empty((h * d, dm), dtype=torch.bfloat16, device=dev) if dw_o is None else dw_o
+    _check_tensor("d_o", d_o, (B, h, n, d), torch.bfloat16)
+    _check_tensor("dw_o", dw_o, (h * d, dm), torch.bfloat16)
+    need = lib.attn_out_projection_bwd_workspace_bytes(B, n, dm, h, d)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+    st = lib.attn_out_projection_bwd(_vptr(o), _vptr(w_o), _vptr(dy), _vptr(d_o), _vptr(dw_o), B, n, dm, h, d,
+                                     _vptr(workspace), workspace.numel() * workspace.element_size(),
+                                     _stream_handle(stream))
+    if st != ATTN_OK:
+        raise AttnError(st, "attn_out_projection_bwd")
+    return d_o, dw_o
 
 
 def attn_get_device_status(stream=None) -> int:

@@ -630,6 +630,209 @@ int attn_out_projection(const void* o, const void* w_o, void* y, int B, int n, i
              : ATTN_ERR_CUDA;
 }
 
+// ---------------------------------------------------------------- projection backward
+
+// Token splits of the QKV weight gradient: d_model x 3 h d outputs, the longer
+// of the two token ranges in 64-token chunks.
+static int qkv_bwd_splits(int B, int n, int m, int d_model, int h, int d) {
+  const long long hd = static_cast<long long>(h) * d;
+  const long long chunks = static_cast<long long>(B) * (((n > m ? n : m) + 63) / 64);
+  return attn::proj_bwd_splits(d_model, static_cast<int>(3 * hd), chunks > 0x7fffffff ? 0x7fffffff
+                                                                                     : static_cast<int>(chunks));
+}
+
+static int out_bwd_splits(int B, int n, int d_model, int h, int d) {
+  const long long chunks = static_cast<long long>(B) * ((n + 63) / 64);
+  return attn::proj_bwd_splits(h * d, d_model, chunks > 0x7fffffff ? 0x7fffffff : static_cast<int>(chunks));
+}
+
+size_t attn_qkv_projection_bwd_workspace_bytes(int B, int n, int m, int d_model, int h, int d) {
+  if (check_proj(B, n, d_model, h, d) != ATTN_OK || m < 0 || (static_cast<long long>(h) * d) % 128 != 0) return 0;
+  if (B == 0 || (n == 0 && m == 0)) return 0;
+  const int z = qkv_bwd_splits(B, n, m, d_model, h, d);
+  return static_cast<size_t>(z) * d_model * (3 * static_cast<size_t>(h) * d) * sizeof(float);
+}
+
+size_t attn_out_projection_bwd_workspace_bytes(int B, int n, int d_model, int h, int d) {
+  if (check_proj(B, n, d_model, h, d) != ATTN_OK) return 0;
+  if (B == 0 || n == 0) return 0;
+  const int z = out_bwd_splits(B, n, d_model, h, d);
+  return static_cast<size_t>(z) * (static_cast<size_t>(h) * d) * d_model * sizeof(float);
+}
+
+int attn_qkv_projection_bwd(const void* x_q, const void* x_kv, const void* w_qkv, const void* dq, const void* dk,
+                            const void* dv, void* dx_q, void* dx_kv, void* dw_qkv, int B, int n, int m,
+                            int d_model, int h, int d, void* workspace, size_t workspace_bytes,
+                            attn_stream_t stream) {
+  int st = check_proj(B, n, d_model, h, d);
+  if (st != ATTN_OK) return st;
+  if (m < 0) return ATTN_ERR_INVALID_ARG;
+  if ((static_cast<long long>(h) * d) % 128 != 0) return ATTN_ERR_UNSUPPORTED;
+  const long long BH = static_cast<long long>(B) * h, hd = static_cast<long long>(h) * d;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (B == 0) return ATTN_OK;
+  if (!w_qkv || !dw_qkv || !aligned16(w_qkv) || !aligned16(dw_qkv)) return ATTN_ERR_INVALID_ARG;
+  if (n == 0 && m == 0) {  // no token: the weight gradient is zero
+    return cudaMemsetAsync(dw_qkv, 0, static_cast<size_t>(d_model) * 3 * hd * 2, s) == cudaSuccess ? ATTN_OK
+                                                                                                    : ATTN_ERR_CUDA;
+  }
+  if (n > 0 && (!x_q || !dq || !dx_q || !aligned16(x_q) || !aligned16(dq) || !aligned16(dx_q)))
+    return ATTN_ERR_INVALID_ARG;
+  if (m > 0 && (!x_kv || !dk || !dv || !dx_kv || !aligned16(x_kv) || !aligned16(dk) || !aligned16(dv) ||
+                !aligned16(dx_kv)))
+    return ATTN_ERR_INVALID_ARG;
+  const int z = qkv_bwd_splits(B, n, m, d_model, h, d);
+  if (z <= 0) return ATTN_ERR_CUDA;
+  const size_t need = static_cast<size_t>(z) * d_model * static_cast<size_t>(3 * hd) * sizeof(float);
+  if (workspace == nullptr || !aligned16(workspace) || workspace_bytes < need) return ATTN_ERR_INVALID_ARG;
+  uint32_t* status = nullptr;
+  if (device_status_word(&status) != cudaSuccess) return ATTN_ERR_CUDA;
+  // W rows as the K-major operand of dX; gradients K-major (dX) and MN-major (dW); x MN-major (dW)
+  CUtensorMap tw, gq, gk, gv, gq64, gk64, gv64, xq64, xkv64, oq, okv;
+  if (!make_map3(&tw, w_qkv, 3 * hd, d_model, 1, 128)) return ATTN_ERR_CUDA;
+  if (n > 0 && (!make_tile_map(&gq, dq, BH, n, d) || !make_tile_map(&gq64, dq, BH, n, d, 64) ||
+                !make_map3(&xq64, x_q, d_model, n, B, 64) || !make_map3(&oq, dx_q, d_model, n, B, 128)))
+    return ATTN_ERR_CUDA;
+  if (m > 0 && (!make_tile_map(&gk, dk, BH, m, d) || !make_tile_map(&gv, dv, BH, m, d) ||
+                !make_tile_map(&gk64, dk, BH, m, d, 64) || !make_tile_map(&gv64, dv, BH, m, d, 64) ||
+                !make_map3(&xkv64, x_kv, d_model, m, B, 64) || !make_map3(&okv, dx_kv, d_model, m, B, 128)))
+    return ATTN_ERR_CUDA;
+  attn::ProjBwdParams p{};
+  p.kind = 0;
+  p.B = B;
+  p.N = d_model;
+  p.h = h;
+  p.d = d;
+  p.a_heads = 1;
+  p.wd.status = status;
+  p.wd.budget_ns = g_watchdog_ns.load();
+  const bool self = x_q == x_kv && n == m;
+  if (self && dx_q == dx_kv) {
+    // dx = Concat(dq | dk | dv) W_qkv^T: one reduction over all 3 h d columns
+    p.S = n;
+    p.K = static_cast<int>(3 * hd);
+    p.k_base = 0;
+    if (attn::launch_proj_bwd(gq, gk, gv, tw, tw, tw, oq, p, s) != cudaSuccess) return ATTN_ERR_CUDA;
+  } else {
+    if (n > 0) {
+      p.S = n;
+      p.K = static_cast<int>(hd);
+      p.k_base = 0;
+      if (attn::launch_proj_bwd(gq, gq, gq, tw, tw, tw, oq, p, s) != cudaSuccess) return ATTN_ERR_CUDA;
+    }
+    if (m > 0) {
+      p.S = m;
+      p.K = static_cast<int>(2 * hd);
+      p.k_base = static_cast<int>(hd);
+      if (attn::launch_proj_bwd(gk, gv, gv, tw, tw, tw, okv, p, s) != cudaSuccess) return ATTN_ERR_CUDA;
+    }
+  }
+  // dW partials [z][d_model][3 h d], then their sum in split order
+  float* ws = static_cast<float*>(workspace);
+  attn::ProjBwdParams q{};
+  q.kind = 1;
+  q.B = B;
+  q.M = d_model;
+  q.h = h;
+  q.d = d;
+  q.a_heads = 0;
+  q.b_heads = 1;
+  q.splits = z;
+  q.ws = ws;
+  q.ws_ld = static_cast<int>(3 * hd);
+  q.wd = p.wd;
+  if (self) {
+    q.S = n;
+    q.N = static_cast<int>(3 * hd);
+    q.n_base = 0;
+    if (attn::launch_proj_bwd(xq64, xq64, xq64, gq64, gk64, gv64, tw, q, s) != cudaSuccess) return ATTN_ERR_CUDA;
+  } else {
+    const size_t pitch = static_cast<size_t>(3 * hd) * sizeof(float), rows = static_cast<size_t>(z) * d_model;
+    if (n > 0) {
+      q.S = n;
+      q.N = static_cast<int>(hd);
+      q.n_base = 0;
+      if (attn::launch_proj_bwd(xq64, xq64, xq64, gq64, gq64, gq64, tw, q, s) != cudaSuccess) return ATTN_ERR_CUDA;
+    } else if (cudaMemset2DAsync(ws, pitch, 0, static_cast<size_t>(hd) * sizeof(float), rows, s) != cudaSuccess) {
+      return ATTN_ERR_CUDA;
+    }
+    if (m > 0) {
+      q.S = m;
+      q.N = static_cast<int>(2 * hd);
+      q.n_base = static_cast<int>(hd);
+      if (attn::launch_proj_bwd(xkv64, xkv64, xkv64, gk64, gk64, gv64, tw, q, s) != cudaSuccess)
+        return ATTN_ERR_CUDA;
+    } else if (cudaMemset2DAsync(ws + hd, pitch, 0, static_cast<size_t>(2 * hd) * sizeof(float), rows, s) !=
+               cudaSuccess) {
+      return ATTN_ERR_CUDA;
+    }
+  }
+  return attn::launch_proj_reduce(ws, dw_qkv, static_cast<long long>(d_model) * 3 * hd, z, s) == cudaSuccess
+             ? ATTN_OK
+             : ATTN_ERR_CUDA;
+}
+
+int attn_out_projection_bwd(const void* o, const void* w_o, const void* dy, void* d_o, void* dw_o, int B, int n,
+                            int d_model, int h, int d, void* workspace, size_t workspace_bytes,
+                            attn_stream_t stream) {
+  int st = check_proj(B, n, d_model, h, d);
+  if (st != ATTN_OK) return st;
+  const long long BH = static_cast<long long>(B) * h, hd = static_cast<long long>(h) * d;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (B == 0) return ATTN_OK;
+  if (!w_o || !dw_o || !aligned16(w_o) || !aligned16(dw_o)) return ATTN_ERR_INVALID_ARG;
+  if (n == 0) {  // no token: the weight gradient is zero
+    return cudaMemsetAsync(dw_o, 0, static_cast<size_t>(hd) * d_model * 2, s) == cudaSuccess ? ATTN_OK
+                                                                                            : ATTN_ERR_CUDA;
+  }
+  if (!o || !dy || !d_o || !aligned16(o) || !aligned16(dy) || !aligned16(d_o)) return ATTN_ERR_INVALID_ARG;
+  const int z = out_bwd_splits(B, n, d_model, h, d);
+  if (z <= 0) return ATTN_ERR_CUDA;
+  const size_t need = static_cast<size_t>(z) * static_cast<size_t>(hd) * d_model * sizeof(float);
+  if (workspace == nullptr || !aligned16(workspace) || workspace_bytes < need) return ATTN_ERR_INVALID_ARG;
+  uint32_t* status = nullptr;
+  if (device_status_word(&status) != cudaSuccess) return ATTN_ERR_CUDA;
+  CUtensorMap tdy, tw, tdo, to64, tdy64;
+  if (!make_map3(&tdy, dy, d_model, n, B, 128) || !make_map3(&tw, w_o, d_model, hd, 1, 128) ||
+      !make_tile_map(&tdo, d_o, BH, n, d) || !make_tile_map(&to64, o, BH, n, d, 64) ||
+      !make_map3(&tdy64, dy, d_model, n, B, 64))
+    return ATTN_ERR_CUDA;
+  // dO = dy (W^O)^T, written in the [B, h, n, d] layout
+  attn::ProjBwdParams p{};
+  p.kind = 0;
+  p.B = B;
+  p.S = n;
+  p.K = d_model;
+  p.N = static_cast<int>(hd);
+  p.h = h;
+  p.d = d;
+  p.a_heads = 0;
+  p.out_heads = 1;
+  p.k_base = 0;
+  p.wd.status = status;
+  p.wd.budget_ns = g_watchdog_ns.load();
+  if (attn::launch_proj_bwd(tdy, tdy, tdy, tw, tw, tw, tdo, p, s) != cudaSuccess) return ATTN_ERR_CUDA;
+  // dW^O = Concat(o)^T dy: partials [z][h d][d_model], then their sum
+  float* ws = static_cast<float*>(workspace);
+  attn::ProjBwdParams q{};
+  q.kind = 1;
+  q.B = B;
+  q.S = n;
+  q.M = static_cast<int>(hd);
+  q.N = d_model;
+  q.h = h;
+  q.d = d;
+  q.a_heads = 1;
+  q.b_heads = 0;
+  q.n_base = 0;
+  q.splits = z;
+  q.ws = ws;
+  q.ws_ld = d_model;
+  q.wd = p.wd;
+  if (attn::launch_proj_bwd(to64, to64, to64, tdy64, tdy64, tdy64, tdo, q, s) != cudaSuccess) return ATTN_ERR_CUDA;
+  return attn::launch_proj_reduce(ws, dw_o, hd * d_model, z, s) == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
 int attn_get_device_status(attn_stream_t stream) {
   if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return ATTN_ERR_CUDA;
   uint32_t* status = nullptr;

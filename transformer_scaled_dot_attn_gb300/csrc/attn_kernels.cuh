@@ -224,4 +224,33 @@ struct ProjParams {
 cudaError_t launch_proj(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& to0,
                         const CUtensorMap& to1, const CUtensorMap& to2, ProjParams p, cudaStream_t stream);
 
+struct ProjBwdParams {
+  int kind;        // 0: out = A W^T (rows = tokens); 1: fp32 partials of A^T B over token splits
+  int B, S;        // sequences, tokens per sequence
+  int K;           // kind 0: reduction (multiple of 64)
+  int N;           // output columns of this launch
+  int M;           // kind 1: output rows (weight rows)
+  int h, d;        // heads and head size of the [B, h, S, d] side
+  int a_heads;     // A from [B, h, S, d] maps (kind 0: ta0 | ta1 | ta2 by column / (h d)); else rows (k, s, b)
+  int b_heads;     // kind 1: B from [B, h, S, d] maps tb0 | tb1 | tb2 by column / (h d); else rows (n, s, b)
+  int out_heads;   // kind 0: output into a [B, h, S, d] map; else rows [B, S, N]
+  int k_base;      // kind 0: first W column of the reduction
+  int n_base;      // kind 1: first column of the partial rows (and of the B side) this launch covers
+  int splits;      // kind 1: token splits
+  float* ws;       // kind 1: partials [splits][M][ws_ld] fp32
+  int ws_ld;
+  int tiles_s, tiles_m, chunks_s, chunks, cps, num_units;  // set by the launcher
+  Watchdog wd;
+};
+// Maps (128-byte swizzle): kind 0: ta* (64, 128, 1) boxes, tb0 the W map
+// (columns, rows) with (64, 128) boxes, to the output map (64, 128). kind 1:
+// ta0 and tb* with (64, 64) boxes over (columns, tokens, sequence [x head]).
+cudaError_t launch_proj_bwd(const CUtensorMap& ta0, const CUtensorMap& ta1, const CUtensorMap& ta2,
+                            const CUtensorMap& tb0, const CUtensorMap& tb1, const CUtensorMap& tb2,
+                            const CUtensorMap& to, ProjBwdParams p, cudaStream_t stream);
+// Token splits of a weight gradient of M x N (0 when the device is unknown).
+int proj_bwd_splits(int M, int N, int chunks);
+// out (bf16) = sum over splits of part[z][0 .. count), count a multiple of 8.
+cudaError_t launch_proj_reduce(const float* part, void* out, long long count, int splits, cudaStream_t stream);
+
 }  // namespace attn
