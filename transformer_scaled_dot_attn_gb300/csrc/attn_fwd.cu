@@ -869,6 +869,51 @@ attn_fwd_persist_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
         pending_q = -1;
       }
     };
+    // An item's epilogue: O / l into its Q tile (no MMA reads it once o_full
+    // completed), one thread stores it (rows past n are clipped by the map), lse.
+    // (Deferring it past the next item's first key tile measured slower for
+    // short items: that item's Q then loads later.)
+    struct ItemOut {
+      int qs, q0, bh, row, oc;
+      float l, m;
+    };
+    auto epilogue = [&](const ItemOut& ep) -> bool {
+      if (!__all_sync(0xffffffffu, guarded_wait(&sh.o_full[g], ep.oc & 1, abort_flag, wd, kSiteOFull))) return false;
+      tc_fence_after();
+      const float inv_l = 1.f / ep.l;
+      uint32_t w[D / 2];
+#pragma unroll
+      for (int q = 0; q < D / 16; ++q) {
+        uint32_t o[16];
+        tmem_ld16(t_o + q * 16, o);
+        tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          w[q * 8 + i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
+      }
+      tc_fence_before();
+      mbar_arrive(&sh.o_free[g]);  // the next item's first P.V may overwrite O
+      uint8_t* qtile = smem + C::OFF_Q + (ep.qs * NQ + g) * C::QTILE;
+#pragma unroll
+      for (int ch = 0; ch < D / 8; ++ch) {
+        const int pc = (D == 64) ? (ch ^ (r & 7)) : (ch ^ ((r >> 1) & 3));
+        *reinterpret_cast<uint4*>(qtile + r * (D * 2) + (pc << 4)) =
+            make_uint4(w[4 * ch], w[4 * ch + 1], w[4 * ch + 2], w[4 * ch + 3]);
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(&sh.o_staged[g]);
+      if (r == 0) {
+        release_pending();  // the previous item's store, long done by now
+        if (guarded_wait(&sh.o_staged[g], ep.oc & 1, abort_flag, wd, kSiteOFull)) {
+          tma_store_3d(&tm_o, qtile, 0, ep.q0 + g * 128, ep.bh);
+          tma_store_commit();
+        }
+        pending_q = ep.qs;
+      }
+      if (ep.row < p.n && p.lse != nullptr)
+        p.lse[static_cast<size_t>(ep.bh) * p.n + ep.row] = (ep.m + log2f(ep.l)) * kLn2;
+      return true;
+    };
     for (int it = blockIdx.x, li = 0; ok && it < items; it += gridDim.x, ++li) {
       int bh, q0, mb, ntile[2], nt, nq_valid;
       item_of(it, bh, q0, mb, ntile, nt, nq_valid);
@@ -890,7 +935,7 @@ attn_fwd_persist_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
           ok = __all_sync(0xffffffffu, guarded_wait(&sh.s_full[g], gj & 1, abort_flag, wd, kSiteSFull));
           if (!ok) break;
           tc_fence_after();
-          if (j == 0) release_pending();
+          if (j <= 1) release_pending();  // (a no-op at j = 1; this placement measured faster)
           uint32_t s[C::CHUNKS][32];
   #pragma unroll
           for (int q = 0; q < C::CHUNKS; ++q) tmem_ld32(t_s + q * 32, s[q]);
@@ -1000,7 +1045,7 @@ attn_fwd_persist_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
           ok = __all_sync(0xffffffffu, guarded_wait(&sh.s_full[g], gj & 1, abort_flag, wd, kSiteSFull));
           if (!ok) break;
           tc_fence_after();
-          if (j == 0) release_pending();
+          if (j <= 1) release_pending();  // (a no-op at j = 1; this placement measured faster)
           uint32_t s[C::CHUNKS][32];
   #pragma unroll
           for (int q = 0; q < C::CHUNKS; ++q) tmem_ld32(t_s + q * 32, s[q]);
@@ -1077,42 +1122,8 @@ attn_fwd_persist_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
         }
       }
       if (!ok) break;
-      // epilogue: O / l into the Q tile of this item (no MMA reads it once o_full
-      // completed), one thread stores it; rows past n are clipped by the map
-      ok = __all_sync(0xffffffffu, guarded_wait(&sh.o_full[g], oc & 1, abort_flag, wd, kSiteOFull));
-      if (!ok) break;
-      tc_fence_after();
-      const float inv_l = 1.f / l;
-      uint32_t w[D / 2];
-#pragma unroll
-      for (int q = 0; q < D / 16; ++q) {
-        uint32_t o[16];
-        tmem_ld16(t_o + q * 16, o);
-        tmem_ld_wait();
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-          w[q * 8 + i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
-      }
-      tc_fence_before();
-      mbar_arrive(&sh.o_free[g]);  // the next item's first P.V may overwrite O
-      uint8_t* qtile = smem + C::OFF_Q + (qs * NQ + g) * C::QTILE;
-#pragma unroll
-      for (int ch = 0; ch < D / 8; ++ch) {
-        const int pc = (D == 64) ? (ch ^ (r & 7)) : (ch ^ ((r >> 1) & 3));
-        *reinterpret_cast<uint4*>(qtile + r * (D * 2) + (pc << 4)) =
-            make_uint4(w[4 * ch], w[4 * ch + 1], w[4 * ch + 2], w[4 * ch + 3]);
-      }
-      fence_proxy_async_smem();
-      mbar_arrive(&sh.o_staged[g]);
-      if (r == 0) {
-        release_pending();  // the previous item's store, long done by now
-        if (guarded_wait(&sh.o_staged[g], oc & 1, abort_flag, wd, kSiteOFull)) {
-          tma_store_3d(&tm_o, qtile, 0, q0 + g * 128, bh);
-          tma_store_commit();
-        }
-        pending_q = qs;
-      }
-      if (row < p.n && p.lse != nullptr) p.lse[static_cast<size_t>(bh) * p.n + row] = (m_used + log2f(l)) * kLn2;
+      release_pending();
+      if (!(ok = epilogue(ItemOut{qs, q0, bh, row, oc, l, m_used}))) break;
       gt += T;
       ++oc;
     }
