@@ -8,6 +8,7 @@ import ctypes
 import os
 import subprocess
 
+import numpy as np
 import pytest
 
 import oracle
@@ -87,3 +88,85 @@ def test_planted_mistake_is_caught(name, tmp_path, monkeypatch):
         except (AssertionError, RuntimeError, ValueError, FloatingPointError):
             failed.append(fn.__name__)
     assert failed, f"no pin caught the planted mistake {name!r}"
+
+
+# ---------------------------------------------------------------- projection gradients (Python oracle)
+
+def _concat(G):
+    b, hh, S, dd = G.shape
+    return G.transpose(0, 2, 1, 3).reshape(b, S, hh * dd)
+
+
+def _qkv_bwd(x_q, x_kv, w_qkv, dq, dk, dv, concat=_concat, swap_kv=False, kv_weights_from=None):
+    """project_qkv_bwd written out again with one switch per planted mistake."""
+    Xq, Xkv, W = (np.asarray(a, dtype=np.float64) for a in (x_q, x_kv, w_qkv))
+    Cq, Ck, Cv = (concat(np.asarray(a, dtype=np.float64)) for a in (dq, dk, dv))
+    hd = Cq.shape[-1]
+    Wk, Wv = W[:, hd:2 * hd], W[:, 2 * hd:]
+    if swap_kv:
+        Wk, Wv = Wv, Wk
+    dx_q = Cq @ W[:, :hd].T
+    dx_kv = Ck @ Wk.T + Cv @ Wv.T
+    Xw = Xkv if kv_weights_from is None else kv_weights_from(Xq, Xkv)
+    dw = np.concatenate([np.einsum("bsc,bsj->cj", Xq, Cq), np.einsum("bsc,bsj->cj", Xw, Ck),
+                         np.einsum("bsc,bsj->cj", Xw, Cv)], axis=1)
+    return dx_q, dx_kv, dw
+
+
+def _plain_reshape(G):  # heads and tokens mixed up
+    return G.reshape(G.shape[0], G.shape[2], -1)
+
+
+def _queries_cut_to_keys(Xq, Xkv):  # x_q where x_kv belongs (cut or padded to the key count)
+    m = Xkv.shape[1]
+    out = np.zeros_like(Xkv)
+    k = min(m, Xq.shape[1])
+    out[:, :k] = Xq[:, :k]
+    return out
+
+
+def _out_bwd(o, w_o, dy, heads_back=True, first_sequence_only=False):
+    O, W, G = (np.asarray(a, dtype=np.float64) for a in (o, w_o, dy))
+    B, h, n, d = O.shape
+    C = O.transpose(0, 2, 1, 3).reshape(B, n, h * d)
+    g = G @ W.T
+    d_o = g.reshape(B, n, h, d).transpose(0, 2, 1, 3) if heads_back else g.reshape(B, h, n, d)
+    dw = np.einsum("bsj,bsc->jc", C[:1], G[:1]) if first_sequence_only else np.einsum("bsj,bsc->jc", C, G)
+    return np.ascontiguousarray(d_o), dw
+
+
+PY_MUTANTS = {
+    "qkv_bwd_kv_blocks_swapped": ("project_qkv_bwd", lambda *a: _qkv_bwd(*a, swap_kv=True)),
+    "qkv_bwd_heads_not_transposed": ("project_qkv_bwd", lambda *a: _qkv_bwd(*a, concat=_plain_reshape)),
+    "qkv_bwd_key_weights_from_queries": ("project_qkv_bwd",
+                                         lambda *a: _qkv_bwd(*a, kv_weights_from=_queries_cut_to_keys)),
+    "out_bwd_heads_not_transposed_back": ("project_out_bwd", lambda *a: _out_bwd(*a, heads_back=False)),
+    "out_bwd_weight_sum_over_one_sequence": ("project_out_bwd", lambda *a: _out_bwd(*a, first_sequence_only=True)),
+}
+
+
+def test_projection_gradient_rewrite_agrees_with_the_oracle():
+    """The rewrite above, with no switch set, is the oracle's result (so a caught mutant is the switch)."""
+    rng = np.random.default_rng(5)
+    xq, xkv = rng.standard_normal((2, 5, 6)), rng.standard_normal((2, 7, 6))
+    w = rng.standard_normal((6, 3 * 4))
+    dq, dk, dv = rng.standard_normal((2, 2, 5, 2)), rng.standard_normal((2, 2, 7, 2)), rng.standard_normal((2, 2, 7, 2))
+    for got, ref in zip(_qkv_bwd(xq, xkv, w, dq, dk, dv), oracle.project_qkv_bwd(xq, xkv, w, dq, dk, dv)):
+        np.testing.assert_allclose(got, ref, rtol=0, atol=1e-12)
+    o, wo, dy = rng.standard_normal((2, 2, 5, 2)), rng.standard_normal((4, 6)), rng.standard_normal((2, 5, 6))
+    for got, ref in zip(_out_bwd(o, wo, dy), oracle.project_out_bwd(o, wo, dy)):
+        np.testing.assert_allclose(got, ref, rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("name", sorted(PY_MUTANTS))
+def test_planted_projection_gradient_mistake_is_caught(name, monkeypatch):
+    attr, fn = PY_MUTANTS[name]
+    monkeypatch.setattr(oracle, attr, fn)
+    failed = 0
+    for pin in (pins.test_projection_gradients_match_finite_differences,
+                pins.test_projection_gradients_against_torch_autograd):
+        try:
+            pin()
+        except (AssertionError, ValueError):
+            failed += 1
+    assert failed >= 1, f"no pin caught the planted mistake {name}"
