@@ -142,6 +142,7 @@ struct BwdParams {
   int num_kblocks;          // ceil(m / 128)
   int BH;                   // heads (set by the launcher)
   int num_items;            // BH * num_kblocks work items (set by the launcher)
+  int head_major;           // item order: head major (1) or key-tile major (0) (set by the launcher)
   const int* kv_len;        // [B] real keys per sequence (key padding) or nullptr
   int h;                    // heads per sequence
   int wl, wr;               // window (see FwdParams)
