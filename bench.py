@@ -330,13 +330,19 @@ def run_gpu(args, w: Workload, world, rank, local):
     total_flops = reduce_sum(step_flops(w) * args.steps, world)
     value = total_flops / (ms_max / 1e3) / 1e12
 
-    # ---- end to end: pinned host inputs -> device -> fwd+bwd -> O, dQ, dK, dV back to host
+    # ---- end to end: pinned host inputs -> device -> fwd+bwd -> O, dQ, dK, dV back to host.
+    # The library's host-buffer step (attn_fwd_bwd_host) splits the heads into
+    # chunks whose copies in both directions overlap the kernels; the plain
+    # sequence (all inputs in, fwd, bwd, all results out, one stream) is timed
+    # beside it. Masked workloads (key padding, windows) have no host step.
     hq, hk, hv, hdo = [t.cpu().pin_memory() for t in sets[0]]
     d_in = [torch.empty_like(t) for t in sets[0]]
     outs_h = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (o, dq, dk, dv)]
     e2e_steps = max(1, min(args.steps, 20))
+    host_step = kvl is None and w.window is None
+    hbuf = A.HostStepBuffers(w.B, w.h, w.n, w.m, w.d_k, w.d_v, w.causal, device=dev) if host_step else None
 
-    def e2e_step():
+    def e2e_serial():
         for dst, src in zip(d_in, (hq, hk, hv, hdo)):
             dst.copy_(src, non_blocking=True)
         A.attn_fwd(d_in[0], d_in[1], d_in[2], causal=w.causal, scale=scale, out=o, lse=lse, kv_len=kvl,
@@ -346,17 +352,27 @@ def run_gpu(args, w: Workload, world, rank, local):
         for dst, src in zip(outs_h, (o, dq, dk, dv)):
             dst.copy_(src, non_blocking=True)
 
-    e2e_step()
-    torch.cuda.synchronize()
-    barrier(world)
-    s2, e2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    s2.record(stream)
-    for _ in range(e2e_steps):
-        e2e_step()
-    e2.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = reduce_max(s2.elapsed_time(e2), world)
-    e2e_value = reduce_sum(step_flops(w) * e2e_steps, world) / (e2e_ms / 1e3) / 1e12
+    def e2e_pipelined():
+        A.attn_fwd_bwd_host(hq, hk, hv, hdo, causal=w.causal, scale=scale, buffers=hbuf, chunks=args.chunks,
+                            out=(outs_h[0], None, outs_h[1], outs_h[2], outs_h[3]), stream=stream)
+
+    def time_e2e(fn):
+        fn()
+        torch.cuda.synchronize()
+        barrier(world)
+        s2, e2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s2.record(stream)
+        for _ in range(e2e_steps):
+            fn()
+        e2.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = reduce_max(s2.elapsed_time(e2), world)
+        return reduce_sum(step_flops(w) * e2e_steps, world) / (e2e_ms / 1e3) / 1e12
+
+    serial_value = time_e2e(e2e_serial)
+    e2e_value = time_e2e(e2e_pipelined) if host_step else serial_value
+    if A.attn_get_device_status() != A.ATTN_OK:
+        raise RuntimeError("device watchdog fired in the end-to-end steps")
     h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hdo))
     d2h = sum(t.numel() * t.element_size() for t in outs_h)
 
@@ -393,7 +409,10 @@ def run_gpu(args, w: Workload, world, rank, local):
     return {
         "value": value, "ms_per_step": ms_max / args.steps, "launches": launches,
         "e2e": {"value": round(e2e_value, 3), "unit": UNIT, "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+                "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+                "api": "attn_fwd_bwd_host" if host_step else "attn_fwd + attn_bwd",
+                "chunks": args.chunks if host_step else None,
+                "serial_value": round(serial_value, 3)},
         "roofline": roof, "kernels": per_kernel, "clocks": clocks, "n_sets": n_sets,
         "l2_bytes": l2, "set_bytes": set_bytes, "peaks": peaks,
     }
@@ -595,6 +614,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--soak-seconds", type=float, default=1.0,
                     help="untimed steps before the warm-up so clocks settle (0 for profiler runs)")
+    ap.add_argument("--chunks", type=int, default=0,
+                    help="head chunks of the end-to-end host step (0: the library chooses)")
     ap.add_argument("--only", choices=("decode", "proj"),
                     help="run only the decoding or the projection sweep and print it (for profiling)")
     args = ap.parse_args()

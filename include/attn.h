@@ -123,6 +123,50 @@ int attn_bwd_noalloc(const void* q, const void* k, const void* v, const void* o,
                      int d_k, int d_v, int causal, float scale, attn_stream_t stream);
 
 /*
+ * One forward and backward pass (attn_fwd then attn_bwd, same arguments and
+ * results) whose inputs and results are in HOST memory: a training step for a
+ * caller that keeps its activations on the host. The B*h heads are split into
+ * `chunks` groups of consecutive heads; the host-to-device copies of a group,
+ * the kernels of an earlier group and the device-to-host copies of a still
+ * earlier one run at the same time, so the step costs about the two
+ * directions' copies sharing the host link rather than the sum of both
+ * directions and the kernels.
+ *   hq, hk, hv, hdO      inputs, host memory, [B,h,S,d] bf16 as for attn_bwd
+ *   ho, hlse             O and lse, host memory; either may be NULL (not copied back)
+ *   hdq, hdk, hdv        gradients, host memory
+ *   q, k, v, dO, o, lse, dq, dk, dv
+ *                        caller-owned device buffers of the full sizes (as
+ *                        attn_fwd / attn_bwd take them); the call copies the
+ *                        inputs into them and leaves every result in them too
+ *   workspace            device memory of at least
+ *                        attn_bwd_workspace_bytes(B, h, n, m, d_k, d_v, causal)
+ *                        bytes (NULL when that is 0); the chunks use it one
+ *                        after another
+ *   chunks               0: chosen by the library (about 24 MiB of inputs a
+ *                        group, at most 8 groups); else the number of groups,
+ *                        capped at 64 and at B*h
+ * Host buffers should be page-locked (cudaHostAlloc / cudaHostRegister):
+ * copies from pageable memory are correct but do not overlap. The work starts
+ * after what is already queued on `stream`, and later work on `stream` starts
+ * after all of it, copies included; the host buffers must stay valid and the
+ * results must not be read before then (synchronise `stream`). The library
+ * creates its copy streams and events on the first call on a device and keeps
+ * them; calls on one device are serialised on the host. The results equal
+ * those of attn_fwd + attn_bwd on the whole batch (every head is computed
+ * alone; only the accumulation order of dQ in the long-sequence backward may
+ * differ). Returns the codes of attn_fwd / attn_bwd, checked before anything
+ * is enqueued; ATTN_ERR_INVALID_ARG also for a null host pointer (other than
+ * ho, hlse), a null device buffer, a negative `chunks` or a short workspace.
+ * With n == 0 the query-side pointers (hq, hdO, hdq, q, dO, o, lse, dq) may be
+ * NULL and the call returns dK = dV = 0. B*h == 0: ATTN_OK, nothing enqueued. There is no key padding or window
+ * variant. This entry point is an addition of this library.
+ */
+int attn_fwd_bwd_host(const void* hq, const void* hk, const void* hv, const void* hdO, void* ho, float* hlse,
+                      void* hdq, void* hdk, void* hdv, void* q, void* k, void* v, void* dO, void* o, float* lse,
+                      void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes, int B, int h, int n,
+                      int m, int d_k, int d_v, int causal, float scale, int chunks, attn_stream_t stream);
+
+/*
  * Key-padding variants (variable-length batches). The pages batch sentences
  * of similar length (§5.1) and pad them (the <pad> positions of
  * Figure 3); here sequence b of the batch has kv_len[b] real keys, the first
@@ -219,32 +263,6 @@ int attn_profile_enable(int on);
 int attn_profile_read(int kind, int* launches, double* total_ms);
 
 /*
- * One incremental decoding step with a key/value cache ("Attention Is All You
- * Need" §3: the decoder emits one symbol at a time; each step attends to every
- * position produced so far, itself included). Sequence b has L_b = kv_len[b]
- * cached positions (all m when kv_len is NULL; clamped to [0, m]); its n
- * newest positions, L_b - n .. L_b - 1, are the queries: query i sees the keys
- * j <= L_b - n + i (the decoder's causal mask aligned to the end of the cache;
- * a query before the cache start, when L_b < n, sees nothing and is the empty
- * sum: O = 0, lse = -inf).
- *   q    [B, h, n, d_k]  bf16, device, 16-byte aligned; 1 <= n <= 16
- *   k, v [B, h, m, d]    bf16, device, 16-byte aligned: the caches, capacity m
- *   o    [B, h, n, d_v]  bf16 out;  lse [B, h, n] fp32 out (natural log) or NULL
- *   kv_len [B]           int32, device, 4-byte aligned, or NULL
- *   scale                multiplies q.k (1/sqrt(d_k) for eq. (1)); finite
- *   workspace            caller-owned device memory of at least
- *                        attn_decode_workspace_bytes(B, h, n, m, d_k, d_v)
- *                        bytes, 16-byte aligned (fp32 partial results of the
- *                        key chunks); every byte the step reads it writes first
- * The keys of each head are split into chunks processed by separate CTAs on
- * the FP32 pipes (the step reads each cached element once and is bound by
- * HBM); a second kernel merges the chunks. d_k = d_v in {32, 64, 128}.
- * Returns ATTN_OK, ATTN_ERR_INVALID_ARG (null or misaligned pointer, n outside
- * [1, 16], m < 1, short workspace, non-finite scale), ATTN_ERR_UNSUPPORTED
- * (d_k != d_v, other head sizes, B*h too large) or ATTN_ERR_CUDA. B*h = 0:
- * ATTN_OK, nothing launched. Asynchronous on `stream`, like attn_fwd.
- */
-/*
  * The multi-head projections around eq. (1) ("Attention Is All You Need"
  * §3.2.2: head_i = Attention(Q W_i^Q, K W_i^K, V W_i^V), MultiHead =
  * Concat(head_1, ..., head_h) W^O), as tcgen05 GEMMs (bf16 operands, fp32
@@ -304,6 +322,32 @@ int attn_out_projection_bwd(const void* o, const void* w_o, const void* dy, void
                             int d_model, int h, int d, void* workspace, size_t workspace_bytes,
                             attn_stream_t stream);
 
+/*
+ * One incremental decoding step with a key/value cache ("Attention Is All You
+ * Need" §3: the decoder emits one symbol at a time; each step attends to every
+ * position produced so far, itself included). Sequence b has L_b = kv_len[b]
+ * cached positions (all m when kv_len is NULL; clamped to [0, m]); its n
+ * newest positions, L_b - n .. L_b - 1, are the queries: query i sees the keys
+ * j <= L_b - n + i (the decoder's causal mask aligned to the end of the cache;
+ * a query before the cache start, when L_b < n, sees nothing and is the empty
+ * sum: O = 0, lse = -inf).
+ *   q    [B, h, n, d_k]  bf16, device, 16-byte aligned; 1 <= n <= 16
+ *   k, v [B, h, m, d]    bf16, device, 16-byte aligned: the caches, capacity m
+ *   o    [B, h, n, d_v]  bf16 out;  lse [B, h, n] fp32 out (natural log) or NULL
+ *   kv_len [B]           int32, device, 4-byte aligned, or NULL
+ *   scale                multiplies q.k (1/sqrt(d_k) for eq. (1)); finite
+ *   workspace            caller-owned device memory of at least
+ *                        attn_decode_workspace_bytes(B, h, n, m, d_k, d_v)
+ *                        bytes, 16-byte aligned (fp32 partial results of the
+ *                        key chunks); every byte the step reads it writes first
+ * The keys of each head are split into chunks processed by separate CTAs on
+ * the FP32 pipes (the step reads each cached element once and is bound by
+ * HBM); a second kernel merges the chunks. d_k = d_v in {32, 64, 128}.
+ * Returns ATTN_OK, ATTN_ERR_INVALID_ARG (null or misaligned pointer, n outside
+ * [1, 16], m < 1, short workspace, non-finite scale), ATTN_ERR_UNSUPPORTED
+ * (d_k != d_v, other head sizes, B*h too large) or ATTN_ERR_CUDA. B*h = 0:
+ * ATTN_OK, nothing launched. Asynchronous on `stream`, like attn_fwd.
+ */
 size_t attn_decode_workspace_bytes(int B, int h, int n, int m, int d_k, int d_v);
 int attn_decode(const void* q, const void* k, const void* v, void* o, float* lse, const int* kv_len,
                 int B, int h, int n, int m, int d_k, int d_v, float scale, void* workspace,

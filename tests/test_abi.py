@@ -133,3 +133,43 @@ def test_varlen_argument_checks(lib):
     st = lib.attn_fwd_varlen(vp(FAKE), vp(FAKE), vp(FAKE), vp(FAKE), f, vp(FAKE), 1, 1, 8, 8, 48, 48, 0,
                              0.125, None)
     assert st == A.ATTN_ERR_UNSUPPORTED
+
+
+def test_host_step_argument_checks(lib):
+    """attn_fwd_bwd_host refuses bad arguments before it enqueues anything."""
+    vp = ctypes.c_void_p
+    f = ctypes.cast(vp(FAKE), ctypes.POINTER(ctypes.c_float))
+
+    def call(B_=1, h=2, n=8, m=8, d=64, chunks=0, hq=FAKE, dq=FAKE, q=FAKE, ws=None, ws_bytes=0,
+             scale=0.125):
+        host = [vp(hq) if hq else None, vp(FAKE), vp(FAKE), vp(FAKE), None, None,
+                vp(FAKE), vp(FAKE), vp(FAKE)]
+        dev = [vp(q) if q else None, vp(FAKE), vp(FAKE), vp(FAKE), vp(FAKE), f,
+               vp(dq) if dq else None, vp(FAKE), vp(FAKE)]
+        return lib.attn_fwd_bwd_host(*host, *dev, vp(ws) if ws else None, ws_bytes, B_, h, n, m, d, d, 0,
+                                     scale, chunks, None)
+
+    assert call(chunks=-1) == A.ATTN_ERR_INVALID_ARG
+    assert call(B_=-1) == A.ATTN_ERR_INVALID_ARG
+    assert call(m=0) == A.ATTN_ERR_INVALID_ARG
+    assert call(scale=float("nan")) == A.ATTN_ERR_INVALID_ARG
+    assert call(d=48) == A.ATTN_ERR_UNSUPPORTED
+    assert call(hq=0) == A.ATTN_ERR_INVALID_ARG
+    assert call(dq=0) == A.ATTN_ERR_INVALID_ARG
+    assert call(q=FAKE + 8) == A.ATTN_ERR_INVALID_ARG
+    # n = 300 takes the general backward: it needs the whole batch's workspace
+    need = A.attn_bwd_workspace_bytes(1, 2, 300, 8, 64, 64, False)
+    assert need > 0
+    assert call(n=300) == A.ATTN_ERR_INVALID_ARG
+    assert call(n=300, ws=FAKE, ws_bytes=need - 16) == A.ATTN_ERR_INVALID_ARG
+    # nothing to compute: OK with null pointers everywhere
+    assert lib.attn_fwd_bwd_host(*([None] * 18), None, 0, 0, 4, 8, 8, 64, 64, 0, 0.125, 0, None) == A.ATTN_OK
+
+
+def test_host_step_binding_checks_host_tensors(lib):
+    import torch
+    x = torch.zeros(1, 1, 4, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="float32|bfloat16"):
+        A.attn_fwd_bwd_host(x.float(), x, x, x)
+    with pytest.raises(ValueError, match="shape"):
+        A.attn_fwd_bwd_host(x, x, x, x[:, :, :2])

@@ -29,7 +29,7 @@ __all__ = [
     "attn_debug_exp2", "attn_bwd_noalloc", "attn_decode", "attn_decode_workspace_bytes",
     "attn_qkv_projection", "attn_out_projection", "attn_qkv_projection_bwd", "attn_out_projection_bwd",
     "attn_qkv_projection_bwd_workspace_bytes", "attn_out_projection_bwd_workspace_bytes",
-    "EXPORTED_SYMBOLS", "KERNEL_KINDS",
+    "attn_fwd_bwd_host", "HostStepBuffers", "EXPORTED_SYMBOLS", "KERNEL_KINDS",
 ]
 # attn_fwd / attn_bwd take an optional ``kv_len`` (int32 CUDA tensor [B]: real
 # keys per sequence) and an optional ``window`` = (left, right) (restricted
@@ -50,6 +50,7 @@ EXPORTED_SYMBOLS = (
     "attn_bwd_varlen", "attn_fwd_masked", "attn_bwd_masked", "attn_decode_workspace_bytes", "attn_decode",
     "attn_qkv_projection", "attn_out_projection", "attn_qkv_projection_bwd_workspace_bytes",
     "attn_qkv_projection_bwd", "attn_out_projection_bwd_workspace_bytes", "attn_out_projection_bwd",
+    "attn_fwd_bwd_host",
 )
 
 # Kernel kinds of attn_profile_read.
@@ -115,6 +116,9 @@ def load_library():
         lib.attn_out_projection_bwd_workspace_bytes.restype = SZ
         lib.attn_out_projection_bwd.argtypes = [vp, vp, vp, vp, vp, I, I, I, I, I, vp, SZ, vp]
         lib.attn_out_projection_bwd.restype = I
+        lib.attn_fwd_bwd_host.argtypes = [vp, vp, vp, vp, vp, fp, vp, vp, vp, vp, vp, vp, vp, vp, fp, vp, vp, vp,
+                                          vp, SZ, I, I, I, I, I, I, I, F, I, vp]
+        lib.attn_fwd_bwd_host.restype = I
         lib.attn_bwd_workspace_bytes.argtypes = [I, I, I, I, I, I, I]
         lib.attn_bwd_workspace_bytes.restype = SZ
         lib.attn_get_device_status.argtypes = [vp]
@@ -287,6 +291,89 @@ def attn_bwd(q, k, v, o, lse, dO, causal: bool = False, scale: Optional[float] =
     if st != ATTN_OK:
         raise AttnError(st, "attn_bwd")
     return dq, dk, dv
+
+
+class HostStepBuffers:
+    """Device buffers of attn_fwd_bwd_host for one set of sizes (allocated once,
+    reused by every call): q, k, v, dO, o, lse, dq, dk, dv and the workspace."""
+
+    def __init__(self, B, h, n, m, d_k, d_v, causal=False, device=None):
+        import torch
+        dev = torch.device("cuda") if device is None else torch.device(device)
+        bf = torch.bfloat16
+        self.shape = (B, h, n, m, d_k, d_v)
+        self.q = torch.empty((B, h, n, d_k), dtype=bf, device=dev)
+        self.k = torch.empty((B, h, m, d_k), dtype=bf, device=dev)
+        self.v = torch.empty((B, h, m, d_v), dtype=bf, device=dev)
+        self.dO = torch.empty((B, h, n, d_v), dtype=bf, device=dev)
+        self.o = torch.empty((B, h, n, d_v), dtype=bf, device=dev)
+        self.lse = torch.empty((B, h, n), dtype=torch.float32, device=dev)
+        self.dq, self.dk, self.dv = torch.empty_like(self.q), torch.empty_like(self.k), torch.empty_like(self.v)
+        need = attn_bwd_workspace_bytes(B, h, n, m, d_k, d_v, causal)
+        self.workspace = torch.empty(max(need, 16) // 4 + 4, dtype=torch.float32, device=dev)
+
+
+def _check_host(name, t, shape, dtype):
+    import torch
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.is_cuda:
+        raise ValueError(f"{name} must be a host (CPU) tensor")
+    if t.dtype != dtype or not t.is_contiguous() or tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must be a contiguous {dtype} tensor of shape {tuple(shape)}")
+
+
+def attn_fwd_bwd_host(q, k, v, dO, causal: bool = False, scale: Optional[float] = None, out=None,
+                      buffers: Optional[HostStepBuffers] = None, chunks: int = 0, need_lse: bool = True,
+                      stream=None):
+    """Forward and backward with HOST inputs and results: q, dO [B,h,n,d], k, v
+    [B,h,m,d] bf16 CPU tensors (page-locked for the copies to overlap).
+
+    Returns host tensors (O, lse, dQ, dK, dV) (lse None when need_lse is False);
+    ``out`` may give them (same order). ``buffers`` holds the device memory
+    (allocated here when None). The copies and kernels are enqueued on
+    ``stream``'s device and the call returns without waiting: synchronise the
+    stream before reading the results."""
+    import torch
+    lib = load_library()
+    if q.dim() != 4 or k.dim() != 4 or v.dim() != 4:
+        raise ValueError("q, k, v must be [B, h, S, d]")
+    B, h, n, d_k = q.shape
+    m, d_v = k.shape[2], v.shape[3]
+    bf = torch.bfloat16
+    for name, t, shp in (("q", q, (B, h, n, d_k)), ("k", k, (B, h, m, d_k)), ("v", v, (B, h, m, d_v)),
+                         ("dO", dO, (B, h, n, d_v))):
+        _check_host(name, t, shp, bf)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d_k)
+    if buffers is None:
+        buffers = HostStepBuffers(B, h, n, m, d_k, d_v, causal)
+    if buffers.shape != (B, h, n, m, d_k, d_v):
+        raise ValueError(f"buffers are for sizes {buffers.shape}, not {(B, h, n, m, d_k, d_v)}")
+    pin = torch.cuda.is_available()
+    if out is None:
+        out = (torch.empty((B, h, n, d_v), dtype=bf, pin_memory=pin),
+               torch.empty((B, h, n), dtype=torch.float32, pin_memory=pin) if need_lse else None,
+               torch.empty((B, h, n, d_k), dtype=bf, pin_memory=pin),
+               torch.empty((B, h, m, d_k), dtype=bf, pin_memory=pin),
+               torch.empty((B, h, m, d_v), dtype=bf, pin_memory=pin))
+    ho, hlse, hdq, hdk, hdv = out
+    _check_host("out O", ho, (B, h, n, d_v), bf)
+    if hlse is not None:
+        _check_host("out lse", hlse, (B, h, n), torch.float32)
+    _check_host("out dQ", hdq, (B, h, n, d_k), bf)
+    _check_host("out dK", hdk, (B, h, m, d_k), bf)
+    _check_host("out dV", hdv, (B, h, m, d_v), bf)
+    b = buffers
+    ws = b.workspace
+    st = lib.attn_fwd_bwd_host(_vptr(q), _vptr(k), _vptr(v), _vptr(dO), _vptr(ho), _fptr(hlse), _vptr(hdq),
+                               _vptr(hdk), _vptr(hdv), _vptr(b.q), _vptr(b.k), _vptr(b.v), _vptr(b.dO),
+                               _vptr(b.o), _fptr(b.lse), _vptr(b.dq), _vptr(b.dk), _vptr(b.dv), _vptr(ws),
+                               ws.numel() * ws.element_size(), B, h, n, m, d_k, d_v, int(bool(causal)),
+                               float(scale), int(chunks), _stream_handle(stream))
+    if st != ATTN_OK:
+        raise AttnError(st, "attn_fwd_bwd_host")
+    return ho, hlse, hdq, hdk, hdv
 
 
 def attn_decode_workspace_bytes(B, h, n, m, d_k, d_v) -> int:
