@@ -120,3 +120,25 @@ def test_full_size_padded_encoder_sampled():
         assert_close(f"dQ b{b}", dq[b, hh, rows], rdq, grad=True, extra=bq)
         assert_close(f"dK b{b}", dk[b, hh, krows], rdk, grad=True, extra=bk)
         assert_close(f"dV b{b}", dv[b, hh, krows], rdv, grad=True)
+
+
+def test_long_causal_padded_forward_sampled_rows():
+    """Causal forward with key padding at 8192 query rows, where the persistent
+    kernel takes causal work (longest query blocks first, speculative exponentials
+    from the third key tile): sampled rows of every sequence against the oracle,
+    including rows past a sequence's last real key and the tile edges."""
+    B, h, n, d = 3, 2, 8192, 64
+    lens = [8192, 5000, 129]
+    w = Workload("kpad_long_causal", B, h, n, n, d, d, True, 79)
+    q, k, v = workload_inputs(w)
+    kvl = torch.tensor(lens, dtype=torch.int32, device=DEV)
+    o, lse = A.attn_fwd(q.to(DEV), k.to(DEV), v.to(DEV), causal=True, kv_len=kvl)
+    assert A.attn_get_device_status() == A.ATTN_OK
+    o, lse = o.cpu(), lse.cpu()
+    rng = np.random.default_rng(79)
+    rows = sorted({0, 1, 127, 128, 129, 255, 256, 4999, 5000, 5001, n - 129, n - 128, n - 1}
+                  | set(rng.choice(n, size=40, replace=False).tolist()))
+    ro, rl = oracle.fwd(q, k, v, True, w.default_scale, rows=rows, kv_len=lens)
+    for b in range(B):
+        assert_close(f"O b{b}", o[b][:, rows], ro[b][:, rows])
+        assert_close(f"lse b{b}", lse[b][:, rows][..., None], rl[b][:, rows][..., None])
