@@ -80,27 +80,28 @@ def load_peaks():
     return dict(PEAKS_FALLBACK), "fallback"
 
 
-def kernel_source_hash() -> str:
-    """Hash of the sources that hold device code (host-only files such as the
-    copy pipeline of the host-buffer step do not change a kernel's traffic)."""
+# Sources of each kernel whose DRAM traffic is recorded: its own file and the
+# device headers every kernel includes.
+KERNEL_HEADERS = ("attn_kernels.cuh", "sm103_ptx.cuh")
+
+
+def kernel_source_hash(files) -> str:
+    """Hash of the given kernel sources (file names under csrc/)."""
     h = hashlib.sha256()
-    for f in sorted(os.listdir(CSRC)):
-        if f.endswith((".cu", ".cuh")):
-            with open(os.path.join(CSRC, f), "rb") as fh:
-                data = fh.read()
-            if b"__global__" in data or b"__device__" in data:
-                h.update(f.encode() + data)
+    for f in sorted(set(files) | set(KERNEL_HEADERS)):
+        with open(os.path.join(CSRC, f), "rb") as fh:
+            h.update(f.encode() + fh.read())
     return h.hexdigest()[:16]
 
 
 def recorded_traffic(kernel: str, workload: str):
-    """DRAM bytes per launch from a committed ncu capture, if it matches the current sources."""
+    """DRAM bytes per launch from a committed ncu capture, if that kernel's sources are unchanged."""
     if not os.path.exists(TRAFFIC_FILE):
         return None
     with open(TRAFFIC_FILE) as f:
         d = json.load(f)
     rec = d.get(workload, {}).get(kernel)
-    if not rec or rec.get("source_hash") != kernel_source_hash():
+    if not rec or not rec.get("sources") or rec.get("source_hash") != kernel_source_hash(rec["sources"]):
         return None
     return rec.get("bytes_per_launch")
 

@@ -441,15 +441,14 @@ attn_bwd_head_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
     for (int bh = blockIdx.x; ok && bh < p.BH; bh += gridDim.x) {
       for (int t = 0; t < NQT; ++t) {
         const int kk = k + t, slot = kk % C::NSLOT;
-        // the slot's previous statistics are no longer read once its new tile has landed
-        ok = __all_sync(0xffffffffu, guarded_wait(&sh.qdo_full[slot], (kk / C::NSLOT) & 1, abort_flag, wd,
-                                                  kSiteBwdLoad));
-        if (!ok) break;
+        // The statistics depend only on O, dO and lse in global memory: they are
+        // formed before the wait for the slot, so that their loads (O comes from
+        // HBM) overlap it instead of following it at every head's start.
+        float nlse2[2], dsum[2];
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
-          const int r = u + 64 * half;
-          const int row = t * 128 + r;
-          float dsum = 0.f, lse2 = INFINITY;
+          const int row = t * 128 + u + 64 * half;
+          float ds = 0.f, lse2 = INFINITY;
           if (row < p.n) {
             const size_t off = (static_cast<size_t>(bh) * p.n + row) * D;
             const uint4* o4 = reinterpret_cast<const uint4*>(p.o + off);
@@ -461,16 +460,25 @@ attn_bwd_head_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
 #pragma unroll
               for (int w = 0; w < 4; ++w) {
                 const float2 x = unpack_bf16x2(av[w]), y = unpack_bf16x2(bv[w]);
-                dsum = fmaf(x.x, y.x, dsum);
-                dsum = fmaf(x.y, y.y, dsum);
+                ds = fmaf(x.x, y.x, ds);
+                ds = fmaf(x.y, y.y, ds);
               }
             }
             // a row that saw no key (lse = -inf, O = 0) keeps lse2 = +inf: weight 0
             const float lse = p.lse[static_cast<size_t>(bh) * p.n + row];
             if (lse > -INFINITY) lse2 = lse * kLog2eH;
           }
-          stat[slot * 256 + r] = -lse2;
-          stat[slot * 256 + 128 + r] = dsum;
+          nlse2[half] = -lse2;
+          dsum[half] = ds;
+        }
+        // the slot's previous statistics are no longer read once its new tile has landed
+        ok = __all_sync(0xffffffffu, guarded_wait(&sh.qdo_full[slot], (kk / C::NSLOT) & 1, abort_flag, wd,
+                                                  kSiteBwdLoad));
+        if (!ok) break;
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          stat[slot * 256 + u + 64 * half] = nlse2[half];
+          stat[slot * 256 + 128 + u + 64 * half] = dsum[half];
         }
         mbar_arrive(&sh.stat_full[slot]);
       }
