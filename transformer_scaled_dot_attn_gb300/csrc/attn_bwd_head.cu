@@ -498,6 +498,20 @@ attn_bwd_head_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
     const int sw = r & 7;
     bool ok = true;
     int g = 0, k = 0, ki = 0;
+    // Region h carried the previous key tile's dV / dK out. Thread 0 issued that
+    // TMA store and checks that it has read the region only when this key tile
+    // first writes there (its first dS, or its own output when no query tile
+    // reads it), so that the group forms the key tile's first P meanwhile.
+    bool store_pending = false;
+    auto region_free = [&]() -> bool {
+      if (ki == 0) return true;
+      if (r == 0 && store_pending) {
+        bulk_wait_read_all();
+        mbar_arrive(&sh.out_free[h]);
+        store_pending = false;
+      }
+      return __all_sync(0xffffffffu, guarded_wait(&sh.out_free[h], (ki - 1) & 1, abort_flag, wd, kSiteBwdFinal));
+    };
     for (int bh = blockIdx.x; ok && bh < p.BH; bh += gridDim.x) {
       const int mb = head_keys(p.kv_len, bh, p.h, p.m);  // real keys of this head
       for (int kb = 0; ok && kb < NKT; ++kb, ++ki) {
@@ -507,12 +521,6 @@ attn_bwd_head_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         const int T = t1 - t0;
         int qlo, qhi;  // query rows that see this key
         query_range(key, key, p.n, p.causal, wl, wr, qlo, qhi);
-        // region h carried the previous key tile's dV / dK out: its TMA store
-        // must have read it before dS (or this key tile's output) overwrites it
-        if (ki >= 1) {
-          ok = __all_sync(0xffffffffu, guarded_wait(&sh.out_free[h], (ki - 1) & 1, abort_flag, wd, kSiteBwdFinal));
-          if (!ok) break;
-        }
         for (int t = t0; t < t1; ++t) {
           const int gt = g + (t - t0);
           const int kk = k + t, slot = kk % C::NSLOT;
@@ -562,6 +570,7 @@ attn_bwd_head_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
             ok = __all_sync(0xffffffffu, guarded_wait(&sh.ds_empty, (gt - 1) & 1, abort_flag, wd, kSiteBwdDS));
             if (!ok) break;
           }
+          if (t == t0 && !(ok = region_free())) break;
 #pragma unroll
           for (int q = 0; q < 2; ++q) {
             uint32_t dp[32];
@@ -618,6 +627,9 @@ attn_bwd_head_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         // the accumulators are read: the next key tile's dV / dK may start
         tc_fence_before();
         mbar_arrive(&sh.acc_free);
+        // a key tile that no query tile reads wrote no dS: the region is first
+        // written here
+        if (T == 0 && !(ok = region_free())) break;
         // stage this row in region h and let one thread store the tile (rows
         // past m are clipped by the tensor map)
         uint8_t* region = smem + C::OFF_DS + h * C::DS_REGION;
@@ -628,9 +640,8 @@ attn_bwd_head_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
           if (guarded_wait(&sh.out_staged[h], ki & 1, abort_flag, wd, kSiteBwdFinal)) {
             tma_store_3d(h ? &tm_dk : &tm_dv, region, 0, kb * 128, bh);
             tma_store_commit();
-            bulk_wait_read_all();
           }
-          mbar_arrive(&sh.out_free[h]);
+          store_pending = true;  // released where the next key tile first writes the region
         }
         g += T;
       }
