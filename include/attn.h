@@ -108,15 +108,17 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const f
  * statistics, as sized by attn_bwd_workspace_bytes) lives in one fixed 32 MiB device array
  * inside the library: every GPU that loads the library holds it until the
  * process exits. Sizes whose scratch exceeds 32 MiB are refused with
- * ATTN_ERR_UNSUPPORTED before anything is launched. The call makes no
+ * ATTN_ERR_UNSUPPORTED before any other argument check and before anything
+ * is launched. The call makes no
  * cudaMalloc/cudaFree and no other allocation. Its first call on a device
  * looks up the array's device address (cudaGetSymbolAddress) with that
  * device current; make that first call before any stream capture. Every
  * call shares the one array and clears on its stream what must start at
  * zero, so calls that can overlap on the GPU (different streams, no
  * ordering between them) race and must not be issued. Watchdog reports go to
- * the word attn_get_device_status reads once any other call of this library
- * has created it on the device.
+ * the device word that attn_get_device_status reads, or, while no other call
+ * of this library has created that word on the device, to a fixed word of
+ * the library that attn_get_device_status reads and clears as well.
  */
 int attn_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const float* lse,
                      const void* dO, void* dq, void* dk, void* dv, int B, int h, int n, int m,
@@ -237,14 +239,6 @@ int attn_set_watchdog_ns(unsigned long long budget_ns);
  * or ATTN_ERR_INVALID_ARG for an unknown mode.
  */
 int attn_debug_inject(int mode);
-
-/*
- * Test hook: y_poly[i] = 2^x[i] computed by the forward kernel's FMA-pipe
- * polynomial, y_mufu[i] = 2^x[i] by the hardware approximation (ex2.approx),
- * for n device floats (either output may be NULL). Enqueued on `stream`.
- * Returns ATTN_OK, ATTN_ERR_INVALID_ARG (null x, n < 0) or ATTN_ERR_CUDA.
- */
-int attn_debug_exp2(const float* x, float* y_poly, float* y_mufu, int n, attn_stream_t stream);
 
 /*
  * Per-kernel device timing, for profiling. While enabled (on != 0), every

@@ -26,7 +26,7 @@ __all__ = [
     "ATTN_ERR_TIMEOUT", "load_library", "library_path", "attn_fwd", "attn_bwd",
     "attn_bwd_workspace_bytes", "attn_get_device_status", "attn_status_string",
     "attn_set_watchdog_ns", "attn_debug_inject", "attn_profile_enable", "attn_profile_read",
-    "attn_debug_exp2", "attn_bwd_noalloc", "attn_decode", "attn_decode_workspace_bytes",
+    "attn_bwd_noalloc", "attn_decode", "attn_decode_workspace_bytes",
     "attn_qkv_projection", "attn_out_projection", "attn_qkv_projection_bwd", "attn_out_projection_bwd",
     "attn_qkv_projection_bwd_workspace_bytes", "attn_out_projection_bwd_workspace_bytes",
     "attn_fwd_bwd_host", "HostStepBuffers", "EXPORTED_SYMBOLS", "KERNEL_KINDS",
@@ -46,7 +46,7 @@ ATTN_ERR_TIMEOUT = 4
 EXPORTED_SYMBOLS = (
     "attn_fwd", "attn_bwd", "attn_bwd_workspace_bytes", "attn_get_device_status",
     "attn_status_string", "attn_set_watchdog_ns", "attn_debug_inject", "attn_profile_enable",
-    "attn_profile_read", "attn_debug_exp2", "attn_bwd_noalloc", "attn_fwd_varlen",
+    "attn_profile_read", "attn_bwd_noalloc", "attn_fwd_varlen",
     "attn_bwd_varlen", "attn_fwd_masked", "attn_bwd_masked", "attn_decode_workspace_bytes", "attn_decode",
     "attn_qkv_projection", "attn_out_projection", "attn_qkv_projection_bwd_workspace_bytes",
     "attn_qkv_projection_bwd", "attn_out_projection_bwd_workspace_bytes", "attn_out_projection_bwd",
@@ -132,8 +132,6 @@ def load_library():
         lib.attn_bwd_noalloc.argtypes = [vp, vp, vp, vp, fp, vp, vp, vp, vp, I, I, I, I, I, I, I, F,
                                          vp]
         lib.attn_bwd_noalloc.restype = I
-        lib.attn_debug_exp2.argtypes = [vp, vp, vp, I, vp]
-        lib.attn_debug_exp2.restype = I
         lib.attn_profile_enable.argtypes = [I]
         lib.attn_profile_enable.restype = I
         lib.attn_profile_read.argtypes = [I, ctypes.POINTER(I), ctypes.POINTER(ctypes.c_double)]
@@ -565,18 +563,6 @@ def attn_profile_read(kind) -> Tuple[int, float]:
     if st != ATTN_OK:
         raise AttnError(st, "attn_profile_read")
     return int(n.value), float(ms.value)
-
-
-def attn_debug_exp2(x, stream=None):
-    """(2^x by the forward's FMA-pipe polynomial, 2^x by ex2.approx) for a CUDA fp32 tensor."""
-    import torch
-    _check_tensor("x", x, dtype=torch.float32)
-    yp = torch.empty_like(x)
-    ym = torch.empty_like(x)
-    st = load_library().attn_debug_exp2(_vptr(x), _vptr(yp), _vptr(ym), x.numel(), _stream_handle(stream))
-    if st != ATTN_OK:
-        raise AttnError(st, "attn_debug_exp2")
-    return yp, ym
 
 
 def attn_bwd_noalloc(q, k, v, o, lse, dO, causal: bool = False, scale: Optional[float] = None,

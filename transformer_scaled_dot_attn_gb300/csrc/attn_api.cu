@@ -201,15 +201,29 @@ void prof_end(int kind, cudaStream_t stream) {
 
 }  // namespace attn
 
-extern "C" {
+// ---------------------------------------------------------------- allocation-free backward
+//
+// Scratch of attn_bwd_noalloc: the fp32 dQ accumulator and the two padded
+// per-row statistics live in this fixed device array instead of a
+// caller-provided workspace. It exists once per device that loads the
+// library and stays until the process exits.
+namespace {
 
-int attn_debug_exp2(const float* x, float* y_poly, float* y_mufu, int n, attn_stream_t stream) {
-  if (x == nullptr || n < 0) return ATTN_ERR_INVALID_ARG;
-  return attn::launch_exp2_probe(x, y_poly, y_mufu, n, reinterpret_cast<cudaStream_t>(stream)) ==
-                 cudaSuccess
-             ? ATTN_OK
-             : ATTN_ERR_CUDA;
-}
+constexpr size_t kNoAllocScratchBytes = size_t(32) << 20;  // 32 MiB
+
+__device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+// Watchdog word for devices on which no attn_fwd/attn_bwd call has created
+// the per-device error word yet (that word needs an allocation).
+__device__ uint32_t g_noalloc_status;
+
+std::once_flag g_noalloc_once[kMaxDevices];
+void* g_noalloc_scratch_ptr[kMaxDevices] = {nullptr};
+uint32_t* g_noalloc_status_ptr[kMaxDevices] = {nullptr};
+cudaError_t g_noalloc_setup_err[kMaxDevices] = {cudaSuccess};
+
+}  // namespace
+
+extern "C" {
 
 int attn_profile_enable(int on) {
   g_prof_on.store(on ? 1 : 0);
@@ -839,34 +853,20 @@ int attn_get_device_status(attn_stream_t stream) {
   if (device_status_word(&status) != cudaSuccess) return ATTN_ERR_CUDA;
   uint32_t v = 0;
   if (cudaMemcpy(&v, status, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return ATTN_ERR_CUDA;
-  if (v == 0) return ATTN_OK;
-  if (cudaMemset(status, 0, sizeof(uint32_t)) != cudaSuccess) return ATTN_ERR_CUDA;
-  return ATTN_ERR_TIMEOUT;
+  if (v != 0 && cudaMemset(status, 0, sizeof(uint32_t)) != cudaSuccess) return ATTN_ERR_CUDA;
+  // attn_bwd_noalloc reports into a word of its own while the word above does
+  // not exist yet on the device (creating it allocates): read and clear it too
+  uint32_t w = 0;
+  if (cudaMemcpyFromSymbol(&w, g_noalloc_status, sizeof(w)) != cudaSuccess) return ATTN_ERR_CUDA;
+  if (w != 0) {
+    const uint32_t zero = 0;
+    if (cudaMemcpyToSymbol(g_noalloc_status, &zero, sizeof(zero)) != cudaSuccess) return ATTN_ERR_CUDA;
+  }
+  return (v == 0 && w == 0) ? ATTN_OK : ATTN_ERR_TIMEOUT;
 }
 
 }  // extern "C"
 
-// ---------------------------------------------------------------- allocation-free backward
-//
-// Scratch of attn_bwd_noalloc: the fp32 dQ accumulator and the two padded
-// per-row statistics live in this fixed device array instead of a
-// caller-provided workspace. It exists once per device that loads the
-// library and stays until the process exits.
-namespace {
-
-constexpr size_t kNoAllocScratchBytes = size_t(32) << 20;  // 32 MiB
-
-__device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
-// Watchdog word for devices on which no attn_fwd/attn_bwd call has created
-// the per-device error word yet (that word needs an allocation).
-__device__ uint32_t g_noalloc_status;
-
-std::once_flag g_noalloc_once[kMaxDevices];
-void* g_noalloc_scratch_ptr[kMaxDevices] = {nullptr};
-uint32_t* g_noalloc_status_ptr[kMaxDevices] = {nullptr};
-cudaError_t g_noalloc_setup_err[kMaxDevices] = {cudaSuccess};
-
-}  // namespace
 
 extern "C" int attn_bwd_noalloc(const void* q, const void* k, const void* v, const void* o,
                                 const float* lse, const void* dO, void* dq, void* dk, void* dv,
@@ -875,6 +875,9 @@ extern "C" int attn_bwd_noalloc(const void* q, const void* k, const void* v, con
   bool empty = false;
   int st = check_common(B, h, n, m, d_k, d_v, scale, &empty);
   if (st != ATTN_OK) return st;
+  // Sizes whose scratch does not fit the fixed array are refused before anything else.
+  if (!empty && attn_bwd_workspace_bytes(B, h, n, m, d_k, d_v, causal) > kNoAllocScratchBytes)
+    return ATTN_ERR_UNSUPPORTED;
   if (!k || !v || !dk || !dv) return ATTN_ERR_INVALID_ARG;
   if (!aligned16(k) || !aligned16(v) || !aligned16(dk) || !aligned16(dv)) return ATTN_ERR_INVALID_ARG;
   const long long BH = static_cast<long long>(B) * h;
@@ -889,9 +892,6 @@ extern "C" int attn_bwd_noalloc(const void* q, const void* k, const void* v, con
   if (!q || !o || !lse || !dO || !dq) return ATTN_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(o) || !aligned16(dO) || !aligned16(dq)) return ATTN_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(lse) & 3u) != 0) return ATTN_ERR_INVALID_ARG;
-  // Sizes whose scratch does not fit the fixed array are refused up front.
-  if (attn_bwd_workspace_bytes(B, h, n, m, d_k, d_v, causal) > kNoAllocScratchBytes)
-    return ATTN_ERR_UNSUPPORTED;
 
   // Set-up, once per device, with that device current: the device address of
   // the scratch array (and of the fallback watchdog word).

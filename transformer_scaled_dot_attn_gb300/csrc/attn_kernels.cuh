@@ -106,9 +106,6 @@ struct FwdParams {
   Watchdog wd;
 };
 
-cudaError_t launch_exp2_probe(const float* x, float* y_poly, float* y_mufu, int n,
-                              cudaStream_t stream);
-
 // Keys per tile the forward kernel streams for head size d and n queries
 // (the K/V TMA box height).
 int fwd_key_tile(int d, int n, int m, int causal, bool windowed);

@@ -427,39 +427,6 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
-// 2^x for a pair of fp32 values on the FMA pipe (no MUFU):
-//   x = n + f with n = round(x) (nearest, via the 1.5*2^23 shifter) and
-//   f in [-1/2, 1/2]; 2^f by a degree-3 polynomial with constant term exactly 1
-//   (so 2^0 = 1, as from the hardware path) whose other coefficients minimise
-//   the maximum relative error on [-1/2, 1/2] (found by linear programming;
-//   1.0e-4 relative, 13.3 bits, evaluated in fp32); 2^n by adding n to the
-//   exponent field. x is clamped to >= -126 so the exponent never underflows
-//   (2^-126 is below every weight that matters). Finite x only.
-__device__ __forceinline__ uint64_t exp2_poly2(uint64_t x2) {
-  float x0, x1;
-  f2_unpack(x2, x0, x1);
-  const uint64_t x = f2_pack(fmaxf(x0, -126.f), fmaxf(x1, -126.f));
-  const uint64_t shifter = f2_pack(12582912.f, 12582912.f);  // 1.5 * 2^23
-  const uint64_t t = add2(x, shifter);       // low mantissa bits of t hold n
-  const uint64_t f = sub2(x, sub2(t, shifter));
-  uint64_t p = fma2(f, f2_pack(5.500893667e-02f, 5.500893667e-02f),
-                    f2_pack(2.422109544e-01f, 2.422109544e-01f));
-  p = fma2(f, p, f2_pack(6.932829022e-01f, 6.932829022e-01f));
-  p = fma2(f, p, f2_pack(1.0f, 1.0f));
-  // bits(t) = bits(1.5*2^23) + n, and bits(1.5*2^23) << 23 vanishes mod 2^32,
-  // so bits(t) * 2^23 adds exactly n to the exponent of p.
-  uint32_t t0, t1, p0, p1;
-  asm("mov.b64 {%0, %1}, %2;" : "=r"(t0), "=r"(t1) : "l"(t));
-  asm("mov.b64 {%0, %1}, %2;" : "=r"(p0), "=r"(p1) : "l"(p));
-  uint64_t r;
-  asm("{\n\t.reg .b32 a, b;\n\t"
-      "mad.lo.u32 a, %1, 8388608, %3;\n\t"
-      "mad.lo.u32 b, %2, 8388608, %4;\n\t"
-      "mov.b64 %0, {a, b};\n\t}"
-      : "=l"(r) : "r"(t0), "r"(t1), "r"(p0), "r"(p1));
-  return r;
-}
-
 // Packs a pair of fp32 (lo, hi) into bf16x2.
 __device__ __forceinline__ uint32_t pack_bf16x2_pair(uint64_t v) {
   float lo, hi;
