@@ -3,9 +3,11 @@ configuration the benchmark times (one attn_fwd + one attn_bwd over the whole ba
 
 The oracle computes sampled outputs one by one: forward rows and dQ rows of
 sampled queries, dK / dV rows of sampled keys (these need a full forward of
-their head). Properties that hold at any size are checked on every head.
+their head). Sequences of 4096 and more rows are sampled deeper: 8 heads, both
+rows at every 128-row tile boundary, the last tile and a uniform sample (at
+least 256 query rows), and 64 key rows. Properties that hold at any size are
+checked on every head.
 """
-import math
 import zlib
 
 import numpy as np
@@ -15,7 +17,7 @@ import torch
 import oracle
 import transformer_scaled_dot_attn_gb300 as A
 from seeded_inputs import WORKLOADS, workload_inputs
-from tests.parity_utils import assert_close, d_term_bounds, to64
+from tests.parity_utils import assert_close, to64
 from tests.test_gpu_parity import invariant_bounds
 
 pytestmark = pytest.mark.gpu
@@ -25,12 +27,26 @@ FULL = ["tiny", "tiny_causal", "encoder", "encoder_sat", "decoder", "cross", "cr
                             for c in ("nc", "c")]
 
 
-def _sample(size, extra, rng):
+def _sample(size, extra, rng, boundaries=False):
     """Tile-boundary rows plus a uniform sample; returns (rows, positions of the uniform part)."""
     edge = {0, 1, 127, 128, 129, 255, 256, size - 2, size - 1}
+    if boundaries:  # both rows at every 128-row tile boundary, and the whole last partial tile's ends
+        edge |= {b + o for b in range(128, size, 128) for o in (-1, 0)}
+        edge |= {(size - 1) // 128 * 128}
     uni = set(rng.choice(size, size=min(size, extra), replace=False).tolist())
     rows = sorted(i for i in edge | uni if 0 <= i < size)
     return rows, [p for p, i in enumerate(rows) if i in uni]
+
+
+def _exception(w, tensor):
+    """The documented exception a tensor of this workload is held to (None: the plain bound)."""
+    if tensor not in ("dQ", "dK", "dV"):
+        return None
+    if w.q_mult != 1.0:
+        return "saturated_softmax_backward"
+    if w.causal:
+        return "few_term_cancellation"
+    return None
 
 
 @pytest.mark.parametrize("name", FULL)
@@ -45,26 +61,30 @@ def test_full_size_sampled_parity(name):
     assert A.attn_get_device_status() == A.ATTN_OK
 
     H = w.heads
-    heads = sorted({0, H - 1, H // 2})
-    key_heads = heads if w.n * w.m <= 4096 * 4096 else [H // 2]
+    deep = w.n >= 4096
+    if deep:
+        heads = sorted(set(np.linspace(0, H - 1, 8).round().astype(int).tolist()))
+        key_heads = heads
+        n_uni, k_uni = 256, 64
+    else:
+        heads = sorted({0, H - 1, H // 2})
+        key_heads = heads if w.n * w.m <= 4096 * 4096 else [H // 2]
+        n_uni, k_uni = 48, 24
     o3, lse3 = o.view(H, w.n, w.d_v), lse.view(H, w.n)
     dq3, dk3, dv3 = dq.view(H, w.n, w.d_k), dk.view(H, w.m, w.d_k), dv.view(H, w.m, w.d_v)
     q3, k3, v3, do3 = (t.view(H, t.shape[2], t.shape[3]) for t in (q, k, v, do))
     for h in heads:
-        rows, uni = _sample(w.n, 48, rng)
+        rows, uni = _sample(w.n, n_uni, rng, boundaries=deep)
+        assert not deep or len(rows) >= 256
         ro, rl = oracle.fwd(q3[h], k3[h], v3[h], w.causal, scale, rows=rows)
-        assert_close(f"O head {h}", o3[h, rows], ro[rows], rel_rows=uni)
-        assert_close(f"lse head {h}", lse3[h, rows][None], rl[rows][None], rel_rows=None)
-        krows, kuni = _sample(w.m, 24, rng) if h in key_heads else ([], [])
+        assert_close(f"{name} O head {h}", o3[h, rows], ro[rows], rel_rows=uni)
+        assert_close(f"{name} lse head {h}", lse3[h, rows][None], rl[rows][None], rel_rows=None)
+        krows, kuni = _sample(w.m, k_uni, rng) if h in key_heads else ([], [])
         rdq, rdk, rdv = oracle.bwd_rows(q3[h], k3[h], v3[h], do3[h], w.causal, scale, rows, krows)
-        bq, bk = d_term_bounds(q3[h], k3[h], v3[h], do3[h], w.causal, scale, rows, krows)
-        # the saturated Q x 4 variant: D_i from the bf16 O dominates the small gradients
-        rel = 1e-2 if w.q_mult != 1.0 else 5e-3
-        assert_close(f"dQ head {h}", dq3[h, rows], rdq, grad=True, rel_rows=uni, extra=bq, rel_l2=rel)
+        assert_close(f"{name} dQ head {h}", dq3[h, rows], rdq, rel_rows=uni, allow=_exception(w, "dQ"))
         if krows:
-            assert_close(f"dK head {h}", dk3[h, krows], rdk, grad=True, rel_rows=kuni, extra=bk,
-                         rel_l2=rel)
-            assert_close(f"dV head {h}", dv3[h, krows], rdv, grad=True, rel_rows=kuni, rel_l2=rel)
+            assert_close(f"{name} dK head {h}", dk3[h, krows], rdk, rel_rows=kuni, allow=_exception(w, "dK"))
+            assert_close(f"{name} dV head {h}", dv3[h, krows], rdv, rel_rows=kuni, allow=_exception(w, "dV"))
 
     # invariants on every head: sum_j dK_j = 0 and sum_j dV_j = sum_i dO_i, within the
     # rounding budget of bf16 arithmetic

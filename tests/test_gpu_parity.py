@@ -8,7 +8,7 @@ import torch
 import oracle
 import transformer_scaled_dot_attn_gb300 as A
 from seeded_inputs import WORKLOADS, Workload, normal_bf16, ragged_workloads, workload_inputs
-from tests.parity_utils import assert_close, d_term_bounds, default_scale, errors, to64
+from tests.parity_utils import assert_close, default_scale, errors, to64
 
 pytestmark = pytest.mark.gpu
 
@@ -54,12 +54,12 @@ def test_fwd_bwd_match_oracle(w):
     o, lse = run_fwd(q, k, v, w.causal, scale)
     dq, dk, dv = run_bwd(q, k, v, o, lse, do, w.causal, scale)
     rdq, rdk, rdv, ro, rlse = oracle.bwd(q, k, v, do, w.causal, scale)
-    bq, bk = d_term_bounds(q, k, v, do, w.causal, scale)
+    ex = "few_term_cancellation" if w.causal else None
     assert_close("O", o, ro)
     assert_close("lse", lse, rlse)
-    assert_close("dQ", dq, rdq, grad=True, extra=bq)
-    assert_close("dK", dk, rdk, grad=True, extra=bk)
-    assert_close("dV", dv, rdv, grad=True)
+    assert_close("dQ", dq, rdq, allow=ex)
+    assert_close("dK", dk, rdk, allow=ex)
+    assert_close("dV", dv, rdv, allow=ex)
 
 
 @pytest.mark.parametrize("d", [32, 64])
@@ -89,23 +89,22 @@ def test_scale_values(scale, causal):
 
     At scale = 1 with d_k = 64 the scores have standard deviation 8 and the
     softmax saturates (the case §3.2.1 gives for the 1/sqrt(d_k) scale): the
-    gradients become small and their relative error is set by D_i = dO_i . O_i
-    formed from the bf16 O, about 5e-3. That backward is checked against the
-    relative-L2 bound 1e-2 instead of 5e-3; everything else uses the standard
-    tolerance.
+    gradients become small and their error is set by D_i = dO_i . O_i formed
+    from the bf16 O. That backward is held to the documented exception
+    "unscaled_scores_backward" (tests/parity_utils.py); causal gradients may use
+    "few_term_cancellation"; everything else the plain bound.
     """
     w = _small("s", 1, 2, 200, 200, 64, causal, 7)
     q, k, v, do = workload_inputs(w, with_grad=True)
     o, lse = run_fwd(q, k, v, causal, scale)
     dq, dk, dv = run_bwd(q, k, v, o, lse, do, causal, scale)
     rdq, rdk, rdv, ro, rlse = oracle.bwd(q, k, v, do, causal, scale)
-    bq, bk = d_term_bounds(q, k, v, do, causal, scale)
     assert_close("O", o, ro)
     assert_close("lse", lse, rlse)
-    rel = 1e-2 if abs(scale) >= 1.0 else 5e-3
-    assert_close("dQ", dq, rdq, grad=True, rel_l2=rel, extra=bq)
-    assert_close("dK", dk, rdk, grad=True, rel_l2=rel, extra=bk)
-    assert_close("dV", dv, rdv, grad=True, rel_l2=rel)
+    sat = "unscaled_scores_backward" if abs(scale) >= 1.0 else ("few_term_cancellation" if causal else None)
+    assert_close("dQ", dq, rdq, allow=sat)
+    assert_close("dK", dk, rdk, allow=sat)
+    assert_close("dV", dv, rdv, allow=sat)
 
 
 @pytest.mark.parametrize("scale", [0.0, 1.0, -0.2, 0.03])
@@ -194,7 +193,7 @@ def test_single_key():
         rdq, rdk, rdv, _, rlse = oracle.bwd(q, k, v, do, causal, 0.125)
         assert_close("lse", lse, rlse)
         assert np.abs(to64(dq)).max() < 1e-2 and np.abs(to64(dk)).max() < 1e-2
-        assert_close("dV", dv, rdv, grad=True)
+        assert_close("dV", dv, rdv)
 
 
 def invariant_bounds(q, v, do, dk, dv, scale):
