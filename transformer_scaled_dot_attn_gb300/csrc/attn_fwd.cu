@@ -105,7 +105,7 @@ struct Fwd {
 };
 
 constexpr int kMaxNQ = 4;
-constexpr int kMaxStages = 4;
+constexpr int kMaxStages = 5;
 
 struct FwdShared {
   uint64_t q_full;
@@ -158,14 +158,26 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, const
 }
 
 // p = 2^(s*c - m) for one 32-column chunk of a row held in registers; packs
-// the bf16 weights and adds them, as rounded, into lsum: the row sum l is the
-// sum of the weights the P.V product applies, so O / l is an exact convex
-// combination of value rows (a row dominated by one key returns that value
-// row even when the reference m lags the row maximum). MASKED: columns at or
-// past `rem` or before `rlo` (keys this row may not see) get weight exactly 0.
-template <bool MASKED>
+// the bf16 weights into pk and adds the weights into lsum. MASKED: columns at
+// or past `rem` or before `rlo` (keys this row may not see) get weight exactly 0.
+// EXACT_SUM: the weights are added as rounded to bf16 (mixed-precision adds),
+// so the row sum l is the sum of the weights the P.V product applies and O / l
+// is an exact convex combination of value rows (a row dominated by one key
+// returns that value row even when the reference m lags the row maximum).
+// Otherwise the fp32 weights are added in pairs (one packed add per two
+// weights): on GB300 the exp unit bounds this loop, and the mixed-precision
+// adds take 30 % of its throughput (1.79 k against 1.38 k clocks per 128-key
+// tile for two warps per scheduler, measured in isolation). The two sums
+// differ by the bf16 rounding of the weights, relative 2^-9 at most; only
+// rows that one key dominates see it in O.
+template <bool MASKED, bool EXACT_SUM>
 __device__ __forceinline__ void exp_chunk(const uint32_t (&s)[32], int col0, int rlo, int rem, uint64_t c2,
                                           uint64_t nm2, float (&lsum)[4], uint32_t (&pk)[16]) {
+  uint64_t acc[2];
+  if (!EXACT_SUM) {
+    acc[0] = f2_pack(lsum[0], lsum[1]);
+    acc[1] = f2_pack(lsum[2], lsum[3]);
+  }
 #pragma unroll
   for (int i = 0; i < 16; ++i) {
     const uint64_t x2 = fma2(f2_pack(__uint_as_float(s[2 * i]), __uint_as_float(s[2 * i + 1])), c2, nm2);
@@ -177,7 +189,12 @@ __device__ __forceinline__ void exp_chunk(const uint32_t (&s)[32], int col0, int
     }
     const uint64_t p2 = f2_pack(ex2(x0), ex2(x1));
     pk[i] = pack_bf16x2_pair(p2);
-    acc_bf16x2(lsum[(i & 1) * 2], lsum[(i & 1) * 2 + 1], pk[i]);
+    if (EXACT_SUM) acc_bf16x2(lsum[(i & 1) * 2], lsum[(i & 1) * 2 + 1], pk[i]);
+    else acc[i & 1] = add2(acc[i & 1], p2);
+  }
+  if (!EXACT_SUM) {
+    f2_unpack(acc[0], lsum[0], lsum[1]);
+    f2_unpack(acc[1], lsum[2], lsum[3]);
   }
 }
 
@@ -481,9 +498,9 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         // masked scores already hold -inf, and 2^(-inf * c - m) = 0 for c > 0;
         // only c = 0 (scale 0) needs the explicit mask (-inf * 0 is NaN)
         if (masked && c == 0.f)
-          exp_chunk<true>(s[q], q * 32, rlo, rem, c2, nm2, lsum, pk);
+          exp_chunk<true, true>(s[q], q * 32, rlo, rem, c2, nm2, lsum, pk);
         else
-          exp_chunk<false>(s[q], q * 32, rlo, rem, c2, nm2, lsum, pk);
+          exp_chunk<false, true>(s[q], q * 32, rlo, rem, c2, nm2, lsum, pk);
         tmem_st16(t_p + q * 16, pk);
       }
       if (turns) mbar_arrive(&sh.exp_turn[g ^ 1]);  // the other group's turn
@@ -615,7 +632,10 @@ struct FwdP {
   static constexpr uint32_t SBO = 8u * ATOM * 2u;
   static constexpr uint32_t QTILE = 128u * D * 2u;
   static constexpr uint32_t KTILE = BN * D * 2u;
-  static constexpr int STAGES = 4;
+  // K/V ring depth: a tile takes about 2.5 us from its TMA issue to its
+  // arrival when every SM streams keys (measured with a clock64 trace at
+  // n = m = 16384, d = 64), more than four stages of about 1.2 us cover
+  static constexpr int STAGES = 5;
   static constexpr uint32_t OFF_Q = 0;                    // 2 sets x NQ tiles
   static constexpr uint32_t OFF_K = 2 * NQ * QTILE;
   static constexpr uint32_t OFF_V = OFF_K + STAGES * KTILE;
@@ -626,6 +646,7 @@ struct FwdP {
   // softmax keeps a tile's scores and its packed weights in registers at once
   static constexpr int REG_SOFTMAX = 224, REG_OTHER = 56;
   static_assert(NQ * 128 * REG_SOFTMAX + 128 * REG_OTHER <= 384 * 168, "register split");
+  static_assert(SMEM + sizeof(uint64_t) * 64 <= 227u * 1024u, "shared memory per block");
   static constexpr int CHUNKS = BN / 32;
   static constexpr uint32_t P_COLS = BN / 2;
   __host__ __device__ static constexpr uint32_t tm_s(int g) { return g * BN; }
@@ -718,7 +739,7 @@ attn_fwd_persist_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
     // ------------------------------------------------------------ TMA producer
     if constexpr (SPEC) reg_dealloc<C::REG_OTHER>();
     if (lane == 0) {
-      // per stage s, group g (bit g * 4 + s): `users` = the stage's last tile was
+      // per stage s, group g (bit g * 8 + s): `users` = the stage's last tile was
       // used by group g; `uses` = parity of group g's uses of stage s so far
       uint32_t users = 0, uses = 0, kv_filled = 0, kv_ph = 0, q_filled = 0, q_ph = 0;
       int jj = 0;
@@ -745,7 +766,7 @@ attn_fwd_persist_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
           // the stage's previous tile must be released by every query tile that used it
 #pragma unroll
           for (int g = 0; g < NQ; ++g) {
-            const uint32_t bit = 1u << (g * 4 + st);
+            const uint32_t bit = 1u << (g * 8 + st);
             if (ok && (users & bit))
               ok = guarded_wait(&sh.kv_empty[g][st], ((uses & bit) ? 1u : 0u) ^ 1u, abort_flag, wd, kSiteKEmpty);
           }
@@ -758,7 +779,7 @@ attn_fwd_persist_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
             tma_load_3d(smem + C::OFF_V + st * C::KTILE, &tm_v, &sh.kv_full[st], 0, j * BN, bh);
 #pragma unroll
           for (int g = 0; g < NQ; ++g) {
-            const uint32_t bit = 1u << (g * 4 + st);
+            const uint32_t bit = 1u << (g * 8 + st);
             if (j < ntile[g]) {
               users |= bit;
               uses ^= bit;
@@ -995,9 +1016,9 @@ attn_fwd_persist_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
               // masked scores already hold -inf, and 2^(-inf * c - m) = 0 for c > 0;
               // only c = 0 (scale 0) needs the explicit mask (-inf * 0 is NaN)
               if (masked && c == 0.f)
-                exp_chunk<true>(s[q], q * 32, 0, rem, c2, nm2, lsum, pk[q]);
+                exp_chunk<true, false>(s[q], q * 32, 0, rem, c2, nm2, lsum, pk[q]);
               else
-                exp_chunk<false>(s[q], q * 32, 0, rem, c2, nm2, lsum, pk[q]);
+                exp_chunk<false, false>(s[q], q * 32, 0, rem, c2, nm2, lsum, pk[q]);
             }
             return (lsum[0] + lsum[1]) + (lsum[2] + lsum[3]);
           };
@@ -1096,9 +1117,9 @@ attn_fwd_persist_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
             // masked scores already hold -inf, and 2^(-inf * c - m) = 0 for c > 0;
             // only c = 0 (scale 0) needs the explicit mask (-inf * 0 is NaN)
             if (masked && c == 0.f)
-              exp_chunk<true>(s[q], q * 32, 0, rem, c2, nm2, lsum, pk);
+              exp_chunk<true, true>(s[q], q * 32, 0, rem, c2, nm2, lsum, pk);
             else
-              exp_chunk<false>(s[q], q * 32, 0, rem, c2, nm2, lsum, pk);
+              exp_chunk<false, true>(s[q], q * 32, 0, rem, c2, nm2, lsum, pk);
             tmem_st16(t_p + q * 16, pk);
           }
           {
@@ -1189,23 +1210,6 @@ cudaError_t launch_fwd_persist(const CUtensorMap& tq, const CUtensorMap& tk, con
   return launch_fwd_persist_cfg<D, false>(tq, tk, tv, to, p, BH, stream);
 }
 
-__global__ void exp2_probe_kernel(const float* x, float* y_poly, float* y_mufu, int n) {
-  const int i = 2 * (blockIdx.x * blockDim.x + threadIdx.x);
-  if (i >= n) return;
-  const float x0 = x[i];
-  const float x1 = (i + 1 < n) ? x[i + 1] : 0.f;
-  float p0, p1;
-  f2_unpack(exp2_poly2(f2_pack(x0, x1)), p0, p1);
-  if (y_poly) {
-    y_poly[i] = p0;
-    if (i + 1 < n) y_poly[i + 1] = p1;
-  }
-  if (y_mufu) {
-    y_mufu[i] = ex2(x0);
-    if (i + 1 < n) y_mufu[i + 1] = ex2(x1);
-  }
-}
-
 }  // namespace
 
 // Which forward kernel runs (measured on GB300, see the launcher below).
@@ -1225,14 +1229,6 @@ bool fwd_persistent(int d, int n, int m, int causal, bool windowed) {
 int fwd_key_tile(int d, int n, int m, int causal, bool windowed) {
   if (fwd_persistent(d, n, m, causal, windowed)) return 128;
   return (d >= 128 || n > 256) ? 128 : 64;
-}
-
-cudaError_t launch_exp2_probe(const float* x, float* y_poly, float* y_mufu, int n,
-                              cudaStream_t stream) {
-  if (n == 0) return cudaSuccess;
-  const int pairs = (n + 1) / 2;
-  exp2_probe_kernel<<<(pairs + 255) / 256, 256, 0, stream>>>(x, y_poly, y_mufu, n);
-  return cudaGetLastError();
 }
 
 // Configuration: two 128-row query tiles per item. Non-causal d <= 64 with
