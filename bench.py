@@ -3,8 +3,10 @@
 
 One step = attn_fwd followed by attn_bwd (the whole path: O, lse, dQ, dK, dV)
 over one synthetic batch of the chosen workload, inputs resident in HBM.
-Default workload: encoder self-attention of the base model, B=96, h=8,
-n=m=256, d_k=d_v=64, non-causal (the paper's base model, §3.2.2).
+Default workload: the largest single-GPU training configuration, B=4, h=16,
+n=m=16384, d_k=d_v=128, non-causal (long-sequence training; the paper's
+O(n^2 d) cost per layer, §4 and Table 1, is what this shape stresses). The
+short-sequence configurations of the base and big models are in the sweep.
 
 metric: attention TFLOPS (bf16, fwd and bwd) with the FLOP convention
 4*B*h*n*m*d_k for the forward (halved when causal) and 2.5x that for the
@@ -37,11 +39,35 @@ METRIC = "attention TFLOPS (bf16, fwd and bwd) and % of GB300 dense BF16 tensor 
 UNIT = "TFLOP/s"
 PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+DEFAULT_WORKLOAD = "long_n16384_d128_nc"
+# L2 size used to size the rotating input sets. The same number on every arm
+# and box keeps `config` identical between the two arms; the GPU arm checks
+# that the sets exceed twice the device's real L2.
+NOMINAL_L2_BYTES = 136 * 10**6
 CSRC = os.path.join(ROOT, "transformer_scaled_dot_attn_gb300", "csrc")
 
 
 def step_flops(w: Workload) -> float:
     return w.fwd_flops() + w.bwd_flops()
+
+
+def input_sets(w: Workload, l2_bytes: int = NOMINAL_L2_BYTES):
+    """(number of rotating input sets, bytes of one set): Q, K, V, dO of the
+    batch; enough sets that their total exceeds twice the L2."""
+    set_bytes = 2 * (2 * w.heads * w.n * w.d_k + 2 * w.heads * w.m * w.d_k)
+    n_sets = max(2, min(64, math.ceil(2 * l2_bytes / max(set_bytes, 1)) + 1))
+    return n_sets, set_bytes
+
+
+def workload_config(w: Workload, world: int) -> dict:
+    n_sets, set_bytes = input_sets(w)
+    return {"workload": f"{w.name}: B={w.B}, h={w.h}, n={w.n}, m={w.m}, d_k=d_v={w.d_k}, "
+                        f"causal={w.causal}" + (f", Q x {w.q_mult:g}" if w.q_mult != 1 else "")
+                        + (f", window={w.window}" if w.window is not None else ""),
+            "global_batch": w.B * world, "seq_len": w.n, "kv_len": w.m, "heads": w.h,
+            "head_dim": w.d_k, "causal": w.causal,
+            "parallelism": f"replicas x{world} (independent batches)", "step": "attn_fwd + attn_bwd",
+            "l2": f"inputs larger than L2: {n_sets} rotating input sets of {set_bytes / 1e6:.0f} MB"}
 
 
 def whole_head_backward(w: Workload) -> bool:
@@ -218,32 +244,74 @@ def barrier(world: int):
 
 # ----------------------------------------------------------------- CPU oracle sample
 
-def oracle_sample(w: Workload, target_s: float):
-    """Time the fp64 oracle (forward + backward) on the first few heads of ``w``.
+def visible_keys(w: Workload, i: int) -> int:
+    """Keys that query row i of a head sees (no key padding): causal mask and window."""
+    hi = w.m
+    if w.causal:
+        hi = min(hi, i + 1)
+    lo = 0
+    if w.window is not None:
+        wl, wr = w.window
+        if wr >= 0:
+            hi = min(hi, i + wr + 1)
+        if wl >= 0:
+            lo = max(0, i - wl)
+    return max(0, hi - lo)
 
-    Heads are added until about ``target_s`` seconds of CPU work (at most all
-    of them). Returns (TFLOP/s in the step's FLOP convention, seconds, heads, threads).
+
+def oracle_sample(w: Workload, target_s: float):
+    """Time the fp64 oracle on a bounded sample of ``w``, about ``target_s`` seconds of CPU work.
+
+    Whole heads (forward + backward, the step's FLOP convention) while one head
+    takes under half of ``target_s``; otherwise evenly spaced query rows of the
+    first head: their forward rows (O, lse) and their dQ rows, counted as
+    4*d FLOPs per visible key for the forward row and 6*d for the dQ row (the
+    score recomputation, dP and dQ: three of the backward's five products).
+    Returns (TFLOP/s, seconds, sample description, threads).
     """
     import oracle
     from seeded_inputs import workload_inputs
     oracle.build()
-    per_head = step_flops(w) / w.heads
+    scale = w.default_scale
+    q1, k1, v1, do1 = (t[0, 0] for t in workload_inputs(w, with_grad=True, heads=1))
 
-    def run(heads):
-        q, k, v, do = workload_inputs(w, with_grad=True, heads=heads)
+    def run_rows(rows):
         t0 = time.perf_counter()
-        oracle.bwd(q, k, v, do, w.causal, w.default_scale, window=w.window)
+        oracle.fwd(q1, k1, v1, w.causal, scale, rows=rows, window=w.window)
+        oracle.bwd_rows(q1, k1, v1, do1, w.causal, scale, qrows=rows, window=w.window)
         return time.perf_counter() - t0
 
-    probe = 1
-    t = run(probe)
-    while t < 0.5 and probe < w.heads:
-        probe = min(w.heads, probe * 4)
-        t = run(probe)
-    heads = max(1, min(w.heads, int(probe * target_s / max(t, 1e-9))))
-    if heads != probe:
+    def rows_flops(rows):
+        return sum(10.0 * w.d_k * visible_keys(w, i) for i in rows)
+
+    def spaced(r):
+        r = max(1, min(w.n, r))
+        return sorted({int(i * w.n / r) for i in range(r)})
+
+    rows = spaced(8)
+    run_rows(rows)  # the first call pays one-time costs (library load, thread start)
+    t = run_rows(rows)
+    while t < 0.25 and len(rows) < w.n:
+        rows = spaced(len(rows) * 4)
+        t = run_rows(rows)
+    rate = rows_flops(rows) / max(t, 1e-9)
+    per_head = step_flops(w) / w.heads
+    if per_head / rate <= target_s / 2:
+        def run(heads):
+            q, k, v, do = workload_inputs(w, with_grad=True, heads=heads)
+            t0 = time.perf_counter()
+            oracle.bwd(q, k, v, do, w.causal, scale, window=w.window)
+            return time.perf_counter() - t0
+
+        heads = max(1, min(w.heads, int(target_s / max(per_head / rate, 1e-9))))
         t = run(heads)
-    return per_head * heads / t / 1e12, t, heads, oracle.num_threads()
+        return (per_head * heads / t / 1e12, t,
+                f"{heads} of {w.heads} heads of {w.name}, forward and backward, {t:.1f} s", oracle.num_threads())
+    rows = spaced(int(len(rows) * target_s / max(t, 1e-9)))
+    t = run_rows(rows)
+    return (rows_flops(rows) / t / 1e12, t,
+            f"{len(rows)} of {w.n} query rows (evenly spaced) of one of {w.heads} heads of {w.name}: "
+            f"forward rows and dQ rows, {t:.1f} s", oracle.num_threads())
 
 
 # ----------------------------------------------------------------- GPU arm
@@ -268,8 +336,9 @@ def run_gpu(args, w: Workload, world, rank, local):
     A.load_library()
     scale = w.default_scale
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    set_bytes = 2 * (2 * w.heads * w.n * w.d_k + 2 * w.heads * w.m * w.d_k)
-    n_sets = max(1, min(8, math.ceil(2 * l2 / max(set_bytes, 1)) + 1))
+    n_sets, set_bytes = input_sets(w)
+    if n_sets * set_bytes <= 2 * l2:
+        raise RuntimeError(f"input sets ({n_sets} x {set_bytes} B) do not exceed twice the L2 ({l2} B)")
     sets = [make_inputs(w, 1000 * rank + 17 * s + w.cfg, dev) for s in range(n_sets)]
     o = torch.empty(w.B, w.h, w.n, w.d_v, dtype=torch.bfloat16, device=dev)
     lse = torch.empty(w.B, w.h, w.n, dtype=torch.float32, device=dev)
@@ -424,7 +493,13 @@ def run_gpu(args, w: Workload, world, rank, local):
 
 
 def run_sweep(args, local):
-    """Quick per-configuration throughput of attn_fwd and attn_bwd (rank 0, N=1 only)."""
+    """Per-configuration throughput of attn_fwd and attn_bwd (rank 0, N=1 only).
+
+    Every case rotates input sets whose total exceeds twice the L2, and takes
+    the median over 5 repeats of at least 10 steps each (at least 50 steps and
+    200 ms per case); the times are the library's per-kernel CUDA events on the
+    launching stream.
+    """
     import torch
     import transformer_scaled_dot_attn_gb300 as A
     dev = torch.device("cuda", local)
@@ -435,34 +510,50 @@ def run_sweep(args, local):
     names += ["long_n16384_d64_band257", "long_n16384_d64_local256"]
     for name in names:
         w = WORKLOADS[name]
-        q, k, v, do = make_inputs(w, 99, dev)
+        n_sets, _ = input_sets(w)
+        sets = [make_inputs(w, 99 + 7 * i, dev) for i in range(n_sets)]
         lens = kv_lengths(w)
         kvl = None if lens is None else torch.tensor(lens, dtype=torch.int32, device=dev)
-        o, lse = A.attn_fwd(q, k, v, causal=w.causal, scale=w.default_scale, kv_len=kvl, window=w.window)
-        dq, dk, dv = A.attn_bwd(q, k, v, o, lse, do, causal=w.causal, scale=w.default_scale, kv_len=kvl,
-                                window=w.window)
+        kw = dict(causal=w.causal, scale=w.default_scale, kv_len=kvl, window=w.window)
+        o, lse = A.attn_fwd(*sets[0][:3], **kw)
+        dq, dk, dv = A.attn_bwd(*sets[0][:3], o, lse, sets[0][3], **kw)
+        ws_bytes = A.attn_bwd_workspace_bytes(w.B, w.h, w.n, w.m, w.d_k, w.d_v, w.causal)
+        ws = torch.empty(max(ws_bytes, 16) // 4 + 4, dtype=torch.float32, device=dev)
         torch.cuda.synchronize()
-        iters = max(3, min(50, int(2e12 / max(step_flops(w), 1))))
-        A.attn_profile_enable(True)
-        for kind in A.KERNEL_KINDS:
-            A.attn_profile_read(kind)
-        for _ in range(iters):
-            A.attn_fwd(q, k, v, causal=w.causal, scale=w.default_scale, out=o, lse=lse, kv_len=kvl,
-                       window=w.window)
-            A.attn_bwd(q, k, v, o, lse, do, causal=w.causal, scale=w.default_scale, dq=dq, dk=dk, dv=dv,
-                       kv_len=kvl, window=w.window)
+
+        def step(i):
+            q, k, v, do = sets[i % n_sets]
+            A.attn_fwd(q, k, v, out=o, lse=lse, **kw)
+            A.attn_bwd(q, k, v, o, lse, do, dq=dq, dk=dk, dv=dv, workspace=ws, **kw)
+
+        t0 = time.perf_counter()
+        for i in range(3):
+            step(i)
         torch.cuda.synchronize()
-        A.attn_profile_enable(False)
-        prof = {kind: A.attn_profile_read(kind) for kind in A.KERNEL_KINDS}
-        f_ms = prof["fwd"][1] / max(prof["fwd"][0], 1)
-        b_ms = sum(prof[kd][1] for kd in ("bwd_pre", "bwd_main", "bwd_post")) / max(prof["bwd_main"][0], 1)
+        est = (time.perf_counter() - t0) / 3
+        per_rep = max(10, math.ceil(0.04 / max(est, 1e-6)))
+        f_list, b_list = [], []
+        for rep in range(5):
+            A.attn_profile_enable(True)
+            for kind in A.KERNEL_KINDS:
+                A.attn_profile_read(kind)
+            for i in range(per_rep):
+                step(i)
+            torch.cuda.synchronize()
+            A.attn_profile_enable(False)
+            prof = {kind: A.attn_profile_read(kind) for kind in A.KERNEL_KINDS}
+            f_list.append(prof["fwd"][1] / max(prof["fwd"][0], 1))
+            b_list.append(sum(prof[kd][1] for kd in ("bwd_pre", "bwd_main", "bwd_post")) /
+                          max(prof["bwd_main"][0], 1))
+        f_ms, b_ms = statistics.median(f_list), statistics.median(b_list)
         ftf = w.fwd_flops() / (f_ms / 1e3) / 1e12
         btf = w.bwd_flops() / (b_ms / 1e3) / 1e12
         out[name] = {"fwd_us": round(f_ms * 1e3, 1), "fwd_tflops": round(ftf, 1),
                      "fwd_frac_peak": round(ftf / peaks["bf16_tflops"], 3),
                      "bwd_us": round(b_ms * 1e3, 1), "bwd_tflops": round(btf, 1),
-                     "bwd_frac_peak": round(btf / peaks["bf16_tflops"], 3), "iters": iters}
-        del q, k, v, do, o, lse, dq, dk, dv, kvl
+                     "bwd_frac_peak": round(btf / peaks["bf16_tflops"], 3),
+                     "steps": 5 * per_rep, "input_sets": n_sets}
+        del sets, o, lse, dq, dk, dv, kvl, ws
         torch.cuda.empty_cache()
     if A.attn_get_device_status() != A.ATTN_OK:
         raise RuntimeError("device watchdog fired in the sweep")
@@ -613,7 +704,7 @@ def main():
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
-    ap.add_argument("--workload", default="encoder", choices=sorted(WORKLOADS))
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
     ap.add_argument("--no-sweep", action="store_true", help="skip the per-configuration sweep")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
@@ -632,26 +723,21 @@ def main():
         return
     world, rank, local = dist_setup()
     w = WORKLOADS[args.workload]
-    config = {"workload": f"{w.name}: B={w.B}, h={w.h}, n={w.n}, m={w.m}, d_k=d_v={w.d_k}, "
-                          f"causal={w.causal}" + (f", Q x {w.q_mult:g}" if w.q_mult != 1 else "")
-                          + (f", window={w.window}" if w.window is not None else ""),
-              "global_batch": w.B * world, "seq_len": w.n, "kv_len": w.m, "heads": w.h,
-              "head_dim": w.d_k, "causal": w.causal, "parallelism": f"replicas x{world} (independent batches)",
-              "step": "attn_fwd + attn_bwd"}
+    config = workload_config(w, world)
 
     if args.impl == "reference":
         if rank != 0:
             return
         per_step = []
-        heads = threads = 0
-        seconds = max(1.0, min(args.cpu_seconds, 60.0 / max(1, args.steps + args.warmup)))
-        for s in range(args.warmup + args.steps):
-            tf, t, heads, threads = oracle_sample(w, seconds)
-            if s >= args.warmup:
+        sample, threads = "", 0
+        seconds = max(1.0, min(args.cpu_seconds, 120.0 / max(1, args.steps + args.warmup)))
+        for st in range(args.warmup + args.steps):
+            tf, t, sample, threads = oracle_sample(w, seconds)
+            if st >= args.warmup:
                 per_step.append((tf, t))
         value = statistics.median(tf for tf, _ in per_step)
         ms = statistics.median(t for _, t in per_step) * 1e3
-        sample = f"{heads} of {w.heads} heads of {w.name} per step (fwd+bwd, fp64 C oracle)"
+        sample = f"per step: {sample} (fp64 C oracle)"
         line = {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": UNIT,
                 "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 2),
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
@@ -671,13 +757,10 @@ def main():
         proj_sweep = run_proj_sweep(args, local)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        tf, t, heads, threads = oracle_sample(w, args.cpu_seconds)
-        cpu = {"value": round(tf, 6), "unit": UNIT, "cores": threads, "kind": "oracle",
-               "sample": f"{heads} of {w.heads} heads of {w.name}, fwd+bwd, {t:.1f} s"}
+        tf, t, sample, threads = oracle_sample(w, args.cpu_seconds)
+        cpu = {"value": round(tf, 6), "unit": UNIT, "cores": threads, "kind": "oracle", "sample": sample}
     if rank != 0:
         return
-    config["l2"] = (f"rotating {res['n_sets']} input sets of {res['set_bytes'] / 1e6:.0f} MB "
-                    f"(> 2x the {res['l2_bytes'] / 1e6:.0f} MB L2)")
     peak = res["peaks"]["bf16_tflops"]
     line = {
         "metric": METRIC, "value": round(res["value"], 3), "unit": UNIT, "n_gpus": world,
