@@ -24,7 +24,8 @@
 //         warps 8-11 one thread per query row: add dQ_i into the fp32
 //                    accumulator with TMA reduce-adds.
 //         warp 12    TMA producer (tiles, and the per-row statistics by
-//                    bulk copy), warp 13 MMA issuer.
+//                    bulk copy); warps 13 and 14 the two MMA issuers, one
+//                    for S^T and dV, one for dP^T, dQ and dK.
 //   post  dQ = bf16(scale * accumulator).
 //
 // TMEM columns: S^T [0,128), dP^T [128,256), dV [256,256+D), dK [256+D,256+2D),
@@ -33,7 +34,7 @@
 // it through the dS buffer, two rounds of 64 columns).
 // Warps (512 threads): 0-3 and 4-7 the two compute warpgroups (query columns
 // 0..63 / 64..127 of every tile), 8-11 dQ accumulation, 12 TMA producer,
-// 13 MMA issuer; registers split 160 / 160 / 72 / 56 with setmaxnreg.
+// 13 and 14 MMA issuers; registers split 152 / 152 / 96 / 88 with setmaxnreg.
 #include "attn_kernels.cuh"
 
 #include <mutex>
@@ -164,7 +165,8 @@ struct Bwd {
 struct BwdShared {
   uint64_t kv_full[2], kv_empty[2];
   uint64_t qdo_full[2], qdo_empty[2];
-  uint64_t s_full, dp_full, p_full, ds_full, ds_empty, dq_full, dq_empty, dkv_full, acc_free, drain;
+  uint64_t s_full, dp_full, p_full, ds_full, ds_empty, dq_full, dq_empty, dkv_full, acc_free, drain, drain_b;
+  uint64_t dk_done;  // d = 128: the dK product has read dS (the dQ staging may overwrite it)
   uint64_t out_staged[2], out_free[2];  // d <= 64: dV / dK leave through dS region 0 / 1
   uint32_t tmem_base;
   int abort_flag;
@@ -256,11 +258,11 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   if (tid == 0) {
     for (int s = 0; s < C::KV_SETS; ++s) {
       mbar_init(&sh.kv_full[s], 1);
-      mbar_init(&sh.kv_empty[s], 1);
+      mbar_init(&sh.kv_empty[s], 2);  // both MMA issuers read the set
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&sh.qdo_full[s], 1);
-      mbar_init(&sh.qdo_empty[s], 1);
+      mbar_init(&sh.qdo_empty[s], 2);  // both MMA issuers read the stage
     }
     mbar_init(&sh.s_full, 1);
     mbar_init(&sh.dp_full, 1);
@@ -269,9 +271,11 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     mbar_init(&sh.ds_empty, 1);
     mbar_init(&sh.dq_full, 1);
     mbar_init(&sh.dq_empty, 128);
-    mbar_init(&sh.dkv_full, 1);
+    mbar_init(&sh.dkv_full, 2);  // dV (issuer A) and dK (issuer B) complete
     mbar_init(&sh.acc_free, 256);
     mbar_init(&sh.drain, 1);
+    mbar_init(&sh.drain_b, 1);
+    mbar_init(&sh.dk_done, 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&sh.out_staged[i], 128);
       mbar_init(&sh.out_free[i], 1);
@@ -348,8 +352,18 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       if (q_last0 >= 0) drain_wait_b(&sh.qdo_full[0], static_cast<uint32_t>(q_last0), wd);
       if (q_last1 >= 0) drain_wait_b(&sh.qdo_full[1], static_cast<uint32_t>(q_last1), wd);
     }
-  } else if (warp == 13) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp == 13 || warp == 14) {
+    // ------------------------------------------------------------ MMA issuers
+    // Two threads feed the tensor pipe, one per chain of products:
+    //   A (warp 13): S^T(t) and dV += P^T(t) dO(t)       (the P path)
+    //   B (warp 14): dP^T(t), dQ(t) = dS K, dK += dS^T Q  (the dS path)
+    // so that neither chain waits behind the other's barriers: A issues dV(t)
+    // and S^T(t+1) as soon as P(t) is in TMEM, while B waits for dS(t) and, at
+    // d = 128, for the dQ tile's columns before dP^T(t+1). The two chains use
+    // disjoint TMEM columns (S^T | dV for A, dP^T | dK | dQ for B) and share
+    // only operands in shared memory, whose stages are released when both
+    // threads' products have read them (barriers with two arrivals).
+    const bool is_a = (warp == 13);
     const uint32_t sQ = smem_u32(smem + C::OFF_Q), sDO = smem_u32(smem + C::OFF_DO);
     const uint32_t sDS = smem_u32(smem + C::OFF_DS);
     const uint32_t id_s = idesc_bf16_f32(128, 128, false, false) | (p.neg ? (1u << 13) : 0u);
@@ -382,23 +396,25 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       const uint32_t sK = smem_u32(smem + C::OFF_K + set * C::TILE);
       const uint32_t sV = smem_u32(smem + C::OFF_V + set * C::TILE);
       if (!(ok = wait_all(&sh.kv_full[set], use & 1, kSiteBwdLoad))) break;
-      // acc_free is waited once per item, in order: below before the first dV
-      // product, or here for an item without query tiles
+      // acc_free is waited once per item, in order: before the item's first dV
+      // (A) or dK (B) product, or here for an item without query tiles
       if (T == 0 && li >= 1 && !(ok = wait_all(&sh.acc_free, (li - 1) & 1, kSiteBwdFinal))) break;
       if (T > 0) {
         if (!(ok = wait_all(&sh.qdo_full[g & 1], (g >> 1) & 1, kSiteBwdLoad))) break;
-        if (lane == 0) {
-          tc_fence_after();
-          issue_kmajor(tmem + C::TM_S, sK, sQ + (g & 1) * C::TILE, id_s);
-          mma_commit(&sh.s_full);
-        }
-        __syncwarp();
-        // for d = 128 dP shares its TMEM columns with the previous tile's dQ
-        if (C::ALIAS_DQ && g >= 1 && !(ok = wait_all(&sh.dq_empty, (g - 1) & 1, kSiteBwdDQ))) break;
-        if (lane == 0) {
-          tc_fence_after();
-          issue_kmajor(tmem + C::TM_DP, sV, sDO + (g & 1) * C::TILE, id_dp);
-          mma_commit(&sh.dp_full);
+        if (is_a) {
+          if (lane == 0) {
+            tc_fence_after();
+            issue_kmajor(tmem + C::TM_S, sK, sQ + (g & 1) * C::TILE, id_s);
+            mma_commit(&sh.s_full);
+          }
+        } else {
+          // for d = 128 dP shares its TMEM columns with the previous tile's dQ
+          if (C::ALIAS_DQ && g >= 1 && !(ok = wait_all(&sh.dq_empty, (g - 1) & 1, kSiteBwdDQ))) break;
+          if (lane == 0) {
+            tc_fence_after();
+            issue_kmajor(tmem + C::TM_DP, sV, sDO + (g & 1) * C::TILE, id_dp);
+            mma_commit(&sh.dp_full);
+          }
         }
         __syncwarp();
       }
@@ -406,78 +422,88 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         const int gt = g + t;
         const int st = gt & 1;
         const uint32_t q_off = st * C::TILE;
-        // dV += P^T dO; P^T (bf16) sits in TMEM columns [0,32) and [64,96) of S^T,
-        // one block per compute warpgroup (queries 0..63 and 64..127)
-        if (!(ok = wait_all(&sh.p_full, gt & 1, kSiteBwdS))) break;
-        // The item's first dV product overwrites the accumulators: the previous
-        // item's epilogue must have read dK and dV out of TMEM. (Waiting here,
-        // not at the item's start, lets this item's S^T and dP^T overlap it.)
-        if (t == 0 && li >= 1 && !(ok = wait_all(&sh.acc_free, (li - 1) & 1, kSiteBwdFinal))) break;
-        if (lane == 0) {
-          tc_fence_after();
-#pragma unroll
-          for (int k = 0; k < 8; ++k)
-            mma_ts(tmem + C::TM_DV, tmem + C::TM_S + (k >> 2) * 64 + (k & 3) * 8, b_mn(sDO + q_off, k), id_kv,
-                   (t > 0 || k > 0) ? 1u : 0u);
-        }
-        __syncwarp();
-        // next S^T while the compute warps form dS
-        if (t + 1 < T) {
-          if (!(ok = wait_all(&sh.qdo_full[st ^ 1], ((gt + 1) >> 1) & 1, kSiteBwdLoad))) break;
-          if (lane == 0) {
-            issue_kmajor(tmem + C::TM_S, sK, sQ + (st ^ 1) * C::TILE, id_s);
-            mma_commit(&sh.s_full);
-          }
-          __syncwarp();
-        }
-        if (!(ok = wait_all(&sh.ds_full, gt & 1, kSiteBwdDS))) break;
-        if (!C::ALIAS_DQ && gt >= 1) {
-          if (!(ok = wait_all(&sh.dq_empty, (gt - 1) & 1, kSiteBwdDQ))) break;
-        }
-        if (lane == 0) {
-          tc_fence_after();
-          // dK += dS^T Q : A = dS^T (K-major over queries), B = Q (MN-major)
-#pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            const uint64_t da = smem_desc(sDS + (k >> 2) * C::DS_REGION + (k & 3) * 32, 16, 1024, 2);
-            mma_ss(tmem + C::TM_DK, da, b_mn(sQ + q_off, k), id_kv, (t > 0 || k > 0) ? 1u : 0u);
-          }
-          // dQ = dS K : A = dS (MN-major: queries contiguous), B = K (MN-major)
-#pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            const uint64_t da = smem_desc(sDS + k * 16 * 128, C::DS_REGION, 1024, 2);
-            mma_ss(tmem + C::TM_DQ, da, b_mn(sK, k), id_dq, k > 0 ? 1u : 0u);
-          }
-          mma_commit(&sh.dq_full);
-          if (!C::DQ_IN_DS) mma_commit(&sh.ds_empty);  // else the dQ warpgroup releases it
-          mma_commit(&sh.qdo_empty[st]);
-        }
-        __syncwarp();
-        if (t + 1 < T) {
-          if (C::ALIAS_DQ) {
-            if (!(ok = wait_all(&sh.dq_empty, gt & 1, kSiteBwdDQ))) break;
-          }
+        if (is_a) {
+          // dV += P^T dO; P^T (bf16) sits in TMEM columns [0,32) and [64,96) of S^T,
+          // one block per compute warpgroup (queries 0..63 and 64..127)
+          if (!(ok = wait_all(&sh.p_full, gt & 1, kSiteBwdS))) break;
+          // The item's first dV product overwrites the accumulator: the previous
+          // item's epilogue must have read dK and dV out of TMEM.
+          if (t == 0 && li >= 1 && !(ok = wait_all(&sh.acc_free, (li - 1) & 1, kSiteBwdFinal))) break;
           if (lane == 0) {
             tc_fence_after();
-            issue_kmajor(tmem + C::TM_DP, sV, sDO + (st ^ 1) * C::TILE, id_dp);
-            mma_commit(&sh.dp_full);
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+              mma_ts(tmem + C::TM_DV, tmem + C::TM_S + (k >> 2) * 64 + (k & 3) * 8, b_mn(sDO + q_off, k), id_kv,
+                     (t > 0 || k > 0) ? 1u : 0u);
           }
           __syncwarp();
+          // next S^T (over this tile's P^T, which dV has read by then in the pipe's order)
+          if (t + 1 < T) {
+            if (!(ok = wait_all(&sh.qdo_full[st ^ 1], ((gt + 1) >> 1) & 1, kSiteBwdLoad))) break;
+            if (lane == 0) {
+              issue_kmajor(tmem + C::TM_S, sK, sQ + (st ^ 1) * C::TILE, id_s);
+              mma_commit(&sh.s_full);
+            }
+          }
+          if (lane == 0) mma_commit(&sh.qdo_empty[st]);  // this thread's reads of Q(t), dO(t) done
+          __syncwarp();
+        } else {
+          if (!(ok = wait_all(&sh.ds_full, gt & 1, kSiteBwdDS))) break;
+          if (!C::ALIAS_DQ && gt >= 1) {
+            if (!(ok = wait_all(&sh.dq_empty, (gt - 1) & 1, kSiteBwdDQ))) break;
+          }
+          // The item's first dK product overwrites the accumulator (see above).
+          if (t == 0 && li >= 1 && !(ok = wait_all(&sh.acc_free, (li - 1) & 1, kSiteBwdFinal))) break;
+          if (lane == 0) {
+            tc_fence_after();
+            // dQ = dS K first: A = dS (MN-major: queries contiguous), B = K (MN-major).
+            // Its drain out of TMEM gates the next dP^T product at d = 128 (the two
+            // share columns), so it goes ahead of dK in the tensor pipe's order.
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+              const uint64_t da = smem_desc(sDS + k * 16 * 128, C::DS_REGION, 1024, 2);
+              mma_ss(tmem + C::TM_DQ, da, b_mn(sK, k), id_dq, k > 0 ? 1u : 0u);
+            }
+            mma_commit(&sh.dq_full);
+            // dK += dS^T Q : A = dS^T (K-major over queries), B = Q (MN-major)
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+              const uint64_t da = smem_desc(sDS + (k >> 2) * C::DS_REGION + (k & 3) * 32, 16, 1024, 2);
+              mma_ss(tmem + C::TM_DK, da, b_mn(sQ + q_off, k), id_kv, (t > 0 || k > 0) ? 1u : 0u);
+            }
+            if (C::DQ_IN_DS) mma_commit(&sh.dk_done);   // the dQ staging may now overwrite dS
+            else mma_commit(&sh.ds_empty);                // (d = 128: the dQ warpgroup releases it)
+            mma_commit(&sh.qdo_empty[st]);  // this thread's reads of Q(t), dO(t) done
+          }
+          __syncwarp();
+          if (t + 1 < T) {
+            if (C::ALIAS_DQ) {
+              if (!(ok = wait_all(&sh.dq_empty, gt & 1, kSiteBwdDQ))) break;
+            }
+            if (!(ok = wait_all(&sh.qdo_full[st ^ 1], ((gt + 1) >> 1) & 1, kSiteBwdLoad))) break;
+            if (lane == 0) {
+              tc_fence_after();
+              issue_kmajor(tmem + C::TM_DP, sV, sDO + (st ^ 1) * C::TILE, id_dp);
+              mma_commit(&sh.dp_full);
+            }
+            __syncwarp();
+          }
         }
       }
       if (!ok) break;
       if (lane == 0) {
-        mma_commit(&sh.dkv_full);
-        mma_commit(&sh.kv_empty[set]);
+        mma_commit(&sh.dkv_full);      // this thread's accumulator (dV or dK) is complete
+        mma_commit(&sh.kv_empty[set]);  // and its reads of K, V are done
       }
       __syncwarp();
       g += T;
     }
-    if (lane == 0) mma_commit(&sh.drain);
+    uint64_t* drain = is_a ? &sh.drain : &sh.drain_b;
+    if (lane == 0) mma_commit(drain);
     __syncwarp();
-    drain_wait_b(&sh.drain, 0, wd);
-  } else if (warp >= 14) {
-    // idle warps: they only complete the fourth warpgroup for the register split
+    drain_wait_b(drain, 0, wd);
+  } else if (warp >= 15) {
+    // idle warp: it only completes the fourth warpgroup for the register split
   } else if (warp < 8) {
     // ------------------------------------------------------------ P, dS, dK/dV epilogue
     // Two warpgroups on the same key rows (TMEM lanes): group h owns query
@@ -673,28 +699,37 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         // even when another role raises the abort flag meanwhile.
 #pragma unroll
         for (int round = 0; round < C::DQ_ROUNDS; ++round) {
-          // the previous reduce must have read the staging tile
-          if (ok && r == 0) bulk_wait_read_all();
-          if (named_bar_or(1, 128, !ok || *abort_flag != 0)) {
-            stop = true;
-            break;
-          }
+          // The round's dQ columns leave TMEM first, and after the last round the
+          // columns are released at once (for d = 128 the next dP^T product
+          // writes them); only then does the group wait for the staging tile.
           tc_fence_after();
+          uint32_t v[C::DQ_BOXES_PER_ROUND][32];
 #pragma unroll
-          for (int b = 0; b < C::DQ_BOXES_PER_ROUND; ++b) {
-            const int q = round * C::DQ_BOXES_PER_ROUND + b;  // 32-column box of dQ
-            uint32_t v[32];
-            tmem_ld32(t_dq + q * 32, v);
-            tmem_ld_wait();
-#pragma unroll
-            for (int ch = 0; ch < 8; ++ch)
-              *reinterpret_cast<uint4*>(stage_row + b * C::DQ_BOX + ((ch ^ sw) << 4)) =
-                  make_uint4(v[4 * ch], v[4 * ch + 1], v[4 * ch + 2], v[4 * ch + 3]);
-          }
+          for (int b = 0; b < C::DQ_BOXES_PER_ROUND; ++b)
+            tmem_ld32(t_dq + (round * C::DQ_BOXES_PER_ROUND + b) * 32, v[b]);  // 32-column boxes of dQ
+          tmem_ld_wait();
           if (round == C::DQ_ROUNDS - 1) {
             tc_fence_before();
             mbar_arrive(&sh.dq_empty);
           }
+          // the previous reduce must have read the staging tile; for d = 128 the
+          // staging tile is the dS buffer, which the dK product reads until dk_done
+          bool staged_ok = ok;
+          if (ok && r == 0) {
+            if (C::DQ_IN_DS && round == 0)
+              staged_ok = guarded_wait(&sh.dk_done, gt & 1, abort_flag, wd, kSiteBwdDQ);
+            bulk_wait_read_all();
+          }
+          if (named_bar_or(1, 128, !staged_ok || *abort_flag != 0)) {
+            stop = true;
+            break;
+          }
+#pragma unroll
+          for (int b = 0; b < C::DQ_BOXES_PER_ROUND; ++b)
+#pragma unroll
+            for (int ch = 0; ch < 8; ++ch)
+              *reinterpret_cast<uint4*>(stage_row + b * C::DQ_BOX + ((ch ^ sw) << 4)) =
+                  make_uint4(v[b][4 * ch], v[b][4 * ch + 1], v[b][4 * ch + 2], v[b][4 * ch + 3]);
           fence_proxy_async_smem();
           named_bar_sync(1, 128);
           if (r == 0) {
