@@ -32,6 +32,10 @@ SMALL = [
     _small("long1024_d64c_s", 1, 1, 1024, 1024, 64, True, 5),
     _small("long1024_d128c_s", 1, 1, 1024, 1024, 128, True, 5),
     _small("long700_d128_s", 1, 1, 700, 700, 128, False, 5),
+    # more short items than SMs, so that every persistent CTA runs several in a
+    # row: one key tile with a partial second query tile, and two key tiles
+    _small("items400_n200_m128_d32", 50, 8, 200, 128, 32, False, 7),
+    _small("items320_n256_m256_d64", 40, 8, 256, 256, 64, False, 8),
 ] + list(ragged_workloads())
 
 

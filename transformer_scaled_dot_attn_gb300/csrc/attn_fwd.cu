@@ -624,7 +624,15 @@ cudaError_t launch_fwd_cfg(const CUtensorMap& tq, const CUtensorMap& tk, const C
 // item's first score product, which only needs S to be free. The next item's
 // first P.V product waits until the epilogue has read O out of TMEM.
 // TMEM: S_0 S_1 [0,256), P_0 P_1 [256,384) (bf16 pairs), O_0 O_1 [384,384+2D).
-template <int D>
+//
+// Items of at most two key tiles (SHORT: m <= 256) are short enough that the
+// item boundary sets their rate. There the next item's first score product is
+// issued as soon as the softmax holds this item's last scores, the softmax
+// takes the next item's first exponentials before this item's epilogue (so
+// the last P.V runs under them), and O leaves through a staging tile of its
+// own, so the issuers release an item's Q set once its last score product has
+// read it (four K/V stages make room for the staging tiles).
+template <int D, bool SHORT = false>
 struct FwdP {
   static constexpr int NQ = 2, BN = 128;
   static constexpr int ATOM = D;                          // one swizzle atom per row (D <= 64)
@@ -635,11 +643,12 @@ struct FwdP {
   // K/V ring depth: a tile takes about 2.5 us from its TMA issue to its
   // arrival when every SM streams keys (measured with a clock64 trace at
   // n = m = 16384, d = 64), more than four stages of about 1.2 us cover
-  static constexpr int STAGES = 5;
+  static constexpr int STAGES = SHORT ? 4 : 5;
   static constexpr uint32_t OFF_Q = 0;                    // 2 sets x NQ tiles
   static constexpr uint32_t OFF_K = 2 * NQ * QTILE;
   static constexpr uint32_t OFF_V = OFF_K + STAGES * KTILE;
-  static constexpr uint32_t SMEM = OFF_V + STAGES * KTILE + 1024;
+  static constexpr uint32_t OFF_OSTG = OFF_V + STAGES * KTILE;  // SHORT: O staging, one tile per query tile
+  static constexpr uint32_t SMEM = OFF_OSTG + (SHORT ? NQ * QTILE : 0u) + 1024;
   static constexpr int THREADS = NQ * 128 + 128;          // softmax, producer, issuers, idle
   static constexpr int PRODUCER = 4 * NQ, ISSUER = 4 * NQ + 1;
   // setmaxnreg split of the 384 x 168 registers the CTA is launched with: the
@@ -660,17 +669,19 @@ struct FwdPShared {
   uint64_t kv_full[kMaxStages];
   uint64_t kv_empty[2][kMaxStages];
   uint64_t s_full[2], s_free[2], p_full[2], pv_done[2], o_full[2], o_free[2], o_staged[2];
+  uint64_t ostg_free[2];  // SHORT: the O store of the staging tile has read it
   uint64_t drain[2];
   uint32_t tmem_base;
   int abort_flag;
 };
 
 template <int D, bool SPEC>
-__global__ void __launch_bounds__(FwdP<D>::THREADS, 1)
+__global__ void __launch_bounds__(FwdP<D, !SPEC>::THREADS, 1)
 attn_fwd_persist_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                         const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
                         const FwdParams p, int BH, int items) {
-  using C = FwdP<D>;
+  using C = FwdP<D, !SPEC>;
+  constexpr bool SHORT = !SPEC;
   constexpr int NQ = C::NQ, BN = C::BN;
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) FwdPShared sh;
@@ -715,6 +726,7 @@ attn_fwd_persist_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
       mbar_init(&sh.o_full[g], 1);
       mbar_init(&sh.o_free[g], 128);
       mbar_init(&sh.o_staged[g], 128);
+      mbar_init(&sh.ostg_free[g], 1);
       mbar_init(&sh.drain[g], 1);
     }
     sh.abort_flag = 0;
@@ -821,20 +833,26 @@ attn_fwd_persist_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
       };
       bool ok = true;
       int jj = 0, gt = 0, oc = 0;  // K/V tiles of earlier items, this tile's S count, items with output
+      bool s0_ahead = false;       // SHORT: this item's first S was issued during the previous item
       for (int it = blockIdx.x, li = 0; ok && it < items; it += gridDim.x, ++li) {
         int bh, q0, mb, ntile[2], nt, nq_valid;
         item_of(it, bh, q0, mb, ntile, nt, nq_valid);
         const int T = g == 0 ? ntile[0] : ntile[1];
         if (T > 0) {
           const uint32_t sQ = smem_u32(smem + C::OFF_Q) + ((li & 1) * NQ + g) * C::QTILE;
-          // S of this item's first tile: Q landed, K_0 landed, the softmax holds the previous S
-          ok = guarded_wait(&sh.q_full[li & 1], (li >> 1) & 1, abort_flag, wd, kSiteQFull) &&
-               guarded_wait(&sh.kv_full[jj % C::STAGES], (jj / C::STAGES) & 1, abort_flag, wd, kSiteKFull) &&
-               (gt == 0 || guarded_wait(&sh.s_free[g], (gt - 1) & 1, abort_flag, wd, kSiteSFull));
-          if (!ok) break;
-          tc_fence_after();
-          issue_s(sQ, jj % C::STAGES);
-          mma_commit(&sh.s_full[g]);
+          if (!s0_ahead) {
+            // S of this item's first tile: Q landed, K_0 landed, the softmax holds the previous S
+            ok = guarded_wait(&sh.q_full[li & 1], (li >> 1) & 1, abort_flag, wd, kSiteQFull) &&
+                 guarded_wait(&sh.kv_full[jj % C::STAGES], (jj / C::STAGES) & 1, abort_flag, wd, kSiteKFull) &&
+                 (gt == 0 || guarded_wait(&sh.s_free[g], (gt - 1) & 1, abort_flag, wd, kSiteSFull));
+            if (!ok) break;
+            tc_fence_after();
+            issue_s(sQ, jj % C::STAGES);
+            mma_commit(&sh.s_full[g]);
+          }
+          s0_ahead = false;
+          // SHORT: the Q set is released to the producer once this item's last S read it
+          if (SHORT && T == 1) mma_commit(&sh.q_empty[li & 1]);
           for (int j = 0; ok && j < T; ++j) {
             const int st = (jj + j) % C::STAGES;
             if (j + 1 < T) {
@@ -845,6 +863,22 @@ attn_fwd_persist_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
               tc_fence_after();
               issue_s(sQ, jn % C::STAGES);
               mma_commit(&sh.s_full[g]);
+              if (SHORT && j + 2 == T) mma_commit(&sh.q_empty[li & 1]);
+            } else if (SHORT && it + static_cast<int>(gridDim.x) < items) {
+              // the next item's first S, ahead of this item's last P.V
+              int bh2, q02, mb2, ntile2[2], nt2, nq2;
+              item_of(it + gridDim.x, bh2, q02, mb2, ntile2, nt2, nq2);
+              if ((g == 0 ? ntile2[0] : ntile2[1]) > 0) {
+                const int l2 = li + 1, jn = jj + nt;
+                ok = guarded_wait(&sh.s_free[g], (gt + j) & 1, abort_flag, wd, kSiteSFull) &&
+                     guarded_wait(&sh.q_full[l2 & 1], (l2 >> 1) & 1, abort_flag, wd, kSiteQFull) &&
+                     guarded_wait(&sh.kv_full[jn % C::STAGES], (jn / C::STAGES) & 1, abort_flag, wd, kSiteKFull);
+                if (!ok) break;
+                tc_fence_after();
+                issue_s(smem_u32(smem + C::OFF_Q) + ((l2 & 1) * NQ + g) * C::QTILE, jn % C::STAGES);
+                mma_commit(&sh.s_full[g]);
+                s0_ahead = true;
+              }
             }
             if (!(ok = guarded_wait(&sh.p_full[g], (gt + j) & 1, abort_flag, wd, kSitePFull))) break;
             // the first P.V of an item overwrites O: the previous item's epilogue must have read it
@@ -858,6 +892,8 @@ attn_fwd_persist_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
           }
           gt += T;
           ++oc;
+        } else if (SHORT) {
+          mbar_arrive(&sh.q_empty[li & 1]);  // no S of this query tile reads the set
         }
         jj += nt;
       }
@@ -879,14 +915,18 @@ attn_fwd_persist_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
     const uint64_t c2 = f2_pack(c, c);
     bool ok = true;
     int gt = 0, oc = 0;
-    // Q set whose O store thread 0 issued but has not yet seen read (-1: none).
-    // The wait for the store is deferred to the next item so that thread 0
-    // (and with it the group) is not held up by the store's latency.
+    // Q set (SHORT: the staging tile, 0) whose O store thread 0 issued but has
+    // not yet seen read (-1: none). The wait for the store is deferred to the
+    // next item so that thread 0 (and with it the group) is not held up by the
+    // store's latency.
     int pending_q = -1;
     auto release_pending = [&]() {
       if (r == 0 && pending_q >= 0) {
         bulk_wait_read_all();
-        mbar_arrive(&sh.q_empty[pending_q]);  // this Q tile may take a later item's rows
+        if (SHORT)
+          mbar_arrive(&sh.ostg_free[g]);  // the staging tile may take the next item's O
+        else
+          mbar_arrive(&sh.q_empty[pending_q]);  // this Q tile may take a later item's rows
         pending_q = -1;
       }
     };
@@ -914,7 +954,13 @@ attn_fwd_persist_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
       }
       tc_fence_before();
       mbar_arrive(&sh.o_free[g]);  // the next item's first P.V may overwrite O
-      uint8_t* qtile = smem + C::OFF_Q + (ep.qs * NQ + g) * C::QTILE;
+      uint8_t* qtile = SHORT ? smem + C::OFF_OSTG + g * C::QTILE : smem + C::OFF_Q + (ep.qs * NQ + g) * C::QTILE;
+      if (SHORT && ep.oc >= 1) {
+        // the previous item's store must have read the staging tile
+        release_pending();
+        if (!__all_sync(0xffffffffu, guarded_wait(&sh.ostg_free[g], (ep.oc - 1) & 1, abort_flag, wd, kSiteOFull)))
+          return false;
+      }
 #pragma unroll
       for (int ch = 0; ch < D / 8; ++ch) {
         const int pc = (D == 64) ? (ch ^ (r & 7)) : (ch ^ ((r >> 1) & 3));
@@ -935,6 +981,9 @@ attn_fwd_persist_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
         p.lse[static_cast<size_t>(ep.bh) * p.n + ep.row] = (ep.m + log2f(ep.l)) * kLn2;
       return true;
     };
+    // SHORT: the previous item's epilogue, taken after this item's first exponentials
+    bool have_ep = false;
+    ItemOut pend{};
     for (int it = blockIdx.x, li = 0; ok && it < items; it += gridDim.x, ++li) {
       int bh, q0, mb, ntile[2], nt, nq_valid;
       item_of(it, bh, q0, mb, ntile, nt, nq_valid);
@@ -942,6 +991,12 @@ attn_fwd_persist_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
       const int qs = li & 1;
       if (T == 0) {
         if (mb == 0) write_empty_row<D>(p, bh, q0 + g * 128 + r, 0, D, true);
+        if (SHORT) {
+          // the previous item's deferred epilogue (SHORT) is written before anything else
+          if (have_ep && !(ok = epilogue(pend))) break;
+          have_ep = false;
+          continue;
+        }
         release_pending();
         // no rows of this item here: the Q set does not wait for this tile's output
         if (r == 0) mbar_arrive(&sh.q_empty[qs]);
@@ -1061,12 +1116,13 @@ attn_fwd_persist_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
           mbar_arrive(&sh.p_full[g]);
         }
       } else {
+        // SHORT items (at most two key tiles): every tile takes its maximum
         for (int j = 0; j < T; ++j) {
           const int gj = gt + j;
           ok = __all_sync(0xffffffffu, guarded_wait(&sh.s_full[g], gj & 1, abort_flag, wd, kSiteSFull));
           if (!ok) break;
           tc_fence_after();
-          if (j <= 1) release_pending();  // (a no-op at j = 1; this placement measured faster)
+          if (j <= 1) release_pending();  // (a no-op at j = 1)
           uint32_t s[C::CHUNKS][32];
   #pragma unroll
           for (int q = 0; q < C::CHUNKS; ++q) tmem_ld32(t_s + q * 32, s[q]);
@@ -1104,27 +1160,32 @@ attn_fwd_persist_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
             rescale = true;
           }
           const uint64_t nm2 = f2_pack(-m_used, -m_used);
+          // the weights stay in registers while the previous P.V (the previous
+          // item's last one at j = 0) finishes and the previous item's O leaves
+          float lsum[4] = {0.f, 0.f, 0.f, 0.f};
+          uint32_t pk[C::CHUNKS][16];
+  #pragma unroll
+          for (int q = 0; q < C::CHUNKS; ++q) {
+            // masked scores already hold -inf, and 2^(-inf * c - m) = 0 for c > 0;
+            // only c = 0 (scale 0) needs the explicit mask (-inf * 0 is NaN)
+            if (masked && c == 0.f)
+              exp_chunk<true, true>(s[q], q * 32, 0, rem, c2, nm2, lsum, pk[q]);
+            else
+              exp_chunk<false, true>(s[q], q * 32, 0, rem, c2, nm2, lsum, pk[q]);
+          }
+          if (j == 0 && have_ep) {
+            have_ep = false;
+            if (!(ok = epilogue(pend))) break;
+          }
           if (gj >= 1) {
             // the previous P.V (possibly the previous item's) still reads P until it completes
             ok = __all_sync(0xffffffffu, guarded_wait(&sh.pv_done[g], (gj - 1) & 1, abort_flag, wd, kSitePFull));
             if (!ok) break;
             tc_fence_after();
           }
-          float lsum[4] = {0.f, 0.f, 0.f, 0.f};
   #pragma unroll
-          for (int q = 0; q < C::CHUNKS; ++q) {
-            uint32_t pk[16];
-            // masked scores already hold -inf, and 2^(-inf * c - m) = 0 for c > 0;
-            // only c = 0 (scale 0) needs the explicit mask (-inf * 0 is NaN)
-            if (masked && c == 0.f)
-              exp_chunk<true, true>(s[q], q * 32, 0, rem, c2, nm2, lsum, pk);
-            else
-              exp_chunk<false, true>(s[q], q * 32, 0, rem, c2, nm2, lsum, pk);
-            tmem_st16(t_p + q * 16, pk);
-          }
-          {
-            l = l * alpha + ((lsum[0] + lsum[1]) + (lsum[2] + lsum[3]));
-          }
+          for (int q = 0; q < C::CHUNKS; ++q) tmem_st16(t_p + q * 16, pk[q]);
+          l = l * alpha + ((lsum[0] + lsum[1]) + (lsum[2] + lsum[3]));
           tmem_st_wait();
           if (j > 0 && __any_sync(0xffffffffu, rescale)) {
   #pragma unroll
@@ -1143,11 +1204,17 @@ attn_fwd_persist_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
         }
       }
       if (!ok) break;
-      release_pending();
-      if (!(ok = epilogue(ItemOut{qs, q0, bh, row, oc, l, m_used}))) break;
+      if (SHORT) {
+        pend = ItemOut{qs, q0, bh, row, oc, l, m_used};
+        have_ep = true;
+      } else {
+        release_pending();
+        if (!(ok = epilogue(ItemOut{qs, q0, bh, row, oc, l, m_used}))) break;
+      }
       gt += T;
       ++oc;
     }
+    if (SHORT && ok && have_ep) ok = epilogue(pend);
     release_pending();
     if (r == 0) tma_store_wait_all();  // stores must complete before the CTA exits
   }
@@ -1163,7 +1230,7 @@ attn_fwd_persist_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
 template <int D, bool SPEC>
 cudaError_t launch_fwd_persist_cfg(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                                    const CUtensorMap& to, FwdParams p, int BH, cudaStream_t stream) {
-  using C = FwdP<D>;
+  using C = FwdP<D, !SPEC>;
   static std::once_flag once[64];
   static int sm_count[64] = {0};
   int dev = 0;
