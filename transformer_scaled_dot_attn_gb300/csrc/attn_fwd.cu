@@ -211,8 +211,13 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int bh = blockIdx.x;
-  const int qb = p.causal ? (p.num_qblocks - 1 - static_cast<int>(blockIdx.y)) : blockIdx.y;
+  // Causal: blocks in order of decreasing length (the longest query blocks of
+  // every head first). Otherwise head-major: the CTAs that run at the same time
+  // share few heads, so their K and V stay in L2 instead of being read from
+  // HBM once per query block.
+  const int lin = static_cast<int>(blockIdx.x + blockIdx.y * gridDim.x);
+  const int bh = p.causal ? static_cast<int>(blockIdx.x) : lin / p.num_qblocks;
+  const int qb = p.causal ? (p.num_qblocks - 1 - static_cast<int>(blockIdx.y)) : lin % p.num_qblocks;
   const int q0 = qb * (NQ * 128);
   volatile int* abort_flag = &sh.abort_flag;
   const Watchdog wd = p.wd;
@@ -693,8 +698,10 @@ attn_fwd_persist_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
   // item -> (head, first query row); key tiles per query tile (0 past n)
   // item -> (head, first query row, real keys of the head)
   auto item_of = [&](int it, int& bh, int& q0, int& mb, int (&ntile)[2], int& nt, int& nq_valid) {
-    bh = it % BH;
-    const int y = it / BH;
+    // causal: the longest query blocks of every head first; otherwise head-major
+    // (CTAs working at the same time share the heads' K and V in L2)
+    bh = p.causal ? it % BH : it / p.num_qblocks;
+    const int y = p.causal ? it / BH : it % p.num_qblocks;
     const int qb = p.causal ? (p.num_qblocks - 1 - y) : y;
     q0 = qb * (NQ * 128);
     mb = head_keys(p.kv_len, bh, p.h, p.m);
