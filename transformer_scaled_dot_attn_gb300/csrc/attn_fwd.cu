@@ -57,6 +57,23 @@ constexpr uint32_t tmem_cols_for(uint32_t c) {
   return c <= 32 ? 32 : c <= 64 ? 64 : c <= 128 ? 128 : c <= 256 ? 256 : 512;
 }
 
+// The O correction after a row's reference maximum moved: O = alpha * O in
+// TMEM. It is rare once a row has seen a few key tiles, and it stays out of
+// line so that the softmax loops do not carry its registers and code (inlined,
+// the never-taken branch cost 5 % at n = m = 16384, d = 64).
+template <int NCOL>
+__device__ __noinline__ void rescale_o(uint32_t t_o, float alpha) {
+#pragma unroll
+  for (int q = 0; q < NCOL / 16; ++q) {
+    uint32_t o[16];
+    tmem_ld16(t_o + q * 16, o);
+    tmem_ld_wait();
+#pragma unroll
+    for (int i = 0; i < 16; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+    tmem_st16(t_o + q * 16, o);
+  }
+}
+
 template <int D, int NQ, int BN>
 struct Fwd {
   // P in TMEM columns of its own (see above)
@@ -159,7 +176,8 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, const
 
 // p = 2^(s*c - m) for one 32-column chunk of a row held in registers; packs
 // the bf16 weights into pk and adds the weights into lsum. MASKED: columns at
-// or past `rem` or before `rlo` (keys this row may not see) get weight exactly 0.
+// or past `rem` or before `rlo` (keys this row may not see) get weight exactly 0
+// (needed for c = 0 only: otherwise their scores hold -inf already).
 // EXACT_SUM: the weights are added as rounded to bf16 (mixed-precision adds),
 // so the row sum l is the sum of the weights the P.V product applies and O / l
 // is an exact convex combination of value rows (a row dominated by one key
@@ -212,12 +230,12 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                                              ~static_cast<uintptr_t>(1023));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   // Causal: blocks in order of decreasing length (the longest query blocks of
-  // every head first). Otherwise head-major: the CTAs that run at the same time
-  // share few heads, so their K and V stay in L2 instead of being read from
-  // HBM once per query block.
-  const int lin = static_cast<int>(blockIdx.x + blockIdx.y * gridDim.x);
-  const int bh = p.causal ? static_cast<int>(blockIdx.x) : lin / p.num_qblocks;
-  const int qb = p.causal ? (p.num_qblocks - 1 - static_cast<int>(blockIdx.y)) : lin % p.num_qblocks;
+  // every head first). Otherwise head-major (the launcher puts the query block
+  // on x): the CTAs that run at the same time share few heads, so their K and
+  // V stay in L2 instead of being read from HBM once per query block.
+  const int bh = p.qb_fast ? static_cast<int>(blockIdx.y) : static_cast<int>(blockIdx.x);
+  const int y = p.qb_fast ? static_cast<int>(blockIdx.x) : static_cast<int>(blockIdx.y);
+  const int qb = p.causal ? (p.num_qblocks - 1 - y) : y;
   const int q0 = qb * (NQ * 128);
   volatile int* abort_flag = &sh.abort_flag;
   const Watchdog wd = p.wd;
@@ -512,15 +530,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       l = l * alpha + ((lsum[0] + lsum[1]) + (lsum[2] + lsum[3]));
       tmem_st_wait();
       if (j > 0 && __any_sync(0xffffffffu, rescale)) {
-#pragma unroll
-        for (int q = 0; q < C::OCOLS / 16; ++q) {
-          uint32_t o[16];
-          tmem_ld16(t_o + q * 16, o);
-          tmem_ld_wait();
-#pragma unroll
-          for (int i = 0; i < 16; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-          tmem_st16(t_o + q * 16, o);
-        }
+        rescale_o<C::OCOLS>(t_o, alpha);
         tmem_st_wait();
       }
       tc_fence_before();
@@ -610,7 +620,10 @@ cudaError_t launch_fwd_cfg(const CUtensorMap& tq, const CUtensorMap& tk, const C
       return cudaErrorInvalidConfiguration;
   }
   p.num_qblocks = (p.n + NQ * 128 - 1) / (NQ * 128);
-  dim3 grid(static_cast<unsigned>(BH), static_cast<unsigned>(p.num_qblocks));
+  // grid y is limited to 65535: heads go on y only where they fit
+  p.qb_fast = (!p.causal && BH <= 65535) ? 1 : 0;
+  const dim3 grid = p.qb_fast ? dim3(static_cast<unsigned>(p.num_qblocks), static_cast<unsigned>(BH))
+                              : dim3(static_cast<unsigned>(BH), static_cast<unsigned>(p.num_qblocks));
   prof_begin(kKindFwd, stream);
   attn_fwd_kernel<D, NQ, BN, WIN><<<grid, C::THREADS, C::SMEM, stream>>>(tq, tk, tv, to, p);
   e = cudaGetLastError();
@@ -918,7 +931,12 @@ attn_fwd_persist_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
     const uint32_t t_s = tmem + lane_base + C::tm_s(g);
     const uint32_t t_p = tmem + lane_base + C::tm_p(g);
     const uint32_t t_o = tmem + lane_base + C::tm_o(g);
-    const float c = p.c;
+    // Scale 0 runs with a tiny positive c instead of 0: every score times c is
+    // then far below the fp32 spacing at the reference, so each visible weight
+    // is exactly 1 as for c = 0, while the masked scores (-inf) keep weight 0
+    // (-inf * 0 would be NaN) without a second, masking copy of the exp loop
+    // (the smaller loop measured 2 % faster at n = m = 16384, d = 64).
+    const float c = p.c > 0.f ? p.c : 1e-30f;
     const uint64_t c2 = f2_pack(c, c);
     bool ok = true;
     int gt = 0, oc = 0;
@@ -1074,18 +1092,12 @@ attn_fwd_persist_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
             const uint64_t nm2 = f2_pack(-m_used, -m_used);
             lsum[0] = lsum[1] = lsum[2] = lsum[3] = 0.f;
   #pragma unroll
-            for (int q = 0; q < C::CHUNKS; ++q) {
-              // masked scores already hold -inf, and 2^(-inf * c - m) = 0 for c > 0;
-              // only c = 0 (scale 0) needs the explicit mask (-inf * 0 is NaN)
-              if (masked && c == 0.f)
-                exp_chunk<true, false>(s[q], q * 32, 0, rem, c2, nm2, lsum, pk[q]);
-              else
-                exp_chunk<false, false>(s[q], q * 32, 0, rem, c2, nm2, lsum, pk[q]);
-            }
+            for (int q = 0; q < C::CHUNKS; ++q) exp_chunk<false, false>(s[q], 0, 0, 0, c2, nm2, lsum, pk[q]);
             return (lsum[0] + lsum[1]) + (lsum[2] + lsum[3]);
           };
           // the weights are computed while the previous P.V still runs, then stored
           float l_tile = exps();
+          bool pv_waited = false;
           if (spec) {
             const bool grew = !(l_tile <= kSpecLimitSum);  // also catches inf / NaN
             if (__any_sync(0xffffffffu, grew)) {
@@ -1093,12 +1105,19 @@ attn_fwd_persist_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
                 const float m_new = tile_max();
                 alpha = ex2(m_used - m_new);
                 m_used = m_new;
-                rescale = true;
               }
               l_tile = exps();  // unchanged for the rows that did not grow
+              // O follows the moved reference (alpha = 1 for the other rows) once
+              // the previous P.V has added to it, before this tile's P.V does; the
+              // vote above is the only one the speculative tiles take for this
+              ok = __all_sync(0xffffffffu, guarded_wait(&sh.pv_done[g], (gj - 1) & 1, abort_flag, wd, kSitePFull));
+              if (!ok) break;
+              tc_fence_after();
+              pv_waited = true;
+              rescale_o<D>(t_o, alpha);
             }
           }
-          if (gj >= 1) {
+          if (gj >= 1 && !pv_waited) {
             // the previous P.V (possibly the previous item's) still reads P until it completes
             ok = __all_sync(0xffffffffu, guarded_wait(&sh.pv_done[g], (gj - 1) & 1, abort_flag, wd, kSitePFull));
             if (!ok) break;
@@ -1107,17 +1126,7 @@ attn_fwd_persist_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
   #pragma unroll
           for (int q = 0; q < C::CHUNKS; ++q) tmem_st16(t_p + q * 16, pk[q]);
           l = l * alpha + l_tile;
-          if (j > 0 && __any_sync(0xffffffffu, rescale)) {
-  #pragma unroll
-            for (int q = 0; q < D / 16; ++q) {
-              uint32_t o[16];
-              tmem_ld16(t_o + q * 16, o);
-              tmem_ld_wait();
-  #pragma unroll
-              for (int i = 0; i < 16; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-              tmem_st16(t_o + q * 16, o);
-            }
-          }
+          if (!spec && j > 0 && __any_sync(0xffffffffu, rescale)) rescale_o<D>(t_o, alpha);
           tmem_st_wait();
           tc_fence_before();
           mbar_arrive(&sh.p_full[g]);
@@ -1172,14 +1181,7 @@ attn_fwd_persist_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
           float lsum[4] = {0.f, 0.f, 0.f, 0.f};
           uint32_t pk[C::CHUNKS][16];
   #pragma unroll
-          for (int q = 0; q < C::CHUNKS; ++q) {
-            // masked scores already hold -inf, and 2^(-inf * c - m) = 0 for c > 0;
-            // only c = 0 (scale 0) needs the explicit mask (-inf * 0 is NaN)
-            if (masked && c == 0.f)
-              exp_chunk<true, true>(s[q], q * 32, 0, rem, c2, nm2, lsum, pk[q]);
-            else
-              exp_chunk<false, true>(s[q], q * 32, 0, rem, c2, nm2, lsum, pk[q]);
-          }
+          for (int q = 0; q < C::CHUNKS; ++q) exp_chunk<false, true>(s[q], 0, 0, 0, c2, nm2, lsum, pk[q]);
           if (j == 0 && have_ep) {
             have_ep = false;
             if (!(ok = epilogue(pend))) break;
@@ -1195,15 +1197,7 @@ attn_fwd_persist_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
           l = l * alpha + ((lsum[0] + lsum[1]) + (lsum[2] + lsum[3]));
           tmem_st_wait();
           if (j > 0 && __any_sync(0xffffffffu, rescale)) {
-  #pragma unroll
-            for (int q = 0; q < D / 16; ++q) {
-              uint32_t o[16];
-              tmem_ld16(t_o + q * 16, o);
-              tmem_ld_wait();
-  #pragma unroll
-              for (int i = 0; i < 16; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-              tmem_st16(t_o + q * 16, o);
-            }
+            rescale_o<D>(t_o, alpha);
             tmem_st_wait();
           }
           tc_fence_before();

@@ -99,6 +99,7 @@ struct FwdParams {
   int neg;            // scale < 0: the score MMA negates Q K^T so that c >= 0
   float c;            // |scale| * log2(e)
   int num_qblocks;    // query blocks (set by the launcher)
+  int qb_fast;        // per-item forward grid: 1 = (query block, head), 0 = (head, query block)
   int inject;         // test hook: 1 = skip the first value-tile load
   const int* kv_len;  // [B] real keys per sequence (key padding) or nullptr
   int h;              // heads per sequence (kv_len is indexed by bh / h)
