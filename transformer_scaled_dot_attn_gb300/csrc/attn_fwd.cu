@@ -440,7 +440,10 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     const uint32_t t_o = tmem + lane_base + C::tm_o(g);
     int klo, khi;  // visible keys [klo, khi) of this row
     key_range(row, mb, p.causal, wl, wr, klo, khi);
-    const float c = p.c;
+    // d <= 64: scale 0 runs with a tiny positive c (see the persistent kernel),
+    // so one exponential loop serves masked and unmasked tiles (2-7 % faster for
+    // the short and the causal shapes; at d = 128 the two loops measured faster)
+    const float c = (D <= 64 && !(p.c > 0.f)) ? 1e-30f : p.c;
     const uint64_t c2 = f2_pack(c, c);
     float m_used = -INFINITY, l = 0.f;
     bool ok = true;
@@ -519,8 +522,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       for (int q = 0; q < C::CHUNKS; ++q) {
         uint32_t pk[16];
         // masked scores already hold -inf, and 2^(-inf * c - m) = 0 for c > 0;
-        // only c = 0 (scale 0) needs the explicit mask (-inf * 0 is NaN)
-        if (masked && c == 0.f)
+        // only c = 0 (scale 0, d = 128) needs the explicit mask (-inf * 0 is NaN)
+        if (D > 64 && masked && c == 0.f)
           exp_chunk<true, true>(s[q], q * 32, rlo, rem, c2, nm2, lsum, pk);
         else
           exp_chunk<false, true>(s[q], q * 32, rlo, rem, c2, nm2, lsum, pk);
