@@ -86,9 +86,10 @@ __global__ void __launch_bounds__(256) attn_bwd_pre_kernel(const BwdPreParams p)
   for (int off = LPR / 2; off > 0; off >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off, LPR);
   if (row < total && sub == 0) {
     p.Dsum[row] = valid ? dot : 0.f;
-    // rows past n and rows that saw no key (lse = -inf) get lse2 = +inf: weight 0
+    // -lse * log2(e), the exponent offset of P; rows past n and rows that saw no
+    // key (lse = -inf) get -inf: weight 0
     const float lse = valid ? p.lse[static_cast<size_t>(bh) * p.n + i] : -INFINITY;
-    p.lse2[row] = (lse > -INFINITY) ? lse * kLog2e : INFINITY;
+    p.lse2[row] = (lse > -INFINITY) ? -lse * kLog2e : -INFINITY;
   }
 }
 
@@ -300,7 +301,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = sh.tmem_base;
-  float* stat = reinterpret_cast<float*>(smem + C::OFF_STAT);  // [stage][lse2 | D][128]
+  float* stat = reinterpret_cast<float*>(smem + C::OFF_STAT);  // [stage][-lse2 | D][128]
 
   if (warp >= 12) {
     reg_dealloc<C::REG_OTHER>();
@@ -516,7 +517,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     const uint32_t t_s = tmem + lane_base + C::TM_S + col0;
     const uint32_t t_dp = tmem + lane_base + C::TM_DP + col0;
     // Scale 0 runs with a tiny positive c instead of 0, as in the forward: each
-    // visible weight stays exactly 2^-lse2, and a score of -inf (a masked
+    // visible weight stays exactly 2^(-lse * log2 e), and a score of -inf (a masked
     // query) gives weight 0 (-inf * 0 would be NaN), so the exponential loop
     // needs no per-element mask test.
     const float c = p.c > 0.f ? p.c : 1e-30f;
@@ -549,10 +550,10 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                                          guarded_wait(&sh.qdo_full[st], (gt >> 1) & 1, abort_flag, wd, kSiteBwdLoad));
         if (!ok) break;
         tc_fence_after();
-        const float* lse2_s = stat + st * 256 + col0;
+        const float* nlse2_s = stat + st * 256 + col0;  // -lse * log2(e) per query column
         const float* D_s = stat + st * 256 + 128 + col0;
-        // P^T in fp32 for dS below; rounded to bf16 for the dV product
-        float P[64];
+        // P^T in fp32 pairs for dS below; rounded to bf16 for the dV product
+        uint64_t P2[32];
         {
           uint32_t s[2][32];
           tmem_ld32(t_s, s[0]);
@@ -570,15 +571,21 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 if (col < lo || col >= hi) s[q][i] = __float_as_uint(-INFINITY);
               }
           }
+          const uint64_t c2 = f2_pack(c, c);
 #pragma unroll
           for (int q = 0; q < 2; ++q) {
 #pragma unroll
             for (int i4 = 0; i4 < 8; ++i4) {
-              const float4 L = *reinterpret_cast<const float4*>(lse2_s + q * 32 + i4 * 4);
-              const float Lv[4] = {L.x, L.y, L.z, L.w};
+              const float4 L = *reinterpret_cast<const float4*>(nlse2_s + q * 32 + i4 * 4);
 #pragma unroll
-              for (int u = 0; u < 4; ++u)
-                P[q * 32 + i4 * 4 + u] = ex2f(fmaf(__uint_as_float(s[q][i4 * 4 + u]), c, -Lv[u]));
+              for (int u = 0; u < 2; ++u) {
+                const int col = i4 * 4 + u * 2;
+                const uint64_t x2 = fma2(f2_pack(__uint_as_float(s[q][col]), __uint_as_float(s[q][col + 1])), c2,
+                                         u ? f2_pack(L.z, L.w) : f2_pack(L.x, L.y));
+                float x0, x1;
+                f2_unpack(x2, x0, x1);
+                P2[q * 16 + i4 * 2 + u] = f2_pack(ex2f(x0), ex2f(x1));
+              }
             }
           }
         }
@@ -586,7 +593,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         for (int q = 0; q < 2; ++q) {
           uint32_t pk[16];
 #pragma unroll
-          for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(P[q * 32 + 2 * i], P[q * 32 + 2 * i + 1]);
+          for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2_pair(P2[q * 16 + i]);
           tmem_st16(t_s + q * 16, pk);
         }
         tmem_st_wait();
@@ -609,12 +616,14 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 #pragma unroll
           for (int i4 = 0; i4 < 8; ++i4) {
             const float4 Dv = *reinterpret_cast<const float4*>(D_s + q * 32 + i4 * 4);
-            const float ds0 = P[q * 32 + i4 * 4 + 0] * (__uint_as_float(dp[i4 * 4 + 0]) - Dv.x);
-            const float ds1 = P[q * 32 + i4 * 4 + 1] * (__uint_as_float(dp[i4 * 4 + 1]) - Dv.y);
-            const float ds2 = P[q * 32 + i4 * 4 + 2] * (__uint_as_float(dp[i4 * 4 + 2]) - Dv.z);
-            const float ds3 = P[q * 32 + i4 * 4 + 3] * (__uint_as_float(dp[i4 * 4 + 3]) - Dv.w);
-            pk[i4 * 2 + 0] = pack_bf16x2(ds0, ds1);
-            pk[i4 * 2 + 1] = pack_bf16x2(ds2, ds3);
+            const uint64_t a = mul2(P2[q * 16 + i4 * 2],
+                                    sub2(f2_pack(__uint_as_float(dp[i4 * 4]), __uint_as_float(dp[i4 * 4 + 1])),
+                                         f2_pack(Dv.x, Dv.y)));
+            const uint64_t b = mul2(P2[q * 16 + i4 * 2 + 1],
+                                    sub2(f2_pack(__uint_as_float(dp[i4 * 4 + 2]), __uint_as_float(dp[i4 * 4 + 3])),
+                                         f2_pack(Dv.z, Dv.w)));
+            pk[i4 * 2 + 0] = pack_bf16x2_pair(a);
+            pk[i4 * 2 + 1] = pack_bf16x2_pair(b);
           }
           // these 32 queries are 16-byte chunks 4q..4q+3 of this row of region h
 #pragma unroll

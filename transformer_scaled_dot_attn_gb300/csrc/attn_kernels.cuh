@@ -121,7 +121,7 @@ struct BwdPreParams {
   const __nv_bfloat16* o;   // [BH, n, d]
   const __nv_bfloat16* dO;  // [BH, n, d]
   const float* lse;         // [BH, n]
-  float* lse2;              // [BH, n_pad]  lse * log2(e)  (padding rows: +inf)
+  float* lse2;              // [BH, n_pad]  -lse * log2(e)  (padding rows: -inf)
   float* Dsum;              // [BH, n_pad]  D_i = sum_c dO_ic O_ic (padding rows: 0)
   float* dq_acc;            // [BH, n_pad, d] zeroed here
   int n, n_pad, d, BH;
