@@ -128,12 +128,17 @@ struct Bwd {
   static constexpr uint32_t DS_REGION = 128u * 64u * 2u;
   // K/V tiles: two sets for d <= 64 so the next work item's keys load while
   // the current one finishes; one set for d = 128 (shared memory is full).
-  static constexpr int KV_SETS = (D <= 64) ? 2 : 1;
+  // Q / dO ring: three stages for d <= 64 (a query tile's loads take about half
+  // a tile's time to land), two for d = 128 (shared memory is full). K/V: two
+  // sets for d = 32 so the next item's keys load early; one otherwise (d = 64
+  // gives its second set to the third Q / dO stage).
+  static constexpr int QS = (D <= 64) ? 3 : 2;
+  static constexpr int KV_SETS = (D <= 32) ? 2 : 1;
   static constexpr uint32_t OFF_K = 0;
   static constexpr uint32_t OFF_V = KV_SETS * TILE;
-  static constexpr uint32_t OFF_Q = 2 * KV_SETS * TILE;          // 2 stages
-  static constexpr uint32_t OFF_DO = OFF_Q + 2 * TILE;           // 2 stages
-  static constexpr uint32_t OFF_DS = OFF_DO + 2 * TILE;          // dS^T: 2 regions [128 keys][64 queries]
+  static constexpr uint32_t OFF_Q = 2 * KV_SETS * TILE;          // QS stages
+  static constexpr uint32_t OFF_DO = OFF_Q + QS * TILE;          // QS stages
+  static constexpr uint32_t OFF_DS = OFF_DO + QS * TILE;         // dS^T: 2 regions [128 keys][64 queries]
   static constexpr uint32_t OFF_STAT = OFF_DS + 2 * DS_REGION;   // per stage: lse*log2(e)[128], D[128]
   static constexpr uint32_t STAT_BYTES = 2u * 128u * 4u;
   // The fp32 dQ tile is staged in shared memory (128-byte swizzled boxes of
@@ -145,7 +150,7 @@ struct Bwd {
   static constexpr bool DQ_IN_DS = (D > 64);
   static constexpr int DQ_ROUNDS = DQ_IN_DS ? 2 : 1;
   static constexpr int DQ_BOXES_PER_ROUND = (D / 32) / DQ_ROUNDS;
-  static constexpr uint32_t OFF_DQS = OFF_STAT + 2 * STAT_BYTES;
+  static constexpr uint32_t OFF_DQS = OFF_STAT + QS * STAT_BYTES;
   static constexpr uint32_t DQS_BYTES = DQ_IN_DS ? 0u : (D / 32) * DQ_BOX;
   static constexpr uint32_t OFF_BAR = OFF_DQS + DQS_BYTES;
   static constexpr uint32_t PAYLOAD = OFF_BAR + 256;
@@ -165,7 +170,7 @@ struct Bwd {
 
 struct BwdShared {
   uint64_t kv_full[2], kv_empty[2];
-  uint64_t qdo_full[2], qdo_empty[2];
+  uint64_t qdo_full[3], qdo_empty[3];
   uint64_t s_full, dp_full, p_full, ds_full, ds_empty, dq_full, dq_empty, dkv_full, acc_free, drain, drain_b;
   uint64_t dk_done;  // d = 128: the dK product has read dS (the dQ staging may overwrite it)
   uint64_t out_staged[2], out_free[2];  // d <= 64: dV / dK leave through dS region 0 / 1
@@ -261,7 +266,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       mbar_init(&sh.kv_full[s], 1);
       mbar_init(&sh.kv_empty[s], 2);  // both MMA issuers read the set
     }
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < C::QS; ++s) {
       mbar_init(&sh.qdo_full[s], 1);
       mbar_init(&sh.qdo_empty[s], 2);  // both MMA issuers read the stage
     }
@@ -311,7 +316,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     if (lane == 0) {
       // parity of the last fill of each K/V set and each Q/dO stage (-1: never filled);
       // scalars rather than arrays so that they stay in registers
-      int kv_last0 = -1, kv_last1 = -1, q_last0 = -1, q_last1 = -1;
+      int kv_last0 = -1, kv_last1 = -1, q_last0 = -1, q_last1 = -1, q_last2 = -1;
       int g = 0, li = 0;
       bool ok = true;
       for (int it = blockIdx.x; ok && it < p.num_items; it += gridDim.x, ++li) {
@@ -330,9 +335,9 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         const float* lse2_h = p.lse2 + static_cast<size_t>(bh) * p.n_pad;
         const float* D_h = p.Dsum + static_cast<size_t>(bh) * p.n_pad;
         for (int t = 0; t < T; ++t, ++g) {
-          const int st = g & 1;
-          const uint32_t ph = (g >> 1) & 1;
-          if (g >= 2 && !guarded_wait(&sh.qdo_empty[st], ph ^ 1, abort_flag, wd, kSiteBwdFree)) {
+          const int st = g % C::QS;
+          const uint32_t ph = (g / C::QS) & 1;
+          if (g >= C::QS && !guarded_wait(&sh.qdo_empty[st], ph ^ 1, abort_flag, wd, kSiteBwdFree)) {
             ok = false;
             break;
           }
@@ -344,7 +349,9 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           }
           bulk_load(stat + st * 256, lse2_h + q_row, 512, &sh.qdo_full[st]);
           bulk_load(stat + st * 256 + 128, D_h + q_row, 512, &sh.qdo_full[st]);
-          if (st == 0) q_last0 = static_cast<int>(ph); else q_last1 = static_cast<int>(ph);
+          if (st == 0) q_last0 = static_cast<int>(ph);
+          else if (st == 1) q_last1 = static_cast<int>(ph);
+          else q_last2 = static_cast<int>(ph);
         }
       }
       // Let every copy this thread started land before shared memory is released.
@@ -352,6 +359,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       if (kv_last1 >= 0) drain_wait_b(&sh.kv_full[1], static_cast<uint32_t>(kv_last1), wd);
       if (q_last0 >= 0) drain_wait_b(&sh.qdo_full[0], static_cast<uint32_t>(q_last0), wd);
       if (q_last1 >= 0) drain_wait_b(&sh.qdo_full[1], static_cast<uint32_t>(q_last1), wd);
+      if (q_last2 >= 0) drain_wait_b(&sh.qdo_full[2], static_cast<uint32_t>(q_last2), wd);
     }
   } else if (warp == 13 || warp == 14) {
     // ------------------------------------------------------------ MMA issuers
@@ -401,11 +409,11 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       // (A) or dK (B) product, or here for an item without query tiles
       if (T == 0 && li >= 1 && !(ok = wait_all(&sh.acc_free, (li - 1) & 1, kSiteBwdFinal))) break;
       if (T > 0) {
-        if (!(ok = wait_all(&sh.qdo_full[g & 1], (g >> 1) & 1, kSiteBwdLoad))) break;
+        if (!(ok = wait_all(&sh.qdo_full[g % C::QS], (g / C::QS) & 1, kSiteBwdLoad))) break;
         if (is_a) {
           if (lane == 0) {
             tc_fence_after();
-            issue_kmajor(tmem + C::TM_S, sK, sQ + (g & 1) * C::TILE, id_s);
+            issue_kmajor(tmem + C::TM_S, sK, sQ + (g % C::QS) * C::TILE, id_s);
             mma_commit(&sh.s_full);
           }
         } else {
@@ -413,7 +421,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           if (C::ALIAS_DQ && g >= 1 && !(ok = wait_all(&sh.dq_empty, (g - 1) & 1, kSiteBwdDQ))) break;
           if (lane == 0) {
             tc_fence_after();
-            issue_kmajor(tmem + C::TM_DP, sV, sDO + (g & 1) * C::TILE, id_dp);
+            issue_kmajor(tmem + C::TM_DP, sV, sDO + (g % C::QS) * C::TILE, id_dp);
             mma_commit(&sh.dp_full);
           }
         }
@@ -421,7 +429,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       }
       for (int t = 0; ok && t < T; ++t) {
         const int gt = g + t;
-        const int st = gt & 1;
+        const int st = gt % C::QS, sn = (gt + 1) % C::QS;  // this tile's stage, the next one's
         const uint32_t q_off = st * C::TILE;
         if (is_a) {
           // dV += P^T dO; P^T (bf16) sits in TMEM columns [0,32) and [64,96) of S^T,
@@ -440,9 +448,9 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           __syncwarp();
           // next S^T (over this tile's P^T, which dV has read by then in the pipe's order)
           if (t + 1 < T) {
-            if (!(ok = wait_all(&sh.qdo_full[st ^ 1], ((gt + 1) >> 1) & 1, kSiteBwdLoad))) break;
+            if (!(ok = wait_all(&sh.qdo_full[sn], ((gt + 1) / C::QS) & 1, kSiteBwdLoad))) break;
             if (lane == 0) {
-              issue_kmajor(tmem + C::TM_S, sK, sQ + (st ^ 1) * C::TILE, id_s);
+              issue_kmajor(tmem + C::TM_S, sK, sQ + sn * C::TILE, id_s);
               mma_commit(&sh.s_full);
             }
           }
@@ -481,10 +489,10 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             if (C::ALIAS_DQ) {
               if (!(ok = wait_all(&sh.dq_empty, gt & 1, kSiteBwdDQ))) break;
             }
-            if (!(ok = wait_all(&sh.qdo_full[st ^ 1], ((gt + 1) >> 1) & 1, kSiteBwdLoad))) break;
+            if (!(ok = wait_all(&sh.qdo_full[sn], ((gt + 1) / C::QS) & 1, kSiteBwdLoad))) break;
             if (lane == 0) {
               tc_fence_after();
-              issue_kmajor(tmem + C::TM_DP, sV, sDO + (st ^ 1) * C::TILE, id_dp);
+              issue_kmajor(tmem + C::TM_DP, sV, sDO + sn * C::TILE, id_dp);
               mma_commit(&sh.dp_full);
             }
             __syncwarp();
@@ -540,14 +548,14 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       }
       for (int t = 0; t < T; ++t) {
         const int gt = g + t;
-        const int st = gt & 1;
+        const int st = gt % C::QS;
         const int q_row0 = q_tile(i_start, T, rot, t) * 128;
         // queries [lo, hi) of this tile may attend to this key
         const int lo = max(0, qlo - q_row0);
         const int hi = (key < mb) ? min(128, qhi - q_row0) : 0;
         const bool masked = __any_sync(0xffffffffu, lo > col0 || hi < col0 + 64);
         ok = __all_sync(0xffffffffu, guarded_wait(&sh.s_full, gt & 1, abort_flag, wd, kSiteBwdS) &&
-                                         guarded_wait(&sh.qdo_full[st], (gt >> 1) & 1, abort_flag, wd, kSiteBwdLoad));
+                                         guarded_wait(&sh.qdo_full[st], (gt / C::QS) & 1, abort_flag, wd, kSiteBwdLoad));
         if (!ok) break;
         tc_fence_after();
         const float* nlse2_s = stat + st * 256 + col0;  // -lse * log2(e) per query column
