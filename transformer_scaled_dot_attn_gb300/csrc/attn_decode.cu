@@ -24,7 +24,10 @@ constexpr int kDecTK = 64;          // keys per tile (TMA box rows)
 constexpr int kDecThreads = 128;
 constexpr float kDecLn2 = 0.69314718055994530942f;
 
-template <int D>
+// NQ: the queries the layout holds (the kernel's compiled query count): the
+// query, score and reduction areas are sized for it, so that steps with few
+// queries fit three CTAs per SM.
+template <int D, int NQ = kDecMaxN>
 struct Dec {
   static constexpr int ATOM = D >= 64 ? 64 : D;            // bf16 per swizzle row
   static constexpr int NATOM = D / ATOM;                   // TMA boxes per tile
@@ -37,10 +40,10 @@ struct Dec {
   static constexpr uint32_t OFF_K = 0;
   static constexpr uint32_t OFF_V = STAGES * TILE;
   static constexpr uint32_t OFF_Q = 2 * STAGES * TILE;                       // [n][D] fp32
-  static constexpr uint32_t OFF_S = OFF_Q + kDecMaxN * D * 4;                // [n][TK] fp32
-  static constexpr uint32_t OFF_A = OFF_S + kDecMaxN * kDecTK * 4;           // [n] fp32
-  static constexpr uint32_t OFF_R = OFF_A + kDecMaxN * 4;                    // [KG][n][D] fp32
-  static constexpr uint32_t SMEM = OFF_R + KG * kDecMaxN * D * 4 + 1024;     // + alignment slack
+  static constexpr uint32_t OFF_S = OFF_Q + NQ * D * 4;                     // [n][TK] fp32
+  static constexpr uint32_t OFF_A = OFF_S + NQ * kDecTK * 4;                 // [n] fp32
+  static constexpr uint32_t OFF_R = (OFF_A + NQ * 4 + 15) & ~15u;            // [KG][n][D] fp32
+  static constexpr uint32_t SMEM = OFF_R + KG * NQ * D * 4 + 1024;          // + alignment slack
   static_assert(kDecThreads % CP == 0 && kDecTK % KG == 0, "thread mapping");
 };
 
@@ -113,7 +116,7 @@ template <int D, int NQ>
 __global__ void __launch_bounds__(kDecThreads)
 attn_decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                    const DecParams p) {
-  using C = Dec<D>;
+  using C = Dec<D, NQ>;
   constexpr int NU = (NQ + 3) / 4;  // queries per warp in the weight phase
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t full[C::STAGES];
@@ -288,15 +291,15 @@ attn_decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
 #pragma unroll
   for (int i = 0; i < NQ; ++i)
     if (i < n) {
-      sR[(kg * kDecMaxN + i) * D + 2 * cp] = acc[i][0];
-      sR[(kg * kDecMaxN + i) * D + 2 * cp + 1] = acc[i][1];
+      sR[(kg * NQ + i) * D + 2 * cp] = acc[i][0];
+      sR[(kg * NQ + i) * D + 2 * cp + 1] = acc[i][1];
     }
   __syncthreads();
   for (int idx = tid; idx < n * D; idx += kDecThreads) {
     const int i = idx / D, c = idx % D;
     float o = 0.f;
 #pragma unroll
-    for (int g = 0; g < C::KG; ++g) o += sR[(g * kDecMaxN + i) * D + c];
+    for (int g = 0; g < C::KG; ++g) o += sR[(g * NQ + i) * D + c];
     part[i * (D + 2) + c] = o;
   }
 #pragma unroll
@@ -356,7 +359,7 @@ __global__ void __launch_bounds__(128) attn_decode_merge_kernel(const DecParams 
 template <int D, int NQ>
 cudaError_t launch_decode_step(const CUtensorMap& tk, const CUtensorMap& tv, const DecParams& p, int BH,
                                cudaStream_t stream) {
-  using C = Dec<D>;
+  using C = Dec<D, NQ>;
   static std::once_flag once[64];
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
