@@ -142,8 +142,8 @@ int attn_bwd_noalloc(const void* q, const void* k, const void* v, const void* o,
  *                        inputs into them and leaves every result in them too
  *   workspace            device memory of at least
  *                        attn_bwd_workspace_bytes(B, h, n, m, d_k, d_v, causal)
- *                        bytes (NULL when that is 0); the chunks use it one
- *                        after another
+ *                        bytes (NULL when that is 0); each chunk uses the
+ *                        part that belongs to its heads
  *   chunks               0: chosen by the library (about 24 MiB of inputs a
  *                        group, at most 8 groups); else the number of groups,
  *                        capped at 64 and at B*h
@@ -151,9 +151,12 @@ int attn_bwd_noalloc(const void* q, const void* k, const void* v, const void* o,
  * copies from pageable memory are correct but do not overlap. The work starts
  * after what is already queued on `stream`, and later work on `stream` starts
  * after all of it, copies included; the host buffers must stay valid and the
- * results must not be read before then (synchronise `stream`). The library
- * creates its copy streams and events on the first call on a device and keeps
- * them; calls on one device are serialised on the host. The results equal
+ * results must not be read before then (synchronise `stream`). The kernels of
+ * the even chunks run on `stream`, those of the odd chunks on a second stream
+ * of the library, so that two neighbouring chunks' kernels can share the GPU.
+ * The library creates its copy and kernel streams and events on the first
+ * call on a device and keeps them; calls on one device are serialised on the
+ * host. The results equal
  * those of attn_fwd + attn_bwd on the whole batch (every head is computed
  * alone; only the accumulation order of dQ in the long-sequence backward may
  * differ). Returns the codes of attn_fwd / attn_bwd, checked before anything

@@ -4,9 +4,13 @@
 // and the device-to-host copies of the chunk before that run at the same
 // time (the two directions use separate copy engines; on GB300 the host
 // link carries about 210 GB/s one way and 336 GB/s both ways at once). The
-// kernels are the library's own attn_fwd and attn_bwd, called per chunk on
-// the caller's stream; this file only orders copies and launches. The
-// declaration is in include/attn.h.
+// kernels are the library's own attn_fwd and attn_bwd, called per chunk;
+// this file only orders copies and launches. The chunks alternate between
+// the caller's stream and a second kernel stream, and each chunk's backward
+// takes its own part of the workspace, so the kernels of two neighbouring
+// chunks may run at once: the SMs that one launch's last, partial wave of
+// work leaves idle take the next chunk's work instead. The declaration is
+// in include/attn.h.
 #include "attn.h"
 
 #include <cuda_runtime.h>
@@ -36,11 +40,12 @@ constexpr int kAutoMaxChunks = 8;
 struct Pipe {
   cudaStream_t h2d = nullptr;
   cudaStream_t d2h = nullptr;
+  cudaStream_t kern = nullptr;  // kernels of the odd chunks (the even ones run on the caller's stream)
   cudaEvent_t start = nullptr;
   cudaEvent_t in_ready[kMaxChunks] = {};   // inputs of chunk c are on the device
   cudaEvent_t fwd_done[kMaxChunks] = {};   // O and lse of chunk c are written
   cudaEvent_t bwd_done[kMaxChunks] = {};   // dQ, dK, dV of chunk c are written
-  cudaEvent_t drained[2] = {};
+  cudaEvent_t drained[3] = {};
   bool ready = false;
 };
 
@@ -59,14 +64,14 @@ cudaError_t pipe_setup(Pipe& P) {
   };
   stream(P.h2d);
   stream(P.d2h);
+  stream(P.kern);
   event(P.start);
   for (int c = 0; c < kMaxChunks; ++c) {
     event(P.in_ready[c]);
     event(P.fwd_done[c]);
     event(P.bwd_done[c]);
   }
-  event(P.drained[0]);
-  event(P.drained[1]);
+  for (int i = 0; i < 3; ++i) event(P.drained[i]);
   if (e == cudaSuccess) P.ready = true;
   return e;
 }
@@ -129,7 +134,8 @@ extern "C" int attn_fwd_bwd_host(const void* hq, const void* hk, const void* hv,
   // The copies into the device buffers start after the work already queued on
   // `stream` (which may still read them).
   if (cudaEventRecord(P.start, s) != cudaSuccess) return ATTN_ERR_CUDA;
-  if (cudaStreamWaitEvent(P.h2d, P.start, 0) != cudaSuccess || cudaStreamWaitEvent(P.d2h, P.start, 0) != cudaSuccess)
+  if (cudaStreamWaitEvent(P.h2d, P.start, 0) != cudaSuccess || cudaStreamWaitEvent(P.d2h, P.start, 0) != cudaSuccess ||
+      cudaStreamWaitEvent(P.kern, P.start, 0) != cudaSuccess)
     return ATTN_ERR_CUDA;  // nothing copied yet: no stream of the call is ahead of `stream`
 
   auto at = [](const void* base, size_t off) {
@@ -156,32 +162,45 @@ extern "C" int attn_fwd_bwd_host(const void* hq, const void* hk, const void* hv,
                     cudaEventRecord(P.in_ready[c], cs) == cudaSuccess;
     if (!ok) status = ATTN_ERR_CUDA;
   }
-  // Stage 2 and 3: per chunk, the kernels on `stream` once its inputs landed,
-  // then its results back on a device-to-host stream (O and lse right after
-  // the forward, the gradients after the backward).
+  // Stage 2 and 3: per chunk, the kernels once its inputs landed, then its
+  // results back on a device-to-host stream (O and lse right after the
+  // forward, the gradients after the backward). A chunk's forward also waits
+  // for the previous chunk's forward, so at most two chunks are in flight and
+  // they finish in order: it runs beside the previous chunk's backward.
   for (int c = 0; c < chunks && status == ATTN_OK; ++c) {
     const int h0 = static_cast<int>(static_cast<long long>(BH) * c / chunks);
     const int h1 = static_cast<int>(static_cast<long long>(BH) * (c + 1) / chunks);
     const int nh = h1 - h0;
-    if (cudaStreamWaitEvent(s, P.in_ready[c], 0) != cudaSuccess) {
+    cudaStream_t ks = (c & 1) ? P.kern : s;
+    if (cudaStreamWaitEvent(ks, P.in_ready[c], 0) != cudaSuccess ||
+        (c > 0 && cudaStreamWaitEvent(ks, P.fwd_done[c - 1], 0) != cudaSuccess)) {
       status = ATTN_ERR_CUDA;
       break;
+    }
+    // The workspace holds the whole batch's per-head scratch in head order;
+    // this chunk takes the part of its own heads.
+    void* ws_c = workspace;
+    size_t ws_c_bytes = workspace_bytes;
+    if (ws_need > 0) {
+      ws_c = at(workspace, attn_bwd_workspace_bytes(h0, 1, n, m, d_k, d_v, causal));
+      ws_c_bytes = attn_bwd_workspace_bytes(nh, 1, n, m, d_k, d_v, causal);
     }
     // A chunk is nh heads of one sequence each: no argument of the kernels
     // depends on how the heads group into sequences (there is no key padding here).
     float* lse_c = reinterpret_cast<float*>(at(lse, h0 * b_lse));
+    const attn_stream_t kst = reinterpret_cast<attn_stream_t>(ks);
     status = attn_fwd(at(q, h0 * b_q), at(k, h0 * b_k), at(v, h0 * b_v), at(o, h0 * b_o), lse_c, nh, 1, n, m, d_k,
-                      d_v, causal, scale, stream);
+                      d_v, causal, scale, kst);
     if (status != ATTN_OK) break;
-    if (cudaEventRecord(P.fwd_done[c], s) != cudaSuccess) {
+    if (cudaEventRecord(P.fwd_done[c], ks) != cudaSuccess) {
       status = ATTN_ERR_CUDA;
       break;
     }
     status = attn_bwd(at(q, h0 * b_q), at(k, h0 * b_k), at(v, h0 * b_v), at(o, h0 * b_o), lse_c, at(dO, h0 * b_o),
                       at(dq, h0 * b_q), at(dk, h0 * b_k), at(dv, h0 * b_v), nh, 1, n, m, d_k, d_v, causal, scale,
-                      workspace, workspace_bytes, stream);
+                      ws_c, ws_c_bytes, kst);
     if (status != ATTN_OK) break;
-    if (cudaEventRecord(P.bwd_done[c], s) != cudaSuccess) {
+    if (cudaEventRecord(P.bwd_done[c], ks) != cudaSuccess) {
       status = ATTN_ERR_CUDA;
       break;
     }
@@ -200,8 +219,10 @@ extern "C" int attn_fwd_bwd_host(const void* hq, const void* hk, const void* hv,
   // error, so that no copy of this call outlives it unordered).
   const bool drained = cudaEventRecord(P.drained[0], P.h2d) == cudaSuccess &&
                        cudaEventRecord(P.drained[1], P.d2h) == cudaSuccess &&
+                       cudaEventRecord(P.drained[2], P.kern) == cudaSuccess &&
                        cudaStreamWaitEvent(s, P.drained[0], 0) == cudaSuccess &&
-                       cudaStreamWaitEvent(s, P.drained[1], 0) == cudaSuccess;
+                       cudaStreamWaitEvent(s, P.drained[1], 0) == cudaSuccess &&
+                       cudaStreamWaitEvent(s, P.drained[2], 0) == cudaSuccess;
   if (!drained && status == ATTN_OK) status = ATTN_ERR_CUDA;
   return status;
 }
