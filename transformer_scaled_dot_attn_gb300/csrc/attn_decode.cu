@@ -195,76 +195,79 @@ attn_decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
   for (; t < ntiles; ++t) {
     const int st = t % C::STAGES;
     const bool ok = spin_wait_dec(&full[st], (t / C::STAGES) & 1, abort_flag, wd, kSiteKFull);
-    if (__syncthreads_or(!ok)) break;
     const uint8_t* sK = smem + C::OFF_K + st * C::TILE;
     const uint8_t* sV = smem + C::OFF_V + st * C::TILE;
     const int kbase = k_begin + t * kDecTK;
-    if constexpr (QPT == 1) {
-      // scores: thread = key j of the tile, queries i = tid / 64, + 2, ...
-      // (n <= 2: one query per thread at most; the key row is loaded whole first)
-      const int j = tid & (kDecTK - 1);
-      const int key = kbase + j;
-      uint4 kr[D / 8];
+    if (ok) {
+      if constexpr (QPT == 1) {
+        // scores: thread = key j of the tile, queries i = tid / 64, + 2, ...
+        // (n <= 2: one query per thread at most; the key row is loaded whole first)
+        const int j = tid & (kDecTK - 1);
+        const int key = kbase + j;
+        uint4 kr[D / 8];
 #pragma unroll
-      for (int cc = 0; cc < D / 8; ++cc) kr[cc] = *reinterpret_cast<const uint4*>(sK + dec_off<D>(j, cc));
-      for (int i = tid >> 6; i < n; i += kDecThreads / kDecTK) {
-        const float* qi = sQ + i * D;
-        float s0 = 0.f, s1 = 0.f;
+        for (int cc = 0; cc < D / 8; ++cc) kr[cc] = *reinterpret_cast<const uint4*>(sK + dec_off<D>(j, cc));
+        for (int i = tid >> 6; i < n; i += kDecThreads / kDecTK) {
+          const float* qi = sQ + i * D;
+          float s0 = 0.f, s1 = 0.f;
 #pragma unroll
+          for (int cc = 0; cc < D / 8; ++cc) {
+            const uint32_t w[4] = {kr[cc].x, kr[cc].y, kr[cc].z, kr[cc].w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float2 kf = bf16x2_to_f2(w[e]);
+              s0 = fmaf(qi[cc * 8 + 2 * e], kf.x, s0);
+              s1 = fmaf(qi[cc * 8 + 2 * e + 1], kf.y, s1);
+            }
+          }
+          // key visible to query i: cached (key < k_end <= L) and not after its position
+          const bool vis = key < k_end && key <= L - n + i;
+          sS[i * kDecTK + j] = vis ? s0 + s1 : -INFINITY;
+        }
+      } else {
+        // scores: thread = key j of the tile, queries i = tid / 64, + 2, ...;
+        // each 16-byte chunk of the key row is unpacked once for all of them,
+        // and the queries' sums interleave (n = 4 at d = 64: 313 -> 287 us
+        // against a loop over the queries that unpacks the row for each).
+        // Query rows past n read a real row of sQ and are not stored.
+        const int j = tid & (kDecTK - 1);
+        const int key = kbase + j;
+        float sa[QPT], sb[QPT];
+#pragma unroll
+        for (int u = 0; u < QPT; ++u) sa[u] = sb[u] = 0.f;
+        // (sixteen queries at d = 128: a partial unroll keeps the loop within the registers)
+#pragma unroll(QPT * D > 512 ? 4 : D / 8)
         for (int cc = 0; cc < D / 8; ++cc) {
-          const uint32_t w[4] = {kr[cc].x, kr[cc].y, kr[cc].z, kr[cc].w};
+          const uint4 kw = *reinterpret_cast<const uint4*>(sK + dec_off<D>(j, cc));
+          const float2 k0 = bf16x2_to_f2(kw.x), k1 = bf16x2_to_f2(kw.y);
+          const float2 k2 = bf16x2_to_f2(kw.z), k3 = bf16x2_to_f2(kw.w);
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float2 kf = bf16x2_to_f2(w[e]);
-            s0 = fmaf(qi[cc * 8 + 2 * e], kf.x, s0);
-            s1 = fmaf(qi[cc * 8 + 2 * e + 1], kf.y, s1);
+          for (int u = 0; u < QPT; ++u) {
+            const int i = (tid >> 6) + 2 * u;
+            if (i < n) {
+              const float4 qa = *reinterpret_cast<const float4*>(sQ + i * D + cc * 8);
+              const float4 qb = *reinterpret_cast<const float4*>(sQ + i * D + cc * 8 + 4);
+              sa[u] = fmaf(qa.x, k0.x, sa[u]);
+              sb[u] = fmaf(qa.y, k0.y, sb[u]);
+              sa[u] = fmaf(qa.z, k1.x, sa[u]);
+              sb[u] = fmaf(qa.w, k1.y, sb[u]);
+              sa[u] = fmaf(qb.x, k2.x, sa[u]);
+              sb[u] = fmaf(qb.y, k2.y, sb[u]);
+              sa[u] = fmaf(qb.z, k3.x, sa[u]);
+              sb[u] = fmaf(qb.w, k3.y, sb[u]);
+            }
           }
         }
-        // key visible to query i: cached (key < k_end <= L) and not after its position
-        const bool vis = key < k_end && key <= L - n + i;
-        sS[i * kDecTK + j] = vis ? s0 + s1 : -INFINITY;
-      }
-    } else {
-      // scores: thread = key j of the tile, queries i = tid / 64, + 2, ...;
-      // each 16-byte chunk of the key row is unpacked once for all of them,
-      // and the queries' sums interleave (n = 4 at d = 64: 313 -> 287 us
-      // against a loop over the queries that unpacks the row for each).
-      // Query rows past n read a real row of sQ and are not stored.
-      const int j = tid & (kDecTK - 1);
-      const int key = kbase + j;
-      float sa[QPT], sb[QPT];
-#pragma unroll
-      for (int u = 0; u < QPT; ++u) sa[u] = sb[u] = 0.f;
-      // (sixteen queries at d = 128: a partial unroll keeps the loop within the registers)
-#pragma unroll(QPT * D > 512 ? 4 : D / 8)
-      for (int cc = 0; cc < D / 8; ++cc) {
-        const uint4 kw = *reinterpret_cast<const uint4*>(sK + dec_off<D>(j, cc));
-        const float2 k0 = bf16x2_to_f2(kw.x), k1 = bf16x2_to_f2(kw.y);
-        const float2 k2 = bf16x2_to_f2(kw.z), k3 = bf16x2_to_f2(kw.w);
 #pragma unroll
         for (int u = 0; u < QPT; ++u) {
           const int i = (tid >> 6) + 2 * u;
-          if (i < n) {
-            const float4 qa = *reinterpret_cast<const float4*>(sQ + i * D + cc * 8);
-            const float4 qb = *reinterpret_cast<const float4*>(sQ + i * D + cc * 8 + 4);
-            sa[u] = fmaf(qa.x, k0.x, sa[u]);
-            sb[u] = fmaf(qa.y, k0.y, sb[u]);
-            sa[u] = fmaf(qa.z, k1.x, sa[u]);
-            sb[u] = fmaf(qa.w, k1.y, sb[u]);
-            sa[u] = fmaf(qb.x, k2.x, sa[u]);
-            sb[u] = fmaf(qb.y, k2.y, sb[u]);
-            sa[u] = fmaf(qb.z, k3.x, sa[u]);
-            sb[u] = fmaf(qb.w, k3.y, sb[u]);
-          }
+          if (i < n) sS[i * kDecTK + j] = (key < k_end && key <= L - n + i) ? sa[u] + sb[u] : -INFINITY;
         }
       }
-#pragma unroll
-      for (int u = 0; u < QPT; ++u) {
-        const int i = (tid >> 6) + 2 * u;
-        if (i < n) sS[i * kDecTK + j] = (key < k_end && key <= L - n + i) ? sa[u] + sb[u] : -INFINITY;
-      }
     }
-    __syncthreads();
+    // the wait's outcome joins the barrier after the scores: a thread whose
+    // wait failed computes none, and every thread leaves the loop together
+    if (__syncthreads_or(!ok)) break;
     // exact running maximum and the weights, one warp per query
 #pragma unroll
     for (int u = 0; u < NU; ++u) {
@@ -321,7 +324,7 @@ attn_decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
   }
   if (t < ntiles) {
     // the watchdog fired at tile t: tiles t .. t + STAGES - 1 (those loaded)
-    // were never waited for; let their copies land before the CTA exits
+    // were not waited for by every thread; let their copies land before the CTA exits
     if (tid == 0)
       for (int x = t; x < t + C::STAGES && x < ntiles; ++x)
         drain_wait_dec(&full[x % C::STAGES], (x / C::STAGES) & 1, wd);
