@@ -37,8 +37,10 @@ struct Dec {
   // three at d = 128 with one query) keep as many bytes in flight as a deep
   // ring with fewer CTAs, and give the SM more warps to cover the barriers
   // (n = 1 over 4096 cached d64: 4 stages 175 us, 3 stages 165 us; over 16384
-  // cached d128: 3 stages 357 us, 2 stages 318 us)
-  static constexpr int STAGES = D <= 64 ? 3 : 2;
+  // cached d128: 3 stages 357 us, 2 stages 318 us). From four queries on, the
+  // step is bound by the barriers more than by loads in flight: 2 stages and
+  // five CTAs per SM at d = 64 (n = 4: 270 -> 260 us).
+  static constexpr int STAGES = D <= 64 ? (NQ >= 4 ? 2 : 3) : 2;
   static constexpr int CP = D / 2;                         // column pairs (P.V phase)
   static constexpr int KG = kDecThreads / CP;              // key groups (P.V phase)
   static constexpr int KPG = kDecTK / KG;                  // keys per group
