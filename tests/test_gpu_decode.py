@@ -6,7 +6,8 @@ step attends to the positions produced so far, itself included. Sequence b has
 L_b cached positions; its n newest are the queries, query i seeing keys
 j <= L_b - n + i. The cases cover one query and sixteen, d = 32, 64, 128, long
 caches split over many CTAs, ragged and empty caches, fewer cached positions
-than queries, a cache of one position, and a negative scale.
+than queries, a cache of one position, and a negative scale; and the
+benchmark's decoding steps at full size, sampled by head.
 """
 import numpy as np
 import pytest
@@ -14,7 +15,7 @@ import torch
 
 import oracle
 import transformer_scaled_dot_attn_gb300 as A
-from seeded_inputs import normal_bf16
+from seeded_inputs import DECODE_WORKLOADS, normal_bf16
 from tests.parity_utils import assert_close
 
 pytestmark = pytest.mark.gpu
@@ -75,3 +76,24 @@ def test_decode_argument_checks():
     ws = torch.zeros(4, dtype=torch.float32, device=DEV)
     with pytest.raises(A.AttnError):
         A.attn_decode(q, k, k, workspace=ws)  # workspace too small
+
+
+@pytest.mark.parametrize("name", list(DECODE_WORKLOADS))
+def test_decode_full_size_sampled(name):
+    """The benchmark's decoding steps at their full sizes (the whole batch in one
+    call, as timed): eight heads spread over the batch, first and last included,
+    against the oracle's step on those heads."""
+    B, h, n, m, d = DECODE_WORKLOADS[name]
+    q = normal_bf16((B, h, n, d), 2500)
+    k = normal_bf16((B, h, m, d), 2501)
+    v = normal_bf16((B, h, m, d), 2502)
+    scale = 1 / np.sqrt(d)
+    o, lse = A.attn_decode(q.to(DEV), k.to(DEV), v.to(DEV), scale=scale)
+    assert A.attn_get_device_status() == A.ATTN_OK
+    o, lse = o.cpu(), lse.cpu()
+    for bh in sorted(set(np.linspace(0, B * h - 1, 8).round().astype(int).tolist())):
+        b, hh = divmod(bh, h)
+        sl = (slice(b, b + 1), slice(hh, hh + 1))
+        ro, rlse = oracle.decode(q[sl], k[sl], v[sl], scale)
+        assert_close(f"{name} O head {bh}", o[sl], ro)
+        assert_close(f"{name} lse head {bh}", lse[sl], rlse)
