@@ -101,6 +101,19 @@ def test_workspace_size(lib):
     assert A.attn_bwd_workspace_bytes(1, 1, 0, 77, 64, 64) == 0
 
 
+@pytest.mark.parametrize("n,d,causal", [(300, 64, False), (16384, 128, False), (1000, 32, True), (257, 128, True)])
+def test_workspace_is_per_head_scratch(lib, n, d, causal):
+    # attn_fwd_bwd_host gives each head chunk the workspace part of its own heads
+    # (offset: the bytes of the heads before it), so the size must be the heads
+    # times one head's bytes, and one head's bytes a multiple of 16 (TMA alignment)
+    one = A.attn_bwd_workspace_bytes(1, 1, n, n, d, d, causal)
+    assert one > 0 and one % 16 == 0
+    for B, h in ((1, 7), (4, 16), (3, 5)):
+        assert A.attn_bwd_workspace_bytes(B, h, n, n, d, d, causal) == B * h * one
+        for h0 in range(B * h):
+            assert A.attn_bwd_workspace_bytes(h0, 1, n, n, d, d, causal) == h0 * one
+
+
 def test_debug_hooks(lib):
     assert A.attn_debug_inject(2) == A.ATTN_ERR_INVALID_ARG
     assert A.attn_debug_inject(0) == A.ATTN_OK
